@@ -1,0 +1,177 @@
+"""Restatement of the plan rules of the library, for a bit-exact metadata check.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+The pages fix what plan() is for, not how it partitions work: "[plan] create
+auxiliary data structures ... cached for multiple kernel runs" ("flashinfer.sparse",
+BlockSparseAttentionWrapper.plan notes) and the MLA scheduler metadata is reusable
+while seq_lens, the query shape and top-k stay unchanged ("Sparse MLA",
+get_batch_decode_metadata_mla). The partition rule below is the library's own design,
+stated here from its specification so that the C++ plan can be compared word for word:
+
+Metadata = 16 header words
+    magic 0x766b7362, kind (1 decode, 2 bsr, 3 mla), units, workers, chunks, slots,
+    merges, tile, off_workers, off_chunks, off_merges, off_aux0, off_aux1, grid,
+    total_words, variant
+followed by sections, each starting at a multiple of 4 words (zero padding):
+    worker_ptr[workers + 1], chunks[chunks][4], merges[merges][3], aux0, aux1.
+
+Linear partition (decode, MLA). Units have lengths len_u (tokens); tiles_u =
+ceil(len_u / tile); NT = sum of tiles; P = min(max_workers, NT); worker w owns the
+global tiles [floor(w NT / P), floor((w+1) NT / P)), cut at unit boundaries into
+chunks (unit, tok_begin, tok_end, slot) with tok_end clipped to len_u. A unit cut into
+>= 2 chunks gives each chunk a partial-state slot, numbered in chunk order; otherwise
+slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units with
+0 chunks (first_slot = -1) or >= 2 chunks.
+  * decode: units (b, kv head) b-major, len = request length, tile 16,
+    max_workers = 8 * num_sms unless given, grid = ceil(P / 8), aux0 = kv_indptr,
+    aux1 = kv_indices, variant 0.
+  * MLA: units (query token n = b*q_len + t, latent half v) n-major, len = seq_lens[b],
+    tile 64, max_workers = num_sms, grid = P, no aux, variant 0.
+
+BSR (longest processing time first). Tensor-core variant (variant 1) when R == 64,
+C == 64, head_dim == 128 and R*g in {128, 256} (g = Hq/Hkv): one unit per (row block
+i, kv head h), rows_per_unit = R*g, at most num_sms CTAs. Otherwise the general
+variant 0: rows_per_unit = 64, row_tiles = ceil(R*g / 64) units per (i, h), at most
+4*num_sms CTAs. Unit u = (i*Hkv + h)*row_tiles + rt; cost_u = 1 + blocks in row i.
+Units sorted by cost descending (stable); each goes to the CTA of least current load
+(ties: lowest CTA index). Chunks list each CTA's units in assignment order as
+(u, i, h, rt); tile = rows_per_unit; grid = number of CTAs; aux0 = indptr,
+aux1 = indices; no slots or merges.
+"""
+
+import heapq
+
+MAGIC = 0x766B7362
+
+
+def _align4(n):
+    return (n + 3) & ~3
+
+
+def _assemble(kind, units, worker_ptr, chunks, slots, merges, tile, aux0, aux1, grid, variant):
+    off_workers = 16
+    off = _align4(off_workers + len(worker_ptr))
+    off_chunks = off
+    off = _align4(off + 4 * len(chunks))
+    off_merges = off
+    off = _align4(off + 3 * len(merges))
+    off_aux0 = off
+    off = _align4(off + len(aux0))
+    off_aux1 = off
+    off = _align4(off + len(aux1))
+    m = [0] * off
+    hdr = [MAGIC, kind, units, max(len(worker_ptr) - 1, 0), len(chunks), slots, len(merges),
+           tile, off_workers, off_chunks, off_merges, off_aux0, off_aux1, grid, off, variant]
+    m[:16] = hdr
+    m[off_workers:off_workers + len(worker_ptr)] = worker_ptr
+    for i, c in enumerate(chunks):
+        m[off_chunks + 4 * i:off_chunks + 4 * i + 4] = list(c)
+    for i, it in enumerate(merges):
+        m[off_merges + 3 * i:off_merges + 3 * i + 3] = list(it)
+    m[off_aux0:off_aux0 + len(aux0)] = list(aux0)
+    m[off_aux1:off_aux1 + len(aux1)] = list(aux1)
+    return m
+
+
+def linear_partition(unit_len, tile, max_workers):
+    tiles = [(L + tile - 1) // tile for L in unit_len]
+    starts = [0]
+    for t in tiles:
+        starts.append(starts[-1] + t)
+    NT = starts[-1]
+    P = min(max_workers, NT)
+    worker_ptr, chunks = [], []
+    u = 0
+    for w in range(P):
+        t0, t1 = (w * NT) // P, ((w + 1) * NT) // P
+        worker_ptr.append(len(chunks))
+        t = t0
+        while t < t1:
+            while starts[u + 1] <= t:
+                u += 1
+            e = min(t1, starts[u + 1])
+            chunks.append([u, (t - starts[u]) * tile, min((e - starts[u]) * tile, unit_len[u]), -1])
+            t = e
+    worker_ptr.append(len(chunks))
+    count = [0] * len(unit_len)
+    for c in chunks:
+        count[c[0]] += 1
+    first = [-1] * len(unit_len)
+    slots = 0
+    for c in chunks:
+        if count[c[0]] >= 2:
+            if first[c[0]] < 0:
+                first[c[0]] = slots
+            c[3] = slots
+            slots += 1
+    merges = [(u, first[u], count[u]) for u in range(len(unit_len)) if count[u] != 1]
+    return worker_ptr, chunks, slots, merges
+
+
+def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_qo_heads,
+                num_kv_heads, num_sms, max_workers=0):
+    lens = []
+    for b in range(batch):
+        n = int(kv_indptr[b + 1]) - int(kv_indptr[b])
+        L = 0 if n == 0 else (n - 1) * page_size + int(kv_last_page_len[b])
+        lens += [L] * num_kv_heads
+    cap = max_workers if max_workers > 0 else 8 * num_sms
+    wp, ch, slots, merges = linear_partition(lens, 16, cap)
+    P = len(wp) - 1
+    nnz = int(kv_indptr[batch]) if batch > 0 else 0
+    aux0 = [int(x) for x in kv_indptr[:batch + 1]] if batch > 0 else []
+    aux1 = [int(x) for x in kv_indices[:nnz]]
+    return _assemble(1, len(lens), wp, ch, slots, merges, 16, aux0, aux1, (P + 7) // 8, 0)
+
+
+def mla_meta(seq_lens, batch, q_len, num_sms):
+    lens = []
+    for b in range(batch):
+        for _t in range(q_len):
+            lens += [int(seq_lens[b])] * 2
+    wp, ch, slots, merges = linear_partition(lens, 64, num_sms)
+    return _assemble(3, len(lens), wp, ch, slots, merges, 64, [], [], len(wp) - 1, 0)
+
+
+def bsr_meta(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, num_sms):
+    MB = (M + R - 1) // R
+    g = num_qo_heads // num_kv_heads
+    tc = R == 64 and C == 64 and head_dim == 128 and R * g in (128, 256)
+    rows = R * g if tc else 64
+    rt_n = (R * g + rows - 1) // rows
+    U = MB * num_kv_heads * rt_n
+    cost = [1 + int(indptr[u // (num_kv_heads * rt_n) + 1]) - int(indptr[u // (num_kv_heads * rt_n)])
+            for u in range(U)]
+    order = sorted(range(U), key=lambda u: -cost[u])  # Python's sort is stable
+    cap = num_sms if tc else 4 * num_sms
+    G = min(cap, U)
+    heap = [(0, c) for c in range(G)]
+    heapq.heapify(heap)
+    lists = [[] for _ in range(G)]
+    for u in order:
+        load, c = heapq.heappop(heap)
+        lists[c].append(u)
+        heapq.heappush(heap, (load + cost[u], c))
+    wp, ch = [], []
+    for c in range(G):
+        wp.append(len(ch))
+        for u in lists[c]:
+            ch.append([u, u // (rt_n * num_kv_heads), (u // rt_n) % num_kv_heads, u % rt_n])
+    wp.append(len(ch))
+    nnz = int(indptr[MB])
+    return _assemble(2, U, wp, ch, 0, [], rows, [int(x) for x in indptr[:MB + 1]],
+                     [int(x) for x in indices[:nnz]], G, 1 if tc else 0)
+
+
+def sections(meta):
+    """Split metadata words into a dict of named sections (for invariant checks)."""
+    h = meta[:16]
+    P, NC, NM = h[3], h[4], h[6]
+    return dict(
+        kind=h[1], units=h[2], workers=P, chunks_n=NC, slots=h[5], merges_n=NM, tile=h[7],
+        grid=h[13], total=h[14], variant=h[15],
+        worker_ptr=meta[h[8]:h[8] + P + 1] if P > 0 else meta[h[8]:h[8] + 1],
+        chunks=[meta[h[9] + 4 * i:h[9] + 4 * i + 4] for i in range(NC)],
+        merges=[meta[h[10] + 3 * i:h[10] + 3 * i + 3] for i in range(NM)],
+    )

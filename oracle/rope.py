@@ -1,0 +1,81 @@
+"""RoPE on the 64-value tail and FP8 quantisation of MLA query/key rows, in float64.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Follows "Sparse MLA" (MATE 0.2.6 API docs), section "RoPE and FP8 quantization"
+(mla_rope_quantize_fp8 parameters), and "FlashInfer Compatibility Wrapper", section
+"RoPE and FP8 quantization":
+  * the cos/sin cache has shape [max_seq_len, 64]; columns [:32] are cosines and
+    columns [32:] sines; every position must lie in [0, max_seq_len);
+  * is_neox=True rotates the two contiguous 32-value halves, is_neox=False rotates
+    adjacent even/odd pairs;
+  * the quant scales multiply the values before the FP8 cast:
+    Q_fp8 = cast(Q * quant_scale_q), KV_fp8 = cast(KV * quant_scale_kv),
+    for both the 512-value NoPE part and the rotated 64-value tail.
+Reading taken where the pages are silent: pair i (i < 32) uses cos = cache[pos, i]
+and sin = cache[pos, 32 + i] in both layouts, and rotates (x, y) to
+(x*cos - y*sin, y*cos + x*sin). The arithmetic is exact float64 on the stored cache
+values; the single rounding is the E4M3 cast.
+"""
+
+import numpy as np
+
+from .numerics import bf16_bits_to_f64, e4m3_encode
+
+ROPE_DIM = 64
+NOPE_DIM = 512
+
+
+def rotate(x, cos, sin, is_neox):
+    """Rotate rows of x [..., 64] by per-row cos/sin [..., 32] (float64)."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    if is_neox:
+        a, b = x[..., :32], x[..., 32:]
+        out[..., :32] = a * cos - b * sin
+        out[..., 32:] = b * cos + a * sin
+    else:
+        a, b = x[..., 0::2], x[..., 1::2]
+        out[..., 0::2] = a * cos - b * sin
+        out[..., 1::2] = b * cos + a * sin
+    return out
+
+
+def cache_rows(cos_sin, pos, cache_dtype="f32"):
+    """Gather (cos, sin) [n, 32] in float64 for positions ``pos`` from the stored cache."""
+    pos = np.asarray(pos, dtype=np.int64)
+    cs = np.asarray(cos_sin)
+    if np.any(pos < 0) or np.any(pos >= cs.shape[0]):
+        raise ValueError("position outside [0, max_seq_len)")
+    if cache_dtype == "f32":
+        rows = cs[pos].astype(np.float64)
+    elif cache_dtype == "bf16":
+        rows = bf16_bits_to_f64(cs[pos])
+    else:
+        raise ValueError(cache_dtype)
+    return rows[:, :32], rows[:, 32:]
+
+
+def mla_rope_quantize_fp8(q_rope_bits, k_rope_bits, q_nope_bits, k_nope_bits, cos_sin,
+                          pos_q, pos_k, is_neox=True, quant_scale_q=1.0, quant_scale_kv=1.0,
+                          cache_dtype="f32"):
+    """Return (q_rope_out, k_rope_out, q_nope_out, k_nope_out) as E4M3 codes.
+
+    q_rope [nq, H, 64], q_nope [nq, H, 512], k_rope [nk, 64], k_nope [nk, 512] are
+    bfloat16 bit patterns; pos_q [nq] and pos_k [nk] are positions. Any group may be
+    None (its outputs are then None). The pages' single-nnz form is pos_q == pos_k.
+    """
+    outs = [None, None, None, None]
+    if q_rope_bits is not None:
+        c, s = cache_rows(cos_sin, pos_q, cache_dtype)
+        qr = bf16_bits_to_f64(q_rope_bits)
+        rq = rotate(qr, c[:, None, :], s[:, None, :], is_neox)
+        outs[0] = e4m3_encode(rq * quant_scale_q)
+        outs[2] = e4m3_encode(bf16_bits_to_f64(q_nope_bits) * quant_scale_q)
+    if k_rope_bits is not None:
+        c, s = cache_rows(cos_sin, pos_k, cache_dtype)
+        kr = bf16_bits_to_f64(k_rope_bits)
+        rk = rotate(kr, c, s, is_neox)
+        outs[1] = e4m3_encode(rk * quant_scale_kv)
+        outs[3] = e4m3_encode(bf16_bits_to_f64(k_nope_bits) * quant_scale_kv)
+    return tuple(outs)

@@ -1,0 +1,248 @@
+"""Pins of the oracle's attention, index expansions and merge (CPU only).
+
+Pins, none of which re-types the oracle's own formula:
+  * the BSR worked example of the FlashInfer sparse page (3x3 mask, R = C = 1): the BSR
+    expansion reproduces the printed boolean mask, and BSR attention equals dense
+    attention under that mask (library routine: torch SDPA with attn_mask, float64);
+  * all blocks present equals unmasked SDPA; causal equals SDPA is_causal; GQA equals
+    SDPA on kv heads repeated with repeat_interleave (head h uses kv head h // g);
+  * brute force: pure-Python triple loop on tiny inputs;
+  * special cases: one visible key gives out = v and lse = logit; identical keys give
+    the mean of v; a row that sees nothing gives 0 and -inf;
+  * paged decode is invariant to page size and page permutation, and one page holding
+    the whole sequence equals dense attention;
+  * merging states of any split equals the unsplit result; merging one state is the
+    identity;
+  * sparse MLA over indices covering a whole small context equals dense attention on
+    the decoded rows; permuting the indices changes nothing; the scale folding rule of
+    the MATE wrapper page holds.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import synth
+from oracle import attention as att
+from oracle import numerics as nx
+from oracle import rope
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _sdpa(q, k, v, scale, mask=None, causal=False):
+    """Library reference: torch SDPA in float64 with kv heads repeated (h -> h // g)."""
+    Hq, Hkv = q.shape[1], k.shape[1]
+    g = Hq // Hkv
+    qt = torch.from_numpy(q).permute(1, 0, 2)
+    kt = torch.from_numpy(k).repeat_interleave(g, dim=1).permute(1, 0, 2)
+    vt = torch.from_numpy(v).repeat_interleave(g, dim=1).permute(1, 0, 2)
+    m = None if mask is None else torch.from_numpy(mask)
+    o = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=m, is_causal=causal, scale=scale)
+    return o.permute(1, 0, 2).numpy()
+
+
+def test_worked_example_mask_and_result():
+    ex = json.load(open(os.path.join(HERE, "golden", "bsr_worked_example.json")))
+    mask = att.bsr_mask(ex["indptr"], ex["indices"], ex["M"], ex["N"], ex["R"], ex["C"])
+    np.testing.assert_array_equal(mask, np.array(ex["mask"], dtype=bool))
+    d = synth.bsr_inputs(7, ex["M"], ex["N"], ex["R"], ex["C"], ex["num_qo_heads"],
+                         ex["num_kv_heads"], ex["head_dim"], pattern="full")
+    out, lse = att.bsr_attention(_bits(d["q"]), _bits(d["k"]), _bits(d["v"]), "fp16",
+                                 ex["indptr"], ex["indices"], ex["M"], ex["N"], ex["R"], ex["C"])
+    q = d["q"].double().numpy(); k = d["k"].double().numpy(); v = d["v"].double().numpy()
+    ref = _sdpa(q, k, v, 1 / math.sqrt(ex["head_dim"]), mask=np.array(ex["mask"], dtype=bool))
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_all_blocks_equals_dense(causal):
+    d = synth.bsr_inputs(11, 48, 48, 16, 8, 4, 2, 32, pattern="full", causal=causal)
+    out, lse = att.bsr_attention(_bits(d["q"]), _bits(d["k"]), _bits(d["v"]), "fp16",
+                                 d["indptr"].numpy(), d["indices"].numpy(), 48, 48, 16, 8,
+                                 causal=causal)
+    q = d["q"].double().numpy(); k = d["k"].double().numpy(); v = d["v"].double().numpy()
+    ref = _sdpa(q, k, v, d["sm_scale"], causal=causal)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    # lse against a direct logsumexp (library routine)
+    g = 2
+    logits = np.einsum("mhd,nhd->mhn", q, np.repeat(k, g, axis=1)) * d["sm_scale"]
+    if causal:
+        logits = np.where(np.tril(np.ones((48, 48), bool))[:, None, :], logits, -np.inf)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.from_numpy(logits), -1).numpy(),
+                               rtol=1e-12)
+
+
+def test_bottom_right_causal_when_m_less_than_n():
+    d = synth.bsr_inputs(12, 8, 24, 4, 8, 2, 1, 16, pattern="full", causal=True)
+    mask = att.bsr_mask(d["indptr"].numpy(), d["indices"].numpy(), 8, 24, 4, 8, causal=True)
+    # query i (of 8) sees keys j <= i + 16: the last query row sees all 24 keys
+    assert mask[-1].all() and mask[0].sum() == 17
+
+
+def test_brute_force_tiny():
+    rng = np.random.default_rng(2)
+    M, N, Hq, Hkv, D = 5, 7, 4, 2, 3
+    q, k, v = rng.standard_normal((M, Hq, D)), rng.standard_normal((N, Hkv, D)), rng.standard_normal((N, Hkv, D))
+    mask = rng.random((M, N)) < 0.6
+    mask[:, 0] = True
+    out, lse = att.masked_attention(q, k, v, 0.7, mask)
+    for i in range(M):
+        for h in range(Hq):
+            kh = h // (Hq // Hkv)
+            logits = [sum(q[i, h, t] * k[j, kh, t] for t in range(D)) * 0.7 if mask[i, j] else None
+                      for j in range(N)]
+            mx = max(x for x in logits if x is not None)
+            w = [math.exp(x - mx) if x is not None else 0.0 for x in logits]
+            tot = sum(w)
+            for t in range(D):
+                ref = sum(w[j] * v[j, kh, t] for j in range(N)) / tot
+                assert abs(out[i, h, t] - ref) < 1e-12
+            assert abs(lse[i, h] - (mx + math.log(tot))) < 1e-12
+
+
+def test_special_cases():
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((2, 2, 8)); k = rng.standard_normal((5, 1, 8)); v = rng.standard_normal((5, 1, 8))
+    mask = np.zeros((2, 5), bool)
+    mask[0, 3] = True  # one visible key; row 1 sees nothing
+    out, lse = att.masked_attention(q, k, v, 0.3, mask)
+    np.testing.assert_allclose(out[0, 0], v[3, 0], rtol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], 0.3 * q[0, 0] @ k[3, 0], rtol=1e-14)
+    assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
+    kk = np.repeat(k[:1], 5, axis=0)
+    out, _ = att.masked_attention(q, kk, v, 0.3)
+    np.testing.assert_allclose(out[:, 0], np.repeat(v[:, 0].mean(0, keepdims=True), 2, 0), rtol=1e-13)
+
+
+def _paged(seed, page_size, lengths, Hq=4, Hkv=2, D=16):
+    return synth.paged_decode_inputs(seed, len(lengths), Hq, Hkv, D, page_size, 0, 0,
+                                     lengths=lengths)
+
+
+def test_paged_invariance_to_page_size_and_permutation():
+    lengths = [1, 17, 40, 64, 5]
+    base = _paged(21, 64, lengths)
+    B, Hq, D = base["q"].shape
+    # Rebuild the same logical K/V with other page sizes and a fresh page permutation.
+    ks, vs = [], []
+    for b in range(B):
+        k, v = att.paged_kv(_bits(base["kv_cache"]), "bf16", base["kv_indptr"].numpy(),
+                            base["kv_indices"].numpy(), base["kv_last_page_len"].numpy(), 64, b)
+        ks.append(k); vs.append(v)
+    ref, ref_lse = att.paged_decode(_bits(base["q"]), _bits(base["kv_cache"]), "bf16",
+                                    base["kv_indptr"].numpy(), base["kv_indices"].numpy(),
+                                    base["kv_last_page_len"].numpy(), 64)
+    for ps, seed in [(1, 1), (16, 2), (7, 3)]:
+        other = _paged(100 + seed, ps, lengths)
+        cache = other["kv_cache"].clone()
+        for b in range(B):
+            pages = other["kv_indices"][other["kv_indptr"][b]:other["kv_indptr"][b + 1]]
+            kb = torch.from_numpy(ks[b]).to(torch.bfloat16)
+            vb = torch.from_numpy(vs[b]).to(torch.bfloat16)
+            for n, p in enumerate(pages.tolist()):
+                seg = slice(n * ps, min((n + 1) * ps, lengths[b]))
+                cnt = seg.stop - seg.start
+                cache[p, 0, :, :cnt] = kb[seg].transpose(0, 1)
+                cache[p, 1, :, :cnt] = vb[seg].transpose(0, 1)
+        out, lse = att.paged_decode(_bits(base["q"]), _bits(cache), "bf16",
+                                    other["kv_indptr"].numpy(), other["kv_indices"].numpy(),
+                                    other["kv_last_page_len"].numpy(), ps)
+        np.testing.assert_array_equal(out, ref)
+        np.testing.assert_array_equal(lse, ref_lse)
+
+
+def test_single_page_equals_dense():
+    d = _paged(31, 64, [64, 64])
+    out, lse = att.paged_decode(_bits(d["q"]), _bits(d["kv_cache"]), "bf16", d["kv_indptr"].numpy(),
+                                d["kv_indices"].numpy(), d["kv_last_page_len"].numpy(), 64)
+    for b in range(2):
+        page = int(d["kv_indices"][b])
+        k = d["kv_cache"][page, 0].transpose(0, 1).double().numpy()
+        v = d["kv_cache"][page, 1].transpose(0, 1).double().numpy()
+        q = d["q"][b:b + 1].double().numpy()
+        np.testing.assert_allclose(out[b], _sdpa(q, k, v, d["sm_scale"])[0], rtol=1e-12, atol=1e-14)
+
+
+def test_merge_of_any_split_equals_unsplit():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((3, 4, 8)); k = rng.standard_normal((50, 4, 8)); v = rng.standard_normal((50, 4, 8))
+    full, full_lse = att.masked_attention(q, k, v, 0.4)
+    cuts = [0, 7, 8, 30, 50]
+    parts = [att.masked_attention(q, k[a:b], v[a:b], 0.4) for a, b in zip(cuts[:-1], cuts[1:])]
+    vv = np.stack([p[0] for p in parts], axis=1)  # [M, S, H, D]
+    ss = np.stack([p[1] for p in parts], axis=1)
+    out, lse = att.merge_states(vv, ss, axis=1)
+    np.testing.assert_allclose(out, full, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, full_lse, rtol=1e-13)
+    one, one_lse = att.merge_states(vv[:, :1], ss[:, :1], axis=1)
+    np.testing.assert_allclose(one, vv[:, 0], rtol=1e-15)
+    np.testing.assert_array_equal(one_lse, ss[:, 0])
+    empty = att.merge_states(np.zeros((1, 2, 1, 4)), np.full((1, 2, 1), -np.inf), axis=1)
+    assert (empty[0] == 0).all() and np.isneginf(empty[1]).all()
+
+
+def _mla_small(seed=41, H=8, pool=256, top_k=128):
+    d = synth.mla_inputs(seed, batch=2, heads=H, top_k=top_k, pool_rows=pool, ctx_lo=top_k,
+                         ctx_hi=top_k, max_seq_len=pool)
+    qr, kr, qn, kn = rope.mla_rope_quantize_fp8(
+        _bits(d["q_rope"]), _bits(d["k_rope"]), _bits(d["q_nope"]), _bits(d["k_nope"]),
+        d["cos_sin"].numpy(), d["pos_q"].numpy(), d["pos_k"].numpy(), True)
+    query = np.concatenate([qn, qr], axis=-1).reshape(2, 1, H, 576)
+    kv = np.concatenate([kn, kr], axis=-1)
+    return d, query, kv
+
+
+def test_mla_full_context_equals_dense_and_is_permutation_invariant():
+    d, query, kv = _mla_small()
+    idx = d["indices"].numpy()
+    scale = 1 / math.sqrt(576)
+    out, lse = att.mla_sparse_decode(query, kv, idx, d["seq_lens"].numpy(), scale, 1.0)
+    for b in range(2):
+        rows = np.sort(idx[b, 0])  # the whole context (top_k == context length)
+        assert len(np.unique(rows)) == len(rows) == 128
+        K = nx.e4m3_decode(kv[rows])
+        Q = nx.e4m3_decode(query[b, 0])
+        ref = _sdpa(Q[None], K[:, None, :], K[:, None, :512], scale)[0]
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-14)
+    perm = idx[:, :, ::-1].copy()
+    out2, lse2 = att.mla_sparse_decode(query, kv, perm, d["seq_lens"].numpy(), scale, 1.0)
+    np.testing.assert_allclose(out2, out, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13)
+
+
+def test_mla_scale_folding():
+    """Quantising with scales (sq, skv) and decoding with bmm1 = a/(sq*skv), bmm2 = 1/skv
+    equals decoding unit-scale rows with bmm1 = a when the scaled values stay exact."""
+    d, query, kv = _mla_small(seed=43)
+    idx, sl = d["indices"].numpy(), d["seq_lens"].numpy()
+    a = 1 / math.sqrt(576)
+    sq, skv = 2.0, 0.5
+    qv, kvv = nx.e4m3_decode(query), nx.e4m3_decode(kv)
+    ok_q = np.abs(qv) >= 2.0 ** -5
+    ok_k = np.abs(kvv) >= 2.0 ** -5
+    q1 = nx.e4m3_encode(np.where(ok_q, qv, 0.0)); k1 = nx.e4m3_encode(np.where(ok_k, kvv, 0.0))
+    q2 = nx.e4m3_encode(nx.e4m3_decode(q1) * sq); k2 = nx.e4m3_encode(nx.e4m3_decode(k1) * skv)
+    o1, l1 = att.mla_sparse_decode(q1, k1, idx, sl, a, 1.0)
+    o2, l2 = att.mla_sparse_decode(q2, k2, idx, sl, a / (sq * skv), 1.0 / skv)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l2, l1, rtol=1e-12)
+
+
+def test_mla_seq_lens_limit_the_rows():
+    d, query, kv = _mla_small(seed=44)
+    idx = d["indices"].numpy()
+    sl = np.array([64, 0], np.int32)
+    out, lse = att.mla_sparse_decode(query, kv, idx, sl, 0.05, 1.0)
+    ref, ref_lse = att.mla_sparse_decode(query, kv, idx[:, :, :64], np.array([64, 0]), 0.05, 1.0)
+    np.testing.assert_array_equal(out, ref)
+    assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
