@@ -1,0 +1,358 @@
+// Host-side plans: validation of the CSR index arrays and the per-CTA work lists.
+//
+// Plans are pure host code (no CUDA call). They turn the caller's index arrays into
+// int32 metadata that the kernels read from the caller's int workspace:
+//   * decode and MLA: a linear split-KV partition. The units (one per request and kv
+//     head, or per query token and latent half) are cut into tiles; the tile sequence
+//     of all units is divided into equal contiguous ranges, one per worker; a unit that
+//     falls into several ranges is computed in pieces whose partial states are merged.
+//   * BSR: longest-processing-time assignment of (row block, kv head) units to
+//     persistent CTAs, heaviest unit first.
+// The rules are deterministic given num_sms, so the metadata is reproducible bit for bit.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <queue>
+#include <utility>
+
+#include "internal.h"
+
+namespace bskv {
+
+namespace {
+
+struct Chunk {
+  int32_t unit, a, b, c;  // meaning per plan kind
+};
+
+size_t align_words(size_t n) { return (n + 3) & ~size_t(3); }
+
+// Lay out header + sections.
+void assemble(bskv_plan* p, int32_t kind, int32_t units, const std::vector<int32_t>& worker_ptr,
+              const std::vector<Chunk>& chunks, int32_t slots,
+              const std::vector<int32_t>& merges /* 3 per item */, int32_t tile,
+              const int32_t* aux0, size_t n_aux0, const int32_t* aux1, size_t n_aux1,
+              int32_t grid, int32_t variant) {
+  size_t off = H_COUNT;
+  const size_t off_workers = off;
+  off = align_words(off + worker_ptr.size());
+  const size_t off_chunks = off;
+  off = align_words(off + 4 * chunks.size());
+  const size_t off_merges = off;
+  off = align_words(off + merges.size());
+  const size_t off_aux0 = off;
+  off = align_words(off + n_aux0);
+  const size_t off_aux1 = off;
+  off = align_words(off + n_aux1);
+  std::vector<int32_t>& m = p->meta;
+  m.assign(off, 0);
+  m[H_MAGIC] = kMetaMagic;
+  m[H_KIND] = kind;
+  m[H_UNITS] = units;
+  m[H_WORKERS] = int32_t(worker_ptr.empty() ? 0 : worker_ptr.size() - 1);
+  m[H_CHUNKS] = int32_t(chunks.size());
+  m[H_SLOTS] = slots;
+  m[H_MERGES] = int32_t(merges.size() / 3);
+  m[H_TILE] = tile;
+  m[H_OFF_WORKERS] = int32_t(off_workers);
+  m[H_OFF_CHUNKS] = int32_t(off_chunks);
+  m[H_OFF_MERGES] = int32_t(off_merges);
+  m[H_OFF_AUX0] = int32_t(off_aux0);
+  m[H_OFF_AUX1] = int32_t(off_aux1);
+  m[H_GRID] = grid;
+  m[H_TOTAL] = int32_t(off);
+  m[H_VARIANT] = variant;
+  std::copy(worker_ptr.begin(), worker_ptr.end(), m.begin() + off_workers);
+  for (size_t i = 0; i < chunks.size(); ++i) {
+    m[off_chunks + 4 * i + 0] = chunks[i].unit;
+    m[off_chunks + 4 * i + 1] = chunks[i].a;
+    m[off_chunks + 4 * i + 2] = chunks[i].b;
+    m[off_chunks + 4 * i + 3] = chunks[i].c;
+  }
+  std::copy(merges.begin(), merges.end(), m.begin() + off_merges);
+  if (n_aux0) std::memcpy(m.data() + off_aux0, aux0, n_aux0 * sizeof(int32_t));
+  if (n_aux1) std::memcpy(m.data() + off_aux1, aux1, n_aux1 * sizeof(int32_t));
+}
+
+// Linear split-KV partition. unit_len[u] tokens per unit, `tile` tokens per tile, at most
+// `max_workers` workers. Chunks: (unit, tok_begin, tok_end, slot); slot = -1 when the
+// unit is computed by a single chunk (written straight to the output), else the index
+// of its partial state. Merge items: (unit, first_slot, count) for units with 0 chunks
+// (zero-filled) or >= 2 chunks (merged), in unit order.
+void linear_partition(const std::vector<int64_t>& unit_len, int64_t tile, int64_t max_workers,
+                      std::vector<int32_t>& worker_ptr, std::vector<Chunk>& chunks,
+                      int32_t& slots, std::vector<int32_t>& merges) {
+  const size_t U = unit_len.size();
+  std::vector<int64_t> tiles(U), tile_start(U + 1, 0);
+  for (size_t u = 0; u < U; ++u) {
+    tiles[u] = (unit_len[u] + tile - 1) / tile;
+    tile_start[u + 1] = tile_start[u] + tiles[u];
+  }
+  const int64_t NT = tile_start[U];
+  const int64_t P = std::min<int64_t>(max_workers, NT);
+  worker_ptr.assign(size_t(P) + 1, 0);
+  chunks.clear();
+  std::vector<int32_t> nchunks(U, 0);
+  size_t u = 0;
+  for (int64_t w = 0; w < P; ++w) {
+    const int64_t t0 = (w * NT) / P;
+    const int64_t t1 = ((w + 1) * NT) / P;
+    worker_ptr[size_t(w)] = int32_t(chunks.size());
+    int64_t t = t0;
+    while (t < t1) {
+      while (tile_start[u + 1] <= t) ++u;  // unit holding global tile t
+      const int64_t e = std::min(t1, tile_start[u + 1]);
+      const int64_t lb = (t - tile_start[u]) * tile;
+      const int64_t le = std::min((e - tile_start[u]) * tile, unit_len[u]);
+      chunks.push_back(Chunk{int32_t(u), int32_t(lb), int32_t(le), -1});
+      nchunks[u] += 1;
+      t = e;
+    }
+  }
+  worker_ptr[size_t(P)] = int32_t(chunks.size());
+  slots = 0;
+  std::vector<int32_t> first_slot(U, -1);
+  for (Chunk& c : chunks) {
+    if (nchunks[size_t(c.unit)] >= 2) {
+      if (first_slot[size_t(c.unit)] < 0) first_slot[size_t(c.unit)] = slots;
+      c.c = slots++;
+    }
+  }
+  merges.clear();
+  for (size_t v = 0; v < U; ++v) {
+    if (nchunks[v] == 1) continue;
+    merges.push_back(int32_t(v));
+    merges.push_back(first_slot[v]);
+    merges.push_back(nchunks[v]);
+  }
+}
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+}  // namespace
+
+}  // namespace bskv
+
+using namespace bskv;
+
+extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t* kv_indices,
+                                        const int32_t* kv_last_page_len, int32_t batch,
+                                        int32_t num_pages, int32_t page_size,
+                                        int32_t num_qo_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t dtype, int32_t num_sms,
+                                        int32_t max_workers, bskv_plan** out_plan) {
+  if (!out_plan) { set_error("plan_decode: out_plan is NULL"); return BSKV_ERR_INVALID_ARG; }
+  *out_plan = nullptr;
+  if (batch < 0 || num_pages < 0 || page_size < 1 || num_sms < 1 || max_workers < 0) {
+    set_error("plan_decode: batch=%d num_pages=%d page_size=%d num_sms=%d max_workers=%d",
+              batch, num_pages, page_size, num_sms, max_workers);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0) {
+    set_error("plan_decode: num_qo_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+              num_qo_heads, num_kv_heads);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (batch > 0 && (!kv_indptr || !kv_last_page_len)) {
+    set_error("plan_decode: NULL index array"); return BSKV_ERR_INVALID_ARG;
+  }
+  const int32_t group = num_qo_heads / num_kv_heads;
+  if (group > 16) { set_error("plan_decode: %d query heads per kv head (max 16)", group); return BSKV_ERR_UNSUPPORTED; }
+  if (head_dim != 64 && head_dim != 128) { set_error("plan_decode: head_dim %d not in {64,128}", head_dim); return BSKV_ERR_UNSUPPORTED; }
+  if (dtype != BSKV_BF16 && dtype != BSKV_FP16) { set_error("plan_decode: dtype %s unsupported", dtype_name(dtype)); return BSKV_ERR_UNSUPPORTED; }
+  if (batch > 0 && kv_indptr[0] != 0) { set_error("plan_decode: kv_indptr[0] must be 0"); return BSKV_ERR_INVALID_ARG; }
+  std::vector<int64_t> len(size_t(batch) * size_t(num_kv_heads));
+  int64_t total_tokens = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t n = int64_t(kv_indptr[b + 1]) - kv_indptr[b];
+    if (n < 0) { set_error("plan_decode: kv_indptr decreases at %d", b); return BSKV_ERR_INVALID_ARG; }
+    int64_t L = 0;
+    if (n > 0) {
+      const int32_t lp = kv_last_page_len[b];
+      if (lp < 1 || lp > page_size) {
+        set_error("plan_decode: kv_last_page_len[%d] = %d outside [1, %d]", b, lp, page_size);
+        return BSKV_ERR_INVALID_ARG;
+      }
+      L = (n - 1) * page_size + lp;
+    }
+    total_tokens += L;
+    for (int32_t h = 0; h < num_kv_heads; ++h) len[size_t(b) * num_kv_heads + h] = L;
+  }
+  const int64_t nnz = batch > 0 ? kv_indptr[batch] : 0;
+  if (nnz > 0 && !kv_indices) { set_error("plan_decode: kv_indices is NULL"); return BSKV_ERR_INVALID_ARG; }
+  for (int64_t i = 0; i < nnz; ++i) {
+    if (kv_indices[i] < 0 || kv_indices[i] >= num_pages) {
+      set_error("plan_decode: kv_indices[%lld] = %d outside [0, %d)", (long long)i, kv_indices[i], num_pages);
+      return BSKV_ERR_INVALID_ARG;
+    }
+  }
+  if (total_tokens * num_kv_heads > INT32_MAX / 2) { set_error("plan_decode: too many tokens"); return BSKV_ERR_UNSUPPORTED; }
+  const int64_t workers_cap = max_workers > 0 ? max_workers : int64_t(num_sms) * kDecodeWarps;
+  std::vector<int32_t> worker_ptr, merges;
+  std::vector<Chunk> chunks;
+  int32_t slots = 0;
+  linear_partition(len, kDecodeTile, workers_cap, worker_ptr, chunks, slots, merges);
+  const int32_t P = int32_t(worker_ptr.size() - 1);
+  const int32_t grid = (P + kDecodeWarps - 1) / kDecodeWarps;
+  bskv_plan* p = new bskv_plan();
+  p->kind = KIND_DECODE;
+  p->batch = batch; p->num_pages = num_pages; p->page_size = page_size;
+  p->num_qo_heads = num_qo_heads; p->num_kv_heads = num_kv_heads; p->head_dim = head_dim;
+  p->dtype = dtype;
+  assemble(p, KIND_DECODE, int32_t(len.size()), worker_ptr, chunks, slots, merges, kDecodeTile,
+           kv_indptr, batch > 0 ? size_t(batch) + 1 : 0, kv_indices, size_t(nnz), grid, 0);
+  p->float_ws_bytes = slots == 0 ? 0
+      : align256(size_t(slots) * group * head_dim * 4) + align256(size_t(slots) * group * 4);
+  *out_plan = p;
+  return BSKV_OK;
+}
+
+extern "C" bskv_status bskv_plan_bsr(const int32_t* indptr, const int32_t* indices, int32_t M,
+                                     int32_t N, int32_t R, int32_t C, int32_t num_qo_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t causal,
+                                     int32_t dtype, int32_t num_sms, bskv_plan** out_plan) {
+  if (!out_plan) { set_error("plan_bsr: out_plan is NULL"); return BSKV_ERR_INVALID_ARG; }
+  *out_plan = nullptr;
+  if (M < 0 || N < 0 || R < 1 || C < 1 || num_sms < 1) {
+    set_error("plan_bsr: M=%d N=%d R=%d C=%d num_sms=%d", M, N, R, C, num_sms);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (N % C != 0) { set_error("plan_bsr: N (%d) must be divisible by C (%d)", N, C); return BSKV_ERR_INVALID_ARG; }
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0) {
+    set_error("plan_bsr: num_qo_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+              num_qo_heads, num_kv_heads);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (head_dim != 64 && head_dim != 128) { set_error("plan_bsr: head_dim %d not in {64,128}", head_dim); return BSKV_ERR_UNSUPPORTED; }
+  if (dtype != BSKV_BF16 && dtype != BSKV_FP16) { set_error("plan_bsr: dtype %s unsupported", dtype_name(dtype)); return BSKV_ERR_UNSUPPORTED; }
+  const int32_t MB = (M + R - 1) / R, NB = N / C;
+  if (!indptr) { set_error("plan_bsr: indptr is NULL"); return BSKV_ERR_INVALID_ARG; }
+  if (indptr[0] != 0) { set_error("plan_bsr: indptr[0] must be 0"); return BSKV_ERR_INVALID_ARG; }
+  for (int32_t i = 0; i < MB; ++i) {
+    if (indptr[i + 1] < indptr[i]) { set_error("plan_bsr: indptr decreases at %d", i); return BSKV_ERR_INVALID_ARG; }
+  }
+  const int32_t nnz = indptr[MB];
+  if (nnz > 0 && !indices) { set_error("plan_bsr: indices is NULL"); return BSKV_ERR_INVALID_ARG; }
+  std::vector<int32_t> seen(size_t(NB), -1);
+  for (int32_t i = 0; i < MB; ++i) {
+    for (int32_t e = indptr[i]; e < indptr[i + 1]; ++e) {
+      const int32_t j = indices[e];
+      if (j < 0 || j >= NB) { set_error("plan_bsr: indices[%d] = %d outside [0, %d)", e, j, NB); return BSKV_ERR_INVALID_ARG; }
+      if (seen[size_t(j)] == i) { set_error("plan_bsr: column block %d listed twice in row block %d", j, i); return BSKV_ERR_INVALID_ARG; }
+      seen[size_t(j)] = i;
+    }
+  }
+  const int32_t group = num_qo_heads / num_kv_heads;
+  const bool tc = (R == 64 && C == 64 && head_dim == 128 && (R * group == 128 || R * group == 256));
+  const int32_t rows_per_unit = tc ? R * group : kBsrGenericRows;
+  const int32_t row_tiles = (R * group + rows_per_unit - 1) / rows_per_unit;
+  const int64_t U = int64_t(MB) * num_kv_heads * row_tiles;
+  if (U > INT32_MAX / 4) { set_error("plan_bsr: too many units"); return BSKV_ERR_UNSUPPORTED; }
+  // Longest-processing-time assignment: cost = 1 + blocks in the unit's row block.
+  std::vector<int32_t> order(static_cast<size_t>(U));
+  std::vector<int64_t> cost(static_cast<size_t>(U));
+  for (int64_t u = 0; u < U; ++u) {
+    const int32_t i = int32_t(u / (int64_t(num_kv_heads) * row_tiles));
+    cost[size_t(u)] = 1 + (indptr[i + 1] - indptr[i]);
+    order[size_t(u)] = int32_t(u);
+  }
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t a, int32_t b) { return cost[size_t(a)] > cost[size_t(b)]; });
+  const int64_t cap = tc ? num_sms : int64_t(num_sms) * kBsrGenericCtasPerSm;
+  const int32_t G = int32_t(std::min<int64_t>(cap, U));
+  using Item = std::pair<int64_t, int32_t>;  // (load, cta), smallest first
+  std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+  for (int32_t c = 0; c < G; ++c) heap.push(Item(0, c));
+  std::vector<std::vector<int32_t>> lists(static_cast<size_t>(G));
+  for (int32_t u : order) {
+    Item it = heap.top();
+    heap.pop();
+    lists[size_t(it.second)].push_back(u);
+    it.first += cost[size_t(u)];
+    heap.push(it);
+  }
+  std::vector<int32_t> worker_ptr(size_t(G) + 1, 0);
+  std::vector<Chunk> chunks;
+  chunks.reserve(size_t(U));
+  for (int32_t c = 0; c < G; ++c) {
+    worker_ptr[size_t(c)] = int32_t(chunks.size());
+    for (int32_t u : lists[size_t(c)]) {
+      const int32_t rt = u % row_tiles;
+      const int32_t h = (u / row_tiles) % num_kv_heads;
+      const int32_t i = u / (row_tiles * num_kv_heads);
+      chunks.push_back(Chunk{u, i, h, rt});
+    }
+  }
+  worker_ptr[size_t(G)] = int32_t(chunks.size());
+  bskv_plan* p = new bskv_plan();
+  p->kind = KIND_BSR;
+  p->M = M; p->N = N; p->R = R; p->C = C; p->causal = causal ? 1 : 0;
+  p->num_qo_heads = num_qo_heads; p->num_kv_heads = num_kv_heads; p->head_dim = head_dim;
+  p->dtype = dtype;
+  std::vector<int32_t> no_merges;
+  assemble(p, KIND_BSR, int32_t(U), worker_ptr, chunks, 0, no_merges, rows_per_unit, indptr,
+           size_t(MB) + 1, indices, size_t(nnz), G, tc ? BSR_TCGEN05 : BSR_GENERIC);
+  p->float_ws_bytes = 0;
+  *out_plan = p;
+  return BSKV_OK;
+}
+
+extern "C" bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                                            int32_t num_heads, int32_t top_k, int32_t num_sms,
+                                            bskv_plan** out_plan) {
+  if (!out_plan) { set_error("plan_mla_sparse: out_plan is NULL"); return BSKV_ERR_INVALID_ARG; }
+  *out_plan = nullptr;
+  if (batch < 0 || q_len < 1 || num_sms < 1 || (batch > 0 && !seq_lens)) {
+    set_error("plan_mla_sparse: batch=%d q_len=%d num_sms=%d", batch, q_len, num_sms);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (top_k < 64 || top_k % 64 != 0) { set_error("plan_mla_sparse: top_k (%d) must be a positive multiple of 64", top_k); return BSKV_ERR_INVALID_ARG; }
+  if (num_heads < 1 || num_heads > 128) { set_error("plan_mla_sparse: num_heads %d outside [1,128]", num_heads); return BSKV_ERR_UNSUPPORTED; }
+  std::vector<int64_t> len;
+  len.reserve(size_t(batch) * q_len * kMlaVSplit);
+  for (int32_t b = 0; b < batch; ++b) {
+    if (seq_lens[b] < 0 || seq_lens[b] > top_k) {
+      set_error("plan_mla_sparse: seq_lens[%d] = %d outside [0, top_k=%d]", b, seq_lens[b], top_k);
+      return BSKV_ERR_INVALID_ARG;
+    }
+    for (int32_t t = 0; t < q_len; ++t)
+      for (int32_t v = 0; v < kMlaVSplit; ++v) len.push_back(seq_lens[b]);
+  }
+  std::vector<int32_t> worker_ptr, merges;
+  std::vector<Chunk> chunks;
+  int32_t slots = 0;
+  linear_partition(len, kMlaTile, num_sms, worker_ptr, chunks, slots, merges);
+  const int32_t P = int32_t(worker_ptr.size() - 1);
+  bskv_plan* p = new bskv_plan();
+  p->kind = KIND_MLA;
+  p->batch = batch; p->q_len = q_len; p->num_qo_heads = num_heads; p->top_k = top_k;
+  p->head_dim = 576; p->dtype = BSKV_E4M3;
+  assemble(p, KIND_MLA, int32_t(len.size()), worker_ptr, chunks, slots, merges, kMlaTile,
+           nullptr, 0, nullptr, 0, P, 0);
+  p->float_ws_bytes = slots == 0 ? 0
+      : align256(size_t(slots) * 128 * kMlaVDim * 4) + align256(size_t(slots) * 128 * 4);
+  *out_plan = p;
+  return BSKV_OK;
+}
+
+extern "C" bskv_status bskv_plan_destroy(bskv_plan* plan) {
+  delete plan;
+  return BSKV_OK;
+}
+
+extern "C" bskv_status bskv_plan_metadata(const bskv_plan* plan, const int32_t** meta,
+                                          int64_t* num_words) {
+  if (!plan || !meta || !num_words) { set_error("plan_metadata: NULL argument"); return BSKV_ERR_INVALID_ARG; }
+  *meta = plan->meta.data();
+  *num_words = int64_t(plan->meta.size());
+  return BSKV_OK;
+}
+
+extern "C" bskv_status bskv_plan_workspace_sizes(const bskv_plan* plan, size_t* int_ws_bytes,
+                                                 size_t* float_ws_bytes) {
+  if (!plan) { set_error("plan_workspace_sizes: NULL plan"); return BSKV_ERR_INVALID_ARG; }
+  if (int_ws_bytes) *int_ws_bytes = plan->meta.size() * sizeof(int32_t);
+  if (float_ws_bytes) *float_ws_bytes = plan->float_ws_bytes;
+  return BSKV_OK;
+}

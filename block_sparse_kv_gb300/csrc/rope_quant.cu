@@ -1,0 +1,238 @@
+// Fused RoPE + FP8 E4M3 quantisation of MLA query and key rows (512 NoPE + 64 RoPE values).
+//
+// Method: "Sparse MLA" (MATE 0.2.6), mla_rope_quantize_fp8 (rotary arithmetic in float32
+// on the 64-value tail; cos/sin cache columns [:32] cos and [32:] sin; is_neox selects
+// contiguous halves or adjacent even/odd pairs; Q_fp8 = cast(Q * quant_scale_q),
+// K_fp8 = cast(K * quant_scale_kv); outputs may be strided slices of 576-byte rows).
+//
+// GB300 design: a pure HBM stream (2.0 bytes in per byte out, plus the cache row). One warp
+// per row: each lane loads 32 bytes of NoPE (two 16-byte loads) and writes 16 bytes of E4M3,
+// and 4 bytes of the RoPE tail, exchanging rotation partners with one shuffle (neox) or
+// none (even/odd). cvt.rn.satfinite.e4m3x2.f32 does the cast (RNE, saturating to +-448).
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "launch.h"
+
+namespace bskv {
+namespace {
+
+using namespace dev;
+
+struct RopeParams {
+  // query group
+  const __nv_bfloat16* q_rope;
+  int64_t qr_s0, qr_s1;
+  const __nv_bfloat16* q_nope;
+  int64_t qn_s0, qn_s1;
+  const void* pos_q;
+  int64_t nnz_q;
+  int heads;
+  uint8_t* q_rope_out;
+  int64_t qro_s0, qro_s1;
+  uint8_t* q_nope_out;
+  int64_t qno_s0, qno_s1;
+  // key group
+  const __nv_bfloat16* k_rope;
+  int64_t kr_s;
+  const __nv_bfloat16* k_nope;
+  int64_t kn_s;
+  const void* pos_k;
+  int64_t nnz_k;
+  uint8_t* k_rope_out;
+  int64_t kro_s;
+  uint8_t* k_nope_out;
+  int64_t kno_s;
+  // shared
+  const void* cos_sin;
+  int64_t max_seq_len;
+  float scale_q, scale_kv;
+  StatusArgs st;
+};
+
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  return static_cast<uint16_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <bool kNeox, typename PosT, typename CacheT>
+__device__ __forceinline__ void rope_row(const __nv_bfloat16* rope, const __nv_bfloat16* nope,
+                                         uint8_t* rope_out, uint8_t* nope_out, int64_t pos,
+                                         const CacheT* cache, float scale, int lane) {
+  // NoPE: 512 bf16 = 1024 bytes; lane owns elements [16*lane, 16*lane + 16).
+  const uint4* src = reinterpret_cast<const uint4*>(nope) + 2 * lane;
+  const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  uint32_t packed[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t a = cvt_e4m3x2(bf16_lo(w[2 * i]) * scale, bf16_hi(w[2 * i]) * scale);
+    const uint16_t b = cvt_e4m3x2(bf16_lo(w[2 * i + 1]) * scale, bf16_hi(w[2 * i + 1]) * scale);
+    packed[i] = uint32_t(a) | (uint32_t(b) << 16);
+  }
+  *reinterpret_cast<uint4*>(nope_out + 16 * lane) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+
+  // RoPE tail: lane owns elements 2*lane and 2*lane + 1.
+  const uint32_t rw = __ldg(reinterpret_cast<const unsigned int*>(rope) + lane);
+  const float e0 = bf16_lo(rw), e1 = bf16_hi(rw);
+  float c0, c1, s0, s1;
+  const int i0 = kNeox ? ((2 * lane) & 31) : lane;  // frequency index of the first element
+  auto cs = [&](int i) -> float {
+    if constexpr (sizeof(CacheT) == 4) {
+      return __ldg(reinterpret_cast<const float*>(cache) + pos * 64 + i);
+    } else {
+      const uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(cache) + pos * 64 + i);
+      return __uint_as_float(uint32_t(b) << 16);
+    }
+  };
+  float r0, r1;
+  if (kNeox) {
+    // Pair i = (i, i + 32): lanes 0-15 hold the first halves, lanes 16-31 the partners.
+    c0 = cs(i0); c1 = cs(i0 + 1); s0 = cs(32 + i0); s1 = cs(32 + i0 + 1);
+    const float p0 = __shfl_xor_sync(0xffffffffu, e0, 16);
+    const float p1 = __shfl_xor_sync(0xffffffffu, e1, 16);
+    if (lane < 16) {
+      r0 = __fsub_rn(__fmul_rn(e0, c0), __fmul_rn(p0, s0));
+      r1 = __fsub_rn(__fmul_rn(e1, c1), __fmul_rn(p1, s1));
+    } else {
+      r0 = __fadd_rn(__fmul_rn(e0, c0), __fmul_rn(p0, s0));
+      r1 = __fadd_rn(__fmul_rn(e1, c1), __fmul_rn(p1, s1));
+    }
+  } else {
+    c0 = cs(i0); s0 = cs(32 + i0);
+    r0 = __fsub_rn(__fmul_rn(e0, c0), __fmul_rn(e1, s0));
+    r1 = __fadd_rn(__fmul_rn(e1, c0), __fmul_rn(e0, s0));
+  }
+  const uint16_t out = cvt_e4m3x2(__fmul_rn(r0, scale), __fmul_rn(r1, scale));
+  *reinterpret_cast<uint16_t*>(rope_out + 2 * lane) = out;
+}
+
+template <bool kNeox, typename PosT, typename CacheT>
+__global__ void __launch_bounds__(256) rope_quant_kernel(const RopeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t q_rows = p.q_rope ? p.nnz_q * p.heads : 0;
+  const int64_t k_rows = p.k_rope ? p.nnz_k : 0;
+  const CacheT* cache = static_cast<const CacheT*>(p.cos_sin);
+  for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < q_rows + k_rows;
+       r += warps_total) {
+    if (r < q_rows) {
+      const int64_t t = r / p.heads;
+      const int h = int(r % p.heads);
+      const int64_t pos = int64_t(static_cast<const PosT*>(p.pos_q)[t]);
+      if (pos < 0 || pos >= p.max_seq_len) {
+        if (lane == 0) record_error(p.st, BSKV_ERR_DEVICE_INDEX);
+        continue;
+      }
+      rope_row<kNeox, PosT, CacheT>(p.q_rope + t * p.qr_s0 + h * p.qr_s1,
+                                    p.q_nope + t * p.qn_s0 + h * p.qn_s1,
+                                    p.q_rope_out + t * p.qro_s0 + h * p.qro_s1,
+                                    p.q_nope_out + t * p.qno_s0 + h * p.qno_s1, pos, cache,
+                                    p.scale_q, lane);
+    } else {
+      const int64_t t = r - q_rows;
+      const int64_t pos = int64_t(static_cast<const PosT*>(p.pos_k)[t]);
+      if (pos < 0 || pos >= p.max_seq_len) {
+        if (lane == 0) record_error(p.st, BSKV_ERR_DEVICE_INDEX);
+        continue;
+      }
+      rope_row<kNeox, PosT, CacheT>(p.k_rope + t * p.kr_s, p.k_nope + t * p.kn_s,
+                                    p.k_rope_out + t * p.kro_s, p.k_nope_out + t * p.kno_s, pos,
+                                    cache, p.scale_kv, lane);
+    }
+  }
+}
+
+template <bool kNeox>
+bskv_status launch_rope(const RopeParams& p, int pos_dtype, int cache_dtype, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  if (bskv_status s = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return s;
+  if (bskv_status s = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"))
+    return s;
+  const int64_t rows = (p.q_rope ? p.nnz_q * p.heads : 0) + (p.k_rope ? p.nnz_k : 0);
+  if (rows == 0) return BSKV_OK;
+  const int64_t want = (rows + 7) / 8;
+  const int blocks = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+  if (pos_dtype == BSKV_INT32) {
+    if (cache_dtype == BSKV_FP32) rope_quant_kernel<kNeox, int32_t, float><<<blocks, 256, 0, st>>>(p);
+    else rope_quant_kernel<kNeox, int32_t, __nv_bfloat16><<<blocks, 256, 0, st>>>(p);
+  } else {
+    if (cache_dtype == BSKV_FP32) rope_quant_kernel<kNeox, int64_t, float><<<blocks, 256, 0, st>>>(p);
+    else rope_quant_kernel<kNeox, int64_t, __nv_bfloat16><<<blocks, 256, 0, st>>>(p);
+  }
+  return cuda_check(cudaGetLastError(), "rope_quantize_fp8 launch");
+}
+
+}  // namespace
+}  // namespace bskv
+
+using namespace bskv;
+
+extern "C" bskv_status bskv_rope_quantize_fp8(
+    const void* q_rope, const int64_t* q_rope_strides, const void* q_nope,
+    const int64_t* q_nope_strides, const void* pos_q, int64_t nnz_q, int32_t num_heads,
+    void* q_rope_out, const int64_t* q_rope_out_strides, void* q_nope_out,
+    const int64_t* q_nope_out_strides, const void* k_rope, int64_t k_rope_stride,
+    const void* k_nope, int64_t k_nope_stride, const void* pos_k, int64_t nnz_k,
+    void* k_rope_out, int64_t k_rope_out_stride, void* k_nope_out, int64_t k_nope_out_stride,
+    int32_t pos_dtype, const void* cos_sin, int32_t cos_sin_dtype, int64_t max_seq_len,
+    int32_t is_neox, float quant_scale_q, float quant_scale_kv, void* stream) {
+  RopeParams p{};
+  const bool has_q = q_rope || q_nope || q_rope_out || q_nope_out || pos_q;
+  const bool has_k = k_rope || k_nope || k_rope_out || k_nope_out || pos_k;
+  if (pos_dtype != BSKV_INT32 && pos_dtype != BSKV_INT64) { set_error("rope_quantize_fp8: pos dtype %s unsupported", dtype_name(pos_dtype)); return BSKV_ERR_UNSUPPORTED; }
+  if (cos_sin_dtype != BSKV_FP32 && cos_sin_dtype != BSKV_BF16) { set_error("rope_quantize_fp8: cos_sin dtype %s unsupported", dtype_name(cos_sin_dtype)); return BSKV_ERR_UNSUPPORTED; }
+  if (!cos_sin || max_seq_len < 1) { set_error("rope_quantize_fp8: cos_sin cache missing"); return BSKV_ERR_INVALID_ARG; }
+  if (has_q) {
+    if (!q_rope || !q_nope || !q_rope_out || !q_nope_out || !pos_q || !q_rope_strides ||
+        !q_nope_strides || !q_rope_out_strides || !q_nope_out_strides) {
+      set_error("rope_quantize_fp8: the query group needs all of q_rope, q_nope, pos_q and both outputs");
+      return BSKV_ERR_INVALID_ARG;
+    }
+    if (nnz_q < 0 || num_heads < 1) { set_error("rope_quantize_fp8: nnz_q=%lld num_heads=%d", (long long)nnz_q, num_heads); return BSKV_ERR_INVALID_ARG; }
+    const int64_t in_s[4] = {q_rope_strides[0], q_rope_strides[1], q_nope_strides[0], q_nope_strides[1]};
+    for (int i = 0; i < 4; ++i)
+      if ((in_s[i] * 2) % 16) { set_error("rope_quantize_fp8: query input strides must be multiples of 8 elements"); return BSKV_ERR_INVALID_ARG; }
+    if (q_nope_out_strides[0] % 16 || q_nope_out_strides[1] % 16 || q_rope_out_strides[0] % 2 || q_rope_out_strides[1] % 2) {
+      set_error("rope_quantize_fp8: q_nope_out strides must be multiples of 16 bytes, q_rope_out of 2");
+      return BSKV_ERR_INVALID_ARG;
+    }
+    if (!aligned16(q_rope) || !aligned16(q_nope) || !aligned16(q_nope_out) || (reinterpret_cast<uintptr_t>(q_rope_out) & 1)) {
+      set_error("rope_quantize_fp8: misaligned query tensor"); return BSKV_ERR_INVALID_ARG;
+    }
+    p.q_rope = static_cast<const __nv_bfloat16*>(q_rope); p.qr_s0 = q_rope_strides[0]; p.qr_s1 = q_rope_strides[1];
+    p.q_nope = static_cast<const __nv_bfloat16*>(q_nope); p.qn_s0 = q_nope_strides[0]; p.qn_s1 = q_nope_strides[1];
+    p.pos_q = pos_q; p.nnz_q = nnz_q; p.heads = num_heads;
+    p.q_rope_out = static_cast<uint8_t*>(q_rope_out); p.qro_s0 = q_rope_out_strides[0]; p.qro_s1 = q_rope_out_strides[1];
+    p.q_nope_out = static_cast<uint8_t*>(q_nope_out); p.qno_s0 = q_nope_out_strides[0]; p.qno_s1 = q_nope_out_strides[1];
+  }
+  if (has_k) {
+    if (!k_rope || !k_nope || !k_rope_out || !k_nope_out || !pos_k) {
+      set_error("rope_quantize_fp8: the key group needs all of k_rope, k_nope, pos_k and both outputs");
+      return BSKV_ERR_INVALID_ARG;
+    }
+    if (nnz_k < 0) { set_error("rope_quantize_fp8: nnz_k=%lld", (long long)nnz_k); return BSKV_ERR_INVALID_ARG; }
+    if ((k_rope_stride * 2) % 16 || (k_nope_stride * 2) % 16 || k_nope_out_stride % 16 || k_rope_out_stride % 2) {
+      set_error("rope_quantize_fp8: key strides misaligned"); return BSKV_ERR_INVALID_ARG;
+    }
+    if (!aligned16(k_rope) || !aligned16(k_nope) || !aligned16(k_nope_out) || (reinterpret_cast<uintptr_t>(k_rope_out) & 1)) {
+      set_error("rope_quantize_fp8: misaligned key tensor"); return BSKV_ERR_INVALID_ARG;
+    }
+    p.k_rope = static_cast<const __nv_bfloat16*>(k_rope); p.kr_s = k_rope_stride;
+    p.k_nope = static_cast<const __nv_bfloat16*>(k_nope); p.kn_s = k_nope_stride;
+    p.pos_k = pos_k; p.nnz_k = nnz_k;
+    p.k_rope_out = static_cast<uint8_t*>(k_rope_out); p.kro_s = k_rope_out_stride;
+    p.k_nope_out = static_cast<uint8_t*>(k_nope_out); p.kno_s = k_nope_out_stride;
+  }
+  p.cos_sin = cos_sin; p.max_seq_len = max_seq_len;
+  p.scale_q = quant_scale_q; p.scale_kv = quant_scale_kv;
+  if (bskv_status s = status_args(&p.st)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return is_neox ? launch_rope<true>(p, pos_dtype, cos_sin_dtype, st)
+                 : launch_rope<false>(p, pos_dtype, cos_sin_dtype, st);
+}

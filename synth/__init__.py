@@ -14,4 +14,5 @@ from .gen import (  # noqa: F401
     mla_inputs,
     rope_cos_sin_cache,
     CONFIGS,
+    make,
 )

@@ -52,7 +52,7 @@ def _uniform_int(g, lo, hi, n):
 
 def bsr_inputs(seed, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, dtype=torch.float16,
                pattern="random", density=0.5, p_off=0.1, causal=False, q_scale=1.0,
-               device="cpu"):
+               device="cpu", tensors=True):
     """Block-sparse attention inputs.
 
     pattern "random": each of the MB x NB blocks is kept with probability ``density``;
@@ -90,10 +90,12 @@ def bsr_inputs(seed, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, dtype=tor
     indptr[1:] = torch.cumsum(counts, 0).to(torch.int32)
     indices = (torch.cat(rows) if rows else torch.zeros(0, dtype=torch.int64)).to(torch.int32)
 
-    dg = _dev_gen(seed, device)
-    q = _randn((M, num_qo_heads, head_dim), dtype, dg, device, q_scale)
-    k = _randn((N, num_kv_heads, head_dim), dtype, dg, device)
-    v = _randn((N, num_kv_heads, head_dim), dtype, dg, device)
+    q = k = v = None
+    if tensors:
+        dg = _dev_gen(seed, device)
+        q = _randn((M, num_qo_heads, head_dim), dtype, dg, device, q_scale)
+        k = _randn((N, num_kv_heads, head_dim), dtype, dg, device)
+        v = _randn((N, num_kv_heads, head_dim), dtype, dg, device)
     return dict(q=q, k=k, v=v, indptr=indptr, indices=indices, M=M, N=N, R=R, C=C,
                 num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                 causal=causal, sm_scale=1.0 / math.sqrt(head_dim), seed=seed)
@@ -105,7 +107,7 @@ def bsr_inputs(seed, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, dtype=tor
 
 def paged_decode_inputs(seed, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                         len_lo, len_hi, dtype=torch.bfloat16, canary_frac=0.1,
-                        lengths=None, q_scale=1.0, device="cpu"):
+                        lengths=None, q_scale=1.0, device="cpu", tensors=True):
     """One query token per request over a paged KV cache (HND pages).
 
     kv lengths L_b are uniform integers in [len_lo, len_hi] (or ``lengths``). Request b
@@ -132,20 +134,22 @@ def paged_decode_inputs(seed, batch, num_qo_heads, num_kv_heads, head_dim, page_
     last = lengths - (npages - 1) * page_size
     last = torch.where(npages == 0, torch.zeros_like(last), last).to(torch.int32)
 
-    dg = _dev_gen(seed, device)
-    kv_cache = _randn((pool, 2, num_kv_heads, page_size, head_dim), dtype, dg, device)
-    unused = perm[total:].to(device)
-    if unused.numel():
-        kv_cache[unused] = float("nan")
-    for b in range(batch):
-        n = int(npages[b])
-        if n == 0:
-            continue
-        lp = int(kv_indices[int(kv_indptr[b]) + n - 1])
-        lb = int(last[b])
-        if lb < page_size:
-            kv_cache[lp, :, :, lb:, :] = float("nan")
-    q = _randn((batch, num_qo_heads, head_dim), dtype, dg, device, q_scale)
+    kv_cache = q = None
+    if tensors:
+        dg = _dev_gen(seed, device)
+        kv_cache = _randn((pool, 2, num_kv_heads, page_size, head_dim), dtype, dg, device)
+        unused = perm[total:].to(device)
+        if unused.numel():
+            kv_cache[unused] = float("nan")
+        for b in range(batch):
+            n = int(npages[b])
+            if n == 0:
+                continue
+            lp = int(kv_indices[int(kv_indptr[b]) + n - 1])
+            lb = int(last[b])
+            if lb < page_size:
+                kv_cache[lp, :, :, lb:, :] = float("nan")
+        q = _randn((batch, num_qo_heads, head_dim), dtype, dg, device, q_scale)
     return dict(q=q, kv_cache=kv_cache, kv_indptr=kv_indptr, kv_indices=kv_indices,
                 kv_last_page_len=last, kv_lens=lengths.to(torch.int32), batch=batch,
                 num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,

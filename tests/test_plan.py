@@ -1,0 +1,187 @@
+"""Plans: bit-exact metadata against the oracle's restatement, invariants, and host-side
+fault injection (every malformed input is rejected before anything is launched)."""
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_kv_gb300 as bskv
+import synth
+from oracle import plan_ref
+
+SMS = 152
+
+
+def _decode_plan(d, num_sms=SMS, max_workers=0):
+    return bskv.bskv_plan_decode(d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"],
+                                 d["num_pages"], d["page_size"], d["num_qo_heads"],
+                                 d["num_kv_heads"], d["head_dim"], torch.bfloat16,
+                                 num_sms=num_sms, max_workers=max_workers)
+
+
+def _check_linear(meta, unit_len, tile):
+    s = plan_ref.sections(meta)
+    seen = {u: [] for u in range(len(unit_len))}
+    for c in s["chunks"]:
+        seen[c[0]].append((c[1], c[2], c[3]))
+    for u, L in enumerate(unit_len):
+        segs = sorted(seen[u])
+        pos = 0
+        for a, b, slot in segs:
+            assert a == pos and b > a and a % tile == 0
+            pos = b
+        assert pos == L  # every token of every unit exactly once
+        if len(segs) == 1:
+            assert segs[0][2] == -1
+        else:
+            assert all(sl >= 0 for _, _, sl in segs)
+    # balance: tiles per worker differ by at most one
+    per = []
+    for w in range(s["workers"]):
+        cs = s["chunks"][s["worker_ptr"][w]:s["worker_ptr"][w + 1]]
+        per.append(sum((c[2] - c[1] + tile - 1) // tile for c in cs))
+    if per:
+        assert max(per) - min(per) <= 1 + len(unit_len)  # a worker can be cut at unit ends
+        assert sum(per) == sum((L + tile - 1) // tile for L in unit_len)
+    assert s["slots"] == sum(1 for c in s["chunks"] if c[3] >= 0)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("paged_decode", dict(tensors=False)),
+    ("paged_decode", dict(batch=5, len_lo=1, len_hi=100)),
+    ("paged_decode", dict(batch=3, page_size=64, len_lo=64, len_hi=64)),
+    ("split_decode", dict(len_lo=4096, len_hi=4096, batch=2)),
+])
+def test_decode_plan_bit_exact(lib, name, over):
+    d = synth.make(name, **over)
+    p = _decode_plan(d)
+    meta = p.metadata()
+    ref = plan_ref.decode_meta(d["kv_indptr"].tolist(), d["kv_indices"].tolist(),
+                               d["kv_last_page_len"].tolist(), d["batch"], d["page_size"],
+                               d["num_qo_heads"], d["num_kv_heads"], SMS)
+    assert meta == ref
+    lens = [int(L) for L in d["kv_lens"] for _ in range(d["num_kv_heads"])]
+    _check_linear(meta, lens, 16)
+
+
+def test_decode_plan_full_long_context(lib):
+    d = synth.make("split_decode", tensors=False)
+    p = _decode_plan(d)
+    meta = p.metadata()
+    assert meta == plan_ref.decode_meta(d["kv_indptr"].tolist(), d["kv_indices"].tolist(),
+                                        d["kv_last_page_len"].tolist(), 8, 64, 64, 8, SMS)
+    _check_linear(meta, [131072] * 64, 16)
+    s = plan_ref.sections(meta)
+    assert s["workers"] == SMS * 8 and s["grid"] == SMS
+
+
+def test_decode_plan_zero_length_and_max_workers(lib):
+    indptr = [0, 0, 3, 3, 4]
+    idx = [5, 1, 2, 0]
+    last = [0, 7, 0, 16]
+    p = bskv.bskv_plan_decode(indptr, idx, last, 6, 16, 4, 2, 64, torch.bfloat16, num_sms=1,
+                              max_workers=3)
+    meta = p.metadata()
+    assert meta == plan_ref.decode_meta(indptr, idx, last, 4, 16, 4, 2, 1, 3)
+    s = plan_ref.sections(meta)
+    zero_units = {m[0] for m in s["merges"] if m[2] == 0}
+    assert zero_units == {0, 1, 4, 5}  # requests 0 and 2, both kv heads
+
+
+@pytest.mark.parametrize("name,over", [
+    ("bsr_tiny", {}),
+    ("bsr_prefill", {}),
+    ("bsr_prefill", dict(M=2048, N=2048, num_qo_heads=8)),
+    ("bsr_prefill", dict(M=1000, N=1024, R=32, C=16, pattern="random")),
+])
+def test_bsr_plan_bit_exact(lib, name, over):
+    d = synth.make(name, tensors=False, **over)
+    args = (d["indptr"], d["indices"], d["M"], d["N"], d["R"], d["C"], d["num_qo_heads"],
+            d["num_kv_heads"], d["head_dim"])
+    p = bskv.bskv_plan_bsr(*args, causal=d["causal"], dtype=torch.float16, num_sms=SMS)
+    meta = p.metadata()
+    assert meta == plan_ref.bsr_meta(d["indptr"].tolist(), d["indices"].tolist(), *args[2:], SMS)
+    s = plan_ref.sections(meta)
+    units = sorted(c[0] for c in s["chunks"])
+    assert units == list(range(s["units"]))  # each unit exactly once
+    # LPT bound: no CTA exceeds the mean load by more than the largest unit
+    MB = (d["M"] + d["R"] - 1) // d["R"]
+    rows = np.diff(d["indptr"].numpy())
+    per_unit = s["units"] // (MB * d["num_kv_heads"])
+    loads = []
+    for c in range(s["grid"]):
+        us = s["chunks"][s["worker_ptr"][c]:s["worker_ptr"][c + 1]]
+        loads.append(sum(1 + rows[u[1]] for u in us))
+    assert max(loads) <= sum(loads) / len(loads) + 1 + rows.max()
+    g = d["num_qo_heads"] // d["num_kv_heads"]
+    if d["R"] == 64 and d["C"] == 64 and d["head_dim"] == 128 and 64 * g in (128, 256):
+        assert s["variant"] == 1 and per_unit == 1
+    else:
+        assert s["variant"] == 0
+
+
+@pytest.mark.parametrize("batch,q_len,seq", [(128, 1, None), (3, 2, [64, 0, 130]), (1, 1, [2048])])
+def test_mla_plan_bit_exact(lib, batch, q_len, seq):
+    top_k = 2048 if seq is None else 192 if batch == 3 else 2048
+    seq_lens = [top_k] * batch if seq is None else seq
+    p = bskv.bskv_plan_mla_sparse(seq_lens, batch, q_len, 128, top_k, num_sms=SMS)
+    meta = p.metadata()
+    assert meta == plan_ref.mla_meta(seq_lens, batch, q_len, SMS)
+    lens = [s for s in seq_lens for _ in range(q_len) for _ in range(2)]
+    _check_linear(meta, lens, 64)
+
+
+# ---------------------------------------------------------------------------------------
+# fault injection on the host: each malformed input returns an error and plans nothing
+# ---------------------------------------------------------------------------------------
+
+def _expect(status, fn, *a, **k):
+    with pytest.raises(bskv.BskvError) as e:
+        fn(*a, **k)
+    assert e.value.status == status, str(e.value)
+
+
+def test_decode_plan_rejects_bad_inputs(lib):
+    f = bskv.bskv_plan_decode
+    ok = dict(num_pages=4, page_size=16, num_qo_heads=8, num_kv_heads=2, head_dim=128, num_sms=4)
+    f([0, 2], [0, 1], [5], **ok)  # sanity: valid
+    _expect("ERR_INVALID_ARG", f, [1, 2], [0, 1], [5], **ok)           # indptr[0] != 0
+    _expect("ERR_INVALID_ARG", f, [0, 2, 1], [0, 1], [5, 1], **ok)     # decreasing indptr
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 4], [5], **ok)           # page id out of range
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, -1], [5], **ok)
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 1], [0], **ok)           # last page len 0
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 1], [17], **ok)          # > page_size
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 1], [5], **{**ok, "num_kv_heads": 3})
+    _expect("ERR_UNSUPPORTED", f, [0, 2], [0, 1], [5], **{**ok, "head_dim": 96})
+    _expect("ERR_UNSUPPORTED", f, [0, 2], [0, 1], [5], **{**ok, "num_qo_heads": 64, "num_kv_heads": 2})
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 1], [5], **{**ok, "page_size": 0})
+
+
+def test_bsr_plan_rejects_bad_inputs(lib):
+    f = bskv.bskv_plan_bsr
+    f([0, 1, 2], [0, 1], 4, 4, 2, 2, 2, 1, 64, num_sms=2)  # valid
+    _expect("ERR_INVALID_ARG", f, [0, 1, 2], [0, 1], 4, 5, 2, 2, 2, 1, 64, num_sms=2)   # N % C
+    _expect("ERR_INVALID_ARG", f, [0, 1, 2], [0, 2], 4, 4, 2, 2, 2, 1, 64, num_sms=2)   # index >= NB
+    _expect("ERR_INVALID_ARG", f, [0, 2, 2], [1, 1], 4, 4, 2, 2, 2, 1, 64, num_sms=2)   # duplicate
+    _expect("ERR_INVALID_ARG", f, [0, 2, 1], [0, 1], 4, 4, 2, 2, 2, 1, 64, num_sms=2)   # decreasing
+    _expect("ERR_INVALID_ARG", f, [1, 1, 2], [0, 1], 4, 4, 2, 2, 2, 1, 64, num_sms=2)   # indptr[0]
+    _expect("ERR_INVALID_ARG", f, [0, 1, 2], [0, 1], 4, 4, 2, 2, 3, 2, 64, num_sms=2)   # heads
+    _expect("ERR_UNSUPPORTED", f, [0, 1, 2], [0, 1], 4, 4, 2, 2, 2, 1, 80, num_sms=2)   # head_dim
+
+
+def test_mla_plan_rejects_bad_inputs(lib):
+    f = bskv.bskv_plan_mla_sparse
+    f([64], 1, 1, 128, 64, num_sms=2)
+    _expect("ERR_INVALID_ARG", f, [64], 1, 1, 128, 96, num_sms=2)    # top_k % 64
+    _expect("ERR_INVALID_ARG", f, [65], 1, 1, 128, 64, num_sms=2)    # seq_len > top_k
+    _expect("ERR_INVALID_ARG", f, [-1], 1, 1, 128, 64, num_sms=2)
+    _expect("ERR_UNSUPPORTED", f, [64], 1, 1, 256, 64, num_sms=2)    # heads > 128
+
+
+def test_run_without_upload_is_rejected(lib):
+    p = bskv.bskv_plan_bsr([0, 1], [0], 2, 2, 2, 2, 2, 1, 64, num_sms=2)
+    lib_ = bskv.load_library()
+    s = (bskv.ctypes.c_int64 * 2)(64, 64)
+    code = lib_.bskv_run_bsr(p.handle, 16, s, 16, s, 16, s, 16, s, None, 1.0, None, 0, None)
+    assert bskv.STATUS[code] == "ERR_INVALID_ARG"
+    assert "not uploaded" in bskv.bskv_last_error_message()
