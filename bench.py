@@ -1,0 +1,551 @@
+"""Benchmark of CSR-indexed sparse/paged attention on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--rows ...]
+
+One JSON line on rank 0. The headline workload is the paged GQA batch decode (batch 64,
+32 query / 8 kv heads, head_dim 128, bf16, page_size 16, kv lengths U[512, 4096], pages
+randomly permuted in a shared pool): one step = the decode attention kernel plus the
+split-KV merge over the whole batch (the plan is made once, as a serving engine does per
+decode step, and timed apart). The metric is the KV bytes the method must read per second.
+The same run measures the other rows of the hot path on their own workloads (BSR prefill,
+tiny BSR, the MLA prologue and sparse FP8 decode, long-context split-KV decode) and
+reports them under "rows". Inputs are synthetic (seeded) and resident in HBM before the
+timed region; the headline's KV (about 0.6 GB) is larger than L2, the smaller rows flush
+L2 with a 512 MB write between timed iterations.
+
+--impl reference times the float64 CPU oracle (the only reference implementation of
+this method here) on the host cores, on a bounded sample of the same workload.
+With N > 1 (torchrun) every rank runs an independent replica (weak scaling, no
+collective on the data path); value = bytes of all ranks / max-over-ranks time.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention KV GB/s (decode) and TFLOPS (BSR/MLA) as % of 1×GB300 roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend)
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x):
+    if dist is None:
+        return x
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x):
+    if dist is None:
+        return x
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        under = [x for x in sm if mx and x > 0.3 * mx] or sm
+        return {"sm_mhz": statistics.median(under) if under else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------------------
+
+_flush_buf = None
+
+
+def flush_l2():
+    global _flush_buf
+    if _flush_buf is None:
+        _flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    _flush_buf.fill_(1)
+
+
+def time_iters(fn, iters, warmup, flush=False):
+    """Per-iteration CUDA-event times (ms) on the current stream; L2 flushed in between."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    st = torch.cuda.current_stream()
+    for _ in range(iters):
+        if flush:
+            flush_l2()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def summary(ms):
+    return {"median_us": 1e3 * statistics.median(ms), "mean_us": 1e3 * statistics.mean(ms),
+            "std_us": 1e3 * (statistics.pstdev(ms) if len(ms) > 1 else 0.0), "n": len(ms)}
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_sparse_kv_gb300", "csrc", n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(summary_name, kernel_sources):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != source_sha(*kernel_sources):
+        return None
+    return float(t.group(1))
+
+
+# ---------------------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------------------
+
+def decode_kv_bytes(d):
+    return int(d["kv_lens"].to(torch.int64).sum()) * d["num_kv_heads"] * d["head_dim"] * 2 * 2
+
+
+def bench_decode(bskv, synth, name, steps, warmup, dist, sampler=None, headline=False,
+                 **over):
+    """Paged decode (+ merge) on one of the decode workloads."""
+    d = synth.make(name, device="cuda", **over)
+    t0 = time.perf_counter()
+    plan = bskv.bskv_plan_decode(d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"],
+                                 d["num_pages"], d["page_size"], d["num_qo_heads"],
+                                 d["num_kv_heads"], d["head_dim"], torch.bfloat16)
+    plan_us = 1e6 * (time.perf_counter() - t0)
+    plan.upload("cuda")
+    q, kv = d["q"], d["kv_cache"]
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    nmerge = plan.metadata()[6]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        bskv.bskv_run_decode_partial(plan, q, kv, out=out, lse=lse)
+        if ev is not None:
+            ev[1].record()
+        bskv.bskv_decode_merge(plan, out, lse)
+        if ev is not None:
+            ev[2].record()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    if sampler:
+        sampler.start()
+    torch.cuda.synchronize()
+    barrier(dist)
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop() if sampler else None
+    total_ms = evs[0][0].elapsed_time(evs[-1][2])
+    kern_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    merge_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    nbytes = decode_kv_bytes(d)
+    res = dict(workload=name, kv_bytes=nbytes, plan_us=plan_us, total_ms=total_ms,
+               ms_per_step=total_ms / steps, decode_kernel=summary(kern_ms),
+               merge_kernel=summary(merge_ms), launches_per_step=1 + (1 if nmerge else 0),
+               clocks=clocks)
+    res["gbs_step"] = nbytes / (res["ms_per_step"] * 1e-3) / 1e9
+    res["gbs_kernel"] = nbytes / (statistics.mean(kern_ms) * 1e-3) / 1e9
+    del d, kv, q
+    return res, plan
+
+
+def bench_decode_e2e(bskv, synth, steps, warmup):
+    """Same workload through the public API with host buffers: pinned H2D of q, the KV
+    cache and the page table, plan + upload, decode + merge, D2H of the output."""
+    d = synth.make("paged_decode", device="cpu")
+    hq, hkv = d["q"].pin_memory(), d["kv_cache"].pin_memory()
+    hidx = [d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"]]
+    dq = torch.empty_like(hq, device="cuda")
+    dkv = torch.empty_like(hkv, device="cuda")
+    hout = torch.empty_like(hq).pin_memory()
+    plan = bskv.bskv_plan_decode(*hidx, d["num_pages"], d["page_size"], d["num_qo_heads"],
+                                 d["num_kv_heads"], d["head_dim"], torch.bfloat16)
+    plan.upload("cuda")
+    int_ws, float_ws = plan.int_ws, plan.float_ws
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dkv.copy_(hkv, non_blocking=True)
+        p = bskv.bskv_plan_decode(*hidx, d["num_pages"], d["page_size"], d["num_qo_heads"],
+                                  d["num_kv_heads"], d["head_dim"], torch.bfloat16)
+        p.upload("cuda", int_ws=int_ws, float_ws=float_ws)
+        dout = bskv.bskv_run_decode(p, dq, dkv)
+        hout.copy_(dout, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return p
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    ms = 1e3 * (time.perf_counter() - t0) / steps
+    h2d = hq.numel() * 2 + hkv.numel() * 2 + sum(x.numel() * 4 for x in hidx) + \
+        plan.workspace_sizes()[0]
+    d2h = hout.numel() * 2
+    nbytes = decode_kv_bytes(d)
+    return {"value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def bench_split(bskv, synth, steps, warmup, peaks):
+    res, _ = bench_decode(bskv, synth, "split_decode", steps, warmup, None)
+    res["frac_step"] = res["gbs_step"] / peaks["hbm_gbs"]
+    res["frac_kernel"] = res["gbs_kernel"] / peaks["hbm_gbs"]
+    res.pop("clocks", None)
+    return res
+
+
+def bsr_flops(d):
+    """4 * D * Hq * visible (query, key) pairs, causal-exact."""
+    R, C, M, N = d["R"], d["C"], d["M"], d["N"]
+    indptr, indices = d["indptr"].tolist(), d["indices"].tolist()
+    pairs = 0
+    for i in range(len(indptr) - 1):
+        r0, r1 = i * R, min(M, (i + 1) * R)
+        for j in indices[indptr[i]:indptr[i + 1]]:
+            c0, c1 = j * C, (j + 1) * C
+            if not d["causal"]:
+                pairs += (r1 - r0) * (c1 - c0)
+            else:
+                for r in range(r0, r1):
+                    lim = r + (N - M)
+                    pairs += max(0, min(c1, lim + 1) - c0)
+    return 4 * d["head_dim"] * d["num_qo_heads"] * pairs
+
+
+def bench_bsr(bskv, synth, name, steps, warmup, peaks, flush):
+    d = synth.make(name, device="cuda")
+    plan = bskv.bskv_plan_bsr(d["indptr"], d["indices"], d["M"], d["N"], d["R"], d["C"],
+                              d["num_qo_heads"], d["num_kv_heads"], d["head_dim"],
+                              causal=d["causal"], dtype=torch.float16)
+    plan.upload("cuda")
+    out = torch.empty_like(d["q"])
+    fn = lambda: bskv.bskv_run_bsr(plan, d["q"], d["k"], d["v"], out=out)  # noqa: E731
+    ms = time_iters(fn, steps, warmup, flush=flush)
+    fl = bsr_flops(d)
+    med = statistics.median(ms)
+    tf = fl / (med * 1e-3) / 1e12
+    variant = plan.metadata()[15]
+    return dict(workload=name, flops=fl, kernel="tcgen05" if variant == 1 else "general",
+                **summary(ms), tflops=tf, frac=tf / peaks["bf16_tflops"],
+                peak="bf16 dense burst (fp16 rate equal)")
+
+
+def bench_mla(bskv, synth, steps, warmup, peaks):
+    m = synth.make("mla_decode", device="cuda")
+    B, H, K = m["batch"], m["heads"], m["top_k"]
+    query = torch.empty((B, 1, H, 576), dtype=torch.uint8, device="cuda")
+    pool = torch.empty((m["pool_rows"], 576), dtype=torch.uint8, device="cuda")
+
+    pos_k, pos_q = m["pos_k"].cuda(), m["pos_q"].cuda()
+
+    def prologue_k():
+        bskv.bskv_rope_quantize_fp8(None, m["k_rope"], None, m["k_nope"], m["cos_sin"],
+                                    None, True, k_rope_out=pool[:, 512:],
+                                    k_nope_out=pool[:, :512], pos_ids_k=pos_k)
+
+    def prologue_q():
+        bskv.bskv_rope_quantize_fp8(m["q_rope"], None, m["q_nope"], None, m["cos_sin"],
+                                    pos_q, True, q_rope_out=query[:, 0, :, 512:],
+                                    q_nope_out=query[:, 0, :, :512])
+
+    pk = time_iters(prologue_k, steps, warmup, flush=True)
+    pq = time_iters(prologue_q, steps, warmup, flush=True)
+    kbytes = m["pool_rows"] * (1152 + 576 + 256)
+    qbytes = B * H * (1152 + 576) + B * 256
+    res = dict(workload="mla_decode",
+               prologue_k=dict(**summary(pk), bytes=kbytes,
+                               gbs=kbytes / (statistics.median(pk) * 1e-3) / 1e9),
+               prologue_q=dict(**summary(pq), bytes=qbytes,
+                               gbs=qbytes / (statistics.median(pq) * 1e-3) / 1e9))
+    res["prologue_k"]["frac"] = res["prologue_k"]["gbs"] / peaks["hbm_gbs"]
+    try:
+        plan = bskv.bskv_plan_mla_sparse(m["seq_lens"], B, 1, H, K)
+        plan.upload("cuda")
+        idx = m["indices"].cuda()
+        out = torch.empty((B, 1, H, 512), dtype=torch.bfloat16, device="cuda")
+        scale = 1.0 / math.sqrt(576)
+        fn = lambda: bskv.bskv_run_mla_sparse(plan, query, pool, idx, scale, 1.0, out=out)  # noqa
+        for flush in (False, True):
+            ms = time_iters(fn, steps, warmup, flush=flush)
+            fl = 2.0 * H * int(m["seq_lens"].sum()) * (576 + 512)
+            tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+            fp8_peak = 2.0 * peaks["bf16_tflops"]
+            res["decode_l2_flushed" if flush else "decode_l2_warm"] = dict(
+                **summary(ms), flops=fl, tflops=tf, frac=tf / fp8_peak,
+                peak="fp8 = 2 x measured bf16 dense burst (nominal ratio)")
+    except bskv.BskvError as e:
+        res["decode"] = "not available: %s" % e.status
+    return res
+
+
+# ---------------------------------------------------------------------------------------
+# CPU baseline: the float64 oracle on the host cores, on a bounded sample
+# ---------------------------------------------------------------------------------------
+
+def oracle_decode_sample(synth, budget_s=12.0):
+    from oracle import attention as att
+    d = synth.make("paged_decode", device="cpu")
+    qb = d["q"].view(torch.int16).numpy().view(np.uint16)
+    kvb = d["kv_cache"].view(torch.int16).numpy().view(np.uint16)
+    ip, ix, lp = d["kv_indptr"].numpy(), d["kv_indices"].numpy(), d["kv_last_page_len"].numpy()
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    while done < d["batch"] and (time.perf_counter() - t0 < budget_s or done < 2):
+        att.paged_decode(qb, kvb, "bf16", ip, ix, lp, d["page_size"], d["sm_scale"], [done])
+        nbytes += int(d["kv_lens"][done]) * d["num_kv_heads"] * d["head_dim"] * 4
+        done += 1
+    el = time.perf_counter() - t0
+    try:
+        import threadpoolctl
+        threads = max((i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()), default=1)
+    except Exception:  # noqa: BLE001
+        threads = os.cpu_count()
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": int(threads), "kind": "oracle",
+            "sample": "%d of 64 requests of the paged decode workload (float64 numpy), %.1f s"
+                      % (done, el), "seconds": el}
+
+
+# ---------------------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------------------
+
+def run_reference(args):
+    """The oracle as the reference arm: host cores, bounded samples of the same workload."""
+    dist, rank, ws = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import synth
+    vals = []
+    for _ in range(args.warmup):
+        oracle_decode_sample(synth, budget_s=2.0)
+    for _ in range(args.steps):
+        vals.append(oracle_decode_sample(synth, budget_s=10.0 / max(args.steps, 1)))
+    v = statistics.mean(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(x["seconds"] for x in vals),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "paged_decode: batch 64, 32/8 heads, head_dim 128, bf16 "
+                                   "storage, page_size 16, kv len U[512,4096]",
+                       "parallelism": "replicas" if args.gpus > 1 else "single"},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--rows", default="all",
+                    help="comma list of extra rows: bsr_prefill,bsr_tiny,mla,split,e2e,cpu or all/none")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    args.warmup = max(args.warmup, 3)
+
+    import block_sparse_kv_gb300 as bskv
+    import synth
+    bskv.build()
+    dist, rank, ws = dist_setup(args.gpus)
+    peaks, peak_src = load_peaks()
+    rows = set(["bsr_prefill", "bsr_tiny", "mla", "split", "e2e", "cpu"]
+               if args.rows == "all" else [] if args.rows == "none" else args.rows.split(","))
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    head, _ = bench_decode(bskv, synth, "paged_decode", args.steps, args.warmup, dist)
+    t_max = max_over_ranks(dist, head["total_ms"])
+    total_bytes = sum_over_ranks(dist, head["kv_bytes"] * args.steps)
+    value = total_bytes / (t_max * 1e-3) / 1e9
+    status = bskv.bskv_get_device_status()
+
+    extra = {}
+    if rank == 0:
+        K = max(5, min(args.steps, 20))
+        jobs = [("split", "split_decode", lambda: bench_split(bskv, synth, K, args.warmup, peaks)),
+                ("bsr_prefill", "bsr_prefill",
+                 lambda: bench_bsr(bskv, synth, "bsr_prefill", K, args.warmup, peaks, True)),
+                ("bsr_tiny", "bsr_tiny",
+                 lambda: bench_bsr(bskv, synth, "bsr_tiny", K, args.warmup, peaks, True)),
+                ("mla", "mla_decode", lambda: bench_mla(bskv, synth, K, args.warmup, peaks))]
+        for key, name, job in jobs:
+            if key in rows:
+                try:
+                    extra[name] = job()
+                except bskv.BskvError as e:
+                    extra[name] = "not available: %s" % e
+                torch.cuda.empty_cache()
+    clocks = sampler.stop() if sampler else None
+    e2e = None
+    if rank == 0 and "e2e" in rows:
+        e2e = bench_decode_e2e(bskv, synth, max(3, min(args.steps, 10)), 2)
+    cpu = oracle_decode_sample(synth) if (rank == 0 and "cpu" in rows and ws == 1) else None
+    status = status or bskv.bskv_get_device_status()
+
+    if rank != 0:
+        return
+    kern_us = head["decode_kernel"]["mean_us"]
+    achieved = head["kv_bytes"] / (kern_us * 1e-6) / 1e9
+    peak = peaks["hbm_gbs"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, random page permutation, NaN canary pages)",
+        "config": {"workload": "paged_decode: batch 64, 32/8 heads, head_dim 128, bf16, "
+                               "page_size 16, kv len U[512,4096], pages permuted in a shared pool",
+                   "global_batch": 64 * args.gpus, "kv_bytes_per_step": head["kv_bytes"],
+                   "l2": "inputs larger than L2 (0.6 GB KV per step)",
+                   "parallelism": "replicas x%d" % args.gpus if args.gpus > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_src + " (hbm_gbs, burst)",
+                     "kernel": "decode_kernel", "bytes_per_launch": head["kv_bytes"],
+                     "traffic": profile_traffic("decode_kernel_paged_decode.txt",
+                                                ["decode.cu", "common.cuh"])},
+        "clocks": clocks,
+        "gpu_launches": head["launches_per_step"] * args.steps,
+        "plan_us": head["plan_us"],
+        "step_breakdown_us": {"decode_kernel": head["decode_kernel"]["mean_us"],
+                              "merge_kernel": head["merge_kernel"]["mean_us"]},
+        "device_status": bskv.STATUS.get(status, status),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "rows": extra,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

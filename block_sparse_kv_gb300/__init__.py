@@ -20,7 +20,8 @@ __all__ = [
     "BskvError", "Plan", "load_library", "build",
     "bskv_version", "bskv_last_error_message",
     "bskv_plan_decode", "bskv_plan_bsr", "bskv_plan_mla_sparse",
-    "bskv_run_decode", "bskv_run_bsr", "bskv_run_mla_sparse",
+    "bskv_run_decode", "bskv_run_decode_partial", "bskv_decode_merge",
+    "bskv_run_bsr", "bskv_run_mla_sparse",
     "bskv_rope_quantize_fp8", "bskv_merge_states",
     "bskv_get_device_status", "bskv_set_debug_force_timeout",
 ]
@@ -64,6 +65,8 @@ _SIGS = {
     "bskv_plan_workspace_sizes": ([_P, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)], _I32),
     "bskv_plan_upload": ([_P, _P, _SZ, _P], _I32),
     "bskv_run_decode": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P, _SZ, _P], _I32),
+    "bskv_run_decode_partial": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P, _SZ, _P], _I32),
+    "bskv_decode_merge": ([_P, _P, _I64P, _P, _P, _SZ, _P], _I32),
     "bskv_run_bsr": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P, _SZ, _P], _I32),
     "bskv_run_mla_sparse": ([_P, _P, _P, _I64, _P, _F, _F, _P, _P, _P, _SZ, _P], _I32),
     "bskv_rope_quantize_fp8": ([_P, _I64P, _P, _I64P, _P, _I64, _I32, _P, _I64P, _P, _I64P,
@@ -206,7 +209,8 @@ def bskv_plan_decode(kv_indptr, kv_indices, kv_last_page_len, num_pages, page_si
                 num_kv_heads=num_kv_heads, head_dim=head_dim, dtype=dtype, page_size=page_size)
 
 
-def bskv_run_decode(plan, q, kv_cache, out=None, lse=None, return_lse=False, sm_scale=None):
+def bskv_run_decode(plan, q, kv_cache, out=None, lse=None, return_lse=False, sm_scale=None,
+                    _entry="bskv_run_decode"):
     """Decode one query token per request; kv_cache [pages, 2, Hkv, page_size, D] (any
     strides with a contiguous last dim)."""
     lib = load_library()
@@ -221,11 +225,29 @@ def bskv_run_decode(plan, q, kv_cache, out=None, lse=None, return_lse=False, sm_
         sm_scale = 1.0 / math.sqrt(D)
     fw = plan.float_ws
     ks = kv_cache.stride()
-    _check("bskv_run_decode", lib.bskv_run_decode(
+    _check(_entry, getattr(lib, _entry)(
         plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), kv_cache.data_ptr(),
         _strides(ks[0], ks[1], ks[2], ks[3]), out.data_ptr(), _strides(out.stride(0), out.stride(1)),
         _ptr(lse), float(sm_scale), _ptr(fw), 0 if fw is None else fw.numel(), _stream(q)))
     return (out, lse) if return_lse else out
+
+
+def bskv_run_decode_partial(plan, q, kv_cache, out=None, lse=None, return_lse=False,
+                            sm_scale=None):
+    """Attention kernel of the decode only (see bskv_decode_merge)."""
+    return bskv_run_decode(plan, q, kv_cache, out, lse, return_lse, sm_scale,
+                           _entry="bskv_run_decode_partial")
+
+
+def bskv_decode_merge(plan, out, lse=None):
+    """Merge the split-KV partial states a bskv_run_decode_partial left in the plan's
+    float workspace into out (and lse)."""
+    lib = load_library()
+    fw = plan.float_ws
+    _check("bskv_decode_merge", lib.bskv_decode_merge(
+        plan.handle, out.data_ptr(), _strides(out.stride(0), out.stride(1)), _ptr(lse), _ptr(fw),
+        0 if fw is None else fw.numel(), _stream(out)))
+    return out
 
 
 def bskv_plan_bsr(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim,

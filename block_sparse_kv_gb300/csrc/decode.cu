@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
   __syncwarp();
 
+  const bool forced = forced_timeout(p.st);
   const int Hkv = p.num_kv_heads, g = p.group, ps = p.page_size;
   const int box_rows = ps < kTile ? ps : kTile;
   const uint32_t piece_bytes = uint32_t(box_rows) * 128u;
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       l0 = l1 = 0.f;
     }
     const int stage = consumed % kStages;
-    if (!mbar_wait(&bars[stage], (consumed / kStages) & 1u, p.st)) {
+    if (!mbar_wait(&bars[stage], (consumed / kStages) & 1u, p.st, forced)) {
       ok = false;
       break;
     }
@@ -341,9 +342,6 @@ struct MergeParams {
   int num_kv_heads, group, num_qo_heads;
 };
 
-template <typename T>
-__device__ __forceinline__ void store_vec(T* dst, const float* v, int n);
-
 template <int D, typename T>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
   const int32_t* hdr = p.meta;
@@ -456,13 +454,38 @@ bskv_status launch_decode_t(const bskv_plan* plan, const CUtensorMap& map, Decod
     kern<<<grid, kWarps * 32, smem, stream>>>(map, dp);
     if (bskv_status s = cuda_check(cudaGetLastError(), "decode kernel launch")) return s;
   }
+  return BSKV_OK;
+}
+
+template <typename T, int D>
+bskv_status launch_merge_t(const bskv_plan* plan, const MergeParams& mp, cudaStream_t stream) {
   const int nm = meta_word(plan, H_MERGES);
-  if (nm > 0) {
-    MergeParams mp{dp.meta, dp.ws_o, dp.ws_lse, dp.out, dp.o_s0, dp.o_s1, dp.lse,
-                   dp.num_kv_heads, dp.group, dp.num_qo_heads};
-    const int warps = nm * dp.group;
-    decode_merge_kernel<D, T><<<(warps + 3) / 4, 128, 0, stream>>>(mp);
-    if (bskv_status s = cuda_check(cudaGetLastError(), "decode merge launch")) return s;
+  if (nm == 0) return BSKV_OK;
+  const int warps = nm * mp.group;
+  decode_merge_kernel<D, T><<<(warps + 3) / 4, 128, 0, stream>>>(mp);
+  return cuda_check(cudaGetLastError(), "decode merge launch");
+}
+
+// Float-workspace pointers of a decode plan (partial outputs, then their LSE).
+void decode_ws(const bskv_plan* plan, void* float_ws, float** ws_o, float** ws_lse) {
+  const int g = plan->num_qo_heads / plan->num_kv_heads;
+  const int slots = meta_word(plan, H_SLOTS);
+  *ws_o = static_cast<float*>(float_ws);
+  *ws_lse = slots ? reinterpret_cast<float*>(static_cast<uint8_t*>(float_ws) +
+                                             ((size_t(slots) * g * plan->head_dim * 4 + 255) &
+                                              ~size_t(255)))
+                  : nullptr;
+}
+
+bskv_status check_decode_ws(const bskv_plan* plan, void* float_ws, size_t float_ws_bytes) {
+  if (float_ws_bytes < plan->float_ws_bytes || (plan->float_ws_bytes && !float_ws)) {
+    set_error("decode: float workspace of %zu bytes, %zu needed", float_ws_bytes,
+              plan->float_ws_bytes);
+    return BSKV_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (float_ws && !aligned16(float_ws)) {
+    set_error("decode: float workspace must be 16-byte aligned");
+    return BSKV_ERR_INVALID_ARG;
   }
   return BSKV_OK;
 }
@@ -472,7 +495,7 @@ bskv_status launch_decode_t(const bskv_plan* plan, const CUtensorMap& map, Decod
 
 using namespace bskv;
 
-extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
+extern "C" bskv_status bskv_run_decode_partial(const bskv_plan* plan, const void* q,
                                        const int64_t* q_strides, const void* kv_cache,
                                        const int64_t* kv_strides, void* out,
                                        const int64_t* out_strides, float* lse, float sm_scale,
@@ -501,11 +524,7 @@ extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
   }
   if (plan->batch > 0 && (!q || !kv_cache || !out)) { set_error("run_decode: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) { set_error("run_decode: tensors must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
-  if (float_ws_bytes < plan->float_ws_bytes || (plan->float_ws_bytes && !float_ws)) {
-    set_error("run_decode: float workspace of %zu bytes, %zu needed", float_ws_bytes, plan->float_ws_bytes);
-    return BSKV_ERR_WORKSPACE_TOO_SMALL;
-  }
-  if (float_ws && !aligned16(float_ws)) { set_error("run_decode: float workspace must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  if (bskv_status s = check_decode_ws(plan, float_ws, float_ws_bytes)) return s;
   if (plan->batch == 0) return BSKV_OK;
   DecodeParams dp{};
   dp.meta = plan->meta_dev;
@@ -513,11 +532,7 @@ extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
   dp.out = out; dp.o_s0 = out_strides[0]; dp.o_s1 = out_strides[1];
   dp.lse = lse;
   const int g = plan->num_qo_heads / Hkv;
-  const int slots = meta_word(plan, H_SLOTS);
-  dp.ws_o = static_cast<float*>(float_ws);
-  dp.ws_lse = slots ? reinterpret_cast<float*>(static_cast<uint8_t*>(float_ws) +
-                                               ((size_t(slots) * g * D * 4 + 255) & ~size_t(255)))
-                    : nullptr;
+  decode_ws(plan, float_ws, &dp.ws_o, &dp.ws_lse);
   dp.num_kv_heads = Hkv; dp.group = g; dp.page_size = ps; dp.num_qo_heads = plan->num_qo_heads;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
   if (bskv_status s = status_args(&dp.st)) return s;
@@ -538,6 +553,43 @@ extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
   }
   return D == 128 ? launch_decode_t<__half, 128>(plan, map, dp, st)
                   : launch_decode_t<__half, 64>(plan, map, dp, st);
+}
+
+extern "C" bskv_status bskv_decode_merge(const bskv_plan* plan, void* out,
+                                         const int64_t* out_strides, float* lse,
+                                         void* float_ws, size_t float_ws_bytes, void* stream) {
+  if (!plan || plan->kind != KIND_DECODE) { set_error("decode_merge: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
+  if (!plan->meta_dev) { set_error("decode_merge: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
+  if (!out_strides) { set_error("decode_merge: NULL strides"); return BSKV_ERR_INVALID_ARG; }
+  if (bskv_status s = check_decode_ws(plan, float_ws, float_ws_bytes)) return s;
+  if (meta_word(plan, H_MERGES) == 0) return BSKV_OK;
+  if (!out || !aligned16(out)) { set_error("decode_merge: out must be a 16-byte aligned tensor"); return BSKV_ERR_INVALID_ARG; }
+  if ((out_strides[0] * 2) % 4 || (out_strides[1] * 2) % 4) { set_error("decode_merge: out strides must be multiples of 2 elements"); return BSKV_ERR_INVALID_ARG; }
+  MergeParams mp{};
+  mp.meta = plan->meta_dev;
+  decode_ws(plan, float_ws, &mp.ws_o, &mp.ws_lse);
+  mp.out = out; mp.o_s0 = out_strides[0]; mp.o_s1 = out_strides[1];
+  mp.lse = lse;
+  mp.num_kv_heads = plan->num_kv_heads;
+  mp.group = plan->num_qo_heads / plan->num_kv_heads;
+  mp.num_qo_heads = plan->num_qo_heads;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf = plan->dtype == BSKV_BF16;
+  if (plan->head_dim == 128)
+    return bf ? launch_merge_t<__nv_bfloat16, 128>(plan, mp, st) : launch_merge_t<__half, 128>(plan, mp, st);
+  return bf ? launch_merge_t<__nv_bfloat16, 64>(plan, mp, st) : launch_merge_t<__half, 64>(plan, mp, st);
+}
+
+extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
+                                       const int64_t* q_strides, const void* kv_cache,
+                                       const int64_t* kv_strides, void* out,
+                                       const int64_t* out_strides, float* lse, float sm_scale,
+                                       void* float_ws, size_t float_ws_bytes, void* stream) {
+  if (bskv_status s = bskv_run_decode_partial(plan, q, q_strides, kv_cache, kv_strides, out,
+                                              out_strides, lse, sm_scale, float_ws,
+                                              float_ws_bytes, stream))
+    return s;
+  return bskv_decode_merge(plan, out, out_strides, lse, float_ws, float_ws_bytes, stream);
 }
 
 extern "C" bskv_status bskv_merge_states(const float* v, const float* s, int64_t seq_len,

@@ -183,6 +183,22 @@ bskv_status bskv_run_decode(const bskv_plan* plan, const void* q, const int64_t*
                             void* float_ws, size_t float_ws_bytes, void* stream);
 
 /*
+ * The two halves of bskv_run_decode, for callers that want the split-KV partial states
+ * or to time the kernels apart. bskv_run_decode_partial runs the attention kernel only:
+ * requests computed in one piece are written to out/lse, split ones leave normalised
+ * partial outputs and LSE in float_ws. bskv_decode_merge then merges those into out/lse
+ * (and zero-fills requests without tokens); it is a no-op when the plan split nothing.
+ * Same arguments and errors as bskv_run_decode.
+ */
+bskv_status bskv_run_decode_partial(const bskv_plan* plan, const void* q,
+                                    const int64_t* q_strides, const void* kv_cache,
+                                    const int64_t* kv_strides, void* out,
+                                    const int64_t* out_strides, float* lse, float sm_scale,
+                                    void* float_ws, size_t float_ws_bytes, void* stream);
+bskv_status bskv_decode_merge(const bskv_plan* plan, void* out, const int64_t* out_strides,
+                              float* lse, void* float_ws, size_t float_ws_bytes, void* stream);
+
+/*
  * BSR block-sparse attention ([SPARSE] run(q, k, v, out, lse)):
  *   q [M, num_qo_heads, head_dim], k and v [N, num_kv_heads, head_dim] (strides {row,
  *   head} in elements); out like q; lse [M, num_qo_heads] float32 contiguous or NULL.

@@ -23,7 +23,8 @@ def assert_close(got, ref, atol, rtol, what=""):
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     both_inf = np.isinf(ref) & (got == ref)
-    err = np.where(both_inf, 0.0, np.abs(got - ref))
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_inf, 0.0, np.abs(got - ref))
     bad = ~(err <= atol + rtol * np.abs(np.where(both_inf, 0.0, ref)))
     stats = dict(max_abs=float(np.nanmax(err)) if err.size else 0.0,
                  rel_fro=float(np.linalg.norm(np.nan_to_num(err)) / max(np.linalg.norm(np.nan_to_num(np.where(both_inf, 0, ref))), 1e-300)),
