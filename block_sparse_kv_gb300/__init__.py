@@ -20,7 +20,7 @@ __all__ = [
     "BskvError", "Plan", "load_library", "build",
     "bskv_version", "bskv_last_error_message",
     "bskv_plan_decode", "bskv_plan_bsr", "bskv_plan_mla_sparse",
-    "bskv_run_decode", "bskv_run_decode_partial", "bskv_decode_merge",
+    "bskv_run_decode", "bskv_run_decode_partial", "bskv_decode_merge", "bskv_run_decode_noalloc",
     "bskv_run_bsr", "bskv_run_mla_sparse",
     "bskv_rope_quantize_fp8", "bskv_merge_states",
     "bskv_get_device_status", "bskv_set_debug_force_timeout",
@@ -67,6 +67,7 @@ _SIGS = {
     "bskv_run_decode": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P, _SZ, _P], _I32),
     "bskv_run_decode_partial": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P, _SZ, _P], _I32),
     "bskv_decode_merge": ([_P, _P, _I64P, _P, _P, _SZ, _P], _I32),
+    "bskv_run_decode_noalloc": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P], _I32),
     "bskv_run_bsr": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P, _SZ, _P], _I32),
     "bskv_run_mla_sparse": ([_P, _P, _P, _I64, _P, _F, _F, _P, _P, _P, _SZ, _P], _I32),
     "bskv_rope_quantize_fp8": ([_P, _I64P, _P, _I64P, _P, _I64, _I32, _P, _I64P, _P, _I64P,
@@ -247,6 +248,21 @@ def bskv_decode_merge(plan, out, lse=None):
     _check("bskv_decode_merge", lib.bskv_decode_merge(
         plan.handle, out.data_ptr(), _strides(out.stride(0), out.stride(1)), _ptr(lse), _ptr(fw),
         0 if fw is None else fw.numel(), _stream(out)))
+    return out
+
+
+def bskv_run_decode_noalloc(plan, q, kv_cache, out, lse=None, sm_scale=None):
+    """Decode without any device allocation by the library or by this call: for callers
+    that cannot allocate (see bskv.h). The caller passes the output (and optional lse);
+    the plan is not uploaded, its metadata goes into a library-owned static array."""
+    lib = load_library()
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(q.shape[-1])
+    ks = kv_cache.stride()
+    _check("bskv_run_decode_noalloc", lib.bskv_run_decode_noalloc(
+        plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), kv_cache.data_ptr(),
+        _strides(ks[0], ks[1], ks[2], ks[3]), out.data_ptr(), _strides(out.stride(0), out.stride(1)),
+        _ptr(lse), float(sm_scale), _stream(q)))
     return out
 
 

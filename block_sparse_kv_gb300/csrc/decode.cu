@@ -17,6 +17,8 @@
 // partial output and LSE to the float workspace; the merge kernel then combines them.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "launch.h"
@@ -622,4 +624,144 @@ extern "C" bskv_status bskv_merge_states(const float* v, const float* s, int64_t
       return BSKV_ERR_UNSUPPORTED;
   }
   return cuda_check(cudaGetLastError(), "merge_states launch");
+}
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free paged decode
+//
+// For callers that cannot allocate device memory: code embedded in a host framework that
+// hands it only tensors and a stream (no allocator of its own), processes whose device
+// memory is fully reserved by another allocator, and latency-critical loops where a
+// cudaMalloc/cudaFree (which can synchronise the device) is not acceptable. The plan
+// metadata and the split-KV partial states live in two file-scope device arrays instead
+// of caller workspaces. Every GPU that loads the library keeps them (9 MiB) until exit.
+// ---------------------------------------------------------------------------------------
+namespace bskv {
+namespace {
+
+constexpr size_t kNoAllocMetaWords = size_t(1) << 18;     // 1 MiB of plan metadata
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB of split-KV partials
+static __device__ __align__(256) int32_t g_noalloc_meta[kNoAllocMetaWords];
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocPtrs {
+  int32_t* meta = nullptr;
+  uint8_t* scratch = nullptr;
+};
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+NoAllocPtrs g_noalloc_ptrs[kNoAllocMaxDevices];
+
+// Device addresses of the two arrays on the current device, looked up once per device.
+// In host code the arrays' names are host-side stand-ins, never device addresses.
+bskv_status noalloc_ptrs(NoAllocPtrs* out) {
+  int d = 0;
+  if (bskv_status s = cuda_check(cudaGetDevice(&d), "cudaGetDevice")) return s;
+  if (d < 0 || d >= kNoAllocMaxDevices) {
+    set_error("run_decode_noalloc: device ordinal %d too large", d);
+    return BSKV_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocPtrs& p = g_noalloc_ptrs[d];
+  if (!p.meta) {
+    void* m = nullptr;
+    void* s = nullptr;
+    if (bskv_status e = cuda_check(cudaGetSymbolAddress(&m, g_noalloc_meta),
+                                   "run_decode_noalloc: cudaGetSymbolAddress(meta)"))
+      return e;
+    if (bskv_status e = cuda_check(cudaGetSymbolAddress(&s, g_noalloc_scratch),
+                                   "run_decode_noalloc: cudaGetSymbolAddress(scratch)"))
+      return e;
+    p.meta = static_cast<int32_t*>(m);
+    p.scratch = static_cast<uint8_t*>(s);
+  }
+  *out = p;
+  return BSKV_OK;
+}
+
+}  // namespace
+}  // namespace bskv
+
+extern "C" bskv_status bskv_run_decode_noalloc(const bskv_plan* plan, const void* q,
+                                               const int64_t* q_strides, const void* kv_cache,
+                                               const int64_t* kv_strides, void* out,
+                                               const int64_t* out_strides, float* lse,
+                                               float sm_scale, void* stream) {
+  if (!plan || plan->kind != KIND_DECODE) { set_error("run_decode_noalloc: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
+  const size_t meta_words = plan->meta.size();
+  if (meta_words > kNoAllocMetaWords || plan->float_ws_bytes > kNoAllocScratchBytes) {
+    set_error("run_decode_noalloc: plan needs %zu metadata bytes and %zu scratch bytes; the "
+              "static arrays hold %zu and %zu (use bskv_run_decode with caller workspaces)",
+              meta_words * 4, plan->float_ws_bytes, kNoAllocMetaWords * 4, kNoAllocScratchBytes);
+    return BSKV_ERR_UNSUPPORTED;
+  }
+  if (!q_strides || !kv_strides || !out_strides) { set_error("run_decode_noalloc: NULL strides"); return BSKV_ERR_INVALID_ARG; }
+  const int ps = plan->page_size;
+  if (!(ps == 8 || ps % 16 == 0)) {
+    set_error("run_decode_noalloc: page_size %d unsupported (8 or a multiple of 16)", ps);
+    return BSKV_ERR_UNSUPPORTED;
+  }
+  const int esz = 2;
+  const int Hkv = plan->num_kv_heads, D = plan->head_dim;
+  for (int i = 0; i < 4; ++i) {
+    if (kv_strides[i] <= 0 || (kv_strides[i] * esz) % 16 != 0) {
+      set_error("run_decode_noalloc: kv stride %d must be positive and 16-byte aligned", i);
+      return BSKV_ERR_INVALID_ARG;
+    }
+  }
+  if ((q_strides[0] * esz) % 4 || (q_strides[1] * esz) % 4 || (out_strides[0] * esz) % 4 ||
+      (out_strides[1] * esz) % 4) {
+    set_error("run_decode_noalloc: q/out strides must be multiples of 2 elements");
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (plan->batch == 0) return BSKV_OK;
+  if (!q || !kv_cache || !out) { set_error("run_decode_noalloc: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) { set_error("run_decode_noalloc: tensors must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  NoAllocPtrs st_ptrs;
+  if (bskv_status s = noalloc_ptrs(&st_ptrs)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The metadata is copied into the static array on the caller's stream; nothing in the
+  // scratch array has to start at zero (every partial state is written before it is read).
+  if (bskv_status s = cuda_check(cudaMemcpyAsync(st_ptrs.meta, plan->meta.data(), meta_words * 4,
+                                                 cudaMemcpyHostToDevice, st),
+                                 "run_decode_noalloc: metadata copy"))
+    return s;
+  DecodeParams dp{};
+  dp.meta = st_ptrs.meta;
+  dp.q = q; dp.q_s0 = q_strides[0]; dp.q_s1 = q_strides[1];
+  dp.out = out; dp.o_s0 = out_strides[0]; dp.o_s1 = out_strides[1];
+  dp.lse = lse;
+  const int g = plan->num_qo_heads / Hkv;
+  decode_ws(plan, st_ptrs.scratch, &dp.ws_o, &dp.ws_lse);
+  dp.num_kv_heads = Hkv; dp.group = g; dp.page_size = ps; dp.num_qo_heads = plan->num_qo_heads;
+  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  if (bskv_status s = status_args(&dp.st)) return s;
+  CUtensorMap map;
+  const uint64_t dims[5] = {uint64_t(D), uint64_t(ps), uint64_t(Hkv), 2, uint64_t(plan->num_pages)};
+  const uint64_t strides[4] = {uint64_t(kv_strides[3]) * esz, uint64_t(kv_strides[2]) * esz,
+                               uint64_t(kv_strides[1]) * esz, uint64_t(kv_strides[0]) * esz};
+  const uint32_t box[5] = {64, uint32_t(ps < kTile ? ps : kTile), 1, 1, 1};
+  const CUtensorMapDataType dt =
+      plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (bskv_status s = encode_tiled(&map, dt, 5, kv_cache, dims, strides, box,
+                                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return s;
+  MergeParams mp{};
+  mp.meta = st_ptrs.meta;
+  mp.ws_o = dp.ws_o; mp.ws_lse = dp.ws_lse;
+  mp.out = out; mp.o_s0 = out_strides[0]; mp.o_s1 = out_strides[1];
+  mp.lse = lse;
+  mp.num_kv_heads = Hkv; mp.group = g; mp.num_qo_heads = plan->num_qo_heads;
+  const bool bf = plan->dtype == BSKV_BF16;
+  bskv_status s = BSKV_OK;
+  if (D == 128) {
+    s = bf ? launch_decode_t<__nv_bfloat16, 128>(plan, map, dp, st) : launch_decode_t<__half, 128>(plan, map, dp, st);
+    if (s == BSKV_OK)
+      s = bf ? launch_merge_t<__nv_bfloat16, 128>(plan, mp, st) : launch_merge_t<__half, 128>(plan, mp, st);
+  } else {
+    s = bf ? launch_decode_t<__nv_bfloat16, 64>(plan, map, dp, st) : launch_decode_t<__half, 64>(plan, map, dp, st);
+    if (s == BSKV_OK)
+      s = bf ? launch_merge_t<__nv_bfloat16, 64>(plan, mp, st) : launch_merge_t<__half, 64>(plan, mp, st);
+  }
+  return s;
 }

@@ -199,6 +199,28 @@ bskv_status bskv_decode_merge(const bskv_plan* plan, void* out, const int64_t* o
                               float* lse, void* float_ws, size_t float_ws_bytes, void* stream);
 
 /*
+ * Allocation-free paged decode. The pages have no counterpart: this entry point exists for
+ * callers that cannot allocate device memory -- code embedded in a host framework that
+ * hands it only tensors and a stream, processes whose device memory is all reserved by
+ * another allocator, or latency-critical loops where cudaMalloc/cudaFree (which can
+ * synchronise the device) is not acceptable. It computes exactly what bskv_run_decode
+ * computes, with the same arguments minus the float workspace, and needs no
+ * bskv_plan_upload: the plan metadata (at most 1 MiB) is copied on `stream` into a
+ * library-owned static device array, and the split-KV partial states (at most 8 MiB) live
+ * in a second one. Every GPU that loads the library holds these 9 MiB until the process
+ * exits. A plan that needs more returns BSKV_ERR_UNSUPPORTED and launches nothing.
+ * The first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress);
+ * make that first call before any stream capture. All calls share the two arrays, and
+ * each call overwrites what the previous one left there, so calls that overlap on the GPU
+ * (e.g. on two streams) race: serialise them. No call allocates or frees device memory.
+ */
+bskv_status bskv_run_decode_noalloc(const bskv_plan* plan, const void* q,
+                                    const int64_t* q_strides, const void* kv_cache,
+                                    const int64_t* kv_strides, void* out,
+                                    const int64_t* out_strides, float* lse, float sm_scale,
+                                    void* stream);
+
+/*
  * BSR block-sparse attention ([SPARSE] run(q, k, v, out, lse)):
  *   q [M, num_qo_heads, head_dim], k and v [N, num_kv_heads, head_dim] (strides {row,
  *   head} in elements); out like q; lse [M, num_qo_heads] float32 contiguous or NULL.
