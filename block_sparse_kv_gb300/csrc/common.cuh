@@ -100,6 +100,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Warp-uniform bounded wait, for warps that go on to execute .sync.aligned instructions
+// (ldmatrix, mma.sync, tcgen05.ld/st): every lane waits, and the warp proceeds only if all
+// lanes succeeded and no abort was flagged, so no lane can be left behind in a collective.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const StatusArgs& st,
+                                          bool give_up, const volatile int* abort_flag = nullptr) {
+  bool good = !(abort_flag && *abort_flag);
+  if (good) good = mbar_wait(bar, parity, st, give_up);
+  return __all_sync(0xffffffffu, good);
+}
+
 // ---------------------------------------------------------------------------------------
 // bulk and tensor copies (TMA)
 // ---------------------------------------------------------------------------------------

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       l0 = l1 = 0.f;
     }
     const int stage = consumed % kStages;
-    if (!mbar_wait(&bars[stage], (consumed / kStages) & 1u, p.st, forced)) {
+    if (!warp_wait(&bars[stage], (consumed / kStages) & 1u, p.st, forced)) {
       ok = false;
       break;
     }

@@ -1,0 +1,83 @@
+"""GPU parity of the tensor-core (tcgen05) BSR kernel against the oracle.
+
+Shapes with R = C = 64, head_dim 128 and 2 or 4 query heads per kv head take the
+tensor-core path (the plan's variant 1). Gate: |gpu - oracle| <= 1e-2 + 1e-2 |oracle|.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_kv_gb300 as bskv
+import synth
+from oracle import attention as att
+from gpu_util import assert_close, bits, to64
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+def _run(cuda, d, dtype, rows=None, repeat=False):
+    dt = "bf16" if dtype == torch.bfloat16 else "fp16"
+    p = bskv.bskv_plan_bsr(d["indptr"], d["indices"], d["M"], d["N"], d["R"], d["C"],
+                           d["num_qo_heads"], d["num_kv_heads"], d["head_dim"],
+                           causal=d["causal"], dtype=dtype)
+    assert p.metadata()[15] == 1, "expected the tensor-core variant"
+    q, k, v = d["q"].to(cuda), d["k"].to(cuda), d["v"].to(cuda)
+    out, lse = bskv.bskv_run_bsr(p, q, k, v, return_lse=True)
+    if repeat:
+        out2 = bskv.bskv_run_bsr(p, q, k, v)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2)
+    torch.cuda.synchronize()
+    assert bskv.STATUS[bskv.bskv_get_device_status()] == "OK"
+    hq = d["q"].cpu() if rows is None else d["q"].cpu()
+    ref, ref_lse = att.bsr_attention(bits(hq), bits(d["k"]), bits(d["v"]), dt,
+                                     d["indptr"].numpy(), d["indices"].numpy(), d["M"], d["N"],
+                                     d["R"], d["C"], d["sm_scale"], d["causal"], rows)
+    sel = slice(None) if rows is None else torch.as_tensor(rows)
+    st = assert_close(to64(out[sel]), ref, TOL, TOL, "out")
+    assert_close(lse[sel].cpu().numpy(), ref_lse, TOL, TOL, "lse")
+    return st
+
+
+CASES = [
+    # M, N, Hq, Hkv, dtype, pattern, causal
+    (256, 256, 8, 2, torch.float16, "diag_lower", True),    # g = 4: two M tiles
+    (256, 256, 4, 2, torch.bfloat16, "diag_lower", True),   # g = 2: one M tile, bf16
+    (320, 384, 16, 4, torch.float16, "random", False),      # several kv heads, random blocks
+    (200, 256, 8, 2, torch.float16, "random", True),        # ragged M, bottom-right causal
+    (512, 512, 8, 4, torch.bfloat16, "full", True),         # every block, dense causal
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_bsr_tc_small(cuda, case):
+    M, N, Hq, Hkv, dtype, pattern, causal = case
+    d = synth.bsr_inputs(600 + M + Hq, M, N, 64, 64, Hq, Hkv, 128, dtype=dtype, pattern=pattern,
+                         causal=causal, density=0.5, p_off=0.3)
+    _run(cuda, d, dtype, repeat=True)
+
+
+def test_bsr_tc_sharp_softmax_rescales(cuda):
+    """q x 8 makes the running max grow block after block (lazy O rescaling in TMEM)."""
+    d = synth.bsr_inputs(650, 512, 512, 64, 64, 8, 2, 128, pattern="full", causal=False,
+                         q_scale=8.0)
+    st = _run(cuda, d, torch.float16)
+    print("bsr tc sharp:", st)
+
+
+def test_bsr_tc_empty_row_blocks(cuda):
+    d = synth.bsr_inputs(651, 256, 256, 64, 64, 8, 2, 128, pattern="random")
+    d["indptr"] = torch.tensor([0, 0, 2, 2, 3], dtype=torch.int32)
+    d["indices"] = torch.tensor([0, 3, 1], dtype=torch.int32)
+    _run(cuda, d, torch.float16)
+
+
+def test_bsr_tc_full_prefill_workload_sampled_rows(cuda):
+    """M = N = 16384, 32/8 heads, diagonal + 10% lower blocks, causal; 96 sampled rows."""
+    d = synth.make("bsr_prefill", device=cuda)
+    g = torch.Generator().manual_seed(5)
+    rows = sorted(set(torch.randint(0, 16384, (90,), generator=g).tolist()) | {0, 63, 64, 16383})
+    st = _run(cuda, d, torch.float16, rows=np.array(rows), repeat=True)
+    print("bsr prefill sampled rows:", st)
