@@ -238,8 +238,9 @@ bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_
  *           rows; indices are physical token ids = page * page_size + slot).
  *   indices [batch, q_len, top_k] int32 on the device, shared by all heads; entries
  *           [0, seq_lens[b]) are used and must lie in [0, num_rows). An entry outside
- *           that range contributes nothing and raises BSKV_ERR_DEVICE_INDEX in the
- *           device status word (bskv_get_device_status).
+ *           that range is never read (its row is taken as zeros), the output of that query
+ *           is unspecified, and BSKV_ERR_DEVICE_INDEX is raised in the device status word
+ *           (bskv_get_device_status).
  *   s_j = bmm1_scale * <q, kv_j> over 576 values; out = bmm2_scale * sum_j softmax(s)_j
  *   kv_j[:512] (V = the 512 latent values); out bf16 [batch, q_len, num_heads, 512];
  *   lse float32 [batch, q_len, num_heads] of the bmm1-scaled logits, or NULL.
