@@ -10,7 +10,7 @@
 // latent half): all 128 heads form the M=128 rows of every MMA and the CTA accumulates
 // O for one 256-value half of the output in TMEM (256 columns), so S and O fit side by side
 // (the full 128 x 512 fp32 accumulator alone would fill TMEM). S is computed by both halves.
-//   warps 0-7  two gather groups of 128 threads taking alternate tiles: a group stages the
+//   warps 0-5  two gather groups of 96 threads taking alternate tiles: a group stages the
 //              tile's 64 row ids in shared memory, copies the rows with 16-byte cp.async
 //              (consecutive threads, consecutive chunks of a row) into the swizzled panels
 //              (row r, chunk c -> chunk c ^ (r mod 8)) and publishes the tile as soon as its
@@ -18,12 +18,14 @@
 //              128B-swizzled panels of 128 B plus one 64B-swizzled panel for the rotated
 //              tail). On this part many-row gathers are faster through the load/store pipes
 //              than through TMA tile::gather4, which moves 128-byte pieces one at a time;
-//   warp 8     allocates TMEM; lane 0 issues S = Q K^T (M=128, N=64, K=576: 18 MMAs of K=32)
+//   warp 6     allocates TMEM; lane 0 issues S = Q K^T (M=128, N=64, K=576: 18 MMAs of K=32)
 //              and O += P V_half (M=128, N=256, K=64; the gathered panels serve as the
 //              MN-major V operand), advancing prebuilt descriptors by address only;
-//   warps 12-15 softmax: thread = head = TMEM lane; lazy max rescaling (threshold 2^8),
-//              P quantised to E4M3 into a 64B-swizzled tile, epilogue writes bf16 out or the
-//              split-KV partial state.
+//   warps 8-15 two softmax warpgroups; thread = head = TMEM lane, each group owns 32 of a
+//              tile's 64 columns and 128 of the 256 output values. The row max and, at the end,
+//              the row sum are combined through shared memory; lazy max rescaling (threshold
+//              2^8); exponentials as packed f16x2 (ex2.approx.f16x2) converted straight to
+//              E4M3 for the PV MMA; the epilogue writes bf16 out or the split-KV partial state.
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -51,7 +53,10 @@ constexpr uint32_t kSmemKV = kSmemQ + kQBytes;
 constexpr uint32_t kSmemP = kSmemKV + kStages * kStageBytes;
 constexpr uint32_t kSmemBar = kSmemP + 2 * kPBytes;
 constexpr uint32_t kSmemIdx = kSmemBar + 512;  // [stages][64] sanitised row ids
-constexpr uint32_t kSmemBytes = kSmemIdx + kStages * kRows * 4;
+// [3][2 groups][128]: row maxima by tile parity (slots 0, 1) and row sums (slot 2)
+constexpr uint32_t kSmemRed = kSmemIdx + kStages * kRows * 4;
+constexpr uint32_t kSmemBytes = kSmemRed + 3 * 2 * 128 * 4;
+constexpr int kGatherThreads = 96;  // per group
 constexpr uint32_t kTmemCols = 512;
 constexpr int kVD = kMlaVDim;  // 256
 
@@ -79,18 +84,18 @@ struct Bars {
   int abort;
 };
 
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return lo | (hi << 16);
+__device__ __forceinline__ __half2 h2exp2_approx(__half2 x) {
+  uint32_t in = *reinterpret_cast<uint32_t*>(&x), out;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(out) : "r"(in));
+  return *reinterpret_cast<__half2*>(&out);
 }
 
-// Sum of the four E4M3 values packed in w (exact conversions to half, then float).
-__device__ __forceinline__ float sum_e4m3x4(uint32_t w) {
-  const __half2 lo(__nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w & 0xffffu), __NV_E4M3));
-  const __half2 hi(__nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w >> 16), __NV_E4M3));
-  const float2 a = __half22float2(lo), b = __half22float2(hi);
-  return (a.x + a.y) + (b.x + b.y);
+// Two f16 values (low, high) to E4M3 (low byte, high byte), round to nearest even, saturating.
+__device__ __forceinline__ uint32_t half2_to_e4m3x2(__half2 x) {
+  const uint32_t in = *reinterpret_cast<uint32_t*>(&x);
+  uint16_t out;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(out) : "r"(in));
+  return out;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -114,19 +119,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&B.q_empty, 1);
     mbar_init(&B.drain, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&B.kv_full[s], 128);
+      mbar_init(&B.kv_full[s], kGatherThreads);
       mbar_init(&B.kv_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&B.s_full[b], 1);
-      mbar_init(&B.p_full[b], 128);
+      mbar_init(&B.p_full[b], 256);
     }
     mbar_init(&B.o_done, 1);
-    mbar_init(&B.o_free, 128);
+    mbar_init(&B.o_free, 256);
     B.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 6) {
     tmem_alloc(&B.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -136,25 +141,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = B.tmem_base;
   volatile int* abort_flag = &B.abort;
 
-  if (warp < 8) {
+  if (warp < 6) {
     // -------------------------------------------------------------- gather groups
     // Group grp (0/1) owns the tiles with kvc % 2 == grp. A tile is published (kv_full, 128
     // arrivals) once the group's own copies of it are complete, so no tile waits for the
     // issue of another; with three stages, gathering tile t only needs the stage released by
     // PV(t-3), which the MMA issues after QK(t-2): no cycle. Decisions of a group go through
-    // bar_and on its own named barrier (1 + grp, 128 threads).
-    const int grp = threadIdx.x >> 7;
-    const int pt = threadIdx.x & 127;
+    // bar_and on its own named barrier (1 + grp, 96 threads).
+    const int grp = threadIdx.x / kGatherThreads;
+    const int pt = threadIdx.x % kGatherThreads;
     const uint32_t bar_id = 1 + grp;
     int32_t* idx_smem = reinterpret_cast<int32_t*>(sm + kSmemIdx);
-    // This thread's 18 chunks of a tile: chunk id pt + 128 k -> (row, 16-byte column).
-    constexpr int kPer = (kRows * 36) / 128;
+    // This thread's 24 chunks of a tile: chunk id pt + 96 k -> (row, 16-byte column).
+    constexpr int kPer = (kRows * 36) / kGatherThreads;
     uint32_t off[kPer];
     uint16_t col[kPer];
     uint8_t rowk[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int cid = pt + 128 * k;
+      const int cid = pt + kGatherThreads * k;
       const int r = cid / 36, q = cid % 36;
       off[k] = q < 32 ? (q >> 3) * kNopePanelK + r * 128 + (((q & 7) ^ (r & 7)) << 4)
                       : 4 * kNopePanelK + r * 64 + ((((q - 32) & 3) ^ ((r >> 1) & 3)) << 4);
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (grp == 0) ++qc;
-      ok = bar_and(bar_id, 128, good);
+      ok = bar_and(bar_id, kGatherThreads, good);
       if (!ok) break;
       for (int t0 = ch.y; t0 < ch.z; t0 += kRows, ++kvc) {
         if ((kvc & 1u) != uint32_t(grp)) continue;
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         good = !*abort_flag && mbar_wait(&B.kv_empty[s], ((kvc / kStages) & 1u) ^ 1u, p.st, forced);
         int32_t* ib = idx_smem + s * kRows;
         if (pt < kRows) ib[pt] = my_id;
-        ok = bar_and(bar_id, 128, good);
+        ok = bar_and(bar_id, kGatherThreads, good);
         if (!ok) break;
         uint8_t* stage = sm + kSmemKV + s * kStageBytes;
         const int valid = ch.z - t0;
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) *abort_flag = 1;
     if (grp == 0 && pt == 0 && qc > 0 && !ok) mbar_wait(&B.q_full, (qc - 1) & 1u, p.st, false);
-  } else if (warp == 8) {
+  } else if (warp == 6) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc(128, 64, 0, 0, 0, 0);
@@ -280,11 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&B.drain);
       mbar_wait(&B.drain, 0, p.st, false);
     }
-  } else if (warp >= 12) {
-    // -------------------------------------------------------------- softmax warpgroup
+  } else if (warp >= 8) {
+    // -------------------------------------------------------------- softmax warpgroups
+    const int wg = (warp - 8) >> 2;          // 0: columns 0-31 / O 0-127; 1: 32-63 / 128-255
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;  // head
+    const int r = q4 * 32 + lane;            // head
     const uint32_t lane_base = uint32_t(q4 * 32) << 16;
+    float* red = reinterpret_cast<float*>(sm + kSmemRed);  // [parity][group][row]
     uint32_t G = 0, od = 0;
     bool ok = true;
     for (int ci = c0; ci < c1 && ok; ++ci) {
@@ -294,21 +301,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_run = -INFINITY, l_run = 0.f;
       for (int t = 0; t < nt; ++t, ++G) {
         const uint32_t b = G & 1u;
-        if (!warp_wait(&B.s_full[b], (G >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t sr[64];
-        tmem_ld32(tmem + lane_base + 256 + b * 64, sr);
-        tmem_ld32(tmem + lane_base + 256 + b * 64 + 32, sr + 32);
-        tmem_ld_wait();
-        const int valid = min(kRows, ch.z - (ch.y + t * kRows));
-        float s[64];
+        bool good = warp_wait(&B.s_full[b], (G >> 1) & 1u, p.st, forced, abort_flag);
+        uint32_t sr[32];
+        if (good) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_base + 256 + b * 64 + wg * 32, sr);
+          tmem_ld_wait();
+        }
+        const int valid = min(kRows, ch.z - (ch.y + t * kRows)) - wg * 32;
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const float x = c < valid ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-          s[c] = x;
+          sr[c] = __float_as_uint(x);
           mx = fmaxf(mx, x);
         }
+        red[(b * 2 + wg) * 128 + r] = mx;
+        // both groups meet here once per tile (named barrier 3, 256 threads)
+        ok = bar_and(3, 256, good);
+        if (!ok) break;
+        mx = fmaxf(mx, red[(b * 2 + (wg ^ 1)) * 128 + r]);
         float m_use = m_run, alpha = 1.f;
         bool rescale = false;
         if (m_run == -INFINITY) {
@@ -319,18 +331,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float ref = m_use == -INFINITY ? 0.f : m_use;
-        // P is rounded to E4M3 for the PV MMA; the normaliser sums the rounded values, so
-        // O / l is an exact weighted mean of V under the weights the MMA actually used.
-        float sum = 0.f;
-        uint32_t pk[16];
+        // p = 2^(x - ref) in f16x2 pairs, straight to E4M3 pairs; partial row sum in f16x2.
+        uint32_t pk[8];
+        __half2 hsum = __float2half2_rn(0.f);
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float a0 = fast_exp2(s[c] - ref), a1 = fast_exp2(s[c + 1] - ref);
-          const float a2 = fast_exp2(s[c + 2] - ref), a3 = fast_exp2(s[c + 3] - ref);
-          pk[c / 4] = e4m3x4(a0, a1, a2, a3);
-          sum += sum_e4m3x4(pk[c / 4]);
+        for (int c = 0; c < 32; c += 4) {
+          const __half2 h0 = __floats2half2_rn(__uint_as_float(sr[c]) - ref, __uint_as_float(sr[c + 1]) - ref);
+          const __half2 h1 = __floats2half2_rn(__uint_as_float(sr[c + 2]) - ref, __uint_as_float(sr[c + 3]) - ref);
+          const __half2 e0 = h2exp2_approx(h0), e1 = h2exp2_approx(h1);
+          hsum = __hadd2(hsum, __hadd2(e0, e1));
+          pk[c / 4] = half2_to_e4m3x2(e0) | (half2_to_e4m3x2(e1) << 16);
         }
-        l_run = l_run * alpha + sum;
+        const float2 fs = __half22float2(hsum);
+        l_run = l_run * alpha + (fs.x + fs.y);
         m_run = m_use;
         rescale = __any_sync(0xffffffffu, rescale);
         while (od < G) {
@@ -338,21 +351,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++od;
         }
         if (!ok) break;
+        // this group's two 16-byte chunks (2 wg, 2 wg + 1) of the 64-byte P row, SW64 layout
         uint8_t* prow = sm + kSmemP + b * kPBytes + r * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ ((r >> 1) & 3)) << 4)) =
+        for (int c = 0; c < 2; ++c) {
+          const int cc = 2 * wg + c;
+          *reinterpret_cast<uint4*>(prow + ((cc ^ ((r >> 1) & 3)) << 4)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
         if (rescale && t > 0) {
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < kVD; cc += 32) {
+          for (int cc = 0; cc < kVD / 2; cc += 32) {
             uint32_t ov[32];
-            tmem_ld32(tmem + lane_base + cc, ov);
+            const uint32_t ta = tmem + lane_base + wg * (kVD / 2) + cc;
+            tmem_ld32(ta, ov);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tmem_st32(tmem + lane_base + cc, ov);
+            tmem_st32(ta, ov);
           }
           tmem_st_wait();
         }
@@ -361,24 +378,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&B.p_full[b]);
       }
       if (!ok) break;
+      // Epilogue: combine the two partial row sums, then each group stores its 128 values.
+      red[(4 + wg) * 128 + r] = l_run;
+      ok = bar_and(3, 256, true);
+      if (!ok) break;
+      const float l_tot = red[4 * 128 + r] + red[5 * 128 + r];
       while (od < G) {
         if (!warp_wait(&B.o_done, od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
         ++od;
       }
       if (!ok) break;
       tc_fence_after();
-      const float scale = l_run > 0.f ? p.bmm2 / l_run : 0.f;
-      const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      const float scale = l_tot > 0.f ? p.bmm2 / l_tot : 0.f;
+      const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
       const bool row_ok = r < p.heads;
       const int slot = ch.w;
 #pragma unroll 1
-      for (int cc = 0; cc < kVD; cc += 32) {
+      for (int cc = 0; cc < kVD / 2; cc += 32) {
         uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + cc, ov);
+        tmem_ld32(tmem + lane_base + wg * (kVD / 2) + cc, ov);
         tmem_ld_wait();
         if (!row_ok) continue;
+        const int col = wg * (kVD / 2) + cc;
         if (slot < 0) {
-          __nv_bfloat16* dst = p.out + (int64_t(n) * p.heads + r) * 512 + vh * kVD + cc;
+          __nv_bfloat16* dst = p.out + (int64_t(n) * p.heads + r) * 512 + vh * kVD + col;
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 w;
@@ -393,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + c) = w;
           }
         } else {
-          float* dst = p.ws_o + (int64_t(slot) * 128 + r) * kVD + cc;
+          float* dst = p.ws_o + (int64_t(slot) * 128 + r) * kVD + col;
 #pragma unroll
           for (int c = 0; c < 32; c += 4)
             *reinterpret_cast<float4*>(dst + c) =
@@ -401,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __uint_as_float(ov[c + 2]) * scale, __uint_as_float(ov[c + 3]) * scale);
         }
       }
-      if (row_ok) {
+      if (row_ok && wg == 0) {
         if (slot < 0) {
           if (p.lse && vh == 0) p.lse[int64_t(n) * p.heads + r] = lse;
         } else {
@@ -416,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 6) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Merge split-KV pieces of (query token, latent half) units; zero-fill empty ones.
