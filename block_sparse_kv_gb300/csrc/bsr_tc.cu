@@ -9,19 +9,23 @@
 // share kv head h, i.e. one or two M=128 tiles (two heads per tile, head-major), so every
 // K/V block that is loaded feeds all grouped heads.
 //
-// GB300 design (persistent, one CTA per SM, 12 warps):
-//   warp 0   TMA producer: Q tiles (3-D tensor map, 128B swizzle) once per unit, K and V
-//            blocks of the unit's column list into a 3-stage ring;
-//   warp 1   allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//            S_m = Q_m K^T (M=128, N=64, K=128, K-major operands) into a double-buffered
-//            S region of TMEM, then O_m += P_m V (M=128, N=128, K=64; V MN-major);
-//            completion is signalled with tcgen05.commit on mbarriers;
-//   warps 4-7 / 8-11  one warpgroup per M tile: thread = row = TMEM lane. Each reads its S
-//            row (tcgen05.ld), applies scale and the causal mask, keeps a running max with
-//            lazy rescaling (O is rescaled in TMEM only when the max grows by more than 2^8),
-//            writes P (fp16/bf16) into a 128B-swizzled K-major tile for the PV MMA, and in
-//            the epilogue normalises O from TMEM and stores out and lse.
-// The MMA pipe runs QK of block j+1 while the warpgroups do the softmax of block j.
+// GB300 design (persistent, one CTA per SM, 12 warps). A tcgen05.mma costs about the same
+// time for N = 64 and N = 128 and reaches the dense peak only at N = 256, so the column
+// blocks of a row are taken in pairs: one step is S = Q K^T over 128 keys (N = 128) and
+// O += P V over the same 128 keys (K = 128, N = head_dim = 128).
+//   warp 0   TMA producer: Q tiles (3-D tensor map, 128B swizzle) once per unit; K and V of
+//            a block pair into one stage ([128 keys x 128 B] panels), 2 stages (3 for g = 2);
+//   warp 1   allocates 512 TMEM columns; lane 0 issues the MMAs. With two M tiles the jobs
+//            alternate tile 0 / tile 1 (ping-pong): while one warpgroup turns S into P, the
+//            tensor core runs the other tile's PV and next QK. With one M tile, S is double
+//            buffered instead. P is written back into TMEM over S (16-bit, two per column)
+//            and feeds the PV MMA as its A operand; V is an MN-major shared-memory operand;
+//   warps 4-7 / 8-11  one warpgroup per M tile: thread = row = TMEM lane. It reads its
+//            S row once into registers (four loads, one wait), applies scale and the causal
+//            mask, keeps a running max with lazy rescaling (O in TMEM is rescaled only when
+//            the max grows by more than 2^8), forms P = 2^x (packed f16x2 for fp16 inputs)
+//            and stores it over the S columns with tcgen05.st; the epilogue normalises O and
+//            stores out and lse.
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs, frees TMEM and
 // returns after recording BSKV_ERR_TIMEOUT.
 #include <math.h>
@@ -37,13 +41,13 @@ using namespace dev;
 
 constexpr int kBlk = 64;          // R = C = 64
 constexpr int kD = 128;
-constexpr int kStagesKV = 3;
 constexpr int kThreads = 384;
-constexpr uint32_t kKPanel = 64 * 128;      // [64 rows x 64 elements] of 16 bits
-constexpr uint32_t kQTile = 2 * 128 * 128;  // [128 rows x 128 elements]: 2 panels of 16 KB
-constexpr uint32_t kKVStage = 4 * kKPanel;  // K (2 panels) then V (2 panels)
-constexpr uint32_t kPTile = 128 * 128;      // [128 rows x 64 elements]
+constexpr uint32_t kKPanel = 64 * 128;          // [64 rows x 64 elements] of 16 bits
+constexpr uint32_t kPairPanel = 128 * 128;      // [128 rows x 64 elements]
+constexpr uint32_t kQTile = 2 * 128 * 128;      // [128 rows x 128 elements]: 2 panels
+constexpr uint32_t kStageBytes = 4 * kPairPanel;  // K pair (2 panels) then V pair (2 panels)
 constexpr uint32_t kTmemCols = 512;
+// TMEM columns: O of M tile m at 256 m; S (and P over it) of slot z at 128 + 256 z.
 
 struct TcParams {
   const int32_t* meta;
@@ -56,20 +60,19 @@ struct TcParams {
 };
 
 template <int NM>
-struct Smem {
+struct Cfg {
+  static constexpr int kStages = NM == 2 ? 2 : 3;
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kP = kQ + NM * kQTile;
-  static constexpr uint32_t kKV = kP + NM * 2 * kPTile;
-  static constexpr uint32_t kBar = kKV + kStagesKV * kKVStage;
+  static constexpr uint32_t kKV = kQ + NM * kQTile;
+  static constexpr uint32_t kBar = kKV + kStages * kStageBytes;
   static constexpr uint32_t kBytes = kBar + 512;
 };
 
 struct Bars {
   uint64_t q_full, q_empty, drain;
-  uint64_t kv_full[kStagesKV], kv_empty[kStagesKV];
-  uint64_t s_full[2][2];  // [m][buffer]
-  uint64_t p_full[2][2];
-  uint64_t o_done[2], o_free[2];
+  uint64_t kv_full[3], kv_empty[3];
+  uint64_t s_full[2], p_full[2];  // per S slot
+  uint64_t o_done[2], o_free[2];  // per M tile
   uint32_t tmem_base;
   int abort;
 };
@@ -94,11 +97,31 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16, float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// P for two logits (log2 domain, reference subtracted): returns them packed in T and their
+// values as float. fp16 uses the packed f16x2 exponential (P is fp16 anyway); bf16 keeps
+// the fp32 exponential, since a bf16 argument would lose too much precision.
+template <typename T>
+__device__ __forceinline__ uint32_t exp2_pack(float x0, float x1, float2& v);
+template <>
+__device__ __forceinline__ uint32_t exp2_pack<__half>(float x0, float x1, float2& v) {
+  const __half2 in = __floats2half2_rn(x0, x1);
+  uint32_t out;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(out) : "r"(*reinterpret_cast<const uint32_t*>(&in)));
+  v = __half22float2(*reinterpret_cast<const __half2*>(&out));
+  return out;
+}
+template <>
+__device__ __forceinline__ uint32_t exp2_pack<__nv_bfloat16>(float x0, float x1, float2& v) {
+  v = make_float2(fast_exp2(x0), fast_exp2(x1));
+  return pack2(__nv_bfloat16(), v.x, v.y);
+}
+
 template <typename T, int NM>
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const TcParams p) {
-  using L = Smem<NM>;
+  using L = Cfg<NM>;
+  constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -116,17 +139,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&B.q_full, 1);
     mbar_init(&B.q_empty, 1);
     mbar_init(&B.drain, 1);
-    for (int s = 0; s < kStagesKV; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&B.kv_full[s], 1);
       mbar_init(&B.kv_empty[s], 1);
     }
-    for (int m = 0; m < 2; ++m) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&B.s_full[m][b], 1);
-        mbar_init(&B.p_full[m][b], 128);
-      }
-      mbar_init(&B.o_done[m], 1);
-      mbar_init(&B.o_free[m], 128);
+    for (int z = 0; z < 2; ++z) {
+      mbar_init(&B.s_full[z], 1);
+      mbar_init(&B.p_full[z], 128);
+      mbar_init(&B.o_done[z], 1);
+      mbar_init(&B.o_free[z], 128);
     }
     B.abort = 0;
     fence_mbar_init();
@@ -162,30 +183,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
                           pn * 64, h * p.group + m * 2 + hl, i * kBlk, &B.q_full);
         ++qc;
-        for (int e = e0; e < e1; ++e, ++kvc) {
-          const int s = kvc % kStagesKV;
-          if (*abort_flag || !mbar_wait(&B.kv_empty[s], ((kvc / kStagesKV) & 1u) ^ 1u, p.st, forced)) {
+        for (int e = e0; e < e1; e += 2, ++kvc) {
+          const int s = kvc % S;
+          if (*abort_flag || !mbar_wait(&B.kv_empty[s], ((kvc / S) & 1u) ^ 1u, p.st, forced)) {
             ok = false;
             break;
           }
-          const int j = indices[e];
-          uint8_t* dst = sm + L::kKV + s * kKVStage;
-          mbar_arrive_expect_tx(&B.kv_full[s], kKVStage);
-          tma_load_3d(dst, &kmap, 0, h, j * kBlk, &B.kv_full[s]);
-          tma_load_3d(dst + kKPanel, &kmap, 64, h, j * kBlk, &B.kv_full[s]);
-          tma_load_3d(dst + 2 * kKPanel, &vmap, 0, h, j * kBlk, &B.kv_full[s]);
-          tma_load_3d(dst + 3 * kKPanel, &vmap, 64, h, j * kBlk, &B.kv_full[s]);
+          const int nb = min(2, e1 - e);
+          uint8_t* dst = sm + L::kKV + s * kStageBytes;
+          mbar_arrive_expect_tx(&B.kv_full[s], nb * 4 * kKPanel);
+          for (int b = 0; b < nb; ++b) {
+            const int j = indices[e + b];
+            for (int pn = 0; pn < 2; ++pn) {
+              tma_load_3d(dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk, &B.kv_full[s]);
+              tma_load_3d(dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64, h,
+                          j * kBlk, &B.kv_full[s]);
+            }
+          }
         }
       }
       if (!ok) {
         *abort_flag = 1;
-        // Wait (bounded, not forcible) for every copy this thread issued to land.
         if (qc > 0) mbar_wait(&B.q_full, (qc - 1) & 1u, p.st, false);
-        for (int s = 0; s < kStagesKV; ++s) {
-          // the last use of stage s that was issued: kvc' < kvc with kvc' % stages == s
+        for (int s = 0; s < S; ++s) {
           if (kvc > uint32_t(s)) {
-            const uint32_t last = ((kvc - 1 - s) / kStagesKV) * kStagesKV + s;
-            mbar_wait(&B.kv_full[s], (last / kStagesKV) & 1u, p.st, false);
+            const uint32_t last = ((kvc - 1 - s) / S) * S + s;
+            mbar_wait(&B.kv_full[s], (last / S) & 1u, p.st, false);
           }
         }
       }
@@ -194,31 +217,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t fmt = Fmt<T>::v;
-      constexpr uint32_t idesc_qk = umma_idesc(128, 64, fmt, fmt, 0, 0);
+      constexpr uint32_t idesc_qk128 = umma_idesc(128, 128, fmt, fmt, 0, 0);
+      constexpr uint32_t idesc_qk64 = umma_idesc(128, 64, fmt, fmt, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc(128, 128, fmt, fmt, 0, 1);
       const uint32_t sbase = smem_u32(sm);
-      uint32_t qc = 0, kvc = 0, G = 0, uc = 0;
+      // Descriptors are built once; steps advance the start-address field (16-byte units).
+      const uint64_t dq = umma_desc(sbase + L::kQ, 16, 1024, kSwz128);
+      const uint64_t dk = umma_desc(sbase + L::kKV, 16, 1024, kSwz128);
+      const uint64_t dv = umma_desc(sbase + L::kKV + 2 * kPairPanel, kPairPanel, 1024, kSwz128);
+      uint32_t qc = 0, kvc = 0, J = 0, uc = 0;
       bool ok = true;
-      auto pv = [&](uint32_t g_step, uint32_t kv_use, bool first) -> bool {
-        const int s = kv_use % kStagesKV;
-        const uint32_t vaddr = sbase + L::kKV + s * kKVStage + 2 * kKPanel;
-        for (int m = 0; m < NM; ++m) {
-          const uint32_t b = g_step & 1u;
-          if (*abort_flag || !mbar_wait(&B.p_full[m][b], (g_step >> 1) & 1u, p.st, forced)) return false;
-          if (first && (*abort_flag || !mbar_wait(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced))) return false;
-          tc_fence_after();
-          const uint32_t paddr = sbase + L::kP + (m * 2 + b) * kPTile;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = umma_desc(paddr + kk * 32, 16, 1024, kSwz128);
-            const uint64_t bd = umma_desc(vaddr + kk * 2048, kKPanel, 1024, kSwz128);
-            umma_f16(tmem + m * 128, a, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-          }
-          umma_commit(&B.o_done[m]);
-        }
-        umma_commit(&B.kv_empty[s]);
-        return true;
-      };
       for (int ui = u0; ui < u1 && ok; ++ui) {
         const int4 un = units[ui];
         const int i = un.y;
@@ -228,34 +236,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*abort_flag || !mbar_wait(&B.q_full, qc & 1u, p.st, forced)) { ok = false; break; }
         ++qc;
         tc_fence_after();
+        const int steps = (n + 1) >> 1;
+        const int NJ = steps * NM;
         const uint32_t kv_first = kvc;
-        for (int j = 0; j < n; ++j, ++kvc) {
-          const int s = kvc % kStagesKV;
-          if (*abort_flag || !mbar_wait(&B.kv_full[s], (kvc / kStagesKV) & 1u, p.st, forced)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kaddr = sbase + L::kKV + s * kKVStage;
-          const uint32_t gj = G + j;
-          for (int m = 0; m < NM; ++m) {
-            const uint32_t qaddr = sbase + L::kQ + m * kQTile;
-            const uint32_t sd = tmem + 256 + (m * 2 + (gj & 1u)) * 64;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t a = umma_desc(qaddr + (kk / 4) * (kQTile / 2) + (kk % 4) * 32, 16, 1024, kSwz128);
-              const uint64_t bd = umma_desc(kaddr + (kk / 4) * kKPanel + (kk % 4) * 32, 16, 1024, kSwz128);
-              umma_f16(sd, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&B.s_full[m][gj & 1u]);
+        // QK of local job jl into S slot (J + jl) & 1.
+        auto qk = [&](int jl) -> bool {
+          const int j = NM == 2 ? (jl >> 1) : jl;
+          const int m = NM == 2 ? (jl & 1) : 0;
+          const uint32_t step = kv_first + j;
+          const int s = step % S;
+          if (m == 0) {
+            if (*abort_flag || !mbar_wait(&B.kv_full[s], (step / S) & 1u, p.st, forced)) return false;
+            tc_fence_after();
           }
-          if (j >= 1 && !pv(gj - 1, kv_first + j - 1, j == 1)) { ok = false; break; }
+          const int nb = min(2, n - 2 * j);
+          const uint32_t z = (J + jl) & 1u;
+          const uint32_t sd = tmem + 128 + 256 * z;
+          const uint32_t qo = (m * kQTile) >> 4, ko = (s * kStageBytes) >> 4;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t pq = ((kk >> 2) * (kQTile / 2) + (kk & 3) * 32) >> 4;
+            const uint32_t pk = ((kk >> 2) * kPairPanel + (kk & 3) * 32) >> 4;
+            umma_f16(sd, dq + qo + pq, dk + ko + pk, nb == 2 ? idesc_qk128 : idesc_qk64,
+                     kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&B.s_full[z]);
+          return true;
+        };
+        if (!qk(0) || (NJ > 1 && !qk(1))) { ok = false; break; }
+        for (int jl = 0; jl < NJ; ++jl) {
+          const uint32_t Jg = J + jl, z = Jg & 1u;
+          const int j = NM == 2 ? (jl >> 1) : jl;
+          const int m = NM == 2 ? (jl & 1) : 0;
+          if (*abort_flag || !mbar_wait(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced)) { ok = false; break; }
+          if (j == 0 && (*abort_flag || !mbar_wait(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced))) { ok = false; break; }
+          tc_fence_after();
+          const int nb = min(2, n - 2 * j);
+          const int s = (kv_first + j) % S;
+          const uint32_t vo = (s * kStageBytes) >> 4;
+          const uint32_t pa = tmem + 128 + 256 * z;
+          for (int kk = 0; kk < nb * 4; ++kk)
+            umma_f16_ts(tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
+                        (j == 0 && kk == 0) ? 0u : 1u);
+          umma_commit(&B.o_done[m]);
+          if (m == NM - 1) umma_commit(&B.kv_empty[s]);
+          if (jl + 2 < NJ && !qk(jl + 2)) { ok = false; break; }
         }
         if (!ok) break;
-        if (!pv(G + n - 1, kv_first + n - 1, n == 1)) { ok = false; break; }
+        kvc = kv_first + steps;
         umma_commit(&B.q_empty);
-        G += n;
+        J += NJ;
         ++uc;
       }
       if (!ok) *abort_flag = 1;
-      // All MMAs issued by this thread complete before TMEM is released.
       umma_commit(&B.drain);
       mbar_wait(&B.drain, 0, p.st, false);
     }
@@ -266,8 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q4 * 32 + lane;                    // row of the M tile = TMEM lane
     const uint32_t lane_base = uint32_t(q4 * 32) << 16;
     const int hl = m * 2 + r / kBlk;                 // head within the group
-    uint8_t* const prow = sm + L::kP + m * 2 * kPTile + r * 128;
-    uint32_t G = 0, od = 0;
+    uint32_t J = 0, cnt = 0, od = 0;
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui) {
       const int4 un = units[ui];
@@ -284,30 +316,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      const int steps = (n + 1) >> 1;
+      const int lim = tok + (p.N - p.M);
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < n; ++j, ++G) {
-        const uint32_t b = G & 1u;
-        if (!warp_wait(&B.s_full[m][b], (G >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+      for (int j = 0; j < steps; ++j) {
+        const uint32_t Jg = J + (NM == 2 ? 2 * j + m : j), z = Jg & 1u;
+        // the step's column blocks are read before waiting for S (off the critical path)
+        const int nb = min(2, n - 2 * j);
+        const int jb0 = indices[e0 + 2 * j];
+        const int jb1 = nb == 2 ? indices[e0 + 2 * j + 1] : jb0;
+        if (!warp_wait(&B.s_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[64];
-        const uint32_t scol = tmem + lane_base + 256 + (m * 2 + b) * 64;
+        const uint32_t scol = tmem + lane_base + 128 + 256 * z;
+        // The whole S row goes to registers in one read; P may then overwrite it in TMEM.
+        uint32_t sr[128];
         tmem_ld32(scol, sr);
         tmem_ld32(scol + 32, sr + 32);
+        if (nb == 2) {
+          tmem_ld32(scol + 64, sr + 64);
+          tmem_ld32(scol + 96, sr + 96);
+        }
         tmem_ld_wait();
-        float s[64];
-        const int jb = indices[e0 + j];
-        const int lim = tok + (p.N - p.M);
-        const bool mask = p.causal && (jb * kBlk + kBlk - 1 > lim);
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float x = __uint_as_float(sr[c]) * p.scale_log2;
-          if (mask && jb * kBlk + c > lim) x = -INFINITY;
-          s[c] = x;
-          mx = fmaxf(mx, x);
+        for (int bb = 0; bb < 2; ++bb) {
+          if (bb < nb) {
+            const int k0 = (bb ? jb1 : jb0) * kBlk;
+            const bool mask = p.causal && (k0 + kBlk - 1 > lim);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              if (mask && k0 + c > lim) sr[64 * bb + c] = __float_as_uint(-INFINITY);
+              mx = fmaxf(mx, __uint_as_float(sr[64 * bb + c]));
+            }
+          }
         }
-        // Lazy rescaling: keep the reference max unless the row max grew by more than 8
-        // (a factor 2^8), so O in TMEM is rarely touched and P stays below 256.
+        mx *= p.scale_log2;
         float m_use = m_run, alpha = 1.f;
         bool rescale = false;
         if (m_run == -INFINITY) {
@@ -318,51 +361,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float ref = m_use == -INFINITY ? 0.f : m_use;
+        rescale = __any_sync(0xffffffffu, rescale);
+        // P = 2^(s * scale - ref), 32 keys at a time into packed columns [16 ck, 16 ck + 16)
         float sum = 0.f;
-        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float a0 = fast_exp2(s[c] - ref), a1 = fast_exp2(s[c + 1] - ref);
-          sum += a0 + a1;
-          pk[c / 2] = pack2(T(), a0, a1);
+        for (int ck = 0; ck < 4; ++ck) {
+          if (ck < 2 * nb) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float x0 = fmaf(__uint_as_float(sr[32 * ck + c]), p.scale_log2, -ref);
+              const float x1 = fmaf(__uint_as_float(sr[32 * ck + c + 1]), p.scale_log2, -ref);
+              float2 pv;
+              pk[c / 2] = exp2_pack<T>(x0, x1, pv);
+              sum += pv.x + pv.y;
+            }
+            tmem_st16(scol + 16 * ck, pk);
+          }
         }
         l_run = l_run * alpha + sum;
         m_run = m_use;
-        // The O rescale (tcgen05.ld/st, warp-collective) runs for the whole warp when any
-        // of its rows needs it; the other rows multiply by 1.
-        rescale = __any_sync(0xffffffffu, rescale);
-        // P buffer b was last read by PV of step G-2; observe completions up to PV(G-1)
-        // (also required before touching O).
-        while (od < G) {
+        // all earlier PVs into this tile's O must be complete (before a rescale, and so that
+        // this group never falls two completions behind)
+        while (od < cnt) {
           if (!warp_wait(&B.o_done[m], od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           ++od;
         }
         if (!ok) break;
-        uint8_t* pr = prow + b * kPTile;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(pr + ((c ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         if (rescale && j > 0) {
-          tc_fence_after();
-#pragma unroll
+#pragma unroll 1
           for (int cc = 0; cc < kD; cc += 32) {
             uint32_t ov[32];
-            tmem_ld32(tmem + lane_base + m * 128 + cc, ov);
+            tmem_ld32(tmem + lane_base + 256 * m + cc, ov);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tmem_st32(tmem + lane_base + m * 128 + cc, ov);
+            tmem_st32(tmem + lane_base + 256 * m + cc, ov);
           }
-          tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B.p_full[m][b]);
+        mbar_arrive(&B.p_full[z]);
+        ++cnt;
       }
       if (!ok) break;
-      // Epilogue: wait for the unit's last PV, normalise and store.
-      while (od < G) {
+      J += steps * NM;
+      // Epilogue: wait for the unit's last PV into this tile, normalise and store.
+      while (od < cnt) {
         if (!warp_wait(&B.o_done[m], od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
         ++od;
       }
@@ -372,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < kD; cc += 32) {
         uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + m * 128 + cc, ov);
+        tmem_ld32(tmem + lane_base + 256 * m + cc, ov);
         tmem_ld_wait();
         if (tok < p.M) {
 #pragma unroll
@@ -405,7 +450,7 @@ bskv_status launch_t(const bskv_plan* plan, const CUtensorMap& qm, const CUtenso
                      const CUtensorMap& vm, const TcParams& tp, cudaStream_t st) {
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
-  const size_t smem = Smem<NM>::kBytes + 1024;
+  const size_t smem = Cfg<NM>::kBytes + 1024;
   auto kern = bsr_tc_kernel<T, NM>;
   if (bskv_status s = cuda_check(
           cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
