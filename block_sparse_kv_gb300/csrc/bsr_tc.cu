@@ -337,19 +337,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(scol + 96, sr + 96);
         }
         tmem_ld_wait();
-        float mx = -INFINITY;
+        // row max as 8 independent partial maxima (short dependency chains)
+        float mxp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mxp[q] = -INFINITY;
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           if (bb < nb) {
             const int k0 = (bb ? jb1 : jb0) * kBlk;
-            const bool mask = p.causal && (k0 + kBlk - 1 > lim);
+            if (p.causal && (k0 + kBlk - 1 > lim)) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              if (mask && k0 + c > lim) sr[64 * bb + c] = __float_as_uint(-INFINITY);
-              mx = fmaxf(mx, __uint_as_float(sr[64 * bb + c]));
+              for (int c = 0; c < 64; ++c)
+                if (k0 + c > lim) sr[64 * bb + c] = __float_as_uint(-INFINITY);
             }
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], __uint_as_float(sr[64 * bb + c]));
           }
         }
+        float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                         fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         mx *= p.scale_log2;
         float m_use = m_run, alpha = 1.f;
         bool rescale = false;
@@ -363,7 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ref = m_use == -INFINITY ? 0.f : m_use;
         rescale = __any_sync(0xffffffffu, rescale);
         // P = 2^(s * scale - ref), 32 keys at a time into packed columns [16 ck, 16 ck + 16)
-        float sum = 0.f;
+        float sp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sp[q] = 0.f;
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
           if (ck < 2 * nb) {
@@ -374,20 +382,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float x1 = fmaf(__uint_as_float(sr[32 * ck + c + 1]), p.scale_log2, -ref);
               float2 pv;
               pk[c / 2] = exp2_pack<T>(x0, x1, pv);
-              sum += pv.x + pv.y;
+              sp[(c >> 1) & 7] += pv.x + pv.y;
             }
             tmem_st16(scol + 16 * ck, pk);
           }
         }
+        const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         l_run = l_run * alpha + sum;
         m_run = m_use;
-        // all earlier PVs into this tile's O must be complete (before a rescale, and so that
-        // this group never falls two completions behind)
-        while (od < cnt) {
-          if (!warp_wait(&B.o_done[m], od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
-          ++od;
+        // All earlier PVs into this tile's O must be complete before a rescale. With two M
+        // tiles that is already implied: this tile's previous PV was issued before the QK
+        // whose completion produced S, so exactly cnt PVs have completed (od = cnt keeps the
+        // phase count exact for the epilogue's wait). With one tile, wait for it.
+        if (NM == 2) {
+          od = cnt;
+        } else {
+          while (od < cnt) {
+            if (!warp_wait(&B.o_done[m], od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+            ++od;
+          }
+          if (!ok) break;
         }
-        if (!ok) break;
         if (rescale && j > 0) {
 #pragma unroll 1
           for (int cc = 0; cc < kD; cc += 32) {
