@@ -261,6 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kk > 0 ? 1u : 0u);
           }
           umma_commit(&B.s_full[z]);
+          // Q is not read after the unit's last QK: release it so the next unit's Q loads
+          // while this unit's last PVs and epilogue run.
+          if (jl == NJ - 1) umma_commit(&B.q_empty);
           return true;
         };
         if (!qk(0) || (NJ > 1 && !qk(1))) { ok = false; break; }
@@ -284,7 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         kvc = kv_first + steps;
-        umma_commit(&B.q_empty);
         J += NJ;
         ++uc;
       }
