@@ -11,7 +11,8 @@ The same run measures the other rows of the hot path on their own workloads (BSR
 tiny BSR, the MLA prologue and sparse FP8 decode, long-context split-KV decode) and
 reports them under "rows". Inputs are synthetic (seeded) and resident in HBM before the
 timed region; the headline's KV (about 0.6 GB) is larger than L2, the smaller rows flush
-L2 with a 512 MB write between timed iterations.
+L2 between timed iterations (a 512 MiB write, then a 256 MiB read so that the write-back
+of the flushed lines is not charged to the timed kernel).
 
 --impl reference times the float64 CPU oracle (the only reference implementation of
 this method here) on the host cores, on a bounded sample of the same workload.
@@ -152,13 +153,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------
 
 _flush_buf = None
+_clean_buf = None
 
 
 def flush_l2():
-    global _flush_buf
+    """Write 512 MiB (4x the 129 MB L2), then read 256 MiB of another buffer: the read
+    evicts the written lines, so their write-back to HBM happens here and not inside the
+    timed kernel that follows."""
+    global _flush_buf, _clean_buf
     if _flush_buf is None:
         _flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        _clean_buf = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
     _flush_buf.fill_(1)
+    _clean_buf.sum()
 
 
 def time_iters(fn, iters, warmup, flush=False):

@@ -5,11 +5,16 @@
 // contiguous halves or adjacent even/odd pairs; Q_fp8 = cast(Q * quant_scale_q),
 // K_fp8 = cast(K * quant_scale_kv); outputs may be strided slices of 576-byte rows).
 //
-// GB300 design: a pure HBM stream (2.0 bytes in per byte out, plus the cache row). One warp
-// per row: each lane loads 32 bytes of NoPE (two 16-byte loads) and writes 16 bytes of E4M3,
-// and 4 bytes of the RoPE tail, exchanging rotation partners with one shuffle (neox) or
-// none (even/odd). cvt.rn.satfinite.e4m3x2.f32 does the cast (RNE, saturating to +-448).
+// GB300 design: a pure HBM stream (2.0 bytes in per byte out, plus the cache row). A warp
+// handles two rows per iteration and issues every load of both (row data, positions, then
+// the cos/sin values the positions select) before it converts anything, so the position ->
+// cache dependency costs one latency per two rows. Each lane loads 32 bytes of NoPE (two
+// 16-byte loads) and writes 16 bytes of E4M3, and 4 bytes of the RoPE tail, exchanging
+// rotation partners with one shuffle (neox) or none (even/odd).
+// cvt.rn.satfinite.e4m3x2.f32 does the cast (RNE, saturating to +-448).
 #include <cuda_fp8.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -56,17 +61,110 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
       __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
+// Streaming loads: each input byte is read once, so keep it out of L1.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// One row's inputs, loaded before any of them is used so that a warp keeps the loads of
+// two rows in flight at once (the row data does not wait for the position, and only the
+// cos/sin values depend on it).
+struct RowIn {
+  uint4 x0, x1;      // this lane's 16 NoPE values
+  uint32_t rw;       // this lane's 2 RoPE values
+  float c0, c1, s0, s1;
+  bool valid;        // position inside [0, max_seq_len)
+};
+
 template <bool kNeox, typename PosT, typename CacheT>
-__device__ __forceinline__ void rope_row(const __nv_bfloat16* rope, const __nv_bfloat16* nope,
-                                         uint8_t* rope_out, uint8_t* nope_out, int64_t pos,
-                                         const CacheT* cache, float scale, int lane) {
-  // NoPE: 512 bf16 = 1024 bytes; lane owns elements [16*lane, 16*lane + 16).
+__device__ __forceinline__ void row_ptrs(const RopeParams& p, int64_t r, int64_t q_rows,
+                                         const __nv_bfloat16*& rope, const __nv_bfloat16*& nope,
+                                         uint8_t*& rope_out, uint8_t*& nope_out, int64_t& pos,
+                                         float& scale) {
+  if (r < q_rows) {
+    const int64_t t = r / p.heads;
+    const int h = int(r % p.heads);
+    rope = p.q_rope + t * p.qr_s0 + h * p.qr_s1;
+    nope = p.q_nope + t * p.qn_s0 + h * p.qn_s1;
+    rope_out = p.q_rope_out + t * p.qro_s0 + h * p.qro_s1;
+    nope_out = p.q_nope_out + t * p.qno_s0 + h * p.qno_s1;
+    pos = int64_t(__ldg(static_cast<const PosT*>(p.pos_q) + t));
+    scale = p.scale_q;
+  } else {
+    const int64_t t = r - q_rows;
+    rope = p.k_rope + t * p.kr_s;
+    nope = p.k_nope + t * p.kn_s;
+    rope_out = p.k_rope_out + t * p.kro_s;
+    nope_out = p.k_nope_out + t * p.kno_s;
+    pos = int64_t(__ldg(static_cast<const PosT*>(p.pos_k) + t));
+    scale = p.scale_kv;
+  }
+}
+
+template <bool kNeox, typename CacheT>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* rope, const __nv_bfloat16* nope,
+                                         int64_t pos, int64_t max_seq_len, const CacheT* cache,
+                                         int lane, RowIn& in) {
   const uint4* src = reinterpret_cast<const uint4*>(nope) + 2 * lane;
-  const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
-  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  in.x0 = ld_stream16(src);
+  in.x1 = ld_stream16(src + 1);
+  in.rw = ld_stream4(reinterpret_cast<const unsigned int*>(rope) + lane);
+  in.valid = pos >= 0 && pos < max_seq_len;
+  const int64_t pc = in.valid ? pos : 0;  // loads stay in bounds; the row is skipped later
+  const int i0 = kNeox ? ((2 * lane) & 31) : lane;  // frequency index of the first element
+  auto cs = [&](int i) -> float {
+    if constexpr (sizeof(CacheT) == 4) {
+      return __ldg(reinterpret_cast<const float*>(cache) + pc * 64 + i);
+    } else {
+      const uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(cache) + pc * 64 + i);
+      return __uint_as_float(uint32_t(b) << 16);
+    }
+  };
+  in.c0 = cs(i0);
+  in.s0 = cs(32 + i0);
+  if (kNeox) {
+    in.c1 = cs(i0 + 1);
+    in.s1 = cs(32 + i0 + 1);
+  }
+}
+
+template <bool kNeox>
+__device__ __forceinline__ void store_row(const RowIn& in, uint8_t* rope_out, uint8_t* nope_out,
+                                          float scale, int lane, const StatusArgs& st) {
+  // The neox partner exchange is a warp shuffle, so it runs before the validity test.
+  const float e0 = bf16_lo(in.rw), e1 = bf16_hi(in.rw);
+  float r0, r1;
+  if (kNeox) {
+    // Pair i = (i, i + 32): lanes 0-15 hold the first halves, lanes 16-31 the partners.
+    const float p0 = __shfl_xor_sync(0xffffffffu, e0, 16);
+    const float p1 = __shfl_xor_sync(0xffffffffu, e1, 16);
+    if (lane < 16) {
+      r0 = __fsub_rn(__fmul_rn(e0, in.c0), __fmul_rn(p0, in.s0));
+      r1 = __fsub_rn(__fmul_rn(e1, in.c1), __fmul_rn(p1, in.s1));
+    } else {
+      r0 = __fadd_rn(__fmul_rn(e0, in.c0), __fmul_rn(p0, in.s0));
+      r1 = __fadd_rn(__fmul_rn(e1, in.c1), __fmul_rn(p1, in.s1));
+    }
+  } else {
+    r0 = __fsub_rn(__fmul_rn(e0, in.c0), __fmul_rn(e1, in.s0));
+    r1 = __fadd_rn(__fmul_rn(e1, in.c0), __fmul_rn(e0, in.s0));
+  }
+  if (!in.valid) {
+    if (lane == 0) record_error(st, BSKV_ERR_DEVICE_INDEX);
+    return;
+  }
+  const uint32_t w[8] = {in.x0.x, in.x0.y, in.x0.z, in.x0.w, in.x1.x, in.x1.y, in.x1.z, in.x1.w};
   uint32_t packed[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -76,96 +174,77 @@ __device__ __forceinline__ void rope_row(const __nv_bfloat16* rope, const __nv_b
   }
   *reinterpret_cast<uint4*>(nope_out + 16 * lane) =
       make_uint4(packed[0], packed[1], packed[2], packed[3]);
-
-  // RoPE tail: lane owns elements 2*lane and 2*lane + 1.
-  const uint32_t rw = __ldg(reinterpret_cast<const unsigned int*>(rope) + lane);
-  const float e0 = bf16_lo(rw), e1 = bf16_hi(rw);
-  float c0, c1, s0, s1;
-  const int i0 = kNeox ? ((2 * lane) & 31) : lane;  // frequency index of the first element
-  auto cs = [&](int i) -> float {
-    if constexpr (sizeof(CacheT) == 4) {
-      return __ldg(reinterpret_cast<const float*>(cache) + pos * 64 + i);
-    } else {
-      const uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(cache) + pos * 64 + i);
-      return __uint_as_float(uint32_t(b) << 16);
-    }
-  };
-  float r0, r1;
-  if (kNeox) {
-    // Pair i = (i, i + 32): lanes 0-15 hold the first halves, lanes 16-31 the partners.
-    c0 = cs(i0); c1 = cs(i0 + 1); s0 = cs(32 + i0); s1 = cs(32 + i0 + 1);
-    const float p0 = __shfl_xor_sync(0xffffffffu, e0, 16);
-    const float p1 = __shfl_xor_sync(0xffffffffu, e1, 16);
-    if (lane < 16) {
-      r0 = __fsub_rn(__fmul_rn(e0, c0), __fmul_rn(p0, s0));
-      r1 = __fsub_rn(__fmul_rn(e1, c1), __fmul_rn(p1, s1));
-    } else {
-      r0 = __fadd_rn(__fmul_rn(e0, c0), __fmul_rn(p0, s0));
-      r1 = __fadd_rn(__fmul_rn(e1, c1), __fmul_rn(p1, s1));
-    }
-  } else {
-    c0 = cs(i0); s0 = cs(32 + i0);
-    r0 = __fsub_rn(__fmul_rn(e0, c0), __fmul_rn(e1, s0));
-    r1 = __fadd_rn(__fmul_rn(e1, c0), __fmul_rn(e0, s0));
-  }
-  const uint16_t out = cvt_e4m3x2(__fmul_rn(r0, scale), __fmul_rn(r1, scale));
-  *reinterpret_cast<uint16_t*>(rope_out + 2 * lane) = out;
+  *reinterpret_cast<uint16_t*>(rope_out + 2 * lane) =
+      cvt_e4m3x2(__fmul_rn(r0, scale), __fmul_rn(r1, scale));
 }
 
 template <bool kNeox, typename PosT, typename CacheT>
 __global__ void __launch_bounds__(256) rope_quant_kernel(const RopeParams p) {
   const int lane = threadIdx.x & 31;
-  const int64_t warps_total = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t W = (int64_t(gridDim.x) * blockDim.x) >> 5;
   const int64_t q_rows = p.q_rope ? p.nnz_q * p.heads : 0;
-  const int64_t k_rows = p.k_rope ? p.nnz_k : 0;
+  const int64_t total = q_rows + (p.k_rope ? p.nnz_k : 0);
   const CacheT* cache = static_cast<const CacheT*>(p.cos_sin);
-  for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < q_rows + k_rows;
-       r += warps_total) {
-    if (r < q_rows) {
-      const int64_t t = r / p.heads;
-      const int h = int(r % p.heads);
-      const int64_t pos = int64_t(static_cast<const PosT*>(p.pos_q)[t]);
-      if (pos < 0 || pos >= p.max_seq_len) {
-        if (lane == 0) record_error(p.st, BSKV_ERR_DEVICE_INDEX);
-        continue;
-      }
-      rope_row<kNeox, PosT, CacheT>(p.q_rope + t * p.qr_s0 + h * p.qr_s1,
-                                    p.q_nope + t * p.qn_s0 + h * p.qn_s1,
-                                    p.q_rope_out + t * p.qro_s0 + h * p.qro_s1,
-                                    p.q_nope_out + t * p.qno_s0 + h * p.qno_s1, pos, cache,
-                                    p.scale_q, lane);
-    } else {
-      const int64_t t = r - q_rows;
-      const int64_t pos = int64_t(static_cast<const PosT*>(p.pos_k)[t]);
-      if (pos < 0 || pos >= p.max_seq_len) {
-        if (lane == 0) record_error(p.st, BSKV_ERR_DEVICE_INDEX);
-        continue;
-      }
-      rope_row<kNeox, PosT, CacheT>(p.k_rope + t * p.kr_s, p.k_nope + t * p.kn_s,
-                                    p.k_rope_out + t * p.kro_s, p.k_nope_out + t * p.kno_s, pos,
-                                    cache, p.scale_kv, lane);
-    }
+  // Two rows per warp per iteration (rows ra and ra + W), all loads issued before use.
+  for (int64_t ra = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; ra < total; ra += 2 * W) {
+    const int64_t rb = ra + W;
+    const bool has_b = rb < total;
+    const __nv_bfloat16 *rope_a, *nope_a, *rope_b, *nope_b;
+    uint8_t *ro_a, *no_a, *ro_b, *no_b;
+    int64_t pos_a, pos_b;
+    float sc_a, sc_b;
+    row_ptrs<kNeox, PosT, CacheT>(p, ra, q_rows, rope_a, nope_a, ro_a, no_a, pos_a, sc_a);
+    row_ptrs<kNeox, PosT, CacheT>(p, has_b ? rb : ra, q_rows, rope_b, nope_b, ro_b, no_b, pos_b, sc_b);
+    RowIn a, b;
+    load_row<kNeox, CacheT>(rope_a, nope_a, pos_a, p.max_seq_len, cache, lane, a);
+    load_row<kNeox, CacheT>(rope_b, nope_b, pos_b, p.max_seq_len, cache, lane, b);
+    store_row<kNeox>(a, ro_a, no_a, sc_a, lane, p.st);
+    if (has_b) store_row<kNeox>(b, ro_b, no_b, sc_b, lane, p.st);
   }
+}
+
+// Blocks of this kernel resident on one SM times the SM count, cached per device.
+template <typename Kernel>
+bskv_status resident_grid(Kernel kernel, int threads, int* out) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (bskv_status s = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return s;
+  const int slot = dev < 64 ? dev : 63;
+  int v = dev < 64 ? cache[slot].load(std::memory_order_relaxed) : 0;
+  if (v == 0) {
+    int sms = 0, occ = 0;
+    if (bskv_status s = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"))
+      return s;
+    if (bskv_status s = cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0), "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
+      return s;
+    v = sms * (occ > 0 ? occ : 1);
+    if (dev < 64) cache[slot].store(v, std::memory_order_relaxed);
+  }
+  *out = v;
+  return BSKV_OK;
+}
+
+template <bool kNeox, typename PosT, typename CacheT>
+bskv_status launch_rope_t(const RopeParams& p, int64_t rows, cudaStream_t st) {
+  auto kernel = rope_quant_kernel<kNeox, PosT, CacheT>;
+  int resident = 0;
+  if (bskv_status s = resident_grid(kernel, 256, &resident)) return s;
+  // One wave of resident blocks; fewer when there are fewer than one row per warp.
+  const int64_t want = (rows + 7) / 8;
+  const int blocks = int(want < resident ? want : resident);
+  kernel<<<blocks, 256, 0, st>>>(p);
+  return cuda_check(cudaGetLastError(), "rope_quantize_fp8 launch");
 }
 
 template <bool kNeox>
 bskv_status launch_rope(const RopeParams& p, int pos_dtype, int cache_dtype, cudaStream_t st) {
-  int dev = 0, sms = 0;
-  if (bskv_status s = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return s;
-  if (bskv_status s = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"))
-    return s;
   const int64_t rows = (p.q_rope ? p.nnz_q * p.heads : 0) + (p.k_rope ? p.nnz_k : 0);
   if (rows == 0) return BSKV_OK;
-  const int64_t want = (rows + 7) / 8;
-  const int blocks = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-  if (pos_dtype == BSKV_INT32) {
-    if (cache_dtype == BSKV_FP32) rope_quant_kernel<kNeox, int32_t, float><<<blocks, 256, 0, st>>>(p);
-    else rope_quant_kernel<kNeox, int32_t, __nv_bfloat16><<<blocks, 256, 0, st>>>(p);
-  } else {
-    if (cache_dtype == BSKV_FP32) rope_quant_kernel<kNeox, int64_t, float><<<blocks, 256, 0, st>>>(p);
-    else rope_quant_kernel<kNeox, int64_t, __nv_bfloat16><<<blocks, 256, 0, st>>>(p);
-  }
-  return cuda_check(cudaGetLastError(), "rope_quantize_fp8 launch");
+  if (pos_dtype == BSKV_INT32)
+    return cache_dtype == BSKV_FP32 ? launch_rope_t<kNeox, int32_t, float>(p, rows, st)
+                                    : launch_rope_t<kNeox, int32_t, __nv_bfloat16>(p, rows, st);
+  return cache_dtype == BSKV_FP32 ? launch_rope_t<kNeox, int64_t, float>(p, rows, st)
+                                  : launch_rope_t<kNeox, int64_t, __nv_bfloat16>(p, rows, st);
 }
 
 }  // namespace
