@@ -4,9 +4,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--r
 
 One JSON line on rank 0. The headline workload is the paged GQA batch decode (batch 64,
 32 query / 8 kv heads, head_dim 128, bf16, page_size 16, kv lengths U[512, 4096], pages
-randomly permuted in a shared pool): one step = the decode attention kernel plus the
-split-KV merge over the whole batch (the plan is made once, as a serving engine does per
-decode step, and timed apart). The metric is the KV bytes the method must read per second.
+randomly permuted in a shared pool): one step = bskv_run_decode over the whole batch, one
+kernel launch that computes the attention and merges the split-KV partial states (the
+plan is made once, as a serving engine does per decode step, and timed apart). The metric is the KV bytes the method must read per second.
 The same run measures the other rows of the hot path on their own workloads (BSR prefill,
 tiny BSR, the MLA prologue and sparse FP8 decode, long-context split-KV decode) and
 reports them under "rows". Inputs are synthetic (seeded) and resident in HBM before the
@@ -224,6 +224,15 @@ def decode_kv_bytes(d):
     return int(d["kv_lens"].to(torch.int64).sum()) * d["num_kv_heads"] * d["head_dim"] * 2 * 2
 
 
+def decode_launches(meta):
+    """Kernels one bskv_run_decode launches for a plan (metadata header: merges at word 6,
+    grid at 13, merge-section offset at 10): the attention kernel, plus the merge kernel
+    when no worker exists or some unit has more than 8 pieces."""
+    nm, grid, off = meta[6], meta[13], meta[10]
+    most = max([meta[off + 3 * i + 2] for i in range(nm)] or [0])
+    return (1 if grid > 0 else 0) + (1 if nm > 0 and (grid == 0 or most > 8) else 0)
+
+
 def bench_decode(bskv, synth, name, steps, warmup, dist, sampler=None, headline=False,
                  **over):
     """Paged decode (+ merge) on one of the decode workloads."""
@@ -237,23 +246,21 @@ def bench_decode(bskv, synth, name, steps, warmup, dist, sampler=None, headline=
     q, kv = d["q"], d["kv_cache"]
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
-    nmerge = plan.metadata()[6]
+    meta = plan.metadata()
 
     def step(ev=None):
+        # the attention kernel, which merges split units itself unless they have many pieces
         if ev is not None:
             ev[0].record()
-        bskv.bskv_run_decode_partial(plan, q, kv, out=out, lse=lse)
+        bskv.bskv_run_decode(plan, q, kv, out=out, lse=lse)
         if ev is not None:
             ev[1].record()
-        bskv.bskv_decode_merge(plan, out, lse)
-        if ev is not None:
-            ev[2].record()
 
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     barrier(dist)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     if sampler:
         sampler.start()
     torch.cuda.synchronize()
@@ -263,14 +270,14 @@ def bench_decode(bskv, synth, name, steps, warmup, dist, sampler=None, headline=
     torch.cuda.synchronize()
     barrier(dist)
     clocks = sampler.stop() if sampler else None
-    total_ms = evs[0][0].elapsed_time(evs[-1][2])
+    total_ms = evs[0][0].elapsed_time(evs[-1][1])
     kern_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    merge_ms = [e[1].elapsed_time(e[2]) for e in evs]
     nbytes = decode_kv_bytes(d)
     res = dict(workload=name, kv_bytes=nbytes, plan_us=plan_us, total_ms=total_ms,
                ms_per_step=total_ms / steps, decode_kernel=summary(kern_ms),
-               merge_kernel=summary(merge_ms), launches_per_step=1 + (1 if nmerge else 0),
-               clocks=clocks)
+               variant="page-major (all kv heads of a page per CTA)" if meta[15] == 1
+               else "per kv head (one worker per warp)",
+               split_units=meta[6], launches_per_step=decode_launches(meta), clocks=clocks)
     res["gbs_step"] = nbytes / (res["ms_per_step"] * 1e-3) / 1e9
     res["gbs_kernel"] = nbytes / (statistics.mean(kern_ms) * 1e-3) / 1e9
     del d, kv, q
@@ -471,8 +478,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
                     help="comma list of extra rows: bsr_prefill,bsr_tiny,mla,split,e2e,cpu or all/none")
@@ -538,14 +545,14 @@ def main():
                    "parallelism": "replicas x%d" % args.gpus if args.gpus > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src + " (hbm_gbs, burst)",
-                     "kernel": "decode_kernel", "bytes_per_launch": head["kv_bytes"],
-                     "traffic": profile_traffic("decode_kernel_paged_decode.txt",
+                     "kernel": "decode_group_kernel", "bytes_per_launch": head["kv_bytes"],
+                     "traffic": profile_traffic("decode_group_kernel_paged_decode.txt",
                                                 ["decode.cu", "common.cuh"])},
         "clocks": clocks,
         "gpu_launches": head["launches_per_step"] * args.steps,
         "plan_us": head["plan_us"],
-        "step_breakdown_us": {"decode_kernel": head["decode_kernel"]["mean_us"],
-                              "merge_kernel": head["merge_kernel"]["mean_us"]},
+        "step_breakdown_us": {"decode_kernel_with_fused_merge": head["decode_kernel"]["mean_us"]},
+        "decode_variant": head["variant"],
         "device_status": bskv.STATUS.get(status, status),
         "e2e": e2e,
         "cpu_baseline": cpu,

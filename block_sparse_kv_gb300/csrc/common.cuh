@@ -123,6 +123,18 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool pre
   return out != 0;
 }
 
+// Plain named barrier over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 16-byte store to shared memory at a shared-window address.
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------------------
 // bulk and tensor copies (TMA)
 // ---------------------------------------------------------------------------------------
@@ -174,6 +186,35 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, i
       "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
       : "memory");
+}
+
+// L2 policy for data read exactly once (a stream larger than L2): evict it first, so it
+// does not displace data that is read again soon.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load_5d_hint(void* dst, const CUtensorMap* map, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, int32_t c4,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Device-scope atomic add with acquire-release semantics (returns the old value): the
+// writes this thread made or observed before it (a __syncwarp orders the warp's lanes'
+// writes before lane 0's) are visible to whoever observes the new value, and the caller
+// sees every write released by earlier adds.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

@@ -7,14 +7,22 @@
 // cascade.rst (merge_state / merge_states).
 //
 // GB300 design. Decode reads every K/V byte once (O(1) flop per byte), so the kernel is an
-// HBM stream: one CTA per SM with 8 independent worker warps. Each warp owns a contiguous
-// range of 16-token tiles (the plan's linear split-KV partition) and a private 3-stage ring
-// in shared memory filled by TMA tensor copies (128-byte swizzle) straight from the pages;
-// lane 0 issues the copies, the whole warp waits on the stage's mbarrier. The up-to-16
-// query heads that share a kv head form the M=16 rows of mma.sync m16n8k16 (bf16/fp16 in,
-// fp32 accumulate): S = Q K^T, online softmax in registers (exp2), O += P V with P reused
-// from the S accumulators. A unit that is split over several workers writes its normalised
-// partial output and LSE to the float workspace; the merge kernel then combines them.
+// HBM stream, and its efficiency follows from how large the contiguous pieces it asks
+// HBM for are. Two variants, chosen by the plan:
+//   * group (pages of 8 or 16 tokens): one CTA per SM, a producer warp and one consumer
+//     warp per kv head of a group of up to 8. Each 16-token tile is copied by TMA for all
+//     heads of the group at once, so with the contiguous layout a page's K (and V) for 8
+//     heads is one 32 KB piece instead of eight 4 KB ones. A 3-stage ring (64 KB stages
+//     for 8 heads of 128 dims) holds about 128 KB in flight per SM.
+//   * warp (larger pages, or head counts that do not group): 8 independent worker warps
+//     per CTA, each with a private 3-stage ring over its own (request, kv head) range;
+//     a page of 64 tokens is already a 16 KB piece per head.
+// In both, the up-to-16 query heads that share a kv head form the M=16 rows of mma.sync
+// m16n8k16 (bf16/fp16 in, fp32 accumulate): S = Q K^T, online softmax in registers
+// (exp2), O += P V with P reused from the S accumulators. The work is the plan's linear
+// split-KV partition; a unit split over several workers leaves normalised partial states
+// and LSE in the float workspace, and the worker that finishes the unit's last piece
+// (an atomic counter per unit in the int workspace) merges them in the same launch.
 #include <math.h>
 
 #include <mutex>
@@ -32,6 +40,11 @@ constexpr int kTile = kDecodeTile;  // 16 tokens per stage
 constexpr int kStages = 3;
 constexpr int kWarps = kDecodeWarps;
 constexpr int kPanelBytes = kTile * 128;  // 16 rows x 64 elements of 16 bits
+constexpr int kGroupThreads = (kDecodeGroupMax + 1) * 32;  // 8 consumer warps + 1 producer
+constexpr uint32_t kGroupRingBytes = 196608;                // ring budget of the group kernel
+// The group kernel's 9 warps put 3 on one SM sub-partition, which caps a thread at 168
+// registers; its merges keep fewer loads in flight than the 8-warp kernels' (4 x 4).
+constexpr int kGroupMergeSlots = 2, kGroupMergeRows = 2;
 
 struct DecodeParams {
   const int32_t* meta;
@@ -42,7 +55,10 @@ struct DecodeParams {
   float* lse;
   float* ws_o;
   float* ws_lse;
+  int* counters;  // non-null: the last worker to finish a split unit merges it
   int num_kv_heads, group, page_size, num_qo_heads;
+  int heads_per_unit;  // kv heads of one unit: 1 (warp variant) or G (group variant)
+  int stages;          // ring depth of the group variant
   float scale_log2;
   StatusArgs st;
 };
@@ -51,6 +67,275 @@ template <int D>
 __host__ __device__ constexpr int tile_bytes() {
   return (D / 64) * kPanelBytes;
 }
+
+// Where one head's 16 K and V rows of a stage sit in shared memory. Row r of 64-column
+// half hf starts at base + hf * half + (r / 8) * blk8 + (r % 8) * 128; every group of 8
+// rows starts on a 1024-byte boundary, so the 128-byte swizzle of the TMA copy is
+// chunk ^ (r % 8).
+struct KvRows {
+  uint32_t k, v, half, blk8;
+};
+
+__device__ __forceinline__ uint32_t kv_row(const KvRows& g, uint32_t base, int row, int hf) {
+  return base + hf * g.half + (row >> 3) * g.blk8 + (row & 7) * 128;
+}
+
+// One 16-token tile for the (up to 16) query heads of one kv head: S = Q K^T on the
+// tensor cores (mma.sync m16n8k16), online softmax in base 2 on rows r0 = lane/4 and
+// r1 = r0 + 8, O += P V with P taken from the S accumulators.
+template <typename T, int D>
+__device__ __forceinline__ void decode_tile(const KvRows& kv, int valid, float scale_log2,
+                                            int lane, const uint32_t (&qa)[D / 16][4],
+                                            float (&o)[D / 8][4], float& m0, float& m1,
+                                            float& l0, float& l1) {
+  using Mma = MmaOp<T>;
+  const int cq = lane & 3;
+  if (valid < kTile) {
+    // Rows past the unit's end hold whatever the pages hold there (or stale data); zero
+    // the V rows so that 0 * garbage cannot reach the output.
+    const int per_half = (kTile - valid) * 8;
+    for (int i = lane; i < per_half * (D / 64); i += 32) {
+      const int hf = i / per_half, rem = i % per_half;
+      sts128(kv_row(kv, kv.v, valid + rem / 8, hf) + (rem % 8) * 16, make_uint4(0, 0, 0, 0));
+    }
+    __syncwarp();
+  }
+  float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  {
+    const int mi = lane >> 3;
+    const int trow = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int dim = kk * 16 + (mi & 1) * 8;
+      const uint32_t addr =
+          kv_row(kv, kv.k, trow, dim / 64) + ((((dim % 64) / 8) ^ (trow & 7)) << 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(addr, b0, b1, b2, b3);
+      Mma::run(s[0], qa[kk], b0, b1);
+      Mma::run(s[1], qa[kk], b2, b3);
+    }
+  }
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int col = nt * 8 + 2 * cq + (e & 1);
+      const float x = s[nt][e] * scale_log2;
+      s[nt][e] = col < valid ? x : -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+    mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
+  m0 = mn0;
+  m1 = mn1;
+  float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    s[nt][0] = fast_exp2(s[nt][0] - mn0);
+    s[nt][1] = fast_exp2(s[nt][1] - mn0);
+    s[nt][2] = fast_exp2(s[nt][2] - mn1);
+    s[nt][3] = fast_exp2(s[nt][3] - mn1);
+    ps0 += s[nt][0] + s[nt][1];
+    ps1 += s[nt][2] + s[nt][3];
+  }
+  l0 = l0 * a0 + ps0;
+  l1 = l1 * a1 + ps1;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    o[n][0] *= a0;
+    o[n][1] *= a0;
+    o[n][2] *= a1;
+    o[n][3] *= a1;
+  }
+  uint32_t pa[4];
+  pa[0] = Mma::pack(s[0][0], s[0][1]);
+  pa[1] = Mma::pack(s[0][2], s[0][3]);
+  pa[2] = Mma::pack(s[1][0], s[1][1]);
+  pa[3] = Mma::pack(s[1][2], s[1][3]);
+  {
+    const int mi = lane >> 3;
+    const int trow = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int dd = 0; dd < D / 16; ++dd) {
+      const int dim = dd * 16 + (mi >> 1) * 8;
+      const uint32_t addr =
+          kv_row(kv, kv.v, trow, dim / 64) + ((((dim % 64) / 8) ^ (trow & 7)) << 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(addr, b0, b1, b2, b3);
+      Mma::run(o[2 * dd], pa, b0, b1);
+      Mma::run(o[2 * dd + 1], pa, b2, b3);
+    }
+  }
+}
+
+// Query rows r0, r1 (< g) of kv head `kvh` of request b into the A fragments.
+template <typename T, int D>
+__device__ __forceinline__ void load_q(const DecodeParams& p, int b, int kvh, int lane,
+                                       uint32_t (&qa)[D / 16][4]) {
+  const int g = p.group, r0 = lane >> 2, r1 = r0 + 8, cq = lane & 3;
+  const T* qb = static_cast<const T*>(p.q) + b * p.q_s0 + int64_t(kvh) * g * p.q_s1;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int d0 = kk * 16 + 2 * cq;
+    qa[kk][0] = r0 < g ? *reinterpret_cast<const uint32_t*>(qb + r0 * p.q_s1 + d0) : 0u;
+    qa[kk][1] = r1 < g ? *reinterpret_cast<const uint32_t*>(qb + r1 * p.q_s1 + d0) : 0u;
+    qa[kk][2] = r0 < g ? *reinterpret_cast<const uint32_t*>(qb + r0 * p.q_s1 + d0 + 8) : 0u;
+    qa[kk][3] = r1 < g ? *reinterpret_cast<const uint32_t*>(qb + r1 * p.q_s1 + d0 + 8) : 0u;
+  }
+}
+
+// Normalise a finished chunk of kv head `kvh` and write it: straight to out/lse when the
+// unit is one chunk (slot < 0), else as partial state row (slot, row0 + r).
+template <typename T, int D>
+__device__ __forceinline__ void finish_chunk(const DecodeParams& p, int b, int kvh, int slot,
+                                             int slot_rows, int row0, int lane,
+                                             const float (&o)[D / 8][4], float m0, float m1,
+                                             float l0, float l1) {
+  using Mma = MmaOp<T>;
+  const int g = p.group, r0 = lane >> 2, r1 = r0 + 8, cq = lane & 3;
+  float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+  lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+  float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+  lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+  const float inv0 = 1.f / lt0, inv1 = 1.f / lt1;
+  const float lse0 = (m0 + __log2f(lt0)) * kLn2, lse1 = (m1 + __log2f(lt1)) * kLn2;
+  if (slot < 0) {
+    T* ob = static_cast<T*>(p.out) + b * p.o_s0 + int64_t(kvh) * g * p.o_s1;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      const int d = n * 8 + 2 * cq;
+      if (r0 < g)
+        *reinterpret_cast<uint32_t*>(ob + r0 * p.o_s1 + d) = Mma::pack(o[n][0] * inv0, o[n][1] * inv0);
+      if (r1 < g)
+        *reinterpret_cast<uint32_t*>(ob + r1 * p.o_s1 + d) = Mma::pack(o[n][2] * inv1, o[n][3] * inv1);
+    }
+    if (p.lse && cq == 0) {
+      float* lb = p.lse + int64_t(b) * p.num_qo_heads + kvh * g;
+      if (r0 < g) lb[r0] = lse0;
+      if (r1 < g) lb[r1] = lse1;
+    }
+  } else {
+    const int64_t base = int64_t(slot) * slot_rows + row0;
+    float* wo = p.ws_o + base * D;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      const int d = n * 8 + 2 * cq;
+      if (r0 < g) *reinterpret_cast<float2*>(wo + r0 * D + d) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
+      if (r1 < g) *reinterpret_cast<float2*>(wo + r1 * D + d) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
+    }
+    if (cq == 0) {
+      if (r0 < g) p.ws_lse[base + r0] = lse0;
+      if (r1 < g) p.ws_lse[base + r1] = lse1;
+    }
+  }
+}
+
+// Merge `count` partial states of output rows row0..row0+nrows-1 (of slots
+// first..first+count-1, slot_rows rows per slot) into out0 + r * out_stride and lse0[r];
+// count == 0 writes zeros and -inf. One warp; a lane covers 4 values of every (128 / D)-th
+// row, NI rows (2 NI for D = 64) per pass. The slots are loaded B at a time (all in flight
+// together) and combined one by one in slot order (the result depends on neither B nor NI):
+//   m' = max(m, lse_c), s = exp(m - m'), w = exp(lse_c - m'),
+//   l' = l s + w, acc' = acc s + w o_c;  out = acc / l, lse = m + log(l),
+// the log-sum-exp merge of attention states. Partials written by other SMs in the same
+// launch are read through L2 (ld.global.cg).
+template <typename T, int D, int B = 4, int NI = 4>
+__device__ __forceinline__ void merge_rows(int lane, const float* ws_o, const float* ws_lse,
+                                           int first, int count, int slot_rows, int row0,
+                                           int nrows, T* out0, int64_t out_stride, float* lse0) {
+  constexpr int RS = 128 / D;  // rows covered by one pass of the warp
+  const int dl = (lane * 4) % D, rl = (lane * 4) / D;
+  for (int rb = 0; rb < nrows; rb += NI * RS) {
+    float m[NI], tot[NI];
+    float4 acc[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      m[i] = -INFINITY;
+      tot[i] = 0.f;
+      acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int c0 = 0; c0 < count; c0 += B) {
+      float bl[B][NI];
+      float4 bx[B][NI];
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        const int64_t base = int64_t(first + c0 + j) * slot_rows + row0 + rb + rl;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          if (c0 + j < count && rb + rl + RS * i < nrows) {
+            bl[j][i] = __ldcg(ws_lse + base + RS * i);
+            bx[j][i] = __ldcg(reinterpret_cast<const float4*>(ws_o + (base + RS * i) * D + dl));
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          if (c0 + j >= count || rb + rl + RS * i >= nrows) continue;
+          const float mn = fmaxf(m[i], bl[j][i]);
+          const float sc = m[i] == -INFINITY ? 0.f : expf(m[i] - mn);
+          const float w = expf(bl[j][i] - mn);
+          tot[i] = tot[i] * sc + w;
+          acc[i].x = acc[i].x * sc + w * bx[j][i].x;
+          acc[i].y = acc[i].y * sc + w * bx[j][i].y;
+          acc[i].z = acc[i].z * sc + w * bx[j][i].z;
+          acc[i].w = acc[i].w * sc + w * bx[j][i].w;
+          m[i] = mn;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int r = rb + rl + RS * i;
+      if (r >= nrows) continue;
+      const float inv = count > 0 ? 1.f / tot[i] : 0.f;
+      // two 4-byte stores: output strides need only be multiples of 2 elements
+      uint32_t* dst = reinterpret_cast<uint32_t*>(out0 + r * out_stride + dl);
+      dst[0] = MmaOp<T>::pack(acc[i].x * inv, acc[i].y * inv);
+      dst[1] = MmaOp<T>::pack(acc[i].z * inv, acc[i].w * inv);
+      if (lse0 && dl == 0) lse0[r] = count > 0 ? m[i] + logf(tot[i]) : -INFINITY;
+    }
+  }
+}
+
+// The order in which a worker walks its chunks c0..c1-1: its last chunk first, then the
+// others in order. A unit cut between workers w and w+1 is the last chunk of w and the
+// first of w+1, so both pieces are computed early and its merge is off the kernel's tail.
+__device__ __forceinline__ int chunk_at(int c0, int c1, int k) {
+  return c1 - c0 >= 2 ? (k == 0 ? c1 - 1 : c0 + k - 1) : c0 + k;
+}
+
+// Merge item (unit, first_slot, count) of `unit`; items are sorted by unit.
+__device__ __forceinline__ int find_merge_item(const int32_t* merges, int n, int unit) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (merges[3 * mid] < unit) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Output row h*g + r of unit (b, u): rows of kv head u * heads_per_unit + h.
+template <typename T>
+__device__ __forceinline__ T* out_row(const DecodeParams& p, int b, int head) {
+  return static_cast<T*>(p.out) + b * p.o_s0 + int64_t(head) * p.o_s1;
+}
+__device__ __forceinline__ float* lse_row(const DecodeParams& p, int b, int head) {
+  return p.lse ? p.lse + int64_t(b) * p.num_qo_heads + head : nullptr;
+}
+
+// ---------------------------------------------------------------------------------------
+// warp variant: 8 independent workers per CTA, each with a private TMA ring
+// ---------------------------------------------------------------------------------------
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32, 1)
@@ -72,6 +357,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   if (w >= P) return;
   const int32_t* wptr = hdr + hdr[H_OFF_WORKERS];
   const int4* chunks = reinterpret_cast<const int4*>(hdr + hdr[H_OFF_CHUNKS]);
+  const int32_t* merges = hdr + hdr[H_OFF_MERGES];
+  const int NM = hdr[H_MERGES];
   const int32_t* kv_indptr = hdr + hdr[H_OFF_AUX0];
   const int32_t* kv_indices = hdr + hdr[H_OFF_AUX1];
   const int c0 = wptr[w], c1 = wptr[w + 1];
@@ -88,6 +375,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int box_rows = ps < kTile ? ps : kTile;
   const uint32_t piece_bytes = uint32_t(box_rows) * 128u;
 
+  const uint64_t stream_policy = l2_evict_first_policy();  // KV is read once
   // Issue the TMA copies of tile `t` of chunk `c` into `stage` (lane 0 only).
   auto issue = [&](int stage, int c, int t) {
     const int4 ch = chunks[c];
@@ -104,8 +392,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       mbar_arrive_expect_tx(&bars[stage], bytes);
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
-        tma_load_5d(kdst + hf * kPanelBytes, &kv_map, hf * 64, s, kvh, 0, page, &bars[stage]);
-        tma_load_5d(vdst + hf * kPanelBytes, &kv_map, hf * 64, s, kvh, 1, page, &bars[stage]);
+        tma_load_5d_hint(kdst + hf * kPanelBytes, &kv_map, hf * 64, s, kvh, 0, page, &bars[stage],
+                         stream_policy);
+        tma_load_5d_hint(vdst + hf * kPanelBytes, &kv_map, hf * 64, s, kvh, 1, page, &bars[stage],
+                         stream_policy);
       }
     } else {
       const int npages = kv_indptr[b + 1] - pbase;
@@ -118,10 +408,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         const int page = kv_indices[pbase + first + k];
 #pragma unroll
         for (int hf = 0; hf < D / 64; ++hf) {
-          tma_load_5d(kdst + hf * kPanelBytes + k * piece_bytes, &kv_map, hf * 64, 0, kvh, 0,
-                      page, &bars[stage]);
-          tma_load_5d(vdst + hf * kPanelBytes + k * piece_bytes, &kv_map, hf * 64, 0, kvh, 1,
-                      page, &bars[stage]);
+          tma_load_5d_hint(kdst + hf * kPanelBytes + k * piece_bytes, &kv_map, hf * 64, 0, kvh,
+                           0, page, &bars[stage], stream_policy);
+          tma_load_5d_hint(vdst + hf * kPanelBytes + k * piece_bytes, &kv_map, hf * 64, 0, kvh,
+                           1, page, &bars[stage], stream_policy);
         }
       }
     }
@@ -131,41 +421,44 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     return (ch.z - ch.y + kTile - 1) / kTile;
   };
 
-  // Producer cursor (pc, pt) runs kStages tiles ahead of the consumer cursor (cc, ct).
-  int pc = c0, pt = 0;
-  auto advance = [&](int& c, int& t) {
-    if (++t == ntiles(c)) {
-      ++c;
+  // Fused merge: units without tokens are zero-filled by the workers in turn.
+  if (p.counters) {
+    for (int i = w; i < NM; i += P) {
+      if (merges[3 * i + 2] != 0) continue;
+      const int unit = merges[3 * i], b = unit / Hkv, kvh = unit % Hkv;
+      merge_rows<T, D>(lane, p.ws_o, p.ws_lse, 0, 0, g, 0, g, out_row<T>(p, b, kvh * g), p.o_s1,
+                       lse_row(p, b, kvh * g));
+    }
+  }
+
+  // Producer cursor (pk, pt) runs kStages tiles ahead of the consumer cursor (ck, ct);
+  // k counts chunks in the order chunk_at gives.
+  const int nck = c1 - c0;
+  int pk = 0, pt = 0;
+  auto advance = [&](int& k, int& t) {
+    if (++t == ntiles(chunk_at(c0, c1, k))) {
+      ++k;
       t = 0;
     }
   };
   uint32_t issued = 0, consumed = 0;
-  for (int s = 0; s < kStages && pc < c1; ++s) {
-    if (lane == 0) issue(s, pc, pt);
+  for (int s = 0; s < kStages && pk < nck; ++s) {
+    if (lane == 0) issue(s, chunk_at(c0, c1, pk), pt);
     ++issued;
-    advance(pc, pt);
+    advance(pk, pt);
   }
 
-  using Mma = MmaOp<T>;
-  const int r0 = lane >> 2, r1 = r0 + 8, cq = lane & 3;
   uint32_t qa[D / 16][4];
   float o[D / 8][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   bool ok = true;
-  int cc = c0, ct = 0;
-  while (cc < c1) {
+  int ck = 0, ct = 0;
+  while (ck < nck) {
+    const int cc = chunk_at(c0, c1, ck);
     const int4 ch = chunks[cc];
     const int b = ch.x / Hkv, kvh = ch.x % Hkv;
     if (ct == 0) {
-      const T* qb = static_cast<const T*>(p.q) + b * p.q_s0 + int64_t(kvh) * g * p.q_s1;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int d0 = kk * 16 + 2 * cq;
-        qa[kk][0] = r0 < g ? *reinterpret_cast<const uint32_t*>(qb + r0 * p.q_s1 + d0) : 0u;
-        qa[kk][1] = r1 < g ? *reinterpret_cast<const uint32_t*>(qb + r1 * p.q_s1 + d0) : 0u;
-        qa[kk][2] = r0 < g ? *reinterpret_cast<const uint32_t*>(qb + r0 * p.q_s1 + d0 + 8) : 0u;
-        qa[kk][3] = r1 < g ? *reinterpret_cast<const uint32_t*>(qb + r1 * p.q_s1 + d0 + 8) : 0u;
-      }
+      load_q<T, D>(p, b, kvh, lane, qa);
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
       m0 = m1 = -INFINITY;
@@ -176,150 +469,42 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       ok = false;
       break;
     }
-    uint8_t* kt = ring + stage * kStageBytes;
-    uint8_t* vt = kt + kTileBytes;
+    const uint32_t kt = smem_u32(ring + stage * kStageBytes);
+    const KvRows kv{kt, kt + uint32_t(kTileBytes), uint32_t(kPanelBytes), 1024u};
     const int tok0 = ch.y + ct * kTile;
-    const int valid = min(kTile, ch.z - tok0);
-    if (valid < kTile) {
-      // Rows past the unit's end hold whatever the pages hold there (or stale data);
-      // zero the V rows so that 0 * garbage cannot reach the output.
-      for (int i = lane; i < (kTile - valid) * (D / 64) * 8; i += 32) {
-        const int hf = i / ((kTile - valid) * 8);
-        const int rem = i % ((kTile - valid) * 8);
-        const int row = valid + rem / 8;
-        *reinterpret_cast<uint4*>(vt + hf * kPanelBytes + row * 128 + (rem % 8) * 16) =
-            make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-    }
-    // S = Q K^T over the tile's 16 tokens (two n8 tiles).
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
-      const int mi = lane >> 3;
-      const int trow = (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int dim = kk * 16 + (mi & 1) * 8;
-        const uint32_t addr =
-            smem_u32(kt + (dim / 64) * kPanelBytes) + swz(trow, (dim % 64) / 8, 128);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(addr, b0, b1, b2, b3);
-        Mma::run(s[0], qa[kk], b0, b1);
-        Mma::run(s[1], qa[kk], b2, b3);
-      }
-    }
-    // Online softmax (base 2) on rows r0 and r1.
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = nt * 8 + 2 * cq + (e & 1);
-        const float x = s[nt][e] * p.scale_log2;
-        s[nt][e] = col < valid ? x : -INFINITY;
-      }
-      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = fast_exp2(s[nt][0] - mn0);
-      s[nt][1] = fast_exp2(s[nt][1] - mn0);
-      s[nt][2] = fast_exp2(s[nt][2] - mn1);
-      s[nt][3] = fast_exp2(s[nt][3] - mn1);
-      ps0 += s[nt][0] + s[nt][1];
-      ps1 += s[nt][2] + s[nt][3];
-    }
-    l0 = l0 * a0 + ps0;
-    l1 = l1 * a1 + ps1;
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= a0;
-      o[n][1] *= a0;
-      o[n][2] *= a1;
-      o[n][3] *= a1;
-    }
-    // O += P V.
-    uint32_t pa[4];
-    pa[0] = Mma::pack(s[0][0], s[0][1]);
-    pa[1] = Mma::pack(s[0][2], s[0][3]);
-    pa[2] = Mma::pack(s[1][0], s[1][1]);
-    pa[3] = Mma::pack(s[1][2], s[1][3]);
-    {
-      const int mi = lane >> 3;
-      const int trow = (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int dd = 0; dd < D / 16; ++dd) {
-        const int dim = dd * 16 + (mi >> 1) * 8;
-        const uint32_t addr =
-            smem_u32(vt + (dim / 64) * kPanelBytes) + swz(trow, (dim % 64) / 8, 128);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(addr, b0, b1, b2, b3);
-        Mma::run(o[2 * dd], pa, b0, b1);
-        Mma::run(o[2 * dd + 1], pa, b2, b3);
-      }
-    }
+    decode_tile<T, D>(kv, min(kTile, ch.z - tok0), p.scale_log2, lane, qa, o, m0, m1, l0, l1);
     ++consumed;
     __syncwarp();
-    if (pc < c1) {
+    if (pk < nck) {
       if (lane == 0) {
         fence_proxy_async_smem();
-        issue(stage, pc, pt);
+        issue(stage, chunk_at(c0, c1, pk), pt);
       }
       ++issued;
-      advance(pc, pt);
+      advance(pk, pt);
     }
     if (++ct == ntiles(cc)) {
-      // Finish the chunk: normalise and write the output rows or the partial state.
-      float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-      lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
-      float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-      lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
-      const float inv0 = 1.f / lt0, inv1 = 1.f / lt1;
-      const float lse0 = (m0 + __log2f(lt0)) * kLn2, lse1 = (m1 + __log2f(lt1)) * kLn2;
       const int slot = ch.w;
-      if (slot < 0) {
-        T* ob = static_cast<T*>(p.out) + b * p.o_s0 + int64_t(kvh) * g * p.o_s1;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          const int d = n * 8 + 2 * cq;
-          if (r0 < g)
-            *reinterpret_cast<uint32_t*>(ob + r0 * p.o_s1 + d) =
-                Mma::pack(o[n][0] * inv0, o[n][1] * inv0);
-          if (r1 < g)
-            *reinterpret_cast<uint32_t*>(ob + r1 * p.o_s1 + d) =
-                Mma::pack(o[n][2] * inv1, o[n][3] * inv1);
+      finish_chunk<T, D>(p, b, kvh, slot, g, 0, lane, o, m0, m1, l0, l1);
+      if (slot >= 0 && p.counters) {
+        // The last of the unit's chunks to finish merges all of them (release / acquire
+        // through lane 0's atomic, as in the group kernel).
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const int item = find_merge_item(merges, NM, ch.x);
+          const int old = atomic_add_acq_rel(p.counters + item, 1);
+          last = old == merges[3 * item + 2] - 1 ? item + 1 : 0;
         }
-        if (p.lse && cq == 0) {
-          float* lb = p.lse + int64_t(b) * p.num_qo_heads + kvh * g;
-          if (r0 < g) lb[r0] = lse0;
-          if (r1 < g) lb[r1] = lse1;
-        }
-      } else {
-        float* wo = p.ws_o + int64_t(slot) * g * D;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          const int d = n * 8 + 2 * cq;
-          if (r0 < g)
-            *reinterpret_cast<float2*>(wo + r0 * D + d) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
-          if (r1 < g)
-            *reinterpret_cast<float2*>(wo + r1 * D + d) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
-        }
-        if (cq == 0) {
-          if (r0 < g) p.ws_lse[slot * g + r0] = lse0;
-          if (r1 < g) p.ws_lse[slot * g + r1] = lse1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          const int item = last - 1;
+          merge_rows<T, D>(lane, p.ws_o, p.ws_lse, merges[3 * item + 1], merges[3 * item + 2], g,
+                           0, g, out_row<T>(p, b, kvh * g), p.o_s1, lse_row(p, b, kvh * g));
+          if (lane == 0) p.counters[item] = 0;  // ready for the next run
         }
       }
-      ++cc;
+      ++ck;
       ct = 0;
     }
   }
@@ -327,6 +512,207 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     // Drain the copies still in flight before the warp leaves (bounded, not forcible).
     for (uint32_t k = consumed; k < issued; ++k)
       mbar_wait(&bars[k % kStages], (k / kStages) & 1u, p.st, false);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// group variant: one worker per CTA; a producer warp copies each 16-token tile of all G
+// kv heads of a unit (page-contiguous pieces of G * page_size * 256 bytes) into a shared
+// ring, consumer warp h computes kv head h of the group.
+// ---------------------------------------------------------------------------------------
+
+template <int D>
+__host__ __device__ constexpr uint32_t group_stage_bytes(int G) {
+  return 2u * (D / 64) * uint32_t(G) * kPanelBytes;
+}
+
+// Bounded wait that also gives up when the CTA's abort flag is raised.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              const StatusArgs& st, bool give_up,
+                                              const volatile int* abort_flag) {
+  if (give_up) {
+    record_error(st, BSKV_ERR_TIMEOUT);
+    return false;
+  }
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        record_error(st, BSKV_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kGroupThreads, 1)
+    decode_group_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.heads_per_unit, ns = p.stages;
+  const int ps = p.page_size, box_rows = ps < kTile ? ps : kTile;
+  const uint32_t head_bytes = uint32_t(box_rows) * 128u;    // one head, one half, one piece
+  const uint32_t piece_bytes = uint32_t(G) * head_bytes;     // all G heads
+  const uint32_t half_bytes = uint32_t(G) * kPanelBytes;     // 16 rows of all G heads
+  const uint32_t kv_bytes = (D / 64) * half_bytes;           // K (or V) of one stage
+  const uint32_t stage_bytes = 2u * kv_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ns * stage_bytes);
+  uint64_t* empty = full + ns;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + ns);
+
+  const int32_t* hdr = p.meta;
+  const int w = blockIdx.x;
+  const int32_t* wptr = hdr + hdr[H_OFF_WORKERS];
+  const int4* chunks = reinterpret_cast<const int4*>(hdr + hdr[H_OFF_CHUNKS]);
+  const int32_t* merges = hdr + hdr[H_OFF_MERGES];
+  const int NM = hdr[H_MERGES];
+  const int32_t* kv_indptr = hdr + hdr[H_OFF_AUX0];
+  const int32_t* kv_indices = hdr + hdr[H_OFF_AUX1];
+  const int c0 = wptr[w], c1 = wptr[w + 1];
+  const int HG = p.num_kv_heads / G, g = p.group, SR = G * g;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], uint32_t(G));
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&kv_map);
+  }
+  __syncthreads();
+  const bool forced = forced_timeout(p.st);
+  auto ntiles = [&](const int4& ch) { return (ch.z - ch.y + kTile - 1) / kTile; };
+
+  if (warp == kDecodeGroupMax) {
+    // Producer: one thread issues every copy, then waits for its own copies to land.
+    if (lane != 0) return;
+    const uint64_t stream_policy = l2_evict_first_policy();  // KV is read once
+    uint32_t it = 0;
+    bool ok = true;
+    for (int k = 0; k < c1 - c0 && ok; ++k) {
+      const int4 ch = chunks[chunk_at(c0, c1, k)];
+      const int b = ch.x / HG, hg = ch.x % HG;
+      const int pbase = kv_indptr[b];
+      const int nt = ntiles(ch);
+      for (int t = 0; t < nt; ++t, ++it) {
+        const int stage = int(it % uint32_t(ns));
+        if (it >= uint32_t(ns) &&
+            !wait_or_abort(&empty[stage], ((it / ns) & 1u) ^ 1u, p.st, forced, abort_flag)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        uint8_t* kdst = smem + stage * stage_bytes;
+        uint8_t* vdst = kdst + kv_bytes;
+        const int tok = ch.y + t * kTile;
+        if (ps >= kTile) {
+          const int page = kv_indices[pbase + tok / ps];
+          const int s = tok % ps;
+          mbar_arrive_expect_tx(&full[stage], 2u * (D / 64) * piece_bytes);
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            tma_load_5d_hint(kdst + hf * half_bytes, &kv_map, hf * 64, s, hg * G, 0, page,
+                             &full[stage], stream_policy);
+            tma_load_5d_hint(vdst + hf * half_bytes, &kv_map, hf * 64, s, hg * G, 1, page,
+                             &full[stage], stream_policy);
+          }
+        } else {
+          const int npages = kv_indptr[b + 1] - pbase;
+          const int first = tok / ps;
+          int pieces = kTile / ps;
+          if (first + pieces > npages) pieces = npages - first;
+          mbar_arrive_expect_tx(&full[stage], 2u * (D / 64) * piece_bytes * uint32_t(pieces));
+          for (int k = 0; k < pieces; ++k) {
+            const int page = kv_indices[pbase + first + k];
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf) {
+              tma_load_5d_hint(kdst + hf * half_bytes + k * piece_bytes, &kv_map, hf * 64, 0,
+                               hg * G, 0, page, &full[stage], stream_policy);
+              tma_load_5d_hint(vdst + hf * half_bytes + k * piece_bytes, &kv_map, hf * 64, 0,
+                               hg * G, 1, page, &full[stage], stream_policy);
+            }
+          }
+        }
+      }
+    }
+    // Every copy issued must land before the CTA may exit (bounded, not forcible).
+    for (uint32_t k = it > uint32_t(ns) ? it - ns : 0; k < it; ++k)
+      mbar_wait(&full[k % ns], (k / ns) & 1u, p.st, false);
+    return;
+  }
+  if (warp >= G) return;
+
+  // Consumer warp h: kv head hg * G + h of each chunk's unit. After a failed wait it
+  // skips the arithmetic (and the stage releases) of the rest of its work.
+  const int h = warp;
+  if (p.counters) {
+    for (int i = w; i < NM; i += gridDim.x) {
+      if (merges[3 * i + 2] != 0) continue;
+      const int unit = merges[3 * i], b = unit / HG, hg = unit % HG;
+      const int head = (hg * G + h) * g;
+      merge_rows<T, D, kGroupMergeSlots, kGroupMergeRows>(lane, p.ws_o, p.ws_lse, 0, 0, SR, h * g, g, out_row<T>(p, b, head), p.o_s1,
+                       lse_row(p, b, head));
+    }
+  }
+  uint32_t qa[D / 16][4];
+  float o[D / 8][4];
+  float m0, m1, l0, l1;
+  bool ok = true;
+  uint32_t it = 0;
+  for (int k = 0; k < c1 - c0; ++k) {
+    const int4 ch = chunks[chunk_at(c0, c1, k)];
+    const int b = ch.x / HG, hg = ch.x % HG, kvh = hg * G + h;
+    load_q<T, D>(p, b, kvh, lane, qa);
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+    const int nt = ntiles(ch);
+    for (int t = 0; t < nt; ++t, ++it) {
+      const int stage = int(it % uint32_t(ns));
+      if (ok) ok = warp_wait(&full[stage], (it / ns) & 1u, p.st, forced, abort_flag);
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        continue;
+      }
+      const uint32_t kt = smem_u32(smem + stage * stage_bytes) + uint32_t(h) * head_bytes;
+      const KvRows kv{kt, kt + kv_bytes, half_bytes, box_rows == kTile ? 1024u : piece_bytes};
+      const int valid = min(kTile, ch.z - (ch.y + t * kTile));
+      decode_tile<T, D>(kv, valid, p.scale_log2, lane, qa, o, m0, m1, l0, l1);
+      if (valid < kTile) fence_proxy_async_smem();  // zeroed rows before the next copy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    const int slot = ch.w;
+    if (!ok) continue;
+    finish_chunk<T, D>(p, b, kvh, slot, SR, h * g, lane, o, m0, m1, l0, l1);
+    if (slot >= 0 && p.counters) {
+      // Per kv head: the last warp to finish a piece of the unit merges that head's rows.
+      // The warp's partial-state writes are ordered before lane 0's release (the
+      // __syncwarp), and the merging warp reads the other pieces after its acquire.
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        const int item = find_merge_item(merges, NM, ch.x);
+        const int old = atomic_add_acq_rel(p.counters + item * G + h, 1);
+        last = old == merges[3 * item + 2] - 1 ? item + 1 : 0;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        const int item = last - 1;
+        merge_rows<T, D, kGroupMergeSlots, kGroupMergeRows>(lane, p.ws_o, p.ws_lse, merges[3 * item + 1], merges[3 * item + 2], SR,
+                         h * g, g, out_row<T>(p, b, kvh * g), p.o_s1, lse_row(p, b, kvh * g));
+        if (lane == 0) p.counters[item * G + h] = 0;  // ready for the next run
+      }
+    }
   }
 }
 
@@ -341,55 +727,27 @@ struct MergeParams {
   void* out;
   int64_t o_s0, o_s1;
   float* lse;
-  int num_kv_heads, group, num_qo_heads;
+  int units_per_request, slot_rows, num_qo_heads;
 };
 
+// One warp per (merge item, group of 4 rows of the unit; 8 for head_dim 64).
 template <int D, typename T>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
   const int32_t* hdr = p.meta;
   const int NM = hdr[H_MERGES];
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = p.group;
-  if (gw >= NM * g) return;
-  const int item = gw / g, r = gw % g;
+  constexpr int RPW = 4 * (128 / D);  // rows per warp
+  const int SR = p.slot_rows, nchunk = (SR + RPW - 1) / RPW;
+  if (gw >= NM * nchunk) return;
+  const int item = gw / nchunk, r0 = (gw % nchunk) * RPW;
   const int32_t* mi = hdr + hdr[H_OFF_MERGES] + 3 * item;
-  const int unit = mi[0], first = mi[1], count = mi[2];
-  const int b = unit / p.num_kv_heads, kvh = unit % p.num_kv_heads;
-  const int head = kvh * g + r;
-  constexpr int V = D / 32;  // values per lane
-  float acc[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) acc[i] = 0.f;
-  float lse_out = -INFINITY;
-  if (count > 0) {
-    float mx = -INFINITY;
-    for (int c = lane; c < count; c += 32) mx = fmaxf(mx, p.ws_lse[(first + c) * g + r]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float tot = 0.f;
-    for (int c = 0; c < count; ++c) {
-      const float wgt = expf(p.ws_lse[(first + c) * g + r] - mx);
-      tot += wgt;
-      const float* src = p.ws_o + (int64_t(first + c) * g + r) * D + lane * V;
-      if constexpr (V == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] += wgt * x.x; acc[1] += wgt * x.y; acc[2] += wgt * x.z; acc[3] += wgt * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] += wgt * x.x; acc[1] += wgt * x.y;
-      }
-    }
-    const float inv = 1.f / tot;
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] *= inv;
-    lse_out = mx + logf(tot);
-  }
-  T* dst = static_cast<T*>(p.out) + b * p.o_s0 + head * p.o_s1 + lane * V;
-#pragma unroll
-  for (int i = 0; i < V; i += 2)
-    *reinterpret_cast<uint32_t*>(dst + i) = MmaOp<T>::pack(acc[i], acc[i + 1]);
-  if (p.lse && lane == 0) p.lse[int64_t(b) * p.num_qo_heads + head] = lse_out;
+  const int unit = mi[0];
+  const int b = unit / p.units_per_request, u = unit % p.units_per_request;
+  const int head = u * SR + r0;
+  T* dst = static_cast<T*>(p.out) + b * p.o_s0 + head * p.o_s1;
+  merge_rows<T, D>(lane, p.ws_o, p.ws_lse, mi[1], mi[2], SR, r0, min(RPW, SR - r0), dst, p.o_s1,
+                   p.lse ? p.lse + int64_t(b) * p.num_qo_heads + head : nullptr);
 }
 
 template <typename TO>
@@ -445,36 +803,76 @@ template <typename T, int D>
 bskv_status launch_decode_t(const bskv_plan* plan, const CUtensorMap& map, DecodeParams& dp,
                             cudaStream_t stream) {
   const int grid = meta_word(plan, H_GRID);
-  const size_t smem = size_t(kWarps) * kStages * 2 * tile_bytes<D>() + 1024 +
-                      size_t(kWarps) * kStages * sizeof(uint64_t);
-  if (grid > 0) {
+  if (grid <= 0) return BSKV_OK;
+  if (meta_word(plan, H_VARIANT) == DECODE_GROUP) {
+    const uint32_t sb = group_stage_bytes<D>(dp.heads_per_unit);
+    dp.stages = int(kGroupRingBytes / sb) < 8 ? int(kGroupRingBytes / sb) : 8;
+    const size_t smem = size_t(dp.stages) * sb + 1024 + size_t(2 * dp.stages) * 8 + 16;
+    auto kern = decode_group_kernel<T, D>;
+    if (bskv_status s = cuda_check(
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+            "decode: cudaFuncSetAttribute"))
+      return s;
+    kern<<<grid, kGroupThreads, smem, stream>>>(map, dp);
+  } else {
+    const size_t smem = size_t(kWarps) * kStages * 2 * tile_bytes<D>() + 1024 +
+                        size_t(kWarps) * kStages * sizeof(uint64_t);
     auto kern = decode_kernel<T, D>;
     if (bskv_status s = cuda_check(
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
             "decode: cudaFuncSetAttribute"))
       return s;
     kern<<<grid, kWarps * 32, smem, stream>>>(map, dp);
-    if (bskv_status s = cuda_check(cudaGetLastError(), "decode kernel launch")) return s;
   }
-  return BSKV_OK;
+  return cuda_check(cudaGetLastError(), "decode kernel launch");
 }
 
 template <typename T, int D>
 bskv_status launch_merge_t(const bskv_plan* plan, const MergeParams& mp, cudaStream_t stream) {
   const int nm = meta_word(plan, H_MERGES);
   if (nm == 0) return BSKV_OK;
-  const int warps = nm * mp.group;
+  const int rpw = 4 * (128 / D);
+  const int warps = nm * ((mp.slot_rows + rpw - 1) / rpw);
   decode_merge_kernel<D, T><<<(warps + 3) / 4, 128, 0, stream>>>(mp);
   return cuda_check(cudaGetLastError(), "decode merge launch");
 }
 
+bskv_status launch_decode_any(const bskv_plan* plan, const CUtensorMap& map, DecodeParams& dp,
+                              cudaStream_t st) {
+  const bool bf = plan->dtype == BSKV_BF16;
+  if (plan->head_dim == 128)
+    return bf ? launch_decode_t<__nv_bfloat16, 128>(plan, map, dp, st)
+              : launch_decode_t<__half, 128>(plan, map, dp, st);
+  return bf ? launch_decode_t<__nv_bfloat16, 64>(plan, map, dp, st)
+            : launch_decode_t<__half, 64>(plan, map, dp, st);
+}
+
+bskv_status launch_merge_any(const bskv_plan* plan, const MergeParams& mp, cudaStream_t st) {
+  const bool bf = plan->dtype == BSKV_BF16;
+  if (plan->head_dim == 128)
+    return bf ? launch_merge_t<__nv_bfloat16, 128>(plan, mp, st) : launch_merge_t<__half, 128>(plan, mp, st);
+  return bf ? launch_merge_t<__nv_bfloat16, 64>(plan, mp, st) : launch_merge_t<__half, 64>(plan, mp, st);
+}
+
+// Units per request and query heads per unit (= rows of one partial-state slot).
+struct DecodeShape {
+  int heads_per_unit, units_per_request, slot_rows;
+};
+
+DecodeShape decode_shape(const bskv_plan* plan) {
+  const int Hkv = plan->num_kv_heads;
+  const int G = meta_word(plan, H_VARIANT) == DECODE_GROUP
+                    ? decode_group_heads(Hkv, plan->page_size) : 1;
+  return DecodeShape{G, Hkv / G, G * (plan->num_qo_heads / Hkv)};
+}
+
 // Float-workspace pointers of a decode plan (partial outputs, then their LSE).
 void decode_ws(const bskv_plan* plan, void* float_ws, float** ws_o, float** ws_lse) {
-  const int g = plan->num_qo_heads / plan->num_kv_heads;
+  const int rows = decode_shape(plan).slot_rows;
   const int slots = meta_word(plan, H_SLOTS);
   *ws_o = static_cast<float*>(float_ws);
   *ws_lse = slots ? reinterpret_cast<float*>(static_cast<uint8_t*>(float_ws) +
-                                             ((size_t(slots) * g * plan->head_dim * 4 + 255) &
+                                             ((size_t(slots) * rows * plan->head_dim * 4 + 255) &
                                               ~size_t(255)))
                   : nullptr;
 }
@@ -492,6 +890,69 @@ bskv_status check_decode_ws(const bskv_plan* plan, void* float_ws, size_t float_
   return BSKV_OK;
 }
 
+// Argument checks shared by the decode entry points, then the kernel parameters and the
+// KV tensor map (box: 64 elements x min(page_size, 16) tokens x the unit's kv heads).
+bskv_status prepare_decode(const char* who, const bskv_plan* plan, const int32_t* meta,
+                           const void* q, const int64_t* q_strides, const void* kv_cache,
+                           const int64_t* kv_strides, void* out, const int64_t* out_strides,
+                           float* lse, float sm_scale, void* ws, DecodeParams* dp,
+                           CUtensorMap* map) {
+  if (!q_strides || !kv_strides || !out_strides) { set_error("%s: NULL strides", who); return BSKV_ERR_INVALID_ARG; }
+  const int ps = plan->page_size;
+  if (!(ps == 8 || ps % 16 == 0)) {
+    set_error("%s: page_size %d unsupported (8 or a multiple of 16)", who, ps);
+    return BSKV_ERR_UNSUPPORTED;
+  }
+  const int esz = 2;
+  const int Hkv = plan->num_kv_heads, D = plan->head_dim;
+  for (int i = 0; i < 4; ++i) {
+    if (kv_strides[i] <= 0 || (kv_strides[i] * esz) % 16 != 0) {
+      set_error("%s: kv stride %d (%lld elements) must be positive and 16-byte aligned", who, i,
+                (long long)kv_strides[i]);
+      return BSKV_ERR_INVALID_ARG;
+    }
+  }
+  if ((q_strides[0] * esz) % 4 || (q_strides[1] * esz) % 4 || (out_strides[0] * esz) % 4 ||
+      (out_strides[1] * esz) % 4) {
+    set_error("%s: q/out strides must be multiples of 2 elements", who);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (!q || !kv_cache || !out) { set_error("%s: NULL tensor", who); return BSKV_ERR_INVALID_ARG; }
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) { set_error("%s: tensors must be 16-byte aligned", who); return BSKV_ERR_INVALID_ARG; }
+  const DecodeShape sh = decode_shape(plan);
+  *dp = DecodeParams{};
+  dp->meta = meta;
+  dp->q = q; dp->q_s0 = q_strides[0]; dp->q_s1 = q_strides[1];
+  dp->out = out; dp->o_s0 = out_strides[0]; dp->o_s1 = out_strides[1];
+  dp->lse = lse;
+  decode_ws(plan, ws, &dp->ws_o, &dp->ws_lse);
+  dp->num_kv_heads = Hkv; dp->group = plan->num_qo_heads / Hkv; dp->page_size = ps;
+  dp->num_qo_heads = plan->num_qo_heads;
+  dp->heads_per_unit = sh.heads_per_unit;
+  dp->scale_log2 = sm_scale * 1.4426950408889634f;
+  if (bskv_status s = status_args(&dp->st)) return s;
+  const uint64_t dims[5] = {uint64_t(D), uint64_t(ps), uint64_t(Hkv), 2, uint64_t(plan->num_pages)};
+  const uint64_t strides[4] = {uint64_t(kv_strides[3]) * esz, uint64_t(kv_strides[2]) * esz,
+                               uint64_t(kv_strides[1]) * esz, uint64_t(kv_strides[0]) * esz};
+  const uint32_t box[5] = {64, uint32_t(ps < kTile ? ps : kTile), uint32_t(sh.heads_per_unit), 1, 1};
+  const CUtensorMapDataType dt =
+      plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return encode_tiled(map, dt, 5, kv_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+MergeParams merge_params(const bskv_plan* plan, const int32_t* meta, const DecodeParams& dp) {
+  const DecodeShape sh = decode_shape(plan);
+  MergeParams mp{};
+  mp.meta = meta;
+  mp.ws_o = dp.ws_o; mp.ws_lse = dp.ws_lse;
+  mp.out = dp.out; mp.o_s0 = dp.o_s0; mp.o_s1 = dp.o_s1;
+  mp.lse = dp.lse;
+  mp.units_per_request = sh.units_per_request;
+  mp.slot_rows = sh.slot_rows;
+  mp.num_qo_heads = plan->num_qo_heads;
+  return mp;
+}
+
 }  // namespace
 }  // namespace bskv
 
@@ -504,57 +965,14 @@ extern "C" bskv_status bskv_run_decode_partial(const bskv_plan* plan, const void
                                        void* float_ws, size_t float_ws_bytes, void* stream) {
   if (!plan || plan->kind != KIND_DECODE) { set_error("run_decode: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_decode: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
-  if (!q_strides || !kv_strides || !out_strides) { set_error("run_decode: NULL strides"); return BSKV_ERR_INVALID_ARG; }
-  const int ps = plan->page_size;
-  if (!(ps == 8 || ps % 16 == 0)) {
-    set_error("run_decode: page_size %d unsupported (8 or a multiple of 16)", ps);
-    return BSKV_ERR_UNSUPPORTED;
-  }
-  const int esz = 2;
-  const int Hkv = plan->num_kv_heads, D = plan->head_dim;
-  const int64_t* ks = kv_strides;
-  for (int i = 0; i < 4; ++i) {
-    if (ks[i] <= 0 || (ks[i] * esz) % 16 != 0) {
-      set_error("run_decode: kv stride %d (%lld elements) must be positive and 16-byte aligned", i, (long long)ks[i]);
-      return BSKV_ERR_INVALID_ARG;
-    }
-  }
-  if ((q_strides[0] * esz) % 4 || (q_strides[1] * esz) % 4 || (out_strides[0] * esz) % 4 ||
-      (out_strides[1] * esz) % 4) {
-    set_error("run_decode: q/out strides must be multiples of 2 elements");
-    return BSKV_ERR_INVALID_ARG;
-  }
-  if (plan->batch > 0 && (!q || !kv_cache || !out)) { set_error("run_decode: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
-  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) { set_error("run_decode: tensors must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
   if (bskv_status s = check_decode_ws(plan, float_ws, float_ws_bytes)) return s;
   if (plan->batch == 0) return BSKV_OK;
-  DecodeParams dp{};
-  dp.meta = plan->meta_dev;
-  dp.q = q; dp.q_s0 = q_strides[0]; dp.q_s1 = q_strides[1];
-  dp.out = out; dp.o_s0 = out_strides[0]; dp.o_s1 = out_strides[1];
-  dp.lse = lse;
-  const int g = plan->num_qo_heads / Hkv;
-  decode_ws(plan, float_ws, &dp.ws_o, &dp.ws_lse);
-  dp.num_kv_heads = Hkv; dp.group = g; dp.page_size = ps; dp.num_qo_heads = plan->num_qo_heads;
-  dp.scale_log2 = sm_scale * 1.4426950408889634f;
-  if (bskv_status s = status_args(&dp.st)) return s;
+  DecodeParams dp;
   CUtensorMap map;
-  const uint64_t dims[5] = {uint64_t(D), uint64_t(ps), uint64_t(Hkv), 2, uint64_t(plan->num_pages)};
-  const uint64_t strides[4] = {uint64_t(ks[3]) * esz, uint64_t(ks[2]) * esz, uint64_t(ks[1]) * esz,
-                               uint64_t(ks[0]) * esz};
-  const uint32_t box[5] = {64, uint32_t(ps < kTile ? ps : kTile), 1, 1, 1};
-  const CUtensorMapDataType dt =
-      plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (bskv_status s = encode_tiled(&map, dt, 5, kv_cache, dims, strides, box,
-                                   CU_TENSOR_MAP_SWIZZLE_128B))
+  if (bskv_status s = prepare_decode("run_decode", plan, plan->meta_dev, q, q_strides, kv_cache,
+                                     kv_strides, out, out_strides, lse, sm_scale, float_ws, &dp, &map))
     return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (plan->dtype == BSKV_BF16) {
-    return D == 128 ? launch_decode_t<__nv_bfloat16, 128>(plan, map, dp, st)
-                    : launch_decode_t<__nv_bfloat16, 64>(plan, map, dp, st);
-  }
-  return D == 128 ? launch_decode_t<__half, 128>(plan, map, dp, st)
-                  : launch_decode_t<__half, 64>(plan, map, dp, st);
+  return launch_decode_any(plan, map, dp, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" bskv_status bskv_decode_merge(const bskv_plan* plan, void* out,
@@ -567,19 +985,12 @@ extern "C" bskv_status bskv_decode_merge(const bskv_plan* plan, void* out,
   if (meta_word(plan, H_MERGES) == 0) return BSKV_OK;
   if (!out || !aligned16(out)) { set_error("decode_merge: out must be a 16-byte aligned tensor"); return BSKV_ERR_INVALID_ARG; }
   if ((out_strides[0] * 2) % 4 || (out_strides[1] * 2) % 4) { set_error("decode_merge: out strides must be multiples of 2 elements"); return BSKV_ERR_INVALID_ARG; }
-  MergeParams mp{};
-  mp.meta = plan->meta_dev;
-  decode_ws(plan, float_ws, &mp.ws_o, &mp.ws_lse);
-  mp.out = out; mp.o_s0 = out_strides[0]; mp.o_s1 = out_strides[1];
-  mp.lse = lse;
-  mp.num_kv_heads = plan->num_kv_heads;
-  mp.group = plan->num_qo_heads / plan->num_kv_heads;
-  mp.num_qo_heads = plan->num_qo_heads;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool bf = plan->dtype == BSKV_BF16;
-  if (plan->head_dim == 128)
-    return bf ? launch_merge_t<__nv_bfloat16, 128>(plan, mp, st) : launch_merge_t<__half, 128>(plan, mp, st);
-  return bf ? launch_merge_t<__nv_bfloat16, 64>(plan, mp, st) : launch_merge_t<__half, 64>(plan, mp, st);
+  DecodeParams dp{};
+  decode_ws(plan, float_ws, &dp.ws_o, &dp.ws_lse);
+  dp.out = out; dp.o_s0 = out_strides[0]; dp.o_s1 = out_strides[1];
+  dp.lse = lse;
+  return launch_merge_any(plan, merge_params(plan, plan->meta_dev, dp),
+                          static_cast<cudaStream_t>(stream));
 }
 
 extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
@@ -587,11 +998,29 @@ extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
                                        const int64_t* kv_strides, void* out,
                                        const int64_t* out_strides, float* lse, float sm_scale,
                                        void* float_ws, size_t float_ws_bytes, void* stream) {
-  if (bskv_status s = bskv_run_decode_partial(plan, q, q_strides, kv_cache, kv_strides, out,
-                                              out_strides, lse, sm_scale, float_ws,
-                                              float_ws_bytes, stream))
+  if (!plan || plan->kind != KIND_DECODE) { set_error("run_decode: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
+  if (!plan->meta_dev) { set_error("run_decode: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
+  if (bskv_status s = check_decode_ws(plan, float_ws, float_ws_bytes)) return s;
+  if (plan->batch == 0) return BSKV_OK;
+  DecodeParams dp;
+  CUtensorMap map;
+  if (bskv_status s = prepare_decode("run_decode", plan, plan->meta_dev, q, q_strides, kv_cache,
+                                     kv_strides, out, out_strides, lse, sm_scale, float_ws, &dp, &map))
     return s;
-  return bskv_decode_merge(plan, out, out_strides, lse, float_ws, float_ws_bytes, stream);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool merges = meta_word(plan, H_MERGES) > 0;
+  if (meta_word(plan, H_GRID) == 0)  // no tokens at all: only zero-filling is left
+    return merges ? launch_merge_any(plan, merge_params(plan, plan->meta_dev, dp), st) : BSKV_OK;
+  if (merges && plan->max_merge_count > kFusedMergeMaxPieces) {
+    // many pieces per unit: the attention kernel, then the merge kernel
+    if (bskv_status s = launch_decode_any(plan, map, dp, st)) return s;
+    return launch_merge_any(plan, merge_params(plan, plan->meta_dev, dp), st);
+  }
+  if (merges) {
+    if (!plan->counters_dev) { set_error("run_decode: plan has no merge counters (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
+    dp.counters = plan->counters_dev;  // split units are merged inside the decode kernel
+  }
+  return launch_decode_any(plan, map, dp, st);
 }
 
 extern "C" bskv_status bskv_merge_states(const float* v, const float* s, int64_t seq_len,
@@ -695,30 +1124,15 @@ extern "C" bskv_status bskv_run_decode_noalloc(const bskv_plan* plan, const void
               meta_words * 4, plan->float_ws_bytes, kNoAllocMetaWords * 4, kNoAllocScratchBytes);
     return BSKV_ERR_UNSUPPORTED;
   }
-  if (!q_strides || !kv_strides || !out_strides) { set_error("run_decode_noalloc: NULL strides"); return BSKV_ERR_INVALID_ARG; }
-  const int ps = plan->page_size;
-  if (!(ps == 8 || ps % 16 == 0)) {
-    set_error("run_decode_noalloc: page_size %d unsupported (8 or a multiple of 16)", ps);
-    return BSKV_ERR_UNSUPPORTED;
-  }
-  const int esz = 2;
-  const int Hkv = plan->num_kv_heads, D = plan->head_dim;
-  for (int i = 0; i < 4; ++i) {
-    if (kv_strides[i] <= 0 || (kv_strides[i] * esz) % 16 != 0) {
-      set_error("run_decode_noalloc: kv stride %d must be positive and 16-byte aligned", i);
-      return BSKV_ERR_INVALID_ARG;
-    }
-  }
-  if ((q_strides[0] * esz) % 4 || (q_strides[1] * esz) % 4 || (out_strides[0] * esz) % 4 ||
-      (out_strides[1] * esz) % 4) {
-    set_error("run_decode_noalloc: q/out strides must be multiples of 2 elements");
-    return BSKV_ERR_INVALID_ARG;
-  }
   if (plan->batch == 0) return BSKV_OK;
-  if (!q || !kv_cache || !out) { set_error("run_decode_noalloc: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
-  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) { set_error("run_decode_noalloc: tensors must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
   NoAllocPtrs st_ptrs;
   if (bskv_status s = noalloc_ptrs(&st_ptrs)) return s;
+  DecodeParams dp;
+  CUtensorMap map;
+  if (bskv_status s = prepare_decode("run_decode_noalloc", plan, st_ptrs.meta, q, q_strides,
+                                     kv_cache, kv_strides, out, out_strides, lse, sm_scale,
+                                     st_ptrs.scratch, &dp, &map))
+    return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The metadata is copied into the static array on the caller's stream; nothing in the
   // scratch array has to start at zero (every partial state is written before it is read).
@@ -726,42 +1140,7 @@ extern "C" bskv_status bskv_run_decode_noalloc(const bskv_plan* plan, const void
                                                  cudaMemcpyHostToDevice, st),
                                  "run_decode_noalloc: metadata copy"))
     return s;
-  DecodeParams dp{};
-  dp.meta = st_ptrs.meta;
-  dp.q = q; dp.q_s0 = q_strides[0]; dp.q_s1 = q_strides[1];
-  dp.out = out; dp.o_s0 = out_strides[0]; dp.o_s1 = out_strides[1];
-  dp.lse = lse;
-  const int g = plan->num_qo_heads / Hkv;
-  decode_ws(plan, st_ptrs.scratch, &dp.ws_o, &dp.ws_lse);
-  dp.num_kv_heads = Hkv; dp.group = g; dp.page_size = ps; dp.num_qo_heads = plan->num_qo_heads;
-  dp.scale_log2 = sm_scale * 1.4426950408889634f;
-  if (bskv_status s = status_args(&dp.st)) return s;
-  CUtensorMap map;
-  const uint64_t dims[5] = {uint64_t(D), uint64_t(ps), uint64_t(Hkv), 2, uint64_t(plan->num_pages)};
-  const uint64_t strides[4] = {uint64_t(kv_strides[3]) * esz, uint64_t(kv_strides[2]) * esz,
-                               uint64_t(kv_strides[1]) * esz, uint64_t(kv_strides[0]) * esz};
-  const uint32_t box[5] = {64, uint32_t(ps < kTile ? ps : kTile), 1, 1, 1};
-  const CUtensorMapDataType dt =
-      plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (bskv_status s = encode_tiled(&map, dt, 5, kv_cache, dims, strides, box,
-                                   CU_TENSOR_MAP_SWIZZLE_128B))
-    return s;
-  MergeParams mp{};
-  mp.meta = st_ptrs.meta;
-  mp.ws_o = dp.ws_o; mp.ws_lse = dp.ws_lse;
-  mp.out = out; mp.o_s0 = out_strides[0]; mp.o_s1 = out_strides[1];
-  mp.lse = lse;
-  mp.num_kv_heads = Hkv; mp.group = g; mp.num_qo_heads = plan->num_qo_heads;
-  const bool bf = plan->dtype == BSKV_BF16;
-  bskv_status s = BSKV_OK;
-  if (D == 128) {
-    s = bf ? launch_decode_t<__nv_bfloat16, 128>(plan, map, dp, st) : launch_decode_t<__half, 128>(plan, map, dp, st);
-    if (s == BSKV_OK)
-      s = bf ? launch_merge_t<__nv_bfloat16, 128>(plan, mp, st) : launch_merge_t<__half, 128>(plan, mp, st);
-  } else {
-    s = bf ? launch_decode_t<__nv_bfloat16, 64>(plan, map, dp, st) : launch_decode_t<__half, 64>(plan, map, dp, st);
-    if (s == BSKV_OK)
-      s = bf ? launch_merge_t<__nv_bfloat16, 64>(plan, mp, st) : launch_merge_t<__half, 64>(plan, mp, st);
-  }
+  bskv_status s = launch_decode_any(plan, map, dp, st);
+  if (s == BSKV_OK) s = launch_merge_any(plan, merge_params(plan, st_ptrs.meta, dp), st);
   return s;
 }

@@ -42,7 +42,28 @@ constexpr int kMlaTile = 64;           // sparse rows per MLA chunk
 constexpr int kMlaVSplit = 2;          // the 512 latent output values split in halves
 constexpr int kMlaVDim = 512 / kMlaVSplit;
 
+constexpr int kDecodeGroupMax = 8;     // kv heads per CTA in the page-major decode variant
+constexpr int kDecodeGroupMaxPage = 16; // largest page_size that takes the page-major variant
+// bskv_run_decode merges inside the attention kernel when no unit is cut into more pieces
+// than this; beyond it one warp would merge many pieces serially at the kernel's tail, and
+// the separate merge kernel (more warps per unit) is faster.
+constexpr int kFusedMergeMaxPieces = 8;
+
 enum BsrVariant : int32_t { BSR_GENERIC = 0, BSR_TCGEN05 = 1 };
+// DECODE_WARP: one worker per warp, units (request, kv head).
+// DECODE_GROUP: one worker per CTA, units (request, group of G kv heads), G = Hkv when
+// Hkv <= 8, else 8 (Hkv a multiple of 8); every page piece is read for all G heads at once.
+enum DecodeVariant : int32_t { DECODE_WARP = 0, DECODE_GROUP = 1 };
+
+// kv heads per page-major group for a decode shape, 0 when the variant does not apply.
+inline int32_t decode_group_heads(int32_t num_kv_heads, int32_t page_size) {
+  if (page_size > kDecodeGroupMaxPage) return 0;
+  if (num_kv_heads <= kDecodeGroupMax) return num_kv_heads;
+  return num_kv_heads % kDecodeGroupMax == 0 ? kDecodeGroupMax : 0;
+}
+
+// Byte offset in the int workspace of the merge counters (after the metadata).
+inline size_t merge_counter_offset(size_t meta_words) { return ((meta_words * 4 + 255) / 256) * 256; }
 
 void set_error(const char* fmt, ...);
 const char* dtype_name(int32_t dt);
@@ -61,6 +82,11 @@ struct bskv_plan {
   // mla
   int32_t q_len = 0, top_k = 0;
   size_t float_ws_bytes = 0;
+  // int32 merge counters after the metadata in the int workspace (decode: one per merge
+  // item and kv head of the unit)
+  size_t counter_words = 0;
+  int32_t max_merge_count = 0;  // most pieces of one split unit
   // set by bskv_plan_upload
   const int32_t* meta_dev = nullptr;
+  int32_t* counters_dev = nullptr;  // one merge counter per merge item, zero between runs
 };

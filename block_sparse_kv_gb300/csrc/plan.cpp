@@ -162,7 +162,10 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
   if (head_dim != 64 && head_dim != 128) { set_error("plan_decode: head_dim %d not in {64,128}", head_dim); return BSKV_ERR_UNSUPPORTED; }
   if (dtype != BSKV_BF16 && dtype != BSKV_FP16) { set_error("plan_decode: dtype %s unsupported", dtype_name(dtype)); return BSKV_ERR_UNSUPPORTED; }
   if (batch > 0 && kv_indptr[0] != 0) { set_error("plan_decode: kv_indptr[0] must be 0"); return BSKV_ERR_INVALID_ARG; }
-  std::vector<int64_t> len(size_t(batch) * size_t(num_kv_heads));
+  const int32_t G = decode_group_heads(num_kv_heads, page_size);
+  const int32_t variant = G > 0 ? DECODE_GROUP : DECODE_WARP;
+  const int32_t upb = variant == DECODE_GROUP ? num_kv_heads / G : num_kv_heads;  // units per request
+  std::vector<int64_t> len(size_t(batch) * size_t(upb));
   int64_t total_tokens = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int64_t n = int64_t(kv_indptr[b + 1]) - kv_indptr[b];
@@ -177,7 +180,7 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
       L = (n - 1) * page_size + lp;
     }
     total_tokens += L;
-    for (int32_t h = 0; h < num_kv_heads; ++h) len[size_t(b) * num_kv_heads + h] = L;
+    for (int32_t h = 0; h < upb; ++h) len[size_t(b) * upb + h] = L;
   }
   const int64_t nnz = batch > 0 ? kv_indptr[batch] : 0;
   if (nnz > 0 && !kv_indices) { set_error("plan_decode: kv_indices is NULL"); return BSKV_ERR_INVALID_ARG; }
@@ -188,22 +191,27 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
     }
   }
   if (total_tokens * num_kv_heads > INT32_MAX / 2) { set_error("plan_decode: too many tokens"); return BSKV_ERR_UNSUPPORTED; }
-  const int64_t workers_cap = max_workers > 0 ? max_workers : int64_t(num_sms) * kDecodeWarps;
+  const int64_t workers_cap = max_workers > 0 ? max_workers
+                              : variant == DECODE_GROUP ? int64_t(num_sms)
+                                                        : int64_t(num_sms) * kDecodeWarps;
   std::vector<int32_t> worker_ptr, merges;
   std::vector<Chunk> chunks;
   int32_t slots = 0;
   linear_partition(len, kDecodeTile, workers_cap, worker_ptr, chunks, slots, merges);
   const int32_t P = int32_t(worker_ptr.size() - 1);
-  const int32_t grid = (P + kDecodeWarps - 1) / kDecodeWarps;
+  const int32_t grid = variant == DECODE_GROUP ? P : (P + kDecodeWarps - 1) / kDecodeWarps;
+  const int32_t slot_rows = num_qo_heads / upb;  // query heads of one unit
   bskv_plan* p = new bskv_plan();
   p->kind = KIND_DECODE;
   p->batch = batch; p->num_pages = num_pages; p->page_size = page_size;
   p->num_qo_heads = num_qo_heads; p->num_kv_heads = num_kv_heads; p->head_dim = head_dim;
   p->dtype = dtype;
   assemble(p, KIND_DECODE, int32_t(len.size()), worker_ptr, chunks, slots, merges, kDecodeTile,
-           kv_indptr, batch > 0 ? size_t(batch) + 1 : 0, kv_indices, size_t(nnz), grid, 0);
+           kv_indptr, batch > 0 ? size_t(batch) + 1 : 0, kv_indices, size_t(nnz), grid, variant);
   p->float_ws_bytes = slots == 0 ? 0
-      : align256(size_t(slots) * group * head_dim * 4) + align256(size_t(slots) * group * 4);
+      : align256(size_t(slots) * slot_rows * head_dim * 4) + align256(size_t(slots) * slot_rows * 4);
+  p->counter_words = merges.size() / 3 * size_t(num_kv_heads / upb);
+  for (size_t i = 2; i < merges.size(); i += 3) p->max_merge_count = std::max(p->max_merge_count, merges[i]);
   *out_plan = p;
   return BSKV_OK;
 }
@@ -352,7 +360,9 @@ extern "C" bskv_status bskv_plan_metadata(const bskv_plan* plan, const int32_t**
 extern "C" bskv_status bskv_plan_workspace_sizes(const bskv_plan* plan, size_t* int_ws_bytes,
                                                  size_t* float_ws_bytes) {
   if (!plan) { set_error("plan_workspace_sizes: NULL plan"); return BSKV_ERR_INVALID_ARG; }
-  if (int_ws_bytes) *int_ws_bytes = plan->meta.size() * sizeof(int32_t);
+  // metadata, then the int32 merge counters (zeroed by bskv_plan_upload)
+  if (int_ws_bytes)
+    *int_ws_bytes = merge_counter_offset(plan->meta.size()) + plan->counter_words * sizeof(int32_t);
   if (float_ws_bytes) *float_ws_bytes = plan->float_ws_bytes;
   return BSKV_OK;
 }

@@ -96,7 +96,10 @@ extern "C" bskv_status bskv_set_debug_force_timeout(int32_t on) {
 extern "C" bskv_status bskv_plan_upload(bskv_plan* plan, void* int_ws, size_t int_ws_bytes,
                                         void* stream) {
   if (!plan) { set_error("plan_upload: NULL plan"); return BSKV_ERR_INVALID_ARG; }
-  const size_t need = plan->meta.size() * sizeof(int32_t);
+  const size_t meta_bytes = plan->meta.size() * sizeof(int32_t);
+  const size_t cnt_off = merge_counter_offset(plan->meta.size());
+  const size_t cnt_bytes = plan->counter_words * sizeof(int32_t);
+  const size_t need = cnt_off + cnt_bytes;
   if (!int_ws || int_ws_bytes < need) {
     set_error("plan_upload: int workspace of %zu bytes, %zu needed", int_ws_bytes, need);
     return BSKV_ERR_WORKSPACE_TOO_SMALL;
@@ -105,11 +108,18 @@ extern "C" bskv_status bskv_plan_upload(bskv_plan* plan, void* int_ws, size_t in
     set_error("plan_upload: int workspace must be 16-byte aligned");
     return BSKV_ERR_INVALID_ARG;
   }
-  if (bskv_status s = cuda_check(cudaMemcpyAsync(int_ws, plan->meta.data(), need,
-                                                 cudaMemcpyHostToDevice,
-                                                 static_cast<cudaStream_t>(stream)),
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (bskv_status s = cuda_check(cudaMemcpyAsync(int_ws, plan->meta.data(), meta_bytes,
+                                                 cudaMemcpyHostToDevice, st),
                                  "plan_upload cudaMemcpyAsync"))
     return s;
+  int32_t* counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(int_ws) + cnt_off);
+  if (cnt_bytes) {
+    if (bskv_status s = cuda_check(cudaMemsetAsync(counters, 0, cnt_bytes, st),
+                                   "plan_upload cudaMemsetAsync"))
+      return s;
+  }
+  plan->counters_dev = cnt_bytes ? counters : nullptr;
   plan->meta_dev = static_cast<const int32_t*>(int_ws);
   return BSKV_OK;
 }

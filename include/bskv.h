@@ -148,14 +148,21 @@ bskv_status bskv_plan_destroy(bskv_plan* plan);
  */
 bskv_status bskv_plan_metadata(const bskv_plan* plan, const int32_t** meta, int64_t* num_words);
 
-/* Bytes of int workspace (metadata) and float workspace (split-KV partials) a run needs. */
+/*
+ * Bytes of int workspace (the metadata, then at the next 256-byte boundary the int32 merge
+ * counters of a decode plan, one per merge item and kv head of the unit) and of float
+ * workspace (split-KV partials) a run needs.
+ */
 bskv_status bskv_plan_workspace_sizes(const bskv_plan* plan, size_t* int_ws_bytes,
                                       size_t* float_ws_bytes);
 
 /*
  * Copy the metadata into the caller's device int workspace (cudaMemcpyAsync on
- * `stream`; the host copy lives in the plan, so it must outlive the copy). Later runs
- * with this plan read that workspace, which must not be changed meanwhile.
+ * `stream`; the host copy lives in the plan, so it must outlive the copy) and zero the
+ * merge counters after it (cudaMemsetAsync). Later runs with this plan read that
+ * workspace, which must not be changed meanwhile. A complete bskv_run_decode leaves the
+ * counters at zero again; after a run that reported a device error (bskv_get_device_status)
+ * upload the plan again before reusing it.
  */
 bskv_status bskv_plan_upload(bskv_plan* plan, void* int_ws, size_t int_ws_bytes, void* stream);
 
@@ -175,7 +182,12 @@ bskv_status bskv_plan_upload(bskv_plan* plan, void* int_ws, size_t int_ws_bytes,
  *   out   [batch, num_qo_heads, head_dim] in the plan dtype, strides out_strides.
  *   lse   [batch, num_qo_heads] float32 contiguous, or NULL.
  *   float_ws: at least bskv_plan_workspace_sizes().float_ws_bytes (may be NULL if 0).
- * Launches the decode kernel and, when some request is split, the merge kernel.
+ * When no unit (request and kv head, or request and group of kv heads) is cut into more
+ * than 8 pieces, one kernel launch: a split unit is merged by the worker that finishes
+ * its last piece (per kv head), which it learns from an atomic counter in the int
+ * workspace. Otherwise the attention kernel and then the merge kernel. Either way the
+ * merge is the one bskv_decode_merge applies ([CHEAT] merge_state), in the same order, so
+ * the result is bit-identical to bskv_run_decode_partial followed by bskv_decode_merge.
  */
 bskv_status bskv_run_decode(const bskv_plan* plan, const void* q, const int64_t* q_strides,
                             const void* kv_cache, const int64_t* kv_strides, void* out,

@@ -23,9 +23,12 @@ chunks (unit, tok_begin, tok_end, slot) with tok_end clipped to len_u. A unit cu
 >= 2 chunks gives each chunk a partial-state slot, numbered in chunk order; otherwise
 slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units with
 0 chunks (first_slot = -1) or >= 2 chunks.
-  * decode: units (b, kv head) b-major, len = request length, tile 16,
-    max_workers = 8 * num_sms unless given, grid = ceil(P / 8), aux0 = kv_indptr,
-    aux1 = kv_indices, variant 0.
+  * decode: G = decode_group_heads(num_kv_heads, page_size). G > 0 (page_size <= 16
+    and num_kv_heads <= 8 or a multiple of 8): variant 1, units (b, group of G kv
+    heads) b-major, max_workers = num_sms unless given, grid = P. Otherwise variant 0,
+    units (b, kv head) b-major, max_workers = 8 * num_sms unless given,
+    grid = ceil(P / 8). Both: len = request length, tile 16, aux0 = kv_indptr,
+    aux1 = kv_indices.
   * MLA: units (query token n = b*q_len + t, latent half v) n-major, len = seq_lens[b],
     tile 64, max_workers = num_sms, grid = P, no aux, variant 0.
 
@@ -109,20 +112,39 @@ def linear_partition(unit_len, tile, max_workers):
     return worker_ptr, chunks, slots, merges
 
 
-def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_qo_heads,
-                num_kv_heads, num_sms, max_workers=0):
+def decode_group_heads(num_kv_heads, page_size):
+    """kv heads per unit of the page-major decode variant (0: the variant does not apply)."""
+    if page_size > 16:
+        return 0
+    if num_kv_heads <= 8:
+        return num_kv_heads
+    return 8 if num_kv_heads % 8 == 0 else 0
+
+
+def decode_units(kv_indptr, kv_last_page_len, batch, page_size, num_kv_heads):
+    """Token count of every decode unit, in unit order."""
+    G = decode_group_heads(num_kv_heads, page_size)
+    per_request = num_kv_heads // G if G else num_kv_heads
     lens = []
     for b in range(batch):
         n = int(kv_indptr[b + 1]) - int(kv_indptr[b])
         L = 0 if n == 0 else (n - 1) * page_size + int(kv_last_page_len[b])
-        lens += [L] * num_kv_heads
-    cap = max_workers if max_workers > 0 else 8 * num_sms
+        lens += [L] * per_request
+    return lens
+
+
+def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_qo_heads,
+                num_kv_heads, num_sms, max_workers=0):
+    G = decode_group_heads(num_kv_heads, page_size)
+    lens = decode_units(kv_indptr, kv_last_page_len, batch, page_size, num_kv_heads)
+    cap = max_workers if max_workers > 0 else (num_sms if G else 8 * num_sms)
     wp, ch, slots, merges = linear_partition(lens, 16, cap)
     P = len(wp) - 1
     nnz = int(kv_indptr[batch]) if batch > 0 else 0
     aux0 = [int(x) for x in kv_indptr[:batch + 1]] if batch > 0 else []
     aux1 = [int(x) for x in kv_indices[:nnz]]
-    return _assemble(1, len(lens), wp, ch, slots, merges, 16, aux0, aux1, (P + 7) // 8, 0)
+    grid = P if G else (P + 7) // 8
+    return _assemble(1, len(lens), wp, ch, slots, merges, 16, aux0, aux1, grid, 1 if G else 0)
 
 
 def mla_meta(seq_lens, batch, q_len, num_sms):

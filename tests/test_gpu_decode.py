@@ -38,6 +38,9 @@ CASES = [
     (5, 16, 1, 64, 16, 3, 300, torch.float16, 9),      # g = 16, D = 64, fp16
     (6, 4, 4, 128, 8, 1, 90, torch.bfloat16, 4),       # g = 1, page size 8
     (2, 12, 4, 64, 32, 33, 97, torch.float16, 3),      # g = 3 (not a power of two)
+    (3, 32, 16, 64, 16, 20, 300, torch.float16, 6),    # two groups of 8 kv heads per request
+    (2, 24, 12, 128, 16, 10, 200, torch.bfloat16, 4),  # 12 kv heads: per-kv-head variant
+    (4, 64, 8, 128, 8, 1, 200, torch.bfloat16, 5),     # g = 8, page size 8, 8 kv heads
 ]
 
 
@@ -54,6 +57,37 @@ def test_decode_small(cuda, case):
     ref, ref_lse = _oracle(d, dt)
     assert_close(to64(out), ref, TOL, TOL, "out")
     assert_close(lse.cpu().numpy(), ref_lse, TOL, TOL, "lse")
+
+
+@pytest.mark.parametrize("case", [
+    (4, 8, 2, 128, 16, 1, 400, torch.bfloat16, 7),     # page-major variant, fused merges
+    (3, 32, 8, 128, 64, 100, 700, torch.bfloat16, 5),  # per-kv-head variant, fused merges
+    (5, 16, 1, 64, 8, 0, 300, torch.float16, 9),       # page 8, some empty requests
+    (2, 16, 2, 128, 16, 900, 1000, torch.bfloat16, 20),  # > 8 pieces per unit: two kernels
+])
+def test_fused_merge_matches_two_kernel_path(cuda, case):
+    """bskv_run_decode merges split units inside the attention kernel (the last worker of a
+    unit merges it); bskv_run_decode_partial + bskv_decode_merge do it in two kernels.
+    Both apply the same arithmetic in the same order, so they agree bit for bit, and a
+    second fused run (merge counters reset by the first) gives the same bits again."""
+    B, Hq, Hkv, D, ps, lo, hi, dtype, mw = case
+    d = synth.paged_decode_inputs(400 + B + ps, B, Hq, Hkv, D, ps, lo, hi, dtype=dtype)
+    p = _plan(d, dtype, mw)
+    assert p.metadata()[6] > 0, "expected split units"
+    q, kv = d["q"].to(cuda), d["kv_cache"].to(cuda)
+    fused, fused_lse = bskv.bskv_run_decode(p, q, kv, return_lse=True)
+    again, again_lse = bskv.bskv_run_decode(p, q, kv, return_lse=True)
+    two = torch.full_like(fused, float("nan"))
+    two_lse = torch.full_like(fused_lse, float("nan"))
+    bskv.bskv_run_decode_partial(p, q, kv, out=two, lse=two_lse)
+    bskv.bskv_decode_merge(p, two, two_lse)
+    torch.cuda.synchronize()
+    assert bskv.bskv_get_device_status() == 0
+    assert torch.equal(fused, again) and torch.equal(fused_lse, again_lse)
+    assert torch.equal(fused, two) and torch.equal(fused_lse, two_lse)
+    dt = "bf16" if dtype == torch.bfloat16 else "fp16"
+    ref, ref_lse = _oracle(d, dt)
+    assert_close(to64(fused), ref, TOL, TOL, "out")
 
 
 def test_decode_zero_length_requests(cuda):

@@ -60,8 +60,13 @@ def test_decode_plan_bit_exact(lib, name, over):
                                d["kv_last_page_len"].tolist(), d["batch"], d["page_size"],
                                d["num_qo_heads"], d["num_kv_heads"], SMS)
     assert meta == ref
-    lens = [int(L) for L in d["kv_lens"] for _ in range(d["num_kv_heads"])]
+    lens = plan_ref.decode_units(d["kv_indptr"].tolist(), d["kv_last_page_len"].tolist(),
+                                 d["batch"], d["page_size"], d["num_kv_heads"])
     _check_linear(meta, lens, 16)
+    # pages of at most 16 tokens take the page-major variant: one unit per request here
+    group = d["page_size"] <= 16
+    assert plan_ref.sections(meta)["variant"] == (1 if group else 0)
+    assert len(lens) == d["batch"] * (1 if group else d["num_kv_heads"])
 
 
 def test_decode_plan_full_long_context(lib):
@@ -85,7 +90,15 @@ def test_decode_plan_zero_length_and_max_workers(lib):
     assert meta == plan_ref.decode_meta(indptr, idx, last, 4, 16, 4, 2, 1, 3)
     s = plan_ref.sections(meta)
     zero_units = {m[0] for m in s["merges"] if m[2] == 0}
-    assert zero_units == {0, 1, 4, 5}  # requests 0 and 2, both kv heads
+    assert s["variant"] == 1 and zero_units == {0, 2}  # requests 0 and 2 (both kv heads)
+    # the same requests with 32-token pages take the per-kv-head variant
+    p = bskv.bskv_plan_decode(indptr, idx, [0, 7, 0, 32], 6, 32, 4, 2, 64, torch.bfloat16,
+                              num_sms=1, max_workers=3)
+    meta = p.metadata()
+    assert meta == plan_ref.decode_meta(indptr, idx, [0, 7, 0, 32], 4, 32, 4, 2, 1, 3)
+    s = plan_ref.sections(meta)
+    zero_units = {m[0] for m in s["merges"] if m[2] == 0}
+    assert s["variant"] == 0 and zero_units == {0, 1, 4, 5}  # requests 0 and 2, both kv heads
 
 
 @pytest.mark.parametrize("name,over", [
