@@ -38,7 +38,7 @@ constexpr int kDecodeTile = 16;        // tokens per pipeline stage of a decode 
 constexpr int kDecodeWarps = 8;        // decode workers (warps) per CTA, one CTA per SM
 constexpr int kBsrGenericRows = 64;    // packed (token, head) rows per general-BSR unit
 constexpr int kBsrGenericCtasPerSm = 4;
-constexpr int kMlaTile = 64;           // sparse rows per MLA chunk
+constexpr int kMlaTile = 128;          // sparse rows per MLA tile
 constexpr int kMlaVSplit = 2;          // the 512 latent output values split in halves
 constexpr int kMlaVDim = 512 / kMlaVSplit;
 

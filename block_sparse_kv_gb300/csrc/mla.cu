@@ -6,26 +6,30 @@
 // on the QK product and bmm2_scale on the output, BF16 output of 512 values and FP32 LSE;
 // "FlashInfer Compatibility Wrapper", scale folding. V is the first 512 values of a row.
 //
-// GB300 design (persistent, one CTA per SM, 12 warps). The work unit is (query token,
-// latent half): all 128 heads form the M=128 rows of every MMA and the CTA accumulates
-// O for one 256-value half of the output in TMEM (256 columns), so S and O fit side by side
-// (the full 128 x 512 fp32 accumulator alone would fill TMEM). S is computed by both halves.
-//   warps 0-5  two gather groups of 96 threads taking alternate tiles: a group stages the
-//              tile's 64 row ids in shared memory, copies the rows with 16-byte cp.async
-//              (consecutive threads, consecutive chunks of a row) into the swizzled panels
-//              (row r, chunk c -> chunk c ^ (r mod 8)) and publishes the tile as soon as its
-//              own copies have landed. Thread 0 also TMA-loads the query tile (four
-//              128B-swizzled panels of 128 B plus one 64B-swizzled panel for the rotated
-//              tail). On this part many-row gathers are faster through the load/store pipes
-//              than through TMA tile::gather4, which moves 128-byte pieces one at a time;
-//   warp 6     allocates TMEM; lane 0 issues S = Q K^T (M=128, N=64, K=576: 18 MMAs of K=32)
-//              and O += P V_half (M=128, N=256, K=64; the gathered panels serve as the
-//              MN-major V operand), advancing prebuilt descriptors by address only;
-//   warps 8-15 two softmax warpgroups; thread = head = TMEM lane, each group owns 32 of a
-//              tile's 64 columns and 128 of the 256 output values. The row max and, at the end,
-//              the row sum are combined through shared memory; lazy max rescaling (threshold
-//              2^8); exponentials as packed f16x2 (ex2.approx.f16x2) converted straight to
-//              E4M3 for the PV MMA; the epilogue writes bf16 out or the split-KV partial state.
+// GB300 design (persistent, clusters of two CTAs, one CTA per SM, 16 warps). A work unit is
+// one query token; the two CTAs of a cluster take the same units, CTA rank v accumulating
+// the 256 output values of latent half v in TMEM. Both compute the same S = Q K^T (128 heads
+// = the M=128 rows, 128 gathered rows = N, K = 576), so each gathered row is needed by both:
+// each CTA gathers half of a tile's rows and pushes them into its partner's shared memory.
+// TMEM (512 columns): O (256), the query's 512 latent bytes as the E4M3 A operand of QK
+// (128, four values per column), S (128). Shared memory: the query's 64-byte rotated tail,
+// P (E4M3, two buffers), and the gathered tiles split by lifetime: a K part (the other
+// latent half and the tail, freed once QK has read it; two slots) and a V part (the unit's
+// latent half, freed after PV; three slots).
+//   warps 0-5  gather: 192 threads copy this CTA's 64 rows of a tile (16-byte cp.async into
+//              128B-swizzled panels), then the leader arms kv_full for the partner's half and
+//              pushes this half to the partner with five shared-to-shared bulk copies. Row ids
+//              are fetched one tile ahead;
+//   warp 6     allocates TMEM; lane 0 issues QK (16 MMAs with A in TMEM, 2 with the tail in
+//              shared memory, N = 128) and PV (A = P in shared memory, B = the V part read
+//              MN-major, N = 256); slot releases are committed to both CTAs' barriers;
+//   warp 7     TMA-loads the query tail once per token;
+//   warps 8-15 two softmax warpgroups; thread = head = TMEM lane, each group owns 64 of a
+//              tile's columns and 128 of the 256 output values: it reads S (and releases it
+//              for the next QK at once), combines the row max with the other group, applies
+//              lazy rescaling (threshold 2^8), forms P with packed f16x2 exponentials converted
+//              to E4M3, and writes O (bf16) or the split-KV partial state in the epilogue; at a
+//              token's last tile it also writes the next token's query into TMEM.
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -38,30 +42,37 @@ namespace {
 
 using namespace dev;
 
-constexpr int kRows = 64;                     // gathered rows per tile
-constexpr int kStages = 3;
+constexpr int kRows = 128;                    // gathered rows per tile
+constexpr int kKSlots = 2;                    // K parts in flight (freed after QK)
+constexpr int kVSlots = 3;                    // V parts in flight (freed after PV)
 constexpr int kThreads = 512;
-constexpr uint32_t kNopePanelQ = 128 * 128;   // [128 heads x 128 B]
-constexpr uint32_t kRopePanelQ = 128 * 64;    // [128 heads x 64 B]
-constexpr uint32_t kQBytes = 4 * kNopePanelQ + kRopePanelQ;  // 72 KB
-constexpr uint32_t kNopePanelK = kRows * 128;  // 8 KB
-constexpr uint32_t kRopePanelK = kRows * 64;   // 4 KB
-constexpr uint32_t kStageBytes = 4 * kNopePanelK + kRopePanelK;  // 36 KB
-constexpr uint32_t kPBytes = 128 * 64;         // [128 heads x 64 tokens] E4M3
-constexpr uint32_t kSmemQ = 0;
-constexpr uint32_t kSmemKV = kSmemQ + kQBytes;
-constexpr uint32_t kSmemP = kSmemKV + kStages * kStageBytes;
-constexpr uint32_t kSmemBar = kSmemP + 2 * kPBytes;
-constexpr uint32_t kSmemIdx = kSmemBar + 512;  // [stages][64] sanitised row ids
+constexpr int kGatherThreads = 192;           // warps 0-5
+constexpr int kHalfRows = kRows / 2;          // rows each CTA of the pair gathers per tile
+constexpr uint32_t kPanel = kRows * 128;      // [128 rows x 128 B]: 16 KB
+constexpr uint32_t kRopePanel = kRows * 64;   // [128 rows x 64 B]: 8 KB
+constexpr uint32_t kKPart = 2 * kPanel + kRopePanel;  // other latent half + rotated tail
+constexpr uint32_t kVPart = 2 * kPanel;               // the unit's latent half
+// bytes of one CTA's half tile: 64 rows of the four 128-byte panels and of the 64-byte tail
+constexpr uint32_t kHalfTileBytes = 4 * (kHalfRows * 128) + kHalfRows * 64;
+constexpr uint32_t kPBytes = 128 * 128;               // [128 heads x 128 keys] E4M3
+constexpr uint32_t kSmemQR = 0;                                  // query tail, 8 KB
+constexpr uint32_t kSmemP = kSmemQR + kRopePanel;                // 2 x 16 KB
+constexpr uint32_t kSmemK = kSmemP + 2 * kPBytes;                // 2 x 40 KB
+constexpr uint32_t kSmemV = kSmemK + kKSlots * kKPart;           // 3 x 32 KB
+constexpr uint32_t kSmemBar = kSmemV + kVSlots * kVPart;
+constexpr uint32_t kSmemIdx = kSmemBar + 256;                    // [3][128] row ids
 // [3][2 groups][128]: row maxima by tile parity (slots 0, 1) and row sums (slot 2)
-constexpr uint32_t kSmemRed = kSmemIdx + kStages * kRows * 4;
+constexpr uint32_t kSmemRed = kSmemIdx + kVSlots * kRows * 4;
 constexpr uint32_t kSmemBytes = kSmemRed + 3 * 2 * 128 * 4;
-constexpr int kGatherThreads = 96;  // per group
 constexpr uint32_t kTmemCols = 512;
 constexpr int kVD = kMlaVDim;  // 256
+// TMEM columns: O (the unit's 256 output values) at 0, the query's 512 latent bytes at 256
+// (E4M3, four per column: the A operand of QK), S at 384.
+constexpr uint32_t kTmemQ = 256, kTmemS = 384;
 
 struct MlaParams {
   const int32_t* meta;
+  const uint8_t* q;
   const uint8_t* kv;
   int64_t num_rows;
   const int32_t* indices;
@@ -76,13 +87,15 @@ struct MlaParams {
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, drain;
-  uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done, o_free;
+  uint64_t q_full, qr_full, q_empty, drain;
+  uint64_t kv_full[kVSlots], v_empty[kVSlots], k_empty[kKSlots];
+  uint64_t s_full, s_empty, p_full[2], o_done[2];
+  uint64_t o_free;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(kSmemBytes + 1024 <= 232448, "shared memory");
 
 __device__ __forceinline__ __half2 h2exp2_approx(__half2 x) {
   uint32_t in = *reinterpret_cast<uint32_t*>(&x), out;
@@ -98,11 +111,11 @@ __device__ __forceinline__ uint32_t half2_to_e4m3x2(__half2 x) {
   return out;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    mla_kernel(const __grid_constant__ CUtensorMap qmap_nope,
-               const __grid_constant__ CUtensorMap qmap_rope,
-               const __grid_constant__ CUtensorMap kvmap_nope,
-               const __grid_constant__ CUtensorMap kvmap_rope, const MlaParams p) {
+// Query token of a chunk (a unit is one query token; the CTA pair splits its latent halves).
+__device__ __forceinline__ int chunk_token(const int4& ch) { return ch.x; }
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_kernel(const __grid_constant__ CUtensorMap qmap_rope, const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -111,22 +124,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* hdr = p.meta;
   const int32_t* wptr = hdr + hdr[H_OFF_WORKERS];
   const int4* chunks = reinterpret_cast<const int4*>(hdr + hdr[H_OFF_CHUNKS]);
-  const int c0 = wptr[blockIdx.x], c1 = wptr[blockIdx.x + 1];
+  // The two CTAs of a cluster take the same chunks: CTA rank v computes latent half v.
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  const int vh = int(rank);
+  const int c0 = wptr[blockIdx.x >> 1], c1 = wptr[(blockIdx.x >> 1) + 1];
   const bool forced = forced_timeout(p.st);
 
   if (threadIdx.x == 0) {
-    mbar_init(&B.q_full, 1);
+    mbar_init(&B.q_full, 256);
+    mbar_init(&B.qr_full, 1);
     mbar_init(&B.q_empty, 1);
     mbar_init(&B.drain, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&B.kv_full[s], kGatherThreads);
-      mbar_init(&B.kv_empty[s], 1);
+    // kv_full: this CTA's gather leader (after its half landed) + the peer's half as tx bytes;
+    // v_empty / k_empty: both CTAs' MMA issuers (a slot is refilled in both at once).
+    for (int s = 0; s < kVSlots; ++s) {
+      mbar_init(&B.kv_full[s], 1);
+      mbar_init(&B.v_empty[s], 2);
     }
+    for (int s = 0; s < kKSlots; ++s) mbar_init(&B.k_empty[s], 2);
+    mbar_init(&B.s_full, 1);
+    mbar_init(&B.s_empty, 256);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&B.s_full[b], 1);
       mbar_init(&B.p_full[b], 256);
+      mbar_init(&B.o_done[b], 1);
     }
-    mbar_init(&B.o_done, 1);
     mbar_init(&B.o_free, 256);
     B.abort = 0;
     fence_mbar_init();
@@ -136,186 +157,323 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
   volatile int* abort_flag = &B.abort;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&B.abort), peer);
+  auto raise_abort = [&]() {
+    *abort_flag = 1;
+    st_cluster_u32(peer_abort, 1u);
+  };
 
   if (warp < 6) {
-    // -------------------------------------------------------------- gather groups
-    // Group grp (0/1) owns the tiles with kvc % 2 == grp. A tile is published (kv_full, 128
-    // arrivals) once the group's own copies of it are complete, so no tile waits for the
-    // issue of another; with three stages, gathering tile t only needs the stage released by
-    // PV(t-3), which the MMA issues after QK(t-2): no cycle. Decisions of a group go through
-    // bar_and on its own named barrier (1 + grp, 96 threads).
-    const int grp = threadIdx.x / kGatherThreads;
-    const int pt = threadIdx.x % kGatherThreads;
-    const uint32_t bar_id = 1 + grp;
+    // -------------------------------------------------------------- gather group
+    // A tile is 128 rows x 576 bytes; CTA rank c copies rows 64 c .. 64 c + 63 with 16-byte
+    // cp.async (192 threads, 12 chunks each) and its leader then pushes them into the peer's
+    // shared memory with five bulk copies, so each row is read from L2 once per pair. Panels
+    // are 128B-swizzled (row r, 16-byte chunk c -> chunk c ^ (r mod 8)); the 64-byte tail
+    // uses the 64-byte pattern. The unit's latent half goes to a V part, the other half and
+    // the tail to a K part; the peer, computing the other half, files the same panels the
+    // other way round. Decisions go through bar_and on named barrier 1 (192 threads).
+    const int pt = threadIdx.x;
     int32_t* idx_smem = reinterpret_cast<int32_t*>(sm + kSmemIdx);
-    // This thread's 24 chunks of a tile: chunk id pt + 96 k -> (row, 16-byte column).
-    constexpr int kPer = (kRows * 36) / kGatherThreads;
-    uint32_t off[kPer];
+    constexpr int kPer = (kHalfRows * 36) / kGatherThreads;  // 12 chunks per thread
+    uint32_t off[kPer];  // bit 31: V part
     uint16_t col[kPer];
-    uint8_t rowk[kPer];
+    uint8_t rowk[kPer];  // tile row
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int cid = pt + kGatherThreads * k;
-      const int r = cid / 36, q = cid % 36;
-      off[k] = q < 32 ? (q >> 3) * kNopePanelK + r * 128 + (((q & 7) ^ (r & 7)) << 4)
-                      : 4 * kNopePanelK + r * 64 + ((((q - 32) & 3) ^ ((r >> 1) & 3)) << 4);
-      col[k] = uint16_t(q * 16);
-      rowk[k] = uint8_t(r);
+    for (int j = 0; j < kPer; ++j) {
+      const int cid = pt + kGatherThreads * j;
+      const int r = int(rank) * kHalfRows + cid / 36, q = cid % 36;
+      if (q < 32) {
+        const int pn = q >> 3;
+        off[j] = ((pn >> 1) == vh ? 0x80000000u : 0u) |
+                 uint32_t((pn & 1) * kPanel + r * 128 + (((q & 7) ^ (r & 7)) << 4));
+      } else {
+        off[j] = uint32_t(2 * kPanel + r * 64 + ((((q - 32) & 3) ^ ((r >> 1) & 3)) << 4));
+      }
+      col[j] = uint16_t(q * 16);
+      rowk[j] = uint8_t(r);
     }
-    uint32_t qc = 0, kvc = 0;
+    // The peer's copy of this CTA's rows: nope panel pn is in the peer's V part when its half
+    // is the peer's (pn / 2 != vh), else in its K part; the tail always in the K part.
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t peer_base = mapa_shared(sbase, peer);
+    uint32_t kvc = 0, armed = 0;
     bool ok = true;
+    const int tr = int(rank) * kHalfRows + pt;  // tile row whose id this thread loads
+    // Row id of tile row tr of the tile at (chunk cj, first row u0); loaded one tile ahead.
+    auto load_id = [&](int cj, int u0) -> int32_t {
+      if (pt >= kHalfRows || cj >= c1) return 0;
+      const int4 cn = chunks[cj];
+      return u0 + tr < cn.z ? __ldg(p.indices + int64_t(cn.x) * p.top_k + u0 + tr) : 0;
+    };
+    int32_t next_id = c0 < c1 ? load_id(c0, chunks[c0].y) : 0;
     for (int ci = c0; ci < c1 && ok; ++ci) {
       const int4 ch = chunks[ci];
-      const int n = ch.x / kMlaVSplit;
-      const int32_t* idx_row = p.indices + int64_t(n) * p.top_k;
-      bool good = true;
-      if (grp == 0 && pt == 0) {
-        good = !*abort_flag && mbar_wait(&B.q_empty, (qc & 1u) ^ 1u, p.st, forced);
-        if (good) {
-          mbar_arrive_expect_tx(&B.q_full, kQBytes);
-          for (int pn = 0; pn < 4; ++pn)
-            tma_load_2d(sm + kSmemQ + pn * kNopePanelQ, &qmap_nope, pn * 128, n * p.heads, &B.q_full);
-          tma_load_2d(sm + kSmemQ + 4 * kNopePanelQ, &qmap_rope, 512, n * p.heads, &B.q_full);
-        }
-      }
-      if (grp == 0) ++qc;
-      ok = bar_and(bar_id, kGatherThreads, good);
-      if (!ok) break;
       for (int t0 = ch.y; t0 < ch.z; t0 += kRows, ++kvc) {
-        if ((kvc & 1u) != uint32_t(grp)) continue;
-        const int s = kvc % kStages;
-        int32_t my_id = 0;
-        if (pt < kRows && t0 + pt < ch.z) {
-          my_id = __ldg(idx_row + t0 + pt);
-          if (my_id < 0 || my_id >= p.num_rows) {
-            record_error(p.st, BSKV_ERR_DEVICE_INDEX);
-            my_id = 0;
-          }
+        const int v = kvc % kVSlots, k = kvc % kKSlots;
+        int32_t my_id = next_id;
+        next_id = t0 + kRows < ch.z ? load_id(ci, t0 + kRows)
+                                    : (ci + 1 < c1 ? load_id(ci + 1, chunks[ci + 1].y) : 0);
+        if (my_id < 0 || my_id >= p.num_rows) {
+          record_error(p.st, BSKV_ERR_DEVICE_INDEX);
+          my_id = 0;
         }
-        good = !*abort_flag && mbar_wait(&B.kv_empty[s], ((kvc / kStages) & 1u) ^ 1u, p.st, forced);
-        int32_t* ib = idx_smem + s * kRows;
-        if (pt < kRows) ib[pt] = my_id;
-        ok = bar_and(bar_id, kGatherThreads, good);
+        bool good = !*abort_flag &&
+                    mbar_wait(&B.v_empty[v], ((kvc / kVSlots) & 1u) ^ 1u, p.st, forced) &&
+                    mbar_wait(&B.k_empty[k], ((kvc / kKSlots) & 1u) ^ 1u, p.st, forced);
+        // the push of tile kvc - 2 (same K slot) must have read its source before it is
+        // overwritten; the push of kvc - 1 may still be running
+        if (pt == 0) bulk_wait_read1();
+        int32_t* ib = idx_smem + v * kRows;
+        if (pt < kHalfRows) ib[tr] = my_id;
+        ok = bar_and(1, kGatherThreads, good);
         if (!ok) break;
-        uint8_t* stage = sm + kSmemKV + s * kStageBytes;
+        uint8_t* vbase = sm + kSmemV + v * kVPart;
+        uint8_t* kbase = sm + kSmemK + k * kKPart;
         const int valid = ch.z - t0;
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          if (rowk[k] < valid)
-            cp_async_16(stage + off[k], p.kv + int64_t(ib[rowk[k]]) * 576 + col[k]);
+        for (int j = 0; j < kPer; ++j) {
+          uint8_t* dst = ((off[j] >> 31) ? vbase : kbase) + (off[j] & 0x7fffffffu);
+          if (rowk[j] < valid)
+            cp_async_16(dst, p.kv + int64_t(ib[rowk[j]]) * 576 + col[j]);
           else
-            *reinterpret_cast<uint4*>(stage + off[k]) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
         }
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        mbar_arrive(&B.kv_full[s]);
+        ok = bar_and(1, kGatherThreads, !*abort_flag);
+        if (!ok) break;
+        if (pt == 0) {
+          // this half is in place: arm kv_full for the peer's half and push ours to the peer
+          mbar_arrive_expect_tx(&B.kv_full[v], kHalfTileBytes);
+          ++armed;
+          const uint32_t vo = kSmemV + v * kVPart, ko = kSmemK + k * kKPart;
+          const uint32_t rows_off = rank * kHalfRows;
+          const uint32_t mbar = mapa_shared(smem_u32(&B.kv_full[v]), peer);
+#pragma unroll
+          for (int pn = 0; pn < 4; ++pn) {
+            const uint32_t in_panel = (pn & 1) * kPanel + rows_off * 128;
+            const uint32_t src = ((pn >> 1) == vh ? vo : ko) + in_panel;
+            const uint32_t dst = ((pn >> 1) != vh ? vo : ko) + in_panel;
+            bulk_s2s_cluster(peer_base + dst, sm + src, kHalfRows * 128, mbar);
+          }
+          bulk_s2s_cluster(peer_base + ko + 2 * kPanel + rows_off * 64,
+                           sm + ko + 2 * kPanel + rows_off * 64, kHalfRows * 64, mbar);
+          bulk_commit();
+        }
       }
     }
-    if (!ok) *abort_flag = 1;
-    if (grp == 0 && pt == 0 && qc > 0 && !ok) mbar_wait(&B.q_full, (qc - 1) & 1u, p.st, false);
+    if (pt == 0) bulk_wait_read0();
+    if (!ok) raise_abort();
+    if (pt == 0 && !ok) {
+      // tiles this CTA armed may still receive the peer's half: let it land (bounded)
+      const uint32_t from = armed > uint32_t(kVSlots) ? armed - kVSlots : 0u;
+      for (uint32_t a = from; a < armed; ++a)
+        mbar_wait(&B.kv_full[a % kVSlots], (a / kVSlots) & 1u, p.st, false);
+    }
+  } else if (warp == 7) {
+    // -------------------------------------------------------------- query tail loader
+    // The rotated 64-byte tail of the query tile (128 heads, 64B swizzle) is TMA-loaded once
+    // per token; the two latent halves of a token reuse it.
+    if (lane == 0) {
+      uint32_t qc = 0;
+      bool ok = true;
+      int cur = -1;
+      for (int ci = c0; ci < c1; ++ci) {
+        const int n = chunk_token(chunks[ci]);
+        if (n == cur) continue;
+        cur = n;
+        if (*abort_flag || !mbar_wait(&B.q_empty, (qc & 1u) ^ 1u, p.st, forced)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&B.qr_full, kRopePanel);
+        tma_load_2d(sm + kSmemQR, &qmap_rope, 512, n * p.heads, &B.qr_full);
+        ++qc;
+      }
+      if (!ok) raise_abort();
+      // the last load issued must land before the CTA may exit (bounded, not forcible)
+      if (qc > 0) mbar_wait(&B.qr_full, (qc - 1) & 1u, p.st, false);
+    }
   } else if (warp == 6) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc(128, 64, 0, 0, 0, 0);
+      constexpr uint32_t idesc_qk = umma_idesc(128, kRows, 0, 0, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc(128, kVD, 0, 0, 0, 1);
       const uint32_t sbase = smem_u32(sm);
-      uint32_t qc = 0, kvc = 0, G = 0, cc = 0;
+      uint32_t qc = 0, kvc = 0, cc = 0;
       bool ok = true;
-      const uint64_t dp = umma_desc(sbase + kSmemP, 16, 512, kSwz64);
-      const uint64_t dv = umma_desc(sbase + kSmemKV, kNopePanelK, 1024, kSwz128);
-      auto pv = [&](uint32_t g, uint32_t kv_use, bool first, int vh) -> bool {
-        const int s = kv_use % kStages;
-        const uint32_t b = g & 1u;
+      // P: K-major, 128B swizzle. V part: MN-major, 128-byte atoms along the output values
+      // (LBO = panel stride), 8-row groups along the rows (SBO = 1024).
+      const uint64_t dp = umma_desc(sbase + kSmemP, 16, 1024, kSwz128);
+      const uint64_t dv = umma_desc(sbase + kSmemV, kPanel, 1024, kSwz128);
+      const uint64_t dqr = umma_desc(sbase + kSmemQR, 16, 512, kSwz64);
+      const uint64_t dkn = umma_desc(sbase + kSmemK, 16, 1024, kSwz128);
+      const uint64_t dvn = umma_desc(sbase + kSmemV, 16, 1024, kSwz128);
+      const uint64_t dkr = umma_desc(sbase + kSmemK + 2 * kPanel, 16, 512, kSwz64);
+      auto pv = [&](uint32_t g, bool first) -> bool {
+        const uint32_t b = g & 1u, v = g % kVSlots;
         if (*abort_flag || !mbar_wait(&B.p_full[b], (g >> 1) & 1u, p.st, forced)) return false;
         if (first && (*abort_flag || !mbar_wait(&B.o_free, (cc & 1u) ^ 1u, p.st, forced))) return false;
         tc_fence_after();
         const uint64_t a0 = dp + ((b * kPBytes) >> 4);
-        const uint64_t b0 = dv + ((s * kStageBytes + (2 * vh) * kNopePanelK) >> 4);
+        const uint64_t b0 = dv + ((v * kVPart) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
+        for (int kk = 0; kk < kRows / 32; ++kk)
           umma_f8(tmem, a0 + kk * 2, b0 + kk * 256, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        umma_commit(&B.o_done);
-        umma_commit(&B.kv_empty[s]);
+        umma_commit(&B.o_done[b]);
+        umma_commit_mc(&B.v_empty[v], 0x3);  // both CTAs' V part free
         return true;
       };
-      // Descriptors are built once; a k-step only advances the start-address field
-      // (bits 0-13, in 16-byte units), which cannot carry out for shared addresses.
-      const uint64_t dq_n = umma_desc(sbase + kSmemQ, 16, 1024, kSwz128);
-      const uint64_t dq_r = umma_desc(sbase + kSmemQ + 4 * kNopePanelQ, 16, 512, kSwz64);
-      const uint64_t dk_n = umma_desc(sbase + kSmemKV, 16, 1024, kSwz128);
-      const uint64_t dk_r = umma_desc(sbase + kSmemKV + 4 * kNopePanelK, 16, 512, kSwz64);
+      int cur = -1;
       for (int ci = c0; ci < c1 && ok; ++ci) {
         const int4 ch = chunks[ci];
-        const int vh = ch.x % kMlaVSplit;
+        const int n = chunk_token(ch);
         const int nt = (ch.z - ch.y + kRows - 1) / kRows;
-        if (*abort_flag || !mbar_wait(&B.q_full, qc & 1u, p.st, forced)) { ok = false; break; }
-        ++qc;
-        tc_fence_after();
-        const uint32_t kv_first = kvc;
+        const bool last_use = ci + 1 == c1 || chunk_token(chunks[ci + 1]) != n;
+        if (n != cur) {
+          if (*abort_flag || !mbar_wait(&B.q_full, qc & 1u, p.st, forced) ||
+              !mbar_wait(&B.qr_full, qc & 1u, p.st, forced)) { ok = false; break; }
+          ++qc;
+          cur = n;
+        }
+        const uint32_t g0 = kvc;
         for (int t = 0; t < nt; ++t, ++kvc) {
-          const int s = kvc % kStages;
-          if (*abort_flag || !mbar_wait(&B.kv_full[s], (kvc / kStages) & 1u, p.st, forced)) { ok = false; break; }
+          const uint32_t v = kvc % kVSlots, k = kvc % kKSlots;
+          if (*abort_flag || !mbar_wait(&B.kv_full[v], (kvc / kVSlots) & 1u, p.st, forced)) { ok = false; break; }
+          // S is single-buffered: the softmax must have read the previous tile's S.
+          if (kvc > 0 && (*abort_flag || !mbar_wait(&B.s_empty, (kvc - 1) & 1u, p.st, forced))) { ok = false; break; }
           tc_fence_after();
-          const uint32_t so = (s * kStageBytes) >> 4;
-          const uint32_t sd = tmem + 256 + ((G + t) & 1u) * 64;
+          // S = Q K^T over the 512 latent values (A from TMEM) and the 64-value tail.
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk) {
-            const uint32_t qo = ((kk >> 2) * kNopePanelQ + (kk & 3) * 32) >> 4;
-            const uint32_t ko = ((kk >> 2) * kNopePanelK + (kk & 3) * 32) >> 4;
-            umma_f8(sd, dq_n + qo, dk_n + so + ko, idesc_qk, kk > 0 ? 1u : 0u);
+            const int pn = kk >> 2;
+            const uint64_t bd = ((pn >> 1) == vh ? dvn + ((v * kVPart) >> 4) : dkn + ((k * kKPart) >> 4)) +
+                                (((pn & 1) * kPanel + (kk & 3) * 32) >> 4);
+            umma_f8_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
-            umma_f8(sd, dq_r + kk * 2, dk_r + so + kk * 2, idesc_qk, 1u);
-          umma_commit(&B.s_full[(G + t) & 1u]);
-          if (t >= 1 && !pv(G + t - 1, kv_first + t - 1, t == 1, vh)) { ok = false; break; }
+            umma_f8(tmem + kTmemS, dqr + kk * 2, dkr + ((k * kKPart) >> 4) + kk * 2, idesc_qk, 1u);
+          umma_commit(&B.s_full);
+          umma_commit_mc(&B.k_empty[k], 0x3);  // both CTAs' K part free
+          if (t + 1 == nt && last_use) umma_commit(&B.q_empty);
+          if (t >= 1 && !pv(kvc - 1, t == 1)) { ok = false; break; }
         }
         if (!ok) break;
-        if (!pv(G + nt - 1, kv_first + nt - 1, nt == 1, vh)) { ok = false; break; }
-        umma_commit(&B.q_empty);
-        G += nt;
+        if (!pv(g0 + nt - 1, nt == 1)) { ok = false; break; }
         ++cc;
       }
-      if (!ok) *abort_flag = 1;
+      if (!ok) raise_abort();
       umma_commit(&B.drain);
       mbar_wait(&B.drain, 0, p.st, false);
     }
-  } else if (warp >= 8) {
+  } else {
     // -------------------------------------------------------------- softmax warpgroups
-    const int wg = (warp - 8) >> 2;          // 0: columns 0-31 / O 0-127; 1: 32-63 / 128-255
+    // Group wg owns tile columns 64 wg .. 64 wg + 63, output values 128 wg .. 128 wg + 127
+    // and query bytes 256 wg .. 256 wg + 255; thread = head = TMEM lane.
+    const int wg = (warp - 8) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;            // head
     const uint32_t lane_base = uint32_t(q4 * 32) << 16;
-    float* red = reinterpret_cast<float*>(sm + kSmemRed);  // [parity][group][row]
-    uint32_t G = 0, od = 0;
+    float* red = reinterpret_cast<float*>(sm + kSmemRed);  // [slot][group][row]
+    uint32_t G = 0, qc = 0;
+    uint32_t od_next[2] = {0u, 1u};  // next tile of each parity whose PV is not yet waited for
     bool ok = true;
+    // Wait for the PVs of all tiles up to `upto` (the two o_done barriers take alternate
+    // tiles, so neither falls two phases behind).
+    auto consume = [&](int64_t upto) -> bool {
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        while (int64_t(od_next[b]) <= upto) {
+          if (!warp_wait(&B.o_done[b], (od_next[b] >> 1) & 1u, p.st, forced, abort_flag)) return false;
+          od_next[b] += 2;
+        }
+      }
+      return true;
+    };
+    // Query latent bytes of head r for token n into TMEM, once the previous token's last QK
+    // has completed (q_empty); then q_full.
+    auto load_q = [&](int n) -> bool {
+      if (!warp_wait(&B.q_empty, (qc & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
+      ++qc;
+      tc_fence_after();
+#pragma unroll 1
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t qv[32];
+        if (r < p.heads) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              p.q + (int64_t(n) * p.heads + r) * 576 + wg * 256 + hlf * 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 x4 = __ldg(src + i);
+            qv[4 * i] = x4.x; qv[4 * i + 1] = x4.y; qv[4 * i + 2] = x4.z; qv[4 * i + 3] = x4.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) qv[i] = 0u;
+        }
+        tmem_st32(tmem + lane_base + kTmemQ + wg * 64 + hlf * 32, qv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&B.q_full);
+      return true;
+    };
+    int cur = -1;
     for (int ci = c0; ci < c1 && ok; ++ci) {
       const int4 ch = chunks[ci];
-      const int n = ch.x / kMlaVSplit, vh = ch.x % kMlaVSplit;
+      const int n = chunk_token(ch);
       const int nt = (ch.z - ch.y + kRows - 1) / kRows;
+      if (n != cur) {
+        // first chunk of this CTA (later tokens are loaded during the previous chunk)
+        cur = n;
+        ok = load_q(n);
+        if (!ok) break;
+      }
+      // token of the next chunk, if it needs a new query
+      const int n_next = ci + 1 < c1 && chunk_token(chunks[ci + 1]) != n ? chunk_token(chunks[ci + 1]) : -1;
       float m_run = -INFINITY, l_run = 0.f;
       for (int t = 0; t < nt; ++t, ++G) {
         const uint32_t b = G & 1u;
-        bool good = warp_wait(&B.s_full[b], (G >> 1) & 1u, p.st, forced, abort_flag);
-        uint32_t sr[32];
+        bool good = warp_wait(&B.s_full, G & 1u, p.st, forced, abort_flag);
+        uint32_t sr[64];
         if (good) {
           tc_fence_after();
-          tmem_ld32(tmem + lane_base + 256 + b * 64 + wg * 32, sr);
+          const uint32_t sa = tmem + lane_base + kTmemS + wg * 64;
+          tmem_ld32(sa, sr);
+          tmem_ld32(sa + 32, sr + 32);
           tmem_ld_wait();
+          tc_fence_before();
         }
-        const int valid = min(kRows, ch.z - (ch.y + t * kRows)) - wg * 32;
-        float mx = -INFINITY;
+        mbar_arrive(&B.s_empty);  // S may be overwritten by the next QK
+        if (t + 1 == nt && n_next >= 0) {
+          // The last QK of this token has completed (its S is loaded): bring the next
+          // token's query in now, so the next chunk's QK overlaps this tile and the epilogue.
+          good = good && load_q(n_next);
+          cur = n_next;
+        }
+        const int valid = min(kRows, ch.z - (ch.y + t * kRows)) - wg * 64;
+        // scaled logits, kept in place as float bits
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float x = c < valid ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-          sr[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+        for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * p.scale_log2);
+        if (valid < 64) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sr[c] = c < valid ? sr[c] : __float_as_uint(-INFINITY);
         }
+        auto x = [&](int c) { return __uint_as_float(sr[c]); };
+        float m8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          m8[j] = fmaxf(fmaxf(fmaxf(x(j), x(j + 8)), fmaxf(x(j + 16), x(j + 24))),
+                        fmaxf(fmaxf(x(j + 32), x(j + 40)), fmaxf(x(j + 48), x(j + 56))));
+        }
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         red[(b * 2 + wg) * 128 + r] = mx;
         // both groups meet here once per tile (named barrier 3, 256 threads)
         ok = bar_and(3, 256, good);
@@ -331,35 +489,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float ref = m_use == -INFINITY ? 0.f : m_use;
-        // p = 2^(x - ref) in f16x2 pairs, straight to E4M3 pairs; partial row sum in f16x2.
-        uint32_t pk[8];
-        __half2 hsum = __float2half2_rn(0.f);
+        rescale = __any_sync(0xffffffffu, rescale);
+        // P buffer b was last read by the PV of tile G - 2.
+        if (!consume(int64_t(G) - 2)) { ok = false; break; }
+        // p = 2^(x - ref) in f16x2 pairs, straight to E4M3 pairs, 16 keys (one 16-byte chunk
+        // of the 128B-swizzled P row) at a time; row sum in f16x2.
+        uint8_t* prow = sm + kSmemP + b * kPBytes + r * 128;
+        __half2 hs[4];
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const __half2 h0 = __floats2half2_rn(__uint_as_float(sr[c]) - ref, __uint_as_float(sr[c + 1]) - ref);
-          const __half2 h1 = __floats2half2_rn(__uint_as_float(sr[c + 2]) - ref, __uint_as_float(sr[c + 3]) - ref);
-          const __half2 e0 = h2exp2_approx(h0), e1 = h2exp2_approx(h1);
-          hsum = __hadd2(hsum, __hadd2(e0, e1));
-          pk[c / 4] = half2_to_e4m3x2(e0) | (half2_to_e4m3x2(e1) << 16);
+        for (int c16 = 0; c16 < 4; ++c16) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = c16 * 16 + j * 4;
+            const __half2 e0 = h2exp2_approx(__floats2half2_rn(x(c) - ref, x(c + 1) - ref));
+            const __half2 e1 = h2exp2_approx(__floats2half2_rn(x(c + 2) - ref, x(c + 3) - ref));
+            const __half2 s2 = __hadd2(e0, e1);
+            hs[j] = c16 == 0 ? s2 : __hadd2(hs[j], s2);
+            pk[j] = half2_to_e4m3x2(e0) | (half2_to_e4m3x2(e1) << 16);
+          }
+          const int cc = 4 * wg + c16;
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        const float2 fs = __half22float2(hsum);
+        const float2 fs = __half22float2(__hadd2(__hadd2(hs[0], hs[1]), __hadd2(hs[2], hs[3])));
         l_run = l_run * alpha + (fs.x + fs.y);
         m_run = m_use;
-        rescale = __any_sync(0xffffffffu, rescale);
-        while (od < G) {
-          if (!warp_wait(&B.o_done, od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
-          ++od;
-        }
-        if (!ok) break;
-        // this group's two 16-byte chunks (2 wg, 2 wg + 1) of the 64-byte P row, SW64 layout
-        uint8_t* prow = sm + kSmemP + b * kPBytes + r * 64;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int cc = 2 * wg + c;
-          *reinterpret_cast<uint4*>(prow + ((cc ^ ((r >> 1) & 3)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
         if (rescale && t > 0) {
+          if (!consume(int64_t(G) - 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < kVD / 2; cc += 32) {
@@ -383,11 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = bar_and(3, 256, true);
       if (!ok) break;
       const float l_tot = red[4 * 128 + r] + red[5 * 128 + r];
-      while (od < G) {
-        if (!warp_wait(&B.o_done, od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
-        ++od;
-      }
-      if (!ok) break;
+      if (!consume(int64_t(G) - 1)) { ok = false; break; }
       tc_fence_after();
       const float scale = l_tot > 0.f ? p.bmm2 / l_tot : 0.f;
       const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
@@ -416,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + c) = w;
           }
         } else {
-          float* dst = p.ws_o + (int64_t(slot) * 128 + r) * kVD + col;
+          float* dst = p.ws_o + (int64_t(slot * 2 + vh) * 128 + r) * kVD + col;
 #pragma unroll
           for (int c = 0; c < 32; c += 4)
             *reinterpret_cast<float4*>(dst + c) =
@@ -428,21 +580,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (slot < 0) {
           if (p.lse && vh == 0) p.lse[int64_t(n) * p.heads + r] = lse;
         } else {
-          p.ws_lse[int64_t(slot) * 128 + r] = lse;
+          p.ws_lse[int64_t(slot * 2 + vh) * 128 + r] = lse;
         }
       }
       tc_fence_before();
       mbar_arrive(&B.o_free);
     }
-    if (!ok) *abort_flag = 1;
+    if (!ok) raise_abort();
   }
   tc_fence_before();
-  __syncthreads();
+  // Neither CTA leaves while the other may still copy into its shared memory.
+  cluster_sync();
   tc_fence_after();
   if (warp == 6) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merge split-KV pieces of (query token, latent half) units; zero-fill empty ones.
+// Merge split-KV pieces of query-token units (each piece holds both latent halves, slots
+// 2 s and 2 s + 1); zero-fill empty ones. One warp per (unit, half, head).
 __global__ void __launch_bounds__(128)
     mla_merge_kernel(const int32_t* __restrict__ meta, const float* __restrict__ ws_o,
                      const float* __restrict__ ws_lse, int heads, __nv_bfloat16* __restrict__ out,
@@ -450,24 +604,25 @@ __global__ void __launch_bounds__(128)
   const int NM = meta[H_MERGES];
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (gw >= NM * heads) return;
-  const int item = gw / heads, h = gw % heads;
+  if (gw >= NM * kMlaVSplit * heads) return;
+  const int item = gw / (kMlaVSplit * heads), vh = (gw / heads) % kMlaVSplit, h = gw % heads;
   const int32_t* mi = meta + meta[H_OFF_MERGES] + 3 * item;
-  const int unit = mi[0], first = mi[1], count = mi[2];
-  const int n = unit / kMlaVSplit, vh = unit % kMlaVSplit;
+  const int n = mi[0], first = mi[1], count = mi[2];
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float lse_out = -INFINITY;
   if (count > 0) {
     float mx = -INFINITY;
-    for (int c = lane; c < count; c += 32) mx = fmaxf(mx, ws_lse[int64_t(first + c) * 128 + h]);
+    for (int c = lane; c < count; c += 32)
+      mx = fmaxf(mx, ws_lse[(int64_t(first + c) * kMlaVSplit + vh) * 128 + h]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     float tot = 0.f;
     if (mx > -INFINITY) {
       for (int c = 0; c < count; ++c) {
-        const float wgt = expf(ws_lse[int64_t(first + c) * 128 + h] - mx);
+        const int64_t sh = (int64_t(first + c) * kMlaVSplit + vh) * 128 + h;
+        const float wgt = expf(ws_lse[sh] - mx);
         tot += wgt;
-        const float4* src = reinterpret_cast<const float4*>(ws_o + (int64_t(first + c) * 128 + h) * kVD + lane * 8);
+        const float4* src = reinterpret_cast<const float4*>(ws_o + sh * kVD + lane * 8);
         const float4 x0 = src[0], x1 = src[1];
         acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
         acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
@@ -531,30 +686,18 @@ extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* qu
   const int slots = meta_word(plan, H_SLOTS);
   mp.ws_o = static_cast<float*>(float_ws);
   mp.ws_lse = slots ? reinterpret_cast<float*>(static_cast<uint8_t*>(float_ws) +
-                                               ((size_t(slots) * 128 * kVD * 4 + 255) & ~size_t(255)))
+                                               ((size_t(slots) * kMlaVSplit * 128 * kVD * 4 + 255) &
+                                                ~size_t(255)))
                     : nullptr;
   if (bskv_status s = status_args(&mp.st)) return s;
-  CUtensorMap qn, qr;
+  mp.q = static_cast<const uint8_t*>(query);
+  CUtensorMap qr;
   const uint64_t dims[2] = {576, uint64_t(nq * plan->num_qo_heads)};
   const uint64_t str[1] = {576};
-  const uint32_t box_n[2] = {128, 128}, box_r[2] = {64, 128};
-  if (bskv_status s = encode_tiled(&qn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, query, dims, str, box_n,
-                                   CU_TENSOR_MAP_SWIZZLE_128B))
-    return s;
+  const uint32_t box_r[2] = {64, 128};
   if (bskv_status s = encode_tiled(&qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, query, dims, str, box_r,
                                    CU_TENSOR_MAP_SWIZZLE_64B))
     return s;
-  CUtensorMap kn, kr;
-  {
-    const uint64_t kd[2] = {576, uint64_t(num_rows)};
-    const uint32_t gb_n[2] = {128, 1}, gb_r[2] = {64, 1};
-    if (bskv_status s = encode_tiled(&kn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_rows, kd, str, gb_n,
-                                     CU_TENSOR_MAP_SWIZZLE_128B))
-      return s;
-    if (bskv_status s = encode_tiled(&kr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_rows, kd, str, gb_r,
-                                     CU_TENSOR_MAP_SWIZZLE_64B))
-      return s;
-  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = meta_word(plan, H_GRID);
   if (grid > 0) {
@@ -562,12 +705,12 @@ extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* qu
     if (bskv_status s = cuda_check(cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
                                    "mla: cudaFuncSetAttribute"))
       return s;
-    mla_kernel<<<grid, kThreads, smem, st>>>(qn, qr, kn, kr, mp);
+    mla_kernel<<<grid, kThreads, smem, st>>>(qr, mp);
     if (bskv_status s = cuda_check(cudaGetLastError(), "mla kernel launch")) return s;
   }
   const int nm = meta_word(plan, H_MERGES);
   if (nm > 0) {
-    const int warps = nm * plan->num_qo_heads;
+    const int warps = nm * kMlaVSplit * plan->num_qo_heads;
     mla_merge_kernel<<<(warps + 3) / 4, 128, 0, st>>>(plan->meta_dev, mp.ws_o, mp.ws_lse,
                                                       plan->num_qo_heads, mp.out, lse);
     if (bskv_status s = cuda_check(cudaGetLastError(), "mla merge launch")) return s;

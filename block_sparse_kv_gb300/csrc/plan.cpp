@@ -317,29 +317,32 @@ extern "C" bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t bat
   }
   if (top_k < 64 || top_k % 64 != 0) { set_error("plan_mla_sparse: top_k (%d) must be a positive multiple of 64", top_k); return BSKV_ERR_INVALID_ARG; }
   if (num_heads < 1 || num_heads > 128) { set_error("plan_mla_sparse: num_heads %d outside [1,128]", num_heads); return BSKV_ERR_UNSUPPORTED; }
+  // One unit per query token; a worker is a pair of CTAs (a cluster), one per latent half.
   std::vector<int64_t> len;
-  len.reserve(size_t(batch) * q_len * kMlaVSplit);
+  len.reserve(size_t(batch) * q_len);
   for (int32_t b = 0; b < batch; ++b) {
     if (seq_lens[b] < 0 || seq_lens[b] > top_k) {
       set_error("plan_mla_sparse: seq_lens[%d] = %d outside [0, top_k=%d]", b, seq_lens[b], top_k);
       return BSKV_ERR_INVALID_ARG;
     }
-    for (int32_t t = 0; t < q_len; ++t)
-      for (int32_t v = 0; v < kMlaVSplit; ++v) len.push_back(seq_lens[b]);
+    for (int32_t t = 0; t < q_len; ++t) len.push_back(seq_lens[b]);
   }
   std::vector<int32_t> worker_ptr, merges;
   std::vector<Chunk> chunks;
   int32_t slots = 0;
-  linear_partition(len, kMlaTile, num_sms, worker_ptr, chunks, slots, merges);
+  linear_partition(len, kMlaTile, std::max(1, num_sms / kMlaVSplit), worker_ptr, chunks, slots,
+                   merges);
   const int32_t P = int32_t(worker_ptr.size() - 1);
   bskv_plan* p = new bskv_plan();
   p->kind = KIND_MLA;
   p->batch = batch; p->q_len = q_len; p->num_qo_heads = num_heads; p->top_k = top_k;
   p->head_dim = 576; p->dtype = BSKV_E4M3;
   assemble(p, KIND_MLA, int32_t(len.size()), worker_ptr, chunks, slots, merges, kMlaTile,
-           nullptr, 0, nullptr, 0, P, 0);
+           nullptr, 0, nullptr, 0, P * kMlaVSplit, 0);
+  // a slot holds one piece of a unit for both latent halves
   p->float_ws_bytes = slots == 0 ? 0
-      : align256(size_t(slots) * 128 * kMlaVDim * 4) + align256(size_t(slots) * 128 * 4);
+      : align256(size_t(slots) * kMlaVSplit * 128 * kMlaVDim * 4) +
+            align256(size_t(slots) * kMlaVSplit * 128 * 4);
   *out_plan = p;
   return BSKV_OK;
 }

@@ -29,8 +29,9 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
     units (b, kv head) b-major, max_workers = 8 * num_sms unless given,
     grid = ceil(P / 8). Both: len = request length, tile 16, aux0 = kv_indptr,
     aux1 = kv_indices.
-  * MLA: units (query token n = b*q_len + t, latent half v) n-major, len = seq_lens[b],
-    tile 64, max_workers = num_sms, grid = P, no aux, variant 0.
+  * MLA: units = query tokens n = b*q_len + t, len = seq_lens[b], tile 128,
+    max_workers = max(1, num_sms // 2) (a worker is a pair of CTAs, one per latent half),
+    grid = 2 P, no aux, variant 0.
 
 BSR (longest processing time first). Tensor-core variant (variant 1) when R == 64,
 C == 64, head_dim == 128 and R*g in {128, 256} (g = Hq/Hkv): one unit per (row block
@@ -150,10 +151,9 @@ def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_q
 def mla_meta(seq_lens, batch, q_len, num_sms):
     lens = []
     for b in range(batch):
-        for _t in range(q_len):
-            lens += [int(seq_lens[b])] * 2
-    wp, ch, slots, merges = linear_partition(lens, 64, num_sms)
-    return _assemble(3, len(lens), wp, ch, slots, merges, 64, [], [], len(wp) - 1, 0)
+        lens += [int(seq_lens[b])] * q_len
+    wp, ch, slots, merges = linear_partition(lens, 128, max(1, num_sms // 2))
+    return _assemble(3, len(lens), wp, ch, slots, merges, 128, [], [], 2 * (len(wp) - 1), 0)
 
 
 def bsr_meta(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, num_sms):

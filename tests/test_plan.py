@@ -140,8 +140,9 @@ def test_mla_plan_bit_exact(lib, batch, q_len, seq):
     p = bskv.bskv_plan_mla_sparse(seq_lens, batch, q_len, 128, top_k, num_sms=SMS)
     meta = p.metadata()
     assert meta == plan_ref.mla_meta(seq_lens, batch, q_len, SMS)
-    lens = [s for s in seq_lens for _ in range(q_len) for _ in range(2)]
-    _check_linear(meta, lens, 64)
+    lens = [s for s in seq_lens for _ in range(q_len)]
+    _check_linear(meta, lens, 128)
+    assert plan_ref.sections(meta)["grid"] == 2 * plan_ref.sections(meta)["workers"]
 
 
 # ---------------------------------------------------------------------------------------
