@@ -158,6 +158,16 @@ __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, const void* src, 
       "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
       : "memory");
 }
+// 16-byte asynchronous store into another CTA's shared memory; complete_tx of 16 bytes on
+// its mbarrier (cluster addresses for both).
+__device__ __forceinline__ void st_async_v4(uint32_t dst, uint4 v, uint32_t mbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(dst),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the source reads of this thread's committed bulk copies are done (all of
 // them, or all but the most recent group).

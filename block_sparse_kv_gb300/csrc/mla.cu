@@ -596,7 +596,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // Merge split-KV pieces of query-token units (each piece holds both latent halves, slots
-// 2 s and 2 s + 1); zero-fill empty ones. One warp per (unit, half, head).
+// 2 s and 2 s + 1); zero-fill empty ones. One warp per (unit, half, head); a lane owns 8 of
+// the 256 values. Pieces are combined in slot order with the log-sum-exp merge (running
+// max m, scale exp(m - m'), weight exp(lse_c - m')), the loads of four pieces in flight
+// together.
 __global__ void __launch_bounds__(128)
     mla_merge_kernel(const int32_t* __restrict__ meta, const float* __restrict__ ws_o,
                      const float* __restrict__ ws_lse, int heads, __nv_bfloat16* __restrict__ out,
@@ -609,42 +612,47 @@ __global__ void __launch_bounds__(128)
   const int32_t* mi = meta + meta[H_OFF_MERGES] + 3 * item;
   const int n = mi[0], first = mi[1], count = mi[2];
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float lse_out = -INFINITY;
-  if (count > 0) {
-    float mx = -INFINITY;
-    for (int c = lane; c < count; c += 32)
-      mx = fmaxf(mx, ws_lse[(int64_t(first + c) * kMlaVSplit + vh) * 128 + h]);
+  float m = -INFINITY, l = 0.f;
+  for (int c0 = 0; c0 < count; c0 += 4) {
+    float bl[4];
+    float4 bx[4][2];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float tot = 0.f;
-    if (mx > -INFINITY) {
-      for (int c = 0; c < count; ++c) {
-        const int64_t sh = (int64_t(first + c) * kMlaVSplit + vh) * 128 + h;
-        const float wgt = expf(ws_lse[sh] - mx);
-        tot += wgt;
+    for (int j = 0; j < 4; ++j) {
+      if (c0 + j < count) {
+        const int64_t sh = (int64_t(first + c0 + j) * kMlaVSplit + vh) * 128 + h;
+        bl[j] = __ldg(ws_lse + sh);
         const float4* src = reinterpret_cast<const float4*>(ws_o + sh * kVD + lane * 8);
-        const float4 x0 = src[0], x1 = src[1];
-        acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
-        acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+        bx[j][0] = __ldg(src);
+        bx[j][1] = __ldg(src + 1);
       }
-      const float inv = 1.f / tot;
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] *= inv;
-      lse_out = mx + logf(tot);
+    for (int j = 0; j < 4; ++j) {
+      if (c0 + j >= count) continue;
+      const float mn = fmaxf(m, bl[j]);
+      const float sc = m == -INFINITY ? 0.f : expf(m - mn);
+      const float w = expf(bl[j] - mn);
+      l = l * sc + w;
+      const float x[8] = {bx[j][0].x, bx[j][0].y, bx[j][0].z, bx[j][0].w,
+                          bx[j][1].x, bx[j][1].y, bx[j][1].z, bx[j][1].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = acc[i] * sc + w * x[i];
+      m = mn;
     }
   }
+  const float inv = count > 0 ? 1.f / l : 0.f;
   __nv_bfloat16* dst = out + (int64_t(n) * heads + h) * 512 + vh * kVD + lane * 8;
-  uint4 w;
-  __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[0], acc[1]);
-  __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[2], acc[3]);
-  __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[4], acc[5]);
-  __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[6], acc[7]);
-  w.x = *reinterpret_cast<uint32_t*>(&h0);
-  w.y = *reinterpret_cast<uint32_t*>(&h1);
-  w.z = *reinterpret_cast<uint32_t*>(&h2);
-  w.w = *reinterpret_cast<uint32_t*>(&h3);
-  *reinterpret_cast<uint4*>(dst) = w;
-  if (lse && vh == 0 && lane == 0) lse[int64_t(n) * heads + h] = lse_out;
+  uint4 w4;
+  __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+  __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+  __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[4] * inv, acc[5] * inv);
+  __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[6] * inv, acc[7] * inv);
+  w4.x = *reinterpret_cast<uint32_t*>(&h0);
+  w4.y = *reinterpret_cast<uint32_t*>(&h1);
+  w4.z = *reinterpret_cast<uint32_t*>(&h2);
+  w4.w = *reinterpret_cast<uint32_t*>(&h3);
+  *reinterpret_cast<uint4*>(dst) = w4;
+  if (lse && vh == 0 && lane == 0) lse[int64_t(n) * heads + h] = count > 0 ? m + logf(l) : -INFINITY;
 }
 
 }  // namespace
