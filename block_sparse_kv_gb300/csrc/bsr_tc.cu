@@ -100,20 +100,51 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16, float a, float b) {
 // P for two logits (log2 domain, reference subtracted): returns them packed in T and their
 // values as float. fp16 uses the packed f16x2 exponential (P is fp16 anyway); bf16 keeps
 // the fp32 exponential, since a bf16 argument would lose too much precision.
+// Row-sum accumulator of P: for fp16, eight packed f16x2 partial sums (each takes at most
+// 16 pairs of values <= 2^8 per 128-key step, well inside f16 range), turned into one float
+// per step; for bf16, eight float partial sums.
 template <typename T>
-__device__ __forceinline__ uint32_t exp2_pack(float x0, float x1, float2& v);
+struct PSum;
 template <>
-__device__ __forceinline__ uint32_t exp2_pack<__half>(float x0, float x1, float2& v) {
+struct PSum<__half> {
+  __half2 h[8];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = __float2half2_rn(0.f);
+  }
+  __device__ __forceinline__ float total() const {
+    float2 a = __half22float2(__hadd2(__hadd2(h[0], h[1]), __hadd2(h[2], h[3])));
+    float2 b = __half22float2(__hadd2(__hadd2(h[4], h[5]), __hadd2(h[6], h[7])));
+    return (a.x + a.y) + (b.x + b.y);
+  }
+};
+template <>
+struct PSum<__nv_bfloat16> {
+  float f[8];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) f[q] = 0.f;
+  }
+  __device__ __forceinline__ float total() const {
+    return ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+  }
+};
+template <typename T>
+__device__ __forceinline__ uint32_t exp2_pack(float x0, float x1, PSum<T>& acc, int q);
+template <>
+__device__ __forceinline__ uint32_t exp2_pack<__half>(float x0, float x1, PSum<__half>& acc, int q) {
   const __half2 in = __floats2half2_rn(x0, x1);
   uint32_t out;
   asm("ex2.approx.f16x2 %0, %1;" : "=r"(out) : "r"(*reinterpret_cast<const uint32_t*>(&in)));
-  v = __half22float2(*reinterpret_cast<const __half2*>(&out));
+  acc.h[q] = __hadd2(acc.h[q], *reinterpret_cast<const __half2*>(&out));
   return out;
 }
 template <>
-__device__ __forceinline__ uint32_t exp2_pack<__nv_bfloat16>(float x0, float x1, float2& v) {
-  v = make_float2(fast_exp2(x0), fast_exp2(x1));
-  return pack2(__nv_bfloat16(), v.x, v.y);
+__device__ __forceinline__ uint32_t exp2_pack<__nv_bfloat16>(float x0, float x1,
+                                                              PSum<__nv_bfloat16>& acc, int q) {
+  const float v0 = fast_exp2(x0), v1 = fast_exp2(x1);
+  acc.f[q] += v0 + v1;
+  return pack2(__nv_bfloat16(), v0, v1);
 }
 
 template <typename T, int NM>
@@ -371,9 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ref = m_use == -INFINITY ? 0.f : m_use;
         rescale = __any_sync(0xffffffffu, rescale);
         // P = 2^(s * scale - ref), 32 keys at a time into packed columns [16 ck, 16 ck + 16)
-        float sp[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) sp[q] = 0.f;
+        PSum<T> sp;
+        sp.zero();
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
           if (ck < 2 * nb) {
@@ -382,14 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 32; c += 2) {
               const float x0 = fmaf(__uint_as_float(sr[32 * ck + c]), p.scale_log2, -ref);
               const float x1 = fmaf(__uint_as_float(sr[32 * ck + c + 1]), p.scale_log2, -ref);
-              float2 pv;
-              pk[c / 2] = exp2_pack<T>(x0, x1, pv);
-              sp[(c >> 1) & 7] += pv.x + pv.y;
+              pk[c / 2] = exp2_pack<T>(x0, x1, sp, (c >> 1) & 7);
             }
             tmem_st16(scol + 16 * ck, pk);
           }
         }
-        const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        const float sum = sp.total();
         l_run = l_run * alpha + sum;
         m_run = m_use;
         // All earlier PVs into this tile's O must be complete before a rescale. With two M
