@@ -81,3 +81,22 @@ def test_bsr_tc_full_prefill_workload_sampled_rows(cuda):
     rows = sorted(set(torch.randint(0, 16384, (90,), generator=g).tolist()) | {0, 63, 64, 16383})
     st = _run(cuda, d, torch.float16, rows=np.array(rows), repeat=True)
     print("bsr prefill sampled rows:", st)
+
+
+def test_bsr_tc_forced_timeout_is_reported_and_recovers(cuda):
+    """Every bounded wait of the tensor-core kernel gives up at once under the testing hook:
+    the producer, the MMA issuer and both softmax warpgroups leave through the abort path
+    (the issuer drains its MMAs), the status reads TIMEOUT, and the next run is correct."""
+    d = synth.bsr_inputs(652, 256, 256, 64, 64, 8, 2, 128, pattern="random", causal=True)
+    bskv.bskv_get_device_status(reset=True)
+    bskv.bskv_set_debug_force_timeout(True)
+    try:
+        p = bskv.bskv_plan_bsr(d["indptr"], d["indices"], d["M"], d["N"], d["R"], d["C"],
+                               d["num_qo_heads"], d["num_kv_heads"], d["head_dim"],
+                               causal=d["causal"], dtype=torch.float16)
+        bskv.bskv_run_bsr(p, d["q"].to(cuda), d["k"].to(cuda), d["v"].to(cuda))
+        torch.cuda.synchronize()
+    finally:
+        bskv.bskv_set_debug_force_timeout(False)
+    assert bskv.STATUS[bskv.bskv_get_device_status(reset=True)] == "ERR_TIMEOUT"
+    _run(cuda, d, torch.float16)

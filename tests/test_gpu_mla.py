@@ -139,3 +139,24 @@ def test_mla_bad_index_is_reported(cuda):
     bskv.bskv_get_device_status(reset=True)
     _decode(cuda, m, query, kv, [64])
     assert bskv.STATUS[bskv.bskv_get_device_status(reset=True)] == "ERR_DEVICE_INDEX"
+
+
+def test_mla_forced_timeout_is_reported_and_recovers(cuda):
+    """The testing hook makes every bounded wait of the cluster kernel give up at once: both
+    CTAs of each pair leave through the abort path, the device status reads TIMEOUT, and once
+    the hook is cleared the same run is correct."""
+    m = synth.mla_inputs(870, batch=3, heads=128, top_k=256, pool_rows=2048, ctx_lo=256,
+                         ctx_hi=2048, max_seq_len=2048)
+    query, kv = _oracle_rows(m)
+    seq = [256, 200, 130]
+    bskv.bskv_get_device_status(reset=True)
+    bskv.bskv_set_debug_force_timeout(True)
+    try:
+        _decode(cuda, m, query, kv, seq)
+    finally:
+        bskv.bskv_set_debug_force_timeout(False)
+    assert bskv.STATUS[bskv.bskv_get_device_status(reset=True)] == "ERR_TIMEOUT"
+    out, lse = _decode(cuda, m, query, kv, seq)
+    assert bskv.bskv_get_device_status() == 0
+    ref, ref_lse = att.mla_sparse_decode(query, kv, m["indices"].numpy(), np.array(seq), SCALE, 1.0)
+    _check(out, lse, ref, ref_lse)
