@@ -25,7 +25,9 @@
 //            mask, keeps a running max with lazy rescaling (O in TMEM is rescaled only when
 //            the max grows by more than 2^8), forms P = 2^x (packed f16x2 for fp16 inputs)
 //            and stores it over the S columns with tcgen05.st; the epilogue normalises O and
-//            stores out and lse.
+//            stores out and lse. With two M tiles each warp stages its 32 rows of a 64-value
+//            panel (128B-swizzled, 4 KB) in shared memory and writes them with one tensor
+//            store, so the output leaves in whole lines instead of one row per thread.
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs, frees TMEM and
 // returns after recording BSKV_ERR_TIMEOUT.
 #include <math.h>
@@ -64,7 +66,10 @@ struct Cfg {
   static constexpr int kStages = NM == 2 ? 2 : 3;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kKV = kQ + NM * kQTile;
-  static constexpr uint32_t kBar = kKV + kStages * kStageBytes;
+  // epilogue staging with two M tiles: one 4 KB box ([32 rows x 128 B]) per softmax warp
+  static constexpr uint32_t kOut = kKV + kStages * kStageBytes;
+  static constexpr uint32_t kOutBytes = NM == 2 ? 8 * 4096 : 0;
+  static constexpr uint32_t kBar = kOut + kOutBytes;
   static constexpr uint32_t kBytes = kBar + 512;
 };
 
@@ -150,7 +155,8 @@ __device__ __forceinline__ uint32_t exp2_pack<__nv_bfloat16>(float x0, float x1,
 template <typename T, int NM>
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap, const TcParams p) {
+                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                  const TcParams p) {
   using L = Cfg<NM>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -459,20 +465,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      if constexpr (NM == 2) {
+        // Rows q4*32 .. q4*32+31 of the tile are 32 consecutive tokens of one head: per
+        // 64-value panel, lane = token row of a [32 x 128 B] box (16-byte chunk c at
+        // c ^ (row & 7)), then lane 0 stores the box. Tokens past M are clipped by the store.
+        uint8_t* stg = sm + L::kOut + (m * 4 + q4) * 4096;
+        const uint32_t row_addr = smem_u32(stg) + lane * 128;
+#pragma unroll 1
+        for (int pn = 0; pn < 2; ++pn) {
+          // the box's previous store has finished reading it
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + lane_base + 256 * m + pn * 64 + hf * 32, ov);
+            tmem_ld_wait();
 #pragma unroll
-      for (int cc = 0; cc < kD; cc += 32) {
-        uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + 256 * m + cc, ov);
-        tmem_ld_wait();
-        if (tok < p.M) {
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const int c = c4 * 8, c8 = hf * 4 + c4;
+              uint4 w;
+              w.x = pack2(T(), __uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+              w.y = pack2(T(), __uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+              w.z = pack2(T(), __uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+              w.w = pack2(T(), __uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+              sts128(row_addr + ((c8 ^ (lane & 7)) << 4), w);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&omap, stg, pn * 64, head, i * kBlk + (q4 & 1) * 32);
+            bulk_commit();
+          }
+        }
+      } else {
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 w;
-            w.x = pack2(T(), __uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-            w.y = pack2(T(), __uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-            w.z = pack2(T(), __uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-            w.w = pack2(T(), __uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + cc + c) = w;
+        for (int cc = 0; cc < kD; cc += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + 256 * m + cc, ov);
+          tmem_ld_wait();
+          if (tok < p.M) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint4 w;
+              w.x = pack2(T(), __uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+              w.y = pack2(T(), __uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+              w.z = pack2(T(), __uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+              w.w = pack2(T(), __uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + cc + c) = w;
+            }
           }
         }
       }
@@ -483,6 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&B.o_free[m]);
     }
     if (!ok) *abort_flag = 1;
+    // the output stores must be complete before the CTA exits
+    if (NM == 2 && lane == 0) bulk_wait_all0();
   }
   tc_fence_before();
   __syncthreads();
@@ -492,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int NM>
 bskv_status launch_t(const bskv_plan* plan, const CUtensorMap& qm, const CUtensorMap& km,
-                     const CUtensorMap& vm, const TcParams& tp, cudaStream_t st) {
+                     const CUtensorMap& vm, const CUtensorMap& om, const TcParams& tp,
+                     cudaStream_t st) {
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
   const size_t smem = Cfg<NM>::kBytes + 1024;
@@ -501,7 +546,7 @@ bskv_status launch_t(const bskv_plan* plan, const CUtensorMap& qm, const CUtenso
           cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
           "bsr_tc: cudaFuncSetAttribute"))
     return s;
-  kern<<<grid, kThreads, smem, st>>>(qm, km, vm, tp);
+  kern<<<grid, kThreads, smem, st>>>(qm, km, vm, om, tp);
   return cuda_check(cudaGetLastError(), "bsr_tc launch");
 }
 
@@ -526,12 +571,21 @@ bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64
   if (bskv_status s = status_args(&tp.st)) return s;
   const CUtensorMapDataType dt =
       plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap qm, km, vm;
+  CUtensorMap qm, km, vm, om;
   const uint32_t box[3] = {64, 1, 64};
   {
     const uint64_t dims[3] = {uint64_t(kD), uint64_t(plan->num_qo_heads), uint64_t(plan->M)};
     const uint64_t str[2] = {uint64_t(qs[1]) * 2, uint64_t(qs[0]) * 2};
     if (bskv_status s = encode_tiled(&qm, dt, 3, q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  }
+  if (g == 4) {
+    // output boxes of 32 tokens x 1 head x 64 values (the epilogue's per-warp stores)
+    const uint32_t obox[3] = {64, 1, 32};
+    const uint64_t dims[3] = {uint64_t(kD), uint64_t(plan->num_qo_heads), uint64_t(plan->M)};
+    const uint64_t str[2] = {uint64_t(os[1]) * 2, uint64_t(os[0]) * 2};
+    if (bskv_status s = encode_tiled(&om, dt, 3, out, dims, str, obox, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  } else {
+    om = qm;  // unused with one M tile
   }
   {
     const uint64_t dims[3] = {uint64_t(kD), uint64_t(plan->num_kv_heads), uint64_t(plan->N)};
@@ -542,8 +596,10 @@ bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64
   }
   const bool bf = plan->dtype == BSKV_BF16;
   if (g == 4)
-    return bf ? launch_t<__nv_bfloat16, 2>(plan, qm, km, vm, tp, st) : launch_t<__half, 2>(plan, qm, km, vm, tp, st);
-  return bf ? launch_t<__nv_bfloat16, 1>(plan, qm, km, vm, tp, st) : launch_t<__half, 1>(plan, qm, km, vm, tp, st);
+    return bf ? launch_t<__nv_bfloat16, 2>(plan, qm, km, vm, om, tp, st)
+              : launch_t<__half, 2>(plan, qm, km, vm, om, tp, st);
+  return bf ? launch_t<__nv_bfloat16, 1>(plan, qm, km, vm, om, tp, st)
+            : launch_t<__half, 1>(plan, qm, km, vm, om, tp, st);
 }
 
 }  // namespace bskv
