@@ -257,10 +257,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_wait_all0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-// Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int32_t c0,
                                             int32_t c1, int32_t c2, int32_t c3, int32_t c4,

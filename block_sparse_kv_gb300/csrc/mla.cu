@@ -28,7 +28,8 @@
 //              tile's columns and 128 of the 256 output values: it reads S (and releases it
 //              for the next QK at once), combines the row max with the other group, applies
 //              lazy rescaling (threshold 2^8), forms P with packed f16x2 exponentials converted
-//              to E4M3, and writes O (bf16) or the split-KV partial state in the epilogue; at a
+//              to E4M3, and writes O (bf16) or the split-KV partial state in the epilogue
+//              (per warp, 128B-swizzled boxes in the idle P buffers and tensor stores); at a
 //              token's last tile it also writes the next token's query into TMEM.
 #include <cuda_fp8.h>
 #include <math.h>
@@ -115,7 +116,8 @@ __device__ __forceinline__ uint32_t half2_to_e4m3x2(__half2 x) {
 __device__ __forceinline__ int chunk_token(const int4& ch) { return ch.x; }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_kernel(const __grid_constant__ CUtensorMap qmap_rope, const MlaParams p) {
+    mla_kernel(const __grid_constant__ CUtensorMap qmap_rope, const __grid_constant__ CUtensorMap omap,
+               const __grid_constant__ CUtensorMap wmap, const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -545,37 +547,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
       const bool row_ok = r < p.heads;
       const int slot = ch.w;
+      // Each warp stages its 32 heads x 128 bytes of a box (128B-swizzled) in its own 4 KB of
+      // the P buffers, whose PVs have all completed, and lane 0 writes the box with a tensor
+      // store: the output or the split partial leaves in whole lines. A box holds 64 bf16 or
+      // 32 float values per head.
+      uint8_t* stg = sm + kSmemP + (warp - 8) * 4096;
+      const uint32_t row_addr = smem_u32(stg) + lane * 128;
+      const int nbox = slot < 0 ? 2 : 4;
 #pragma unroll 1
-      for (int cc = 0; cc < kVD / 2; cc += 32) {
-        uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + wg * (kVD / 2) + cc, ov);
-        tmem_ld_wait();
-        if (!row_ok) continue;
-        const int col = wg * (kVD / 2) + cc;
+      for (int bx = 0; bx < nbox; ++bx) {
+        if (lane == 0) bulk_wait_read0();  // the previous box has been read
+        __syncwarp();
         if (slot < 0) {
-          __nv_bfloat16* dst = p.out + (int64_t(n) * p.heads + r) * 512 + vh * kVD + col;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + lane_base + wg * (kVD / 2) + bx * 64 + hf * 32, ov);
+            tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 w;
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(ov[c]) * scale, __uint_as_float(ov[c + 1]) * scale);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(ov[c + 2]) * scale, __uint_as_float(ov[c + 3]) * scale);
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(ov[c + 4]) * scale, __uint_as_float(ov[c + 5]) * scale);
-            __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(ov[c + 6]) * scale, __uint_as_float(ov[c + 7]) * scale);
-            w.x = *reinterpret_cast<uint32_t*>(&h0);
-            w.y = *reinterpret_cast<uint32_t*>(&h1);
-            w.z = *reinterpret_cast<uint32_t*>(&h2);
-            w.w = *reinterpret_cast<uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(dst + c) = w;
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const int c = c4 * 8;
+              __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(ov[c]) * scale, __uint_as_float(ov[c + 1]) * scale);
+              __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(ov[c + 2]) * scale, __uint_as_float(ov[c + 3]) * scale);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(ov[c + 4]) * scale, __uint_as_float(ov[c + 5]) * scale);
+              __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(ov[c + 6]) * scale, __uint_as_float(ov[c + 7]) * scale);
+              sts128(row_addr + (((hf * 4 + c4) ^ (lane & 7)) << 4),
+                     make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                                *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3)));
+            }
           }
         } else {
-          float* dst = p.ws_o + (int64_t(slot * 2 + vh) * 128 + r) * kVD + col;
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + wg * (kVD / 2) + bx * 32, ov);
+          tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4*>(dst + c) =
-                make_float4(__uint_as_float(ov[c]) * scale, __uint_as_float(ov[c + 1]) * scale,
-                            __uint_as_float(ov[c + 2]) * scale, __uint_as_float(ov[c + 3]) * scale);
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const int c = c8 * 4;
+            sts128(row_addr + ((c8 ^ (lane & 7)) << 4),
+                   make_uint4(__float_as_uint(__uint_as_float(ov[c]) * scale),
+                              __float_as_uint(__uint_as_float(ov[c + 1]) * scale),
+                              __float_as_uint(__uint_as_float(ov[c + 2]) * scale),
+                              __float_as_uint(__uint_as_float(ov[c + 3]) * scale)));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (slot < 0) {
+            if (q4 * 32 < p.heads)  // rows past the last head are clipped by the store
+              tma_store_3d(&omap, stg, vh * kVD + wg * (kVD / 2) + bx * 64, q4 * 32, n);
+          } else
+            tma_store_2d(&wmap, stg, wg * (kVD / 2) + bx * 32, (slot * 2 + vh) * 128 + q4 * 32);
+          bulk_commit();
         }
       }
+      // The next chunk writes P only after every warp has passed its first tile's group
+      // barrier; this warp gets there after its stores have read the staging.
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
       if (row_ok && wg == 0) {
         if (slot < 0) {
           if (p.lse && vh == 0) p.lse[int64_t(n) * p.heads + r] = lse;
@@ -586,6 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&B.o_free);
     }
+    if (lane == 0) bulk_wait_all0();  // output stores complete before the CTA exits
     if (!ok) raise_abort();
   }
   tc_fence_before();
@@ -706,6 +736,27 @@ extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* qu
   if (bskv_status s = encode_tiled(&qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, query, dims, str, box_r,
                                    CU_TENSOR_MAP_SWIZZLE_64B))
     return s;
+  // epilogue stores: out as [token][head][512] bf16 in boxes of 32 heads x 64 values; the
+  // split partials as [(slot, half, head)][256] float in boxes of 32 rows x 32 values
+  CUtensorMap om, wm;
+  {
+    const uint64_t od[3] = {512, uint64_t(plan->num_qo_heads), uint64_t(nq)};
+    const uint64_t os[2] = {512 * 2, uint64_t(plan->num_qo_heads) * 512 * 2};
+    const uint32_t ob[3] = {64, uint32_t(std::min(32, plan->num_qo_heads)), 1};
+    if (bskv_status s = encode_tiled(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, od, os, ob,
+                                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return s;
+  }
+  if (slots > 0) {
+    const uint64_t wd[2] = {uint64_t(kVD), uint64_t(slots) * kMlaVSplit * 128};
+    const uint64_t ws[1] = {uint64_t(kVD) * 4};
+    const uint32_t wb[2] = {32, 32};
+    if (bskv_status s = encode_tiled(&wm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, float_ws, wd, ws, wb,
+                                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return s;
+  } else {
+    wm = om;  // no split partials
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = meta_word(plan, H_GRID);
   if (grid > 0) {
@@ -713,7 +764,7 @@ extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* qu
     if (bskv_status s = cuda_check(cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
                                    "mla: cudaFuncSetAttribute"))
       return s;
-    mla_kernel<<<grid, kThreads, smem, st>>>(qr, mp);
+    mla_kernel<<<grid, kThreads, smem, st>>>(qr, om, wm, mp);
     if (bskv_status s = cuda_check(cudaGetLastError(), "mla kernel launch")) return s;
   }
   const int nm = meta_word(plan, H_MERGES);
