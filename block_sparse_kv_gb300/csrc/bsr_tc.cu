@@ -74,7 +74,7 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, drain;
+  uint64_t q_full[2], q_empty[2], drain;  // Q per M tile
   uint64_t kv_full[3], kv_empty[3];
   uint64_t s_full[2], p_full[2];  // per S slot
   uint64_t o_done[2], o_free[2];  // per M tile
@@ -173,8 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool forced = forced_timeout(p.st);
 
   if (threadIdx.x == 0) {
-    mbar_init(&B.q_full, 1);
-    mbar_init(&B.q_empty, 1);
+    for (int m = 0; m < 2; ++m) {
+      mbar_init(&B.q_full[m], 1);
+      mbar_init(&B.q_empty[m], 1);
+    }
     mbar_init(&B.drain, 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(&B.kv_full[s], 1);
@@ -206,42 +208,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
       uint32_t qc = 0, kvc = 0;
+      uint32_t qi[2] = {0u, 0u};  // Q tiles issued
       bool ok = true;
+      // Q of M tile m for the unit (row block i, kv head h), once the previous unit's last QK
+      // on that tile has completed.
+      auto load_q = [&](int m, int i, int h) -> bool {
+        if (*abort_flag || !mbar_wait(&B.q_empty[m], (qc & 1u) ^ 1u, p.st, forced)) return false;
+        mbar_arrive_expect_tx(&B.q_full[m], kQTile);
+        for (int hl = 0; hl < 2; ++hl)
+          for (int pn = 0; pn < 2; ++pn)
+            tma_load_3d(sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
+                        pn * 64, h * p.group + m * 2 + hl, i * kBlk, &B.q_full[m]);
+        ++qi[m];
+        return true;
+      };
+      // K and V of column blocks e, e+1 (< e1) of kv head h into the next stage.
+      auto load_kv = [&](int e, int e1, int h) -> bool {
+        const int s = kvc % S;
+        if (*abort_flag || !mbar_wait(&B.kv_empty[s], ((kvc / S) & 1u) ^ 1u, p.st, forced)) return false;
+        const int nb = min(2, e1 - e);
+        uint8_t* dst = sm + L::kKV + s * kStageBytes;
+        mbar_arrive_expect_tx(&B.kv_full[s], nb * 4 * kKPanel);
+        for (int b = 0; b < nb; ++b) {
+          const int j = indices[e + b];
+          for (int pn = 0; pn < 2; ++pn) {
+            tma_load_3d(dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk, &B.kv_full[s]);
+            tma_load_3d(dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64, h,
+                        j * kBlk, &B.kv_full[s]);
+          }
+        }
+        ++kvc;
+        return true;
+      };
       for (int ui = u0; ui < u1 && ok; ++ui) {
         const int4 un = units[ui];
         const int i = un.y, h = un.z;
         const int e0 = indptr[i], e1 = indptr[i + 1];
         if (e1 == e0) continue;
-        if (*abort_flag || !mbar_wait(&B.q_empty, (qc & 1u) ^ 1u, p.st, forced)) { ok = false; break; }
-        mbar_arrive_expect_tx(&B.q_full, NM * kQTile);
-        for (int m = 0; m < NM; ++m)
-          for (int hl = 0; hl < 2; ++hl)
-            for (int pn = 0; pn < 2; ++pn)
-              tma_load_3d(sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
-                          pn * 64, h * p.group + m * 2 + hl, i * kBlk, &B.q_full);
+        // Order: Q of tile 0 (free one job before tile 1's), the first K/V step (its stage
+        // is freed before tile 1's last QK completes), then Q of tile 1 and the other steps.
+        ok = load_q(0, i, h) && load_kv(e0, e1, h) && (NM == 1 || load_q(1, i, h));
+        for (int e = e0 + 2; e < e1 && ok; e += 2) ok = load_kv(e, e1, h);
         ++qc;
-        for (int e = e0; e < e1; e += 2, ++kvc) {
-          const int s = kvc % S;
-          if (*abort_flag || !mbar_wait(&B.kv_empty[s], ((kvc / S) & 1u) ^ 1u, p.st, forced)) {
-            ok = false;
-            break;
-          }
-          const int nb = min(2, e1 - e);
-          uint8_t* dst = sm + L::kKV + s * kStageBytes;
-          mbar_arrive_expect_tx(&B.kv_full[s], nb * 4 * kKPanel);
-          for (int b = 0; b < nb; ++b) {
-            const int j = indices[e + b];
-            for (int pn = 0; pn < 2; ++pn) {
-              tma_load_3d(dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk, &B.kv_full[s]);
-              tma_load_3d(dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64, h,
-                          j * kBlk, &B.kv_full[s]);
-            }
-          }
-        }
       }
       if (!ok) {
         *abort_flag = 1;
-        if (qc > 0) mbar_wait(&B.q_full, (qc - 1) & 1u, p.st, false);
+        for (int m = 0; m < 2; ++m)
+          if (qi[m] > 0) mbar_wait(&B.q_full[m], (qi[m] - 1) & 1u, p.st, false);
         for (int s = 0; s < S; ++s) {
           if (kvc > uint32_t(s)) {
             const uint32_t last = ((kvc - 1 - s) / S) * S + s;
@@ -270,9 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e0 = indptr[i], e1 = indptr[i + 1];
         const int n = e1 - e0;
         if (n == 0) continue;
-        if (*abort_flag || !mbar_wait(&B.q_full, qc & 1u, p.st, forced)) { ok = false; break; }
-        ++qc;
-        tc_fence_after();
         const int steps = (n + 1) >> 1;
         const int NJ = steps * NM;
         const uint32_t kv_first = kvc;
@@ -282,10 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = NM == 2 ? (jl & 1) : 0;
           const uint32_t step = kv_first + j;
           const int s = step % S;
-          if (m == 0) {
-            if (*abort_flag || !mbar_wait(&B.kv_full[s], (step / S) & 1u, p.st, forced)) return false;
-            tc_fence_after();
-          }
+          if (m == 0 && (*abort_flag || !mbar_wait(&B.kv_full[s], (step / S) & 1u, p.st, forced))) return false;
+          if (jl < NM && (*abort_flag || !mbar_wait(&B.q_full[m], qc & 1u, p.st, forced))) return false;
+          tc_fence_after();
           const int nb = min(2, n - 2 * j);
           const uint32_t z = (J + jl) & 1u;
           const uint32_t sd = tmem + 128 + 256 * z;
@@ -298,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kk > 0 ? 1u : 0u);
           }
           umma_commit(&B.s_full[z]);
-          // Q is not read after the unit's last QK: release it so the next unit's Q loads
-          // while this unit's last PVs and epilogue run.
-          if (jl == NJ - 1) umma_commit(&B.q_empty);
+          // Q of tile m is not read after the unit's last QK on it: release it so the next
+          // unit's Q loads while this unit's last jobs and epilogue run.
+          if (jl == NJ - NM + m) umma_commit(&B.q_empty[m]);
           return true;
         };
         if (!qk(0) || (NJ > 1 && !qk(1))) { ok = false; break; }
@@ -326,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         kvc = kv_first + steps;
         J += NJ;
         ++uc;
+        ++qc;
       }
       if (!ok) *abort_flag = 1;
       umma_commit(&B.drain);
