@@ -205,20 +205,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t kvc = 0, armed = 0;
     bool ok = true;
     const int tr = int(rank) * kHalfRows + pt;  // tile row whose id this thread loads
-    // Row id of tile row tr of the tile at (chunk cj, first row u0); loaded one tile ahead.
-    auto load_id = [&](int cj, int u0) -> int32_t {
-      if (pt >= kHalfRows || cj >= c1) return 0;
-      const int4 cn = chunks[cj];
+    // Row id of tile row tr of the tile of chunk cn that starts at row u0, loaded one tile
+    // ahead. The chunk descriptors are held in registers (the next one read at the start of
+    // a chunk), so the id is one independent load that nothing waits for until the next
+    // tile: a load chained behind the descriptor's would stall the id threads, and with
+    // them the whole gather group, for two L2 round trips per tile.
+    auto load_id = [&](const int4& cn, int u0) -> int32_t {
+      if (pt >= kHalfRows) return 0;
       return u0 + tr < cn.z ? __ldg(p.indices + int64_t(cn.x) * p.top_k + u0 + tr) : 0;
     };
-    int32_t next_id = c0 < c1 ? load_id(c0, chunks[c0].y) : 0;
+    int4 ch = c0 < c1 ? chunks[c0] : make_int4(0, 0, 0, 0);
+    int32_t next_id = c0 < c1 ? load_id(ch, ch.y) : 0;
     for (int ci = c0; ci < c1 && ok; ++ci) {
-      const int4 ch = chunks[ci];
+      const int4 nch = ci + 1 < c1 ? chunks[ci + 1] : make_int4(0, 0, 0, 0);
       for (int t0 = ch.y; t0 < ch.z; t0 += kRows, ++kvc) {
         const int v = kvc % kVSlots, k = kvc % kKSlots;
         int32_t my_id = next_id;
-        next_id = t0 + kRows < ch.z ? load_id(ci, t0 + kRows)
-                                    : (ci + 1 < c1 ? load_id(ci + 1, chunks[ci + 1].y) : 0);
+        next_id = t0 + kRows < ch.z ? load_id(ch, t0 + kRows) : (ci + 1 < c1 ? load_id(nch, nch.y) : 0);
         if (my_id < 0 || my_id >= p.num_rows) {
           record_error(p.st, BSKV_ERR_DEVICE_INDEX);
           my_id = 0;
@@ -268,6 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bulk_commit();
         }
       }
+      ch = nch;
     }
     if (pt == 0) bulk_wait_read0();
     if (!ok) raise_abort();
