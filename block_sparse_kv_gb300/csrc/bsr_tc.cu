@@ -209,6 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&vmap);
       uint32_t qc = 0, kvc = 0;
       uint32_t qi[2] = {0u, 0u};  // Q tiles issued
+      // Q is read once (evict first); a K/V block serves every row block that lists it
+      // (evict last), so it stays in L2 while the Q and output streams pass through.
+      const uint64_t pol_q = l2_evict_first_policy(), pol_kv = l2_evict_last_policy();
       bool ok = true;
       // Q of M tile m for the unit (row block i, kv head h), once the previous unit's last QK
       // on that tile has completed.
@@ -217,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&B.q_full[m], kQTile);
         for (int hl = 0; hl < 2; ++hl)
           for (int pn = 0; pn < 2; ++pn)
-            tma_load_3d(sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
-                        pn * 64, h * p.group + m * 2 + hl, i * kBlk, &B.q_full[m]);
+            tma_load_3d_hint(sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
+                             pn * 64, h * p.group + m * 2 + hl, i * kBlk, &B.q_full[m], pol_q);
         ++qi[m];
         return true;
       };
@@ -232,9 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < nb; ++b) {
           const int j = indices[e + b];
           for (int pn = 0; pn < 2; ++pn) {
-            tma_load_3d(dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk, &B.kv_full[s]);
-            tma_load_3d(dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64, h,
-                        j * kBlk, &B.kv_full[s]);
+            tma_load_3d_hint(dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk,
+                             &B.kv_full[s], pol_kv);
+            tma_load_3d_hint(dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64,
+                             h, j * kBlk, &B.kv_full[s], pol_kv);
           }
         }
         ++kvc;
@@ -480,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 64-value panel, lane = token row of a [32 x 128 B] box (16-byte chunk c at
         // c ^ (row & 7)), then lane 0 stores the box. Tokens past M are clipped by the store.
         uint8_t* stg = sm + L::kOut + (m * 4 + q4) * 4096;
+        const uint64_t pol_out = l2_evict_first_policy();  // written once
         const uint32_t row_addr = smem_u32(stg) + lane * 128;
 #pragma unroll 1
         for (int pn = 0; pn < 2; ++pn) {
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&omap, stg, pn * 64, head, i * kBlk + (q4 & 1) * 32);
+            tma_store_3d_hint(&omap, stg, pn * 64, head, i * kBlk + (q4 & 1) * 32, pol_out);
             bulk_commit();
           }
         }

@@ -254,6 +254,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, const void* src,
+                                                  int32_t c0, int32_t c1, int32_t c2,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_wait_all0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -276,6 +284,21 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
+// L2 policy for data read again soon (blocks shared by many work units): evict it last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int32_t c0,
+                                                 int32_t c1, int32_t c2, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_5d_hint(void* dst, const CUtensorMap* map, int32_t c0,
                                                  int32_t c1, int32_t c2, int32_t c3, int32_t c4,
                                                  uint64_t* bar, uint64_t policy) {

@@ -257,12 +257,16 @@ extern "C" bskv_status bskv_plan_bsr(const int32_t* indptr, const int32_t* indic
   const int32_t row_tiles = (R * group + rows_per_unit - 1) / rows_per_unit;
   const int64_t U = int64_t(MB) * num_kv_heads * row_tiles;
   if (U > INT32_MAX / 4) { set_error("plan_bsr: too many units"); return BSKV_ERR_UNSUPPORTED; }
-  // Longest-processing-time assignment: cost = 1 + blocks in the unit's row block.
+  // Longest-processing-time assignment. Cost of a tensor-core unit with n blocks, in
+  // quarters of a step of its kernel: 4 per pair of blocks, 3 for a last single block (its
+  // QK takes as long as a pair's), 2 for the unit's start and epilogue (1 with no blocks);
+  // of a general unit: 1 + n.
   std::vector<int32_t> order(static_cast<size_t>(U));
   std::vector<int64_t> cost(static_cast<size_t>(U));
   for (int64_t u = 0; u < U; ++u) {
     const int32_t i = int32_t(u / (int64_t(num_kv_heads) * row_tiles));
-    cost[size_t(u)] = 1 + (indptr[i + 1] - indptr[i]);
+    const int64_t n = indptr[i + 1] - indptr[i];
+    cost[size_t(u)] = tc ? (n > 0 ? 2 + 4 * (n / 2) + 3 * (n % 2) : 1) : 1 + n;
     order[size_t(u)] = int32_t(u);
   }
   std::stable_sort(order.begin(), order.end(),

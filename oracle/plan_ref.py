@@ -37,7 +37,9 @@ BSR (longest processing time first). Tensor-core variant (variant 1) when R == 6
 C == 64, head_dim == 128 and R*g in {128, 256} (g = Hq/Hkv): one unit per (row block
 i, kv head h), rows_per_unit = R*g, at most num_sms CTAs. Otherwise the general
 variant 0: rows_per_unit = 64, row_tiles = ceil(R*g / 64) units per (i, h), at most
-4*num_sms CTAs. Unit u = (i*Hkv + h)*row_tiles + rt; cost_u = 1 + blocks in row i.
+4*num_sms CTAs. Unit u = (i*Hkv + h)*row_tiles + rt. With n = blocks in row i, cost_u =
+2 + 4*(n // 2) + 3*(n % 2) for a tensor-core unit with n > 0 (1 when n == 0), and 1 + n
+for a general unit.
 Units sorted by cost descending (stable); each goes to the CTA of least current load
 (ties: lowest CTA index). Chunks list each CTA's units in assignment order as
 (u, i, h, rt); tile = rows_per_unit; grid = number of CTAs; aux0 = indptr,
@@ -163,8 +165,14 @@ def bsr_meta(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, 
     rows = R * g if tc else 64
     rt_n = (R * g + rows - 1) // rows
     U = MB * num_kv_heads * rt_n
-    cost = [1 + int(indptr[u // (num_kv_heads * rt_n) + 1]) - int(indptr[u // (num_kv_heads * rt_n)])
-            for u in range(U)]
+    def unit_cost(u):
+        i = u // (num_kv_heads * rt_n)
+        n = int(indptr[i + 1]) - int(indptr[i])
+        if not tc:
+            return 1 + n
+        return 2 + 4 * (n // 2) + 3 * (n % 2) if n > 0 else 1
+
+    cost = [unit_cost(u) for u in range(U)]
     order = sorted(range(U), key=lambda u: -cost[u])  # Python's sort is stable
     cap = num_sms if tc else 4 * num_sms
     G = min(cap, U)
