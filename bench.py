@@ -507,7 +507,7 @@ def main():
 
     extra = {}
     if rank == 0:
-        K = max(5, min(args.steps, 20))
+        K = max(5, min(args.steps, 50))  # timed iterations per row (median and std reported)
         jobs = [("split", "split_decode", lambda: bench_split(bskv, synth, K, args.warmup, peaks)),
                 ("bsr_prefill", "bsr_prefill",
                  lambda: bench_bsr(bskv, synth, "bsr_prefill", K, args.warmup, peaks, True)),
