@@ -75,6 +75,24 @@ def test_mla_decode_small(cuda, heads, q_len, top_k, seq):
     _check(out, lse, ref, ref_lse)
 
 
+def test_mla_duplicate_indices(cuda):
+    """A row listed several times in a query's index list counts once per listing (list
+    semantics, as in the oracle): the second half of each list repeats its first half, and
+    a few single rows repeat further, across tile boundaries and split pieces."""
+    m = synth.mla_inputs(860, batch=3, heads=128, top_k=512, pool_rows=2048, ctx_lo=512,
+                         ctx_hi=2048, max_seq_len=2048)
+    idx = m["indices"].clone()
+    idx[:, :, 256:] = idx[:, :, :256]
+    idx[:, :, 300:310] = idx[:, :, 5:6]
+    m["indices"] = idx
+    query, kv = _oracle_rows(m)
+    seq = [512, 400, 137]
+    out, lse = _decode(cuda, m, query, kv, seq)
+    assert bskv.bskv_get_device_status() == 0
+    ref, ref_lse = att.mla_sparse_decode(query, kv, idx.numpy(), np.array(seq), SCALE, 1.0)
+    _check(out, lse, ref, ref_lse)
+
+
 def test_mla_sharp_softmax(cuda):
     """q x 6: a peaked softmax, reported beside the gate. The PV product takes P in E4M3
     (3 mantissa bits, so each weight carries up to 1/16 relative rounding), which a softmax

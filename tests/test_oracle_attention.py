@@ -220,6 +220,19 @@ def test_mla_full_context_equals_dense_and_is_permutation_invariant():
     np.testing.assert_allclose(lse2, lse, rtol=1e-13)
 
 
+def test_mla_duplicate_indices_count_as_list_entries():
+    """Index lists are lists, not sets (the reading for duplicates): listing every row twice
+    doubles every softmax weight, so the output is unchanged and the LSE grows by ln 2."""
+    d, query, kv = _mla_small(seed=44)
+    idx, sl = d["indices"].numpy(), d["seq_lens"].numpy()
+    scale = 1 / math.sqrt(576)
+    out, lse = att.mla_sparse_decode(query, kv, idx, sl, scale, 1.0)
+    twice = np.concatenate([idx, idx], axis=-1)
+    out2, lse2 = att.mla_sparse_decode(query, kv, twice, 2 * sl, scale, 1.0)
+    np.testing.assert_allclose(out2, out, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse2, lse + math.log(2.0), rtol=1e-13)
+
+
 def test_mla_scale_folding():
     """Quantising with scales (sq, skv) and decoding with bmm1 = a/(sq*skv), bmm2 = 1/skv
     equals decoding unit-scale rows with bmm1 = a when the scaled values stay exact."""
