@@ -158,16 +158,6 @@ __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, const void* src, 
       "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
       : "memory");
 }
-// 16-byte asynchronous store into another CTA's shared memory; complete_tx of 16 bytes on
-// its mbarrier (cluster addresses for both).
-__device__ __forceinline__ void st_async_v4(uint32_t dst, uint4 v, uint32_t mbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
-          "r"(dst),
-      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar)
-      : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the source reads of this thread's committed bulk copies are done (all of
 // them, or all but the most recent group).
@@ -176,17 +166,6 @@ __device__ __forceinline__ void bulk_wait_read0() {
 }
 __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-// Plain named barrier over `nthreads` threads (a multiple of 32).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // 16-byte store to shared memory at a shared-window address.
@@ -200,42 +179,12 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 // bulk and tensor copies (TMA)
 // ---------------------------------------------------------------------------------------
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t c0,
                                             int32_t c1, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Four rows of a 2-D tensor (row ids r0..r3, columns from c0 for the box width) into four
-// consecutive box rows in shared memory; the tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int32_t c0,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0,
-                                            int32_t c1, int32_t c2, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -264,16 +213,6 @@ __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, const 
 }
 __device__ __forceinline__ void bulk_wait_all0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int32_t c0,
-                                            int32_t c1, int32_t c2, int32_t c3, int32_t c4,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
-      : "memory");
 }
 
 // L2 policy for data read exactly once (a stream larger than L2): evict it first, so it
