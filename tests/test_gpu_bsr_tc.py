@@ -48,6 +48,7 @@ CASES = [
     (320, 384, 16, 4, torch.float16, "random", False),      # several kv heads, random blocks
     (200, 256, 8, 2, torch.float16, "random", True),        # ragged M, bottom-right causal
     (512, 512, 8, 4, torch.bfloat16, "full", True),         # every block, dense causal
+    (384, 384, 16, 4, torch.bfloat16, "random", True),      # g = 4 in bf16
 ]
 
 
