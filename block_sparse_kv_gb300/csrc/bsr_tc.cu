@@ -296,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = NM == 2 ? (jl & 1) : 0;
           const uint32_t step = kv_first + j;
           const int s = step % S;
-          if (m == 0 && (*abort_flag || !mbar_wait(&B.kv_full[s], (step / S) & 1u, p.st, forced))) return false;
-          if (jl < NM && (*abort_flag || !mbar_wait(&B.q_full[m], qc & 1u, p.st, forced))) return false;
+          if (m == 0 && !mbar_wait_issuer(&B.kv_full[s], (step / S) & 1u, p.st, forced, abort_flag)) return false;
+          if (jl < NM && !mbar_wait_issuer(&B.q_full[m], qc & 1u, p.st, forced, abort_flag)) return false;
           tc_fence_after();
           const int nb = min(2, n - 2 * j);
           const uint32_t z = (J + jl) & 1u;
@@ -321,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t Jg = J + jl, z = Jg & 1u;
           const int j = NM == 2 ? (jl >> 1) : jl;
           const int m = NM == 2 ? (jl & 1) : 0;
-          if (*abort_flag || !mbar_wait(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced)) { ok = false; break; }
-          if (j == 0 && (*abort_flag || !mbar_wait(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced))) { ok = false; break; }
+          if (!mbar_wait_issuer(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+          if (j == 0 && !mbar_wait_issuer(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nb = min(2, n - 2 * j);
           const int s = (kv_first + j) % S;

@@ -100,6 +100,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Bounded wait that also gives up when *abort_flag is raised, for the thread that issues
+// tensor-core MMAs: the flag is read only after the first test of the phase fails. A memory
+// access by the issuing thread stalls the MMAs it has queued (~200 ns measured), so the
+// common case, a phase already complete, costs one barrier test and nothing else.
+__device__ __forceinline__ bool mbar_wait_issuer(uint64_t* bar, uint32_t parity,
+                                                 const StatusArgs& st, bool give_up,
+                                                 const volatile int* abort_flag) {
+  if (give_up) {
+    record_error(st, BSKV_ERR_TIMEOUT);
+    return false;
+  }
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  if (*abort_flag) return false;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        record_error(st, BSKV_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // Warp-uniform bounded wait, for warps that go on to execute .sync.aligned instructions
 // (ldmatrix, mma.sync, tcgen05.ld/st): every lane waits, and the warp proceeds only if all
 // lanes succeeded and no abort was flagged, so no lane can be left behind in a collective.

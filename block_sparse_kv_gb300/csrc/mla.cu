@@ -323,8 +323,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t dkr = umma_desc(sbase + kSmemK + 2 * kPanel, 16, 512, kSwz64);
       auto pv = [&](uint32_t g, bool first) -> bool {
         const uint32_t b = g & 1u, v = g % kVSlots;
-        if (*abort_flag || !mbar_wait(&B.p_full[b], (g >> 1) & 1u, p.st, forced)) return false;
-        if (first && (*abort_flag || !mbar_wait(&B.o_free, (cc & 1u) ^ 1u, p.st, forced))) return false;
+        if (!mbar_wait_issuer(&B.p_full[b], (g >> 1) & 1u, p.st, forced, abort_flag)) return false;
+        if (first && !mbar_wait_issuer(&B.o_free, (cc & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
         tc_fence_after();
         const uint64_t a0 = dp + ((b * kPBytes) >> 4);
         const uint64_t b0 = dv + ((v * kVPart) >> 4);
@@ -342,17 +342,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nt = (ch.z - ch.y + kRows - 1) / kRows;
         const bool last_use = ci + 1 == c1 || chunk_token(chunks[ci + 1]) != n;
         if (n != cur) {
-          if (*abort_flag || !mbar_wait(&B.q_full, qc & 1u, p.st, forced) ||
-              !mbar_wait(&B.qr_full, qc & 1u, p.st, forced)) { ok = false; break; }
+          if (!mbar_wait_issuer(&B.q_full, qc & 1u, p.st, forced, abort_flag) ||
+              !mbar_wait_issuer(&B.qr_full, qc & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           ++qc;
           cur = n;
         }
         const uint32_t g0 = kvc;
         for (int t = 0; t < nt; ++t, ++kvc) {
           const uint32_t v = kvc % kVSlots, k = kvc % kKSlots;
-          if (*abort_flag || !mbar_wait(&B.kv_full[v], (kvc / kVSlots) & 1u, p.st, forced)) { ok = false; break; }
+          if (!mbar_wait_issuer(&B.kv_full[v], (kvc / kVSlots) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           // S is single-buffered: the softmax must have read the previous tile's S.
-          if (kvc > 0 && (*abort_flag || !mbar_wait(&B.s_empty, (kvc - 1) & 1u, p.st, forced))) { ok = false; break; }
+          if (kvc > 0 && !mbar_wait_issuer(&B.s_empty, (kvc - 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           tc_fence_after();
           // S = Q K^T over the 512 latent values (A from TMEM) and the 64-value tail.
 #pragma unroll
