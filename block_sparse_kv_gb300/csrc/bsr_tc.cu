@@ -269,7 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The warp stays converged through the loop; one elected lane executes the tcgen05
+    // instructions (a lone lane in a divergent branch issues MMAs less than half as fast
+    // while the softmax warps of its SM sub-partition are busy).
+    {
+      const uint32_t leader = elect_leader();
       constexpr uint32_t fmt = Fmt<T>::v;
       constexpr uint32_t idesc_qk128 = umma_idesc(128, 128, fmt, fmt, 0, 0);
       constexpr uint32_t idesc_qk64 = umma_idesc(128, 64, fmt, fmt, 0, 0);
@@ -296,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = NM == 2 ? (jl & 1) : 0;
           const uint32_t step = kv_first + j;
           const int s = step % S;
-          if (m == 0 && !mbar_wait_issuer(&B.kv_full[s], (step / S) & 1u, p.st, forced, abort_flag)) return false;
-          if (jl < NM && !mbar_wait_issuer(&B.q_full[m], qc & 1u, p.st, forced, abort_flag)) return false;
+          if (m == 0 && !issuer_wait(&B.kv_full[s], (step / S) & 1u, p.st, forced, abort_flag)) return false;
+          if (jl < NM && !issuer_wait(&B.q_full[m], qc & 1u, p.st, forced, abort_flag)) return false;
           tc_fence_after();
           const int nb = min(2, n - 2 * j);
           const uint32_t z = (J + jl) & 1u;
@@ -307,13 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t pq = ((kk >> 2) * (kQTile / 2) + (kk & 3) * 32) >> 4;
             const uint32_t pk = ((kk >> 2) * kPairPanel + (kk & 3) * 32) >> 4;
-            umma_f16(sd, dq + qo + pq, dk + ko + pk, nb == 2 ? idesc_qk128 : idesc_qk64,
+            umma_f16_w(leader, sd, dq + qo + pq, dk + ko + pk, nb == 2 ? idesc_qk128 : idesc_qk64,
                      kk > 0 ? 1u : 0u);
           }
-          umma_commit(&B.s_full[z]);
+          umma_commit_w(leader, &B.s_full[z]);
           // Q of tile m is not read after the unit's last QK on it: release it so the next
           // unit's Q loads while this unit's last jobs and epilogue run.
-          if (jl == NJ - NM + m) umma_commit(&B.q_empty[m]);
+          if (jl == NJ - NM + m) umma_commit_w(leader, &B.q_empty[m]);
           return true;
         };
         if (!qk(0) || (NJ > 1 && !qk(1))) { ok = false; break; }
@@ -321,18 +325,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t Jg = J + jl, z = Jg & 1u;
           const int j = NM == 2 ? (jl >> 1) : jl;
           const int m = NM == 2 ? (jl & 1) : 0;
-          if (!mbar_wait_issuer(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
-          if (j == 0 && !mbar_wait_issuer(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced, abort_flag)) { ok = false; break; }
+          if (!issuer_wait(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+          if (j == 0 && !issuer_wait(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nb = min(2, n - 2 * j);
           const int s = (kv_first + j) % S;
           const uint32_t vo = (s * kStageBytes) >> 4;
           const uint32_t pa = tmem + 128 + 256 * z;
           for (int kk = 0; kk < nb * 4; ++kk)
-            umma_f16_ts(tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
+            umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
                         (j == 0 && kk == 0) ? 0u : 1u);
-          umma_commit(&B.o_done[m]);
-          if (m == NM - 1) umma_commit(&B.kv_empty[s]);
+          umma_commit_w(leader, &B.o_done[m]);
+          if (m == NM - 1) umma_commit_w(leader, &B.kv_empty[s]);
           if (jl + 2 < NJ && !qk(jl + 2)) { ok = false; break; }
         }
         if (!ok) break;
@@ -342,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qc;
       }
       if (!ok) *abort_flag = 1;
-      umma_commit(&B.drain);
+      umma_commit_w(leader, &B.drain);
       mbar_wait(&B.drain, 0, p.st, false);
     }
   } else if (warp >= 4 && warp < 4 + 4 * NM) {

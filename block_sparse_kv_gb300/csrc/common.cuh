@@ -100,10 +100,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
-// Bounded wait that also gives up when *abort_flag is raised, for the thread that issues
+// Bounded wait that also gives up when *abort_flag is raised, for the warp that issues
 // tensor-core MMAs: the flag is read only after the first test of the phase fails. A memory
-// access by the issuing thread stalls the MMAs it has queued (~200 ns measured), so the
-// common case, a phase already complete, costs one barrier test and nothing else.
+// access the issuer waits on between groups of queued MMAs costs tensor-pipe time (~35 ns
+// per wait on one CTA, ~180 ns on a CTA pair, measured), so the common case, a phase
+// already complete, costs one barrier test and nothing else.
 __device__ __forceinline__ bool mbar_wait_issuer(uint64_t* bar, uint32_t parity,
                                                  const StatusArgs& st, bool give_up,
                                                  const volatile int* abort_flag) {
@@ -125,6 +126,12 @@ __device__ __forceinline__ bool mbar_wait_issuer(uint64_t* bar, uint32_t parity,
       }
     }
   }
+}
+
+// mbar_wait_issuer for every lane of a converged issuer warp, with one answer for all lanes.
+__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, const StatusArgs& st,
+                                           bool give_up, const volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait_issuer(bar, parity, st, give_up, abort_flag));
 }
 
 // Warp-uniform bounded wait, for warps that go on to execute .sync.aligned instructions
@@ -459,6 +466,44 @@ __device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// ---- MMA issue from a converged warp ---------------------------------------------------
+// The whole issuer warp runs the issue loop and the lane whose `leader` is nonzero executes
+// every tcgen05.mma / tcgen05.commit (commits track the MMAs of the thread that executes
+// them, so it is always the same lane). Measured on GB300 with softmax-like ALU work in the
+// other warps of the SM sub-partition: M = 128, N = 128 MMAs issue at ~39 ns each from a
+// converged warp against ~90 ns from a single lane inside a divergent branch.
+__device__ __forceinline__ uint32_t elect_leader() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(e));
+  return e;
+}
+__device__ __forceinline__ void umma_f16_w(uint32_t leader, uint32_t d_tmem, uint64_t a,
+                                           uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void umma_f16_ts_w(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
+                                              uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_w(uint32_t leader, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(leader)
       : "memory");
 }
 
