@@ -203,10 +203,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tensormap(&qmap);
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
+    // Converged like the MMA issuer; the elected lane issues the copies.
+    {
+      const uint32_t leader = elect_leader();
+      if (leader) {
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+      }
+      __syncwarp();
       uint32_t qc = 0, kvc = 0;
       uint32_t qi[2] = {0u, 0u};  // Q tiles issued
       // Q is read once (evict first); a K/V block serves every row block that lists it
@@ -216,11 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Q of M tile m for the unit (row block i, kv head h), once the previous unit's last QK
       // on that tile has completed.
       auto load_q = [&](int m, int i, int h) -> bool {
-        if (*abort_flag || !mbar_wait(&B.q_empty[m], (qc & 1u) ^ 1u, p.st, forced)) return false;
-        mbar_arrive_expect_tx(&B.q_full[m], kQTile);
+        if (!issuer_wait(&B.q_empty[m], (qc & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
+        mbar_arrive_expect_tx_w(leader, &B.q_full[m], kQTile);
         for (int hl = 0; hl < 2; ++hl)
           for (int pn = 0; pn < 2; ++pn)
-            tma_load_3d_hint(sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
+            tma_load_3d_hint_w(leader, sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
                              pn * 64, h * p.group + m * 2 + hl, i * kBlk, &B.q_full[m], pol_q);
         ++qi[m];
         return true;
@@ -228,16 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K and V of column blocks e, e+1 (< e1) of kv head h into the next stage.
       auto load_kv = [&](int e, int e1, int h) -> bool {
         const int s = kvc % S;
-        if (*abort_flag || !mbar_wait(&B.kv_empty[s], ((kvc / S) & 1u) ^ 1u, p.st, forced)) return false;
+        if (!issuer_wait(&B.kv_empty[s], ((kvc / S) & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
         const int nb = min(2, e1 - e);
         uint8_t* dst = sm + L::kKV + s * kStageBytes;
-        mbar_arrive_expect_tx(&B.kv_full[s], nb * 4 * kKPanel);
+        mbar_arrive_expect_tx_w(leader, &B.kv_full[s], nb * 4 * kKPanel);
         for (int b = 0; b < nb; ++b) {
           const int j = indices[e + b];
           for (int pn = 0; pn < 2; ++pn) {
-            tma_load_3d_hint(dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk,
+            tma_load_3d_hint_w(leader, dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk,
                              &B.kv_full[s], pol_kv);
-            tma_load_3d_hint(dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64,
+            tma_load_3d_hint_w(leader, dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64,
                              h, j * kBlk, &B.kv_full[s], pol_kv);
           }
         }

@@ -307,7 +307,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 6) {
     // -------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The warp stays converged; one elected lane executes the tcgen05 instructions.
+    {
+      const uint32_t leader = elect_leader();
       constexpr uint32_t idesc_qk = umma_idesc(128, kRows, 0, 0, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc(128, kVD, 0, 0, 0, 1);
       const uint32_t sbase = smem_u32(sm);
@@ -323,16 +325,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t dkr = umma_desc(sbase + kSmemK + 2 * kPanel, 16, 512, kSwz64);
       auto pv = [&](uint32_t g, bool first) -> bool {
         const uint32_t b = g & 1u, v = g % kVSlots;
-        if (!mbar_wait_issuer(&B.p_full[b], (g >> 1) & 1u, p.st, forced, abort_flag)) return false;
-        if (first && !mbar_wait_issuer(&B.o_free, (cc & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
+        if (!issuer_wait(&B.p_full[b], (g >> 1) & 1u, p.st, forced, abort_flag)) return false;
+        if (first && !issuer_wait(&B.o_free, (cc & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
         tc_fence_after();
         const uint64_t a0 = dp + ((b * kPBytes) >> 4);
         const uint64_t b0 = dv + ((v * kVPart) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kRows / 32; ++kk)
-          umma_f8(tmem, a0 + kk * 2, b0 + kk * 256, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        umma_commit(&B.o_done[b]);
-        umma_commit_mc(&B.v_empty[v], 0x3);  // both CTAs' V part free
+          umma_f8_w(leader, tmem, a0 + kk * 2, b0 + kk * 256, idesc_pv, (first && kk == 0) ? 0u : 1u);
+        umma_commit_w(leader, &B.o_done[b]);
+        umma_commit_mc_w(leader, &B.v_empty[v], 0x3);  // both CTAs' V part free
         return true;
       };
       int cur = -1;
@@ -342,17 +344,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nt = (ch.z - ch.y + kRows - 1) / kRows;
         const bool last_use = ci + 1 == c1 || chunk_token(chunks[ci + 1]) != n;
         if (n != cur) {
-          if (!mbar_wait_issuer(&B.q_full, qc & 1u, p.st, forced, abort_flag) ||
-              !mbar_wait_issuer(&B.qr_full, qc & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+          if (!issuer_wait(&B.q_full, qc & 1u, p.st, forced, abort_flag) ||
+              !issuer_wait(&B.qr_full, qc & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           ++qc;
           cur = n;
         }
         const uint32_t g0 = kvc;
         for (int t = 0; t < nt; ++t, ++kvc) {
           const uint32_t v = kvc % kVSlots, k = kvc % kKSlots;
-          if (!mbar_wait_issuer(&B.kv_full[v], (kvc / kVSlots) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+          if (!issuer_wait(&B.kv_full[v], (kvc / kVSlots) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           // S is single-buffered: the softmax must have read the previous tile's S.
-          if (kvc > 0 && !mbar_wait_issuer(&B.s_empty, (kvc - 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+          if (kvc > 0 && !issuer_wait(&B.s_empty, (kvc - 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           tc_fence_after();
           // S = Q K^T over the 512 latent values (A from TMEM) and the 64-value tail.
 #pragma unroll
@@ -360,14 +362,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int pn = kk >> 2;
             const uint64_t bd = ((pn >> 1) == vh ? dvn + ((v * kVPart) >> 4) : dkn + ((k * kKPart) >> 4)) +
                                 (((pn & 1) * kPanel + (kk & 3) * 32) >> 4);
-            umma_f8_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            umma_f8_ts_w(leader, tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
-            umma_f8(tmem + kTmemS, dqr + kk * 2, dkr + ((k * kKPart) >> 4) + kk * 2, idesc_qk, 1u);
-          umma_commit(&B.s_full);
-          umma_commit_mc(&B.k_empty[k], 0x3);  // both CTAs' K part free
-          if (t + 1 == nt && last_use) umma_commit(&B.q_empty);
+            umma_f8_w(leader, tmem + kTmemS, dqr + kk * 2, dkr + ((k * kKPart) >> 4) + kk * 2, idesc_qk, 1u);
+          umma_commit_w(leader, &B.s_full);
+          umma_commit_mc_w(leader, &B.k_empty[k], 0x3);  // both CTAs' K part free
+          if (t + 1 == nt && last_use) umma_commit_w(leader, &B.q_empty);
           if (t >= 1 && !pv(kvc - 1, t == 1)) { ok = false; break; }
         }
         if (!ok) break;
@@ -375,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++cc;
       }
       if (!ok) raise_abort();
-      umma_commit(&B.drain);
+      umma_commit_w(leader, &B.drain);
       mbar_wait(&B.drain, 0, p.st, false);
     }
   } else {
