@@ -337,9 +337,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = (kv_first + j) % S;
           const uint32_t vo = (s * kStageBytes) >> 4;
           const uint32_t pa = tmem + 128 + 256 * z;
-          for (int kk = 0; kk < nb * 4; ++kk)
-            umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
-                        (j == 0 && kk == 0) ? 0u : 1u);
+          // a block pair is 8 MMAs (K = 16 keys each), a lone last block 4
+          if (nb == 2) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
+                            (j == 0 && kk == 0) ? 0u : 1u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
+                            (j == 0 && kk == 0) ? 0u : 1u);
+          }
           umma_commit_w(leader, &B.o_done[m]);
           if (m == NM - 1) umma_commit_w(leader, &B.kv_empty[s]);
           if (jl + 2 < NJ && !qk(jl + 2)) { ok = false; break; }
@@ -413,7 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k0 + c > lim) sr[64 * bb + c] = __float_as_uint(-INFINITY);
             }
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], __uint_as_float(sr[64 * bb + c]));
+            for (int c = 0; c < 64; c += 2)
+              mxp[(c >> 1) & 7] = fmax3(mxp[(c >> 1) & 7], __uint_as_float(sr[64 * bb + c]),
+                                        __uint_as_float(sr[64 * bb + c + 1]));
           }
         }
         float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
@@ -433,15 +444,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(s * scale - ref), 32 keys at a time into packed columns [16 ck, 16 ck + 16)
         PSum<T> sp;
         sp.zero();
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nr2 = make_float2(-ref, -ref);
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
           if (ck < 2 * nb) {
             uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              const float x0 = fmaf(__uint_as_float(sr[32 * ck + c]), p.scale_log2, -ref);
-              const float x1 = fmaf(__uint_as_float(sr[32 * ck + c + 1]), p.scale_log2, -ref);
-              pk[c / 2] = exp2_pack<T>(x0, x1, sp, (c >> 1) & 7);
+              const float2 x = ffma2(make_float2(__uint_as_float(sr[32 * ck + c]),
+                                                 __uint_as_float(sr[32 * ck + c + 1])),
+                                     sc2, nr2);
+              pk[c / 2] = exp2_pack<T>(x.x, x.y, sp, (c >> 1) & 7);
             }
             tmem_st16(scol + 16 * ck, pk);
           }
