@@ -467,8 +467,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const int valid = min(kRows, ch.z - (ch.y + t * kRows)) - wg * 64;
         // scaled logits, kept in place as float bits
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), z2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * p.scale_log2);
+        for (int c = 0; c < 64; c += 2) {
+          const float2 y = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, z2);
+          sr[c] = __float_as_uint(y.x);
+          sr[c + 1] = __float_as_uint(y.y);
+        }
         if (valid < 64) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) sr[c] = c < valid ? sr[c] : __float_as_uint(-INFINITY);
@@ -476,12 +481,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto x = [&](int c) { return __uint_as_float(sr[c]); };
         float m8[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          m8[j] = fmaxf(fmaxf(fmaxf(x(j), x(j + 8)), fmaxf(x(j + 16), x(j + 24))),
-                        fmaxf(fmaxf(x(j + 32), x(j + 40)), fmaxf(x(j + 48), x(j + 56))));
-        }
-        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int j = 0; j < 8; ++j)
+          m8[j] = fmax3(fmax3(x(j), x(j + 8), x(j + 16)), fmax3(x(j + 24), x(j + 32), x(j + 40)),
+                        fmaxf(x(j + 48), x(j + 56)));
+        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         red[(b * 2 + wg) * 128 + r] = mx;
         // both groups meet here once per tile (named barrier 3, 256 threads)
         ok = bar_and(3, 256, good);
@@ -503,6 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // p = 2^(x - ref) in f16x2 pairs, straight to E4M3 pairs, 16 keys (one 16-byte chunk
         // of the 128B-swizzled P row) at a time; row sum in f16x2.
         uint8_t* prow = sm + kSmemP + b * kPBytes + r * 128;
+        const float2 one2 = make_float2(1.f, 1.f), nr2 = make_float2(-ref, -ref);
         __half2 hs[4];
 #pragma unroll
         for (int c16 = 0; c16 < 4; ++c16) {
@@ -510,8 +514,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int c = c16 * 16 + j * 4;
-            const __half2 e0 = h2exp2_approx(__floats2half2_rn(x(c) - ref, x(c + 1) - ref));
-            const __half2 e1 = h2exp2_approx(__floats2half2_rn(x(c + 2) - ref, x(c + 3) - ref));
+            const float2 d0 = ffma2(make_float2(x(c), x(c + 1)), one2, nr2);
+            const float2 d1 = ffma2(make_float2(x(c + 2), x(c + 3)), one2, nr2);
+            const __half2 e0 = h2exp2_approx(__floats2half2_rn(d0.x, d0.y));
+            const __half2 e1 = h2exp2_approx(__floats2half2_rn(d1.x, d1.y));
             const __half2 s2 = __hadd2(e0, e1);
             hs[j] = c16 == 0 ? s2 : __hadd2(hs[j], s2);
             pk[j] = half2_to_e4m3x2(e0) | (half2_to_e4m3x2(e1) << 16);
