@@ -417,6 +417,33 @@ def bench_mla(bskv, synth, steps, warmup, peaks):
     return res
 
 
+def bench_mla_paged(bskv, synth, steps, warmup, peaks):
+    """Dense paged MLA decode: 128 requests x 128 heads over all of their 2048-8192 tokens
+    (page_size 64, pages permuted in a pool). Each token row is read once per step, so the
+    row reads (~0.4 GB, larger than L2) and the FP8 contraction are both reported."""
+    d = synth.make("mla_paged", device="cuda")
+    B, H = d["batch"], d["heads"]
+    plan = bskv.bskv_plan_mla_paged(d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"], B,
+                                    d["num_pages"], d["page_size"], H)
+    plan.upload("cuda")
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda")
+    scale = 1.0 / math.sqrt(576)
+    fn = lambda: bskv.bskv_run_mla_paged(plan, d["query"], d["kv_pages"], scale, 1.0, out=out)  # noqa
+    ms = time_iters(fn, steps, warmup, flush=True)
+    tokens = int(d["lens"].sum())
+    fl = 2.0 * H * tokens * (576 + 512)
+    nbytes = tokens * 576 + B * H * (576 + 1024)
+    med = statistics.median(ms) * 1e-3
+    tf = fl / med / 1e12
+    gbs = nbytes / med / 1e9
+    return dict(workload="mla_paged: batch 128, 128 heads, E4M3 rows of 576, page_size 64, "
+                         "kv len U[2048,8192], pages permuted in a pool (L2 flushed)",
+                **summary(ms), flops=fl, tflops=tf, frac=tf / (2.0 * peaks["bf16_tflops"]),
+                peak="fp8 = 2 x measured bf16 dense burst (nominal ratio)",
+                bytes=nbytes, gbs=gbs, hbm_frac=gbs / peaks["hbm_gbs"],
+                launches_per_step=2 + (1 if plan.metadata()[6] > 0 else 0))
+
+
 # ---------------------------------------------------------------------------------------
 # CPU baseline: the float64 oracle on the host cores, on a bounded sample
 # ---------------------------------------------------------------------------------------
@@ -482,7 +509,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of extra rows: bsr_prefill,bsr_tiny,mla,split,e2e,cpu or all/none")
+                    help="comma list of extra rows: bsr_prefill,bsr_tiny,mla,mla_paged,split,e2e,cpu "
+                         "or all/none")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -493,7 +521,7 @@ def main():
     bskv.build()
     dist, rank, ws = dist_setup(args.gpus)
     peaks, peak_src = load_peaks()
-    rows = set(["bsr_prefill", "bsr_tiny", "mla", "split", "e2e", "cpu"]
+    rows = set(["bsr_prefill", "bsr_tiny", "mla", "mla_paged", "split", "e2e", "cpu"]
                if args.rows == "all" else [] if args.rows == "none" else args.rows.split(","))
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -513,7 +541,9 @@ def main():
                  lambda: bench_bsr(bskv, synth, "bsr_prefill", K, args.warmup, peaks, True)),
                 ("bsr_tiny", "bsr_tiny",
                  lambda: bench_bsr(bskv, synth, "bsr_tiny", K, args.warmup, peaks, True)),
-                ("mla", "mla_decode", lambda: bench_mla(bskv, synth, K, args.warmup, peaks))]
+                ("mla", "mla_decode", lambda: bench_mla(bskv, synth, K, args.warmup, peaks)),
+                ("mla_paged", "mla_paged",
+                 lambda: bench_mla_paged(bskv, synth, K, args.warmup, peaks))]
         for key, name, job in jobs:
             if key in rows:
                 try:

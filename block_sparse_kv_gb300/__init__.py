@@ -60,6 +60,8 @@ _SIGS = {
     "bskv_plan_bsr": ([_I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                        ctypes.POINTER(_P)], _I32),
     "bskv_plan_mla_sparse": ([_I32P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(_P)], _I32),
+    "bskv_plan_mla_paged": ([_I32P, _I32P, _I32P, _I32, _I32, _I32, _I32, _I32,
+                             ctypes.POINTER(_P)], _I32),
     "bskv_plan_destroy": ([_P], _I32),
     "bskv_plan_metadata": ([_P, ctypes.POINTER(_I32P), _I64P], _I32),
     "bskv_plan_workspace_sizes": ([_P, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)], _I32),
@@ -70,6 +72,7 @@ _SIGS = {
     "bskv_run_decode_noalloc": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P], _I32),
     "bskv_run_bsr": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P, _SZ, _P], _I32),
     "bskv_run_mla_sparse": ([_P, _P, _P, _I64, _P, _F, _F, _P, _P, _P, _SZ, _P], _I32),
+    "bskv_run_mla_paged": ([_P, _P, _P, _F, _F, _P, _P, _P, _SZ, _P], _I32),
     "bskv_rope_quantize_fp8": ([_P, _I64P, _P, _I64P, _P, _I64, _I32, _P, _I64P, _P, _I64P,
                                 _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64,
                                 _I32, _P, _I32, _I64, _I32, _F, _F, _P], _I32),
@@ -329,6 +332,40 @@ def bskv_run_mla_sparse(plan, query, kv_rows, indices, bmm1_scale, bmm2_scale=1.
         plan.handle, query.data_ptr(), kv_rows.data_ptr(), rows, indices.data_ptr(),
         float(bmm1_scale), float(bmm2_scale), out.data_ptr(), _ptr(lse), _ptr(fw),
         0 if fw is None else fw.numel(), _stream(query)))
+    return (out, lse) if return_lse else out
+
+
+def bskv_plan_mla_paged(kv_indptr, kv_indices, kv_last_page_len, batch, num_pages, page_size,
+                        num_heads, num_sms=None):
+    """Dense paged MLA decode plan from a HOST CSR page table (one query token per request)."""
+    lib = load_library()
+    ip, ipp = _i32_array(kv_indptr)
+    ix, ixp = _i32_array(kv_indices)
+    lp, lpp = _i32_array(kv_last_page_len)
+    h = ctypes.c_void_p()
+    ns = _num_sms() if num_sms is None else num_sms
+    _check("bskv_plan_mla_paged", lib.bskv_plan_mla_paged(
+        ctypes.cast(ipp, _I32P), ctypes.cast(ixp, _I32P), ctypes.cast(lpp, _I32P), int(batch),
+        int(num_pages), int(page_size), int(num_heads), int(ns), ctypes.byref(h)))
+    return Plan(h.value, "mla_paged", batch=batch, num_heads=num_heads, num_pages=num_pages,
+                page_size=page_size)
+
+
+def bskv_run_mla_paged(plan, query, kv_pages, bmm1_scale, bmm2_scale=1.0, out=None, lse=None,
+                       return_lse=False):
+    """query [B, H, 576] uint8/e4m3; kv_pages [num_pages, page_size, 576] uint8/e4m3."""
+    lib = load_library()
+    if plan.int_ws is None:
+        plan.upload(query.device)
+    B, H, _ = query.shape
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=query.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=query.device)
+    fw = plan.float_ws
+    _check("bskv_run_mla_paged", lib.bskv_run_mla_paged(
+        plan.handle, query.data_ptr(), kv_pages.data_ptr(), float(bmm1_scale), float(bmm2_scale),
+        out.data_ptr(), _ptr(lse), _ptr(fw), 0 if fw is None else fw.numel(), _stream(query)))
     return (out, lse) if return_lse else out
 
 

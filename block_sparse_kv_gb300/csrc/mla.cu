@@ -697,30 +697,29 @@ __global__ void __launch_bounds__(128)
   if (lse && vh == 0 && lane == 0) lse[int64_t(n) * heads + h] = count > 0 ? m + logf(l) : -INFINITY;
 }
 
-}  // namespace
-}  // namespace bskv
-
-using namespace bskv;
-
-extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* query,
-                                           const void* kv_rows, int64_t num_rows,
-                                           const int32_t* indices, float bmm1_scale,
-                                           float bmm2_scale, void* out, float* lse,
-                                           void* float_ws, size_t float_ws_bytes, void* stream) {
-  if (!plan || plan->kind != KIND_MLA) { set_error("run_mla_sparse: not an MLA plan"); return BSKV_ERR_INVALID_ARG; }
-  if (!plan->meta_dev) { set_error("run_mla_sparse: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
-  if (plan->batch == 0) return BSKV_OK;
-  if (!query || !kv_rows || !indices || !out) { set_error("run_mla_sparse: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
-  if (!aligned16(query) || !aligned16(kv_rows) || !aligned16(out) || (reinterpret_cast<uintptr_t>(indices) & 3)) {
-    set_error("run_mla_sparse: tensors must be 16-byte aligned (indices 4-byte)");
-    return BSKV_ERR_INVALID_ARG;
+// Row list of the paged decode, from the page table in the metadata (aux0 = kv_indptr,
+// aux1 = kv_indices): rows[b * stride + t] = the cache row of token t of request b while
+// t is inside the request's pages, 0 beyond them (the decode reads only t < L_b).
+__global__ void __launch_bounds__(256) mla_page_rows_kernel(const int32_t* __restrict__ meta,
+                                                            int32_t batch, int32_t stride,
+                                                            int32_t page_size,
+                                                            int32_t* __restrict__ rows) {
+  const int32_t* indptr = meta + meta[H_OFF_AUX0];
+  const int32_t* pages = meta + meta[H_OFF_AUX1];
+  const int64_t total = int64_t(batch) * stride;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int32_t b = int32_t(i / stride), t = int32_t(i % stride);
+    const int32_t slot = indptr[b] + t / page_size;
+    rows[i] = slot < indptr[b + 1] ? pages[slot] * page_size + t % page_size : 0;
   }
-  if (num_rows < 1) { set_error("run_mla_sparse: num_rows must be positive"); return BSKV_ERR_INVALID_ARG; }
-  if (float_ws_bytes < plan->float_ws_bytes || (plan->float_ws_bytes && !float_ws)) {
-    set_error("run_mla_sparse: float workspace of %zu bytes, %zu needed", float_ws_bytes, plan->float_ws_bytes);
-    return BSKV_ERR_WORKSPACE_TOO_SMALL;
-  }
-  if (float_ws && !aligned16(float_ws)) { set_error("run_mla_sparse: float workspace must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+}
+
+// The decode over validated arguments: `indices` holds plan->top_k row ids per query token,
+// the float workspace starts with the split-KV partials.
+bskv_status run_mla(const bskv_plan* plan, const void* query, const void* kv_rows,
+                    int64_t num_rows, const int32_t* indices, float bmm1_scale, float bmm2_scale,
+                    void* out, float* lse, void* float_ws, cudaStream_t st) {
   const int64_t nq = int64_t(plan->batch) * plan->q_len;
   MlaParams mp{};
   mp.meta = plan->meta_dev;
@@ -769,7 +768,6 @@ extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* qu
   } else {
     wm = om;  // no split partials
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = meta_word(plan, H_GRID);
   if (grid > 0) {
     const size_t smem = kSmemBytes + 1024;
@@ -787,4 +785,60 @@ extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* qu
     if (bskv_status s = cuda_check(cudaGetLastError(), "mla merge launch")) return s;
   }
   return BSKV_OK;
+}
+
+}  // namespace
+}  // namespace bskv
+
+using namespace bskv;
+
+extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* query,
+                                           const void* kv_rows, int64_t num_rows,
+                                           const int32_t* indices, float bmm1_scale,
+                                           float bmm2_scale, void* out, float* lse,
+                                           void* float_ws, size_t float_ws_bytes, void* stream) {
+  if (!plan || plan->kind != KIND_MLA || plan->mla_variant != MLA_SPARSE) { set_error("run_mla_sparse: not a sparse MLA plan"); return BSKV_ERR_INVALID_ARG; }
+  if (!plan->meta_dev) { set_error("run_mla_sparse: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
+  if (plan->batch == 0) return BSKV_OK;
+  if (!query || !kv_rows || !indices || !out) { set_error("run_mla_sparse: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
+  if (!aligned16(query) || !aligned16(kv_rows) || !aligned16(out) || (reinterpret_cast<uintptr_t>(indices) & 3)) {
+    set_error("run_mla_sparse: tensors must be 16-byte aligned (indices 4-byte)");
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (num_rows < 1) { set_error("run_mla_sparse: num_rows must be positive"); return BSKV_ERR_INVALID_ARG; }
+  if (float_ws_bytes < plan->float_ws_bytes || (plan->float_ws_bytes && !float_ws)) {
+    set_error("run_mla_sparse: float workspace of %zu bytes, %zu needed", float_ws_bytes, plan->float_ws_bytes);
+    return BSKV_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (float_ws && !aligned16(float_ws)) { set_error("run_mla_sparse: float workspace must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  return run_mla(plan, query, kv_rows, num_rows, indices, bmm1_scale, bmm2_scale, out, lse,
+                 float_ws, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" bskv_status bskv_run_mla_paged(const bskv_plan* plan, const void* query,
+                                          const void* kv_pages, float bmm1_scale,
+                                          float bmm2_scale, void* out, float* lse,
+                                          void* float_ws, size_t float_ws_bytes, void* stream) {
+  if (!plan || plan->kind != KIND_MLA || plan->mla_variant != MLA_PAGED) { set_error("run_mla_paged: not a paged MLA plan"); return BSKV_ERR_INVALID_ARG; }
+  if (!plan->meta_dev) { set_error("run_mla_paged: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
+  if (plan->batch == 0) return BSKV_OK;
+  if (!query || !kv_pages || !out) { set_error("run_mla_paged: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
+  if (!aligned16(query) || !aligned16(kv_pages) || !aligned16(out)) {
+    set_error("run_mla_paged: tensors must be 16-byte aligned");
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (float_ws_bytes < plan->float_ws_bytes || !float_ws) {
+    set_error("run_mla_paged: float workspace of %zu bytes, %zu needed", float_ws_bytes, plan->float_ws_bytes);
+    return BSKV_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (!aligned16(float_ws)) { set_error("run_mla_paged: float workspace must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* rows = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(float_ws) + plan->mla_rows_off);
+  const int64_t total = int64_t(plan->batch) * plan->top_k;
+  const int blocks = int(std::min<int64_t>((total + 255) / 256, 1024));
+  mla_page_rows_kernel<<<blocks, 256, 0, st>>>(plan->meta_dev, plan->batch, plan->top_k,
+                                               plan->page_size, rows);
+  if (bskv_status s = cuda_check(cudaGetLastError(), "mla page rows launch")) return s;
+  return run_mla(plan, query, kv_pages, int64_t(plan->num_pages) * plan->page_size, rows,
+                 bmm1_scale, bmm2_scale, out, lse, float_ws, st);
 }

@@ -351,6 +351,72 @@ extern "C" bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t bat
   return BSKV_OK;
 }
 
+extern "C" bskv_status bskv_plan_mla_paged(const int32_t* kv_indptr, const int32_t* kv_indices,
+                                           const int32_t* kv_last_page_len, int32_t batch,
+                                           int32_t num_pages, int32_t page_size,
+                                           int32_t num_heads, int32_t num_sms,
+                                           bskv_plan** out_plan) {
+  if (!out_plan) { set_error("plan_mla_paged: out_plan is NULL"); return BSKV_ERR_INVALID_ARG; }
+  *out_plan = nullptr;
+  if (batch < 0 || num_sms < 1 || page_size < 1 || num_pages < 1) {
+    set_error("plan_mla_paged: batch=%d num_pages=%d page_size=%d num_sms=%d", batch, num_pages,
+              page_size, num_sms);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (num_heads < 1 || num_heads > 128) { set_error("plan_mla_paged: num_heads %d outside [1,128]", num_heads); return BSKV_ERR_UNSUPPORTED; }
+  if (int64_t(num_pages) * page_size > INT32_MAX) { set_error("plan_mla_paged: num_pages * page_size exceeds int32 row ids"); return BSKV_ERR_UNSUPPORTED; }
+  if (batch > 0 && (!kv_indptr || !kv_last_page_len)) { set_error("plan_mla_paged: NULL index array"); return BSKV_ERR_INVALID_ARG; }
+  if (batch > 0 && kv_indptr[0] != 0) { set_error("plan_mla_paged: kv_indptr[0] must be 0"); return BSKV_ERR_INVALID_ARG; }
+  std::vector<int64_t> len(size_t(batch), 0);
+  int64_t longest = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t n = int64_t(kv_indptr[b + 1]) - kv_indptr[b];
+    if (n < 0) { set_error("plan_mla_paged: kv_indptr decreases at %d", b); return BSKV_ERR_INVALID_ARG; }
+    if (n > 0) {
+      const int32_t lp = kv_last_page_len[b];
+      if (lp < 1 || lp > page_size) {
+        set_error("plan_mla_paged: kv_last_page_len[%d] = %d outside [1, %d]", b, lp, page_size);
+        return BSKV_ERR_INVALID_ARG;
+      }
+      len[size_t(b)] = (n - 1) * page_size + lp;
+    }
+    longest = std::max(longest, len[size_t(b)]);
+  }
+  const int64_t nnz = batch > 0 ? kv_indptr[batch] : 0;
+  if (nnz > 0 && !kv_indices) { set_error("plan_mla_paged: kv_indices is NULL"); return BSKV_ERR_INVALID_ARG; }
+  for (int64_t i = 0; i < nnz; ++i) {
+    if (kv_indices[i] < 0 || kv_indices[i] >= num_pages) {
+      set_error("plan_mla_paged: kv_indices[%lld] = %d outside [0, %d)", (long long)i, kv_indices[i], num_pages);
+      return BSKV_ERR_INVALID_ARG;
+    }
+  }
+  const int64_t stride = std::max<int64_t>(64, (longest + 63) / 64 * 64);
+  if (stride > INT32_MAX / 2) { set_error("plan_mla_paged: a request of %lld tokens is too long", (long long)longest); return BSKV_ERR_UNSUPPORTED; }
+  // One unit per request, partitioned like the sparse decode.
+  std::vector<int32_t> worker_ptr, merges;
+  std::vector<Chunk> chunks;
+  int32_t slots = 0;
+  linear_partition(len, kMlaTile, std::max(1, num_sms / kMlaVSplit), worker_ptr, chunks, slots,
+                   merges);
+  const int32_t P = int32_t(worker_ptr.size() - 1);
+  bskv_plan* p = new bskv_plan();
+  p->kind = KIND_MLA;
+  p->mla_variant = MLA_PAGED;
+  p->batch = batch; p->q_len = 1; p->num_qo_heads = num_heads; p->top_k = int32_t(stride);
+  p->num_pages = num_pages; p->page_size = page_size;
+  p->head_dim = 576; p->dtype = BSKV_E4M3;
+  assemble(p, KIND_MLA, int32_t(len.size()), worker_ptr, chunks, slots, merges, kMlaTile,
+           kv_indptr, batch > 0 ? size_t(batch) + 1 : 0, kv_indices, size_t(nnz), P * kMlaVSplit,
+           MLA_PAGED);
+  const size_t partials = slots == 0 ? 0
+      : align256(size_t(slots) * kMlaVSplit * 128 * kMlaVDim * 4) +
+            align256(size_t(slots) * kMlaVSplit * 128 * 4);
+  p->mla_rows_off = partials;
+  p->float_ws_bytes = partials + align256(size_t(batch) * size_t(stride) * 4);
+  *out_plan = p;
+  return BSKV_OK;
+}
+
 extern "C" bskv_status bskv_plan_destroy(bskv_plan* plan) {
   delete plan;
   return BSKV_OK;

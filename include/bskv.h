@@ -137,6 +137,28 @@ bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t batch, int32_t
                                  int32_t num_heads, int32_t top_k, int32_t num_sms,
                                  bskv_plan** out_plan);
 
+/*
+ * Dense paged MLA FP8 decode plan ([SKILL] Multi-Head Latent Attention (MLA):
+ * BatchMLAPagedAttentionWrapper and trtllm_batch_decode_with_kv_cache_mla over a latent
+ * KV cache; [CHEAT] benchmark README: BatchMLAPagedAttentionWrapper, MLA attention of the
+ * DeepSeek models; page table as in [SKILL] KV-Cache Formats). One query token per
+ * request attends to every token of its request.
+ *   kv_indptr[batch+1], kv_indices[kv_indptr[batch]], kv_last_page_len[batch]: HOST int32
+ *     page table; request b owns pages kv_indices[kv_indptr[b] .. kv_indptr[b+1]) in
+ *     order and L_b = (n_b - 1) * page_size + kv_last_page_len[b] tokens (0 when it owns
+ *     no page); kv_indptr[0] == 0 and non-decreasing, page ids in [0, num_pages),
+ *     1 <= kv_last_page_len[b] <= page_size for a request with pages.
+ *   Token t of request b is cache row kv_indices[kv_indptr[b] + t / page_size] *
+ *   page_size + t % page_size; num_pages * page_size must stay below 2^31.
+ *   num_heads in [1, 128]; num_sms: SM count of the target GPU.
+ * The plan copies the page table into its metadata; runs expand it into the row list of
+ * the sparse MLA kernel (in the float workspace) and run that kernel over it.
+ */
+bskv_status bskv_plan_mla_paged(const int32_t* kv_indptr, const int32_t* kv_indices,
+                                const int32_t* kv_last_page_len, int32_t batch,
+                                int32_t num_pages, int32_t page_size, int32_t num_heads,
+                                int32_t num_sms, bskv_plan** out_plan);
+
 /* Free a plan (NULL is accepted). */
 bskv_status bskv_plan_destroy(bskv_plan* plan);
 
@@ -262,6 +284,21 @@ bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* query, const 
                                 int64_t num_rows, const int32_t* indices, float bmm1_scale,
                                 float bmm2_scale, void* out, float* lse, void* float_ws,
                                 size_t float_ws_bytes, void* stream);
+
+/*
+ * Dense paged MLA FP8 decode (the plan of bskv_plan_mla_paged):
+ *   query    [batch, num_heads, 576] E4M3, contiguous (one token per request).
+ *   kv_pages [num_pages, page_size, 576] E4M3, contiguous: the latent cache, one row of
+ *            512 latent + 64 rotated values per token (the layout the prologue writes).
+ *   s_j, out and lse as for bskv_run_mla_sparse over the L_b tokens of request b:
+ *   out bf16 [batch, num_heads, 512]; lse float32 [batch, num_heads] or NULL. A request
+ *   with no token gets out = 0 and lse = -inf.
+ *   float_ws: at least bskv_plan_workspace_sizes' float bytes (split-KV partials and the
+ *   expanded row list), 16-byte aligned.
+ */
+bskv_status bskv_run_mla_paged(const bskv_plan* plan, const void* query, const void* kv_pages,
+                               float bmm1_scale, float bmm2_scale, void* out, float* lse,
+                               void* float_ws, size_t float_ws_bytes, void* stream);
 
 /*
  * RoPE + FP8 E4M3 quantisation of MLA query/key rows ([MLA] mla_rope_quantize_fp8;

@@ -29,6 +29,11 @@ Sources:
     indices [batch, q_len, top_k] shared by all heads, seq_lens[b] valid entries,
     bmm1_scale on the QK product, bmm2_scale on the output, BF16 output of 512 values
     (kv_lora_rank) and FP32 LSE. Reading: V is the first 512 values of each row.
+  * Dense paged MLA: "FlashInfer" agent-skill summary, Multi-Head Latent Attention (MLA)
+    (BatchMLAPagedAttentionWrapper; trtllm_batch_decode_with_kv_cache_mla over the latent
+    cache) and FlashInfer cheat page, benchmark README (BatchMLAPagedAttentionWrapper: MLA
+    attention of the DeepSeek models). Reading: the sparse MLA contraction over all tokens
+    of the request, whose 576-value latent rows are paged with the page table of Paged KV.
   * merge: FlashInfer cheat page, docs/api/cascade.rst (merge_state, merge_states);
     "FlashInfer" agent-skill summary, Cascade Inference (merge attention states).
 """
@@ -196,6 +201,35 @@ def mla_sparse_decode(query_codes, kv_codes, indices, seq_lens, bmm1_scale, bmm2
         q = e4m3_decode(query_codes[b, t])               # [H, 576]
         o, l = masked_attention(q[None], kv[:, None, :], kv[:, None, :KV_LORA_RANK],
                                 bmm1_scale)
+        outs.append(bmm2_scale * o[0])
+        lses.append(l[0])
+    return np.stack(outs), np.stack(lses)
+
+
+def mla_paged_decode(query_codes, kv_page_codes, kv_indptr, kv_indices, kv_last_page_len,
+                     page_size, bmm1_scale, bmm2_scale, requests=None):
+    """Dense paged MLA decode from E4M3 codes: one query token per request attends to every
+    token of its request.
+
+    query [B, H, 576] and the latent cache [pages, page_size, 576] as uint8 E4M3 codes; the
+    page table as for paged_decode (request b owns pages kv_indices[kv_indptr[b]:
+    kv_indptr[b+1]] in order, length (n_b - 1) * page_size + kv_last_page_len[b]). The
+    request's logical rows are its pages' rows concatenated and cut to that length; then
+    the sparse MLA definition applies to them (same scales, V = the first 512 values).
+    Returns out [n, H, 512] and lse [n, H] (float64).
+    """
+    B, H, Dq = query_codes.shape
+    if Dq != QK_DIM or kv_page_codes.shape[-1] != QK_DIM:
+        raise ValueError("MLA rows must hold 576 values")
+    reqs = range(B) if requests is None else requests
+    outs, lses = [], []
+    for b in reqs:
+        L = paged_kv_len(kv_indptr, kv_last_page_len, page_size, b)
+        pages = np.asarray(kv_indices[int(kv_indptr[b]):int(kv_indptr[b + 1])], dtype=np.int64)
+        rows = kv_page_codes[pages].reshape(-1, QK_DIM)[:L]       # [L, 576] codes, in order
+        kv = e4m3_decode(rows)
+        q = e4m3_decode(query_codes[b])                            # [H, 576]
+        o, l = masked_attention(q[None], kv[:, None, :], kv[:, None, :KV_LORA_RANK], bmm1_scale)
         outs.append(bmm2_scale * o[0])
         lses.append(l[0])
     return np.stack(outs), np.stack(lses)

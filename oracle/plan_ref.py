@@ -32,6 +32,9 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
   * MLA: units = query tokens n = b*q_len + t, len = seq_lens[b], tile 128,
     max_workers = max(1, num_sms // 2) (a worker is a pair of CTAs, one per latent half),
     grid = 2 P, no aux, variant 0.
+  * paged MLA: one unit per request, len = its length from the page table (as for
+    decode), tile 128, max_workers = max(1, num_sms // 2), grid = 2 P, aux0 = kv_indptr,
+    aux1 = kv_indices, variant 1.
 
 BSR (longest processing time first). Tensor-core variant (variant 1) when R == 64,
 C == 64, head_dim == 128 and R*g in {128, 256} (g = Hq/Hkv): one unit per (row block
@@ -156,6 +159,20 @@ def mla_meta(seq_lens, batch, q_len, num_sms):
         lens += [int(seq_lens[b])] * q_len
     wp, ch, slots, merges = linear_partition(lens, 128, max(1, num_sms // 2))
     return _assemble(3, len(lens), wp, ch, slots, merges, 128, [], [], 2 * (len(wp) - 1), 0)
+
+
+def mla_paged_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_sms):
+    lens = [paged_request_len(kv_indptr, kv_last_page_len, page_size, b) for b in range(batch)]
+    wp, ch, slots, merges = linear_partition(lens, 128, max(1, num_sms // 2))
+    nnz = int(kv_indptr[batch]) if batch > 0 else 0
+    aux0 = [int(x) for x in kv_indptr[:batch + 1]] if batch > 0 else []
+    aux1 = [int(x) for x in kv_indices[:nnz]]
+    return _assemble(3, len(lens), wp, ch, slots, merges, 128, aux0, aux1, 2 * (len(wp) - 1), 1)
+
+
+def paged_request_len(kv_indptr, kv_last_page_len, page_size, b):
+    n = int(kv_indptr[b + 1]) - int(kv_indptr[b])
+    return 0 if n == 0 else (n - 1) * page_size + int(kv_last_page_len[b])
 
 
 def bsr_meta(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, num_sms):

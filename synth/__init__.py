@@ -12,6 +12,8 @@ from .gen import (  # noqa: F401
     bsr_inputs,
     paged_decode_inputs,
     mla_inputs,
+    mla_paged_inputs,
+    E4M3_NAN,
     rope_cos_sin_cache,
     CONFIGS,
     make,

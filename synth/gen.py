@@ -1,4 +1,4 @@
-"""Seeded generators for the five workloads of CSR-indexed sparse/paged attention.
+"""Seeded generators for the workloads of CSR-indexed sparse/paged attention.
 
 Every generator takes a seed and the sizes of its workload and returns a dict of
 torch tensors plus the integer parameters. Index structures are always drawn on the
@@ -219,6 +219,62 @@ def mla_inputs(seed, batch, heads, top_k, pool_rows, ctx_lo, ctx_hi, q_len=1,
                 max_seq_len=max_seq_len, seed=seed)
 
 
+E4M3_NAN = 0x7F  # canary code for cache slots no request may read
+
+
+def _e4m3_codes(shape, gen, device, scale=1.0):
+    """uint8 E4M3 codes of N(0,1) float32 draws (torch cast, round to nearest even)."""
+    out = torch.empty(shape, dtype=torch.uint8, device=device)
+    flat = out.view(-1)
+    n = flat.numel()
+    for s in range(0, n, _SLAB):
+        e = min(n, s + _SLAB)
+        x = torch.randn(e - s, generator=gen, dtype=torch.float32, device=device)
+        if scale != 1.0:
+            x.mul_(scale)
+        flat[s:e].copy_(x.to(torch.float8_e4m3fn).view(torch.uint8))
+    return out
+
+
+def mla_paged_inputs(seed, batch, heads, page_size, len_lo, len_hi, spare=0.1, lens=None,
+                     q_scale=1.0, device="cpu"):
+    """Inputs of the dense paged MLA decode.
+
+    * request b has L_b ~ U[len_lo, len_hi] tokens (or ``lens``) in n_b = ceil(L_b / page_size)
+      pages; the pages of all requests are a random permutation of the pool pages
+      [0, P), P = sum n_b + ceil(spare * sum n_b) (the spare pages are canaries);
+    * kv_indptr [batch+1], kv_indices, kv_last_page_len [batch] int32 (the page table);
+    * query [batch, heads, 576] and kv_pages [P, page_size, 576]: uint8 E4M3 codes of
+      N(0,1) draws; every slot past a request's last token and every spare page holds the
+      E4M3 NaN code, so a read outside the request shows up.
+    """
+    g = _cpu_gen(seed)
+    if lens is None:
+        lens = [int(x) for x in _uniform_int(g, len_lo, len_hi, batch)]
+    lens = [int(x) for x in lens]
+    npg = [(L + page_size - 1) // page_size for L in lens]
+    used = sum(npg)
+    P = max(1, used + int(math.ceil(spare * used)))
+    perm = torch.randperm(P, generator=g).to(torch.int32)
+    kv_indptr = torch.zeros(batch + 1, dtype=torch.int32)
+    kv_indptr[1:] = torch.cumsum(torch.tensor(npg, dtype=torch.int64), 0).to(torch.int32)
+    kv_indices = perm[:used].clone()
+    kv_last_page_len = torch.tensor([L - (n - 1) * page_size if n > 0 else 0
+                                     for L, n in zip(lens, npg)], dtype=torch.int32)
+    dg = _dev_gen(seed, device)
+    query = _e4m3_codes((batch, heads, 576), dg, device, q_scale)
+    kv_pages = _e4m3_codes((P, page_size, 576), dg, device)
+    kv_pages[perm[used:].to(torch.int64).to(device)] = E4M3_NAN
+    for b in range(batch):
+        n = npg[b]
+        lp = int(kv_last_page_len[b])
+        if n > 0 and lp < page_size:
+            kv_pages[int(kv_indices[int(kv_indptr[b]) + n - 1]), lp:] = E4M3_NAN
+    return dict(query=query, kv_pages=kv_pages, kv_indptr=kv_indptr, kv_indices=kv_indices,
+                kv_last_page_len=kv_last_page_len, lens=torch.tensor(lens, dtype=torch.int32),
+                batch=batch, heads=heads, page_size=page_size, num_pages=P, seed=seed)
+
+
 # --------------------------------------------------------------------------------------
 # The five workloads at full size (seeds 1000 + index)
 # --------------------------------------------------------------------------------------
@@ -238,6 +294,8 @@ CONFIGS = {
     "split_decode": dict(kind="decode", seed=1004, batch=8, num_qo_heads=64, num_kv_heads=8,
                          head_dim=128, page_size=64, len_lo=131072, len_hi=131072,
                          dtype=torch.bfloat16),
+    "mla_paged": dict(kind="mla_paged", seed=1005, batch=128, heads=128, page_size=64,
+                      len_lo=2048, len_hi=8192),
 }
 
 
@@ -252,4 +310,6 @@ def make(name, device="cpu", **overrides):
         return paged_decode_inputs(device=device, **cfg)
     if kind == "mla":
         return mla_inputs(device=device, **cfg)
+    if kind == "mla_paged":
+        return mla_paged_inputs(device=device, **cfg)
     raise ValueError(kind)

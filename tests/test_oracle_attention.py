@@ -15,7 +15,11 @@ Pins, none of which re-types the oracle's own formula:
     identity;
   * sparse MLA over indices covering a whole small context equals dense attention on
     the decoded rows; permuting the indices changes nothing; the scale folding rule of
-    the MATE wrapper page holds.
+    the MATE wrapper page holds;
+  * dense paged MLA with page_size 1 equals sparse MLA over the page list; it is
+    invariant to page size and to where the pages sit in the pool; canary slots (NaN
+    codes) past a request's end and in spare pages are never read; a request without
+    pages gives 0 and -inf.
 """
 
 import json
@@ -258,4 +262,79 @@ def test_mla_seq_lens_limit_the_rows():
     out, lse = att.mla_sparse_decode(query, kv, idx, sl, 0.05, 1.0)
     ref, ref_lse = att.mla_sparse_decode(query, kv, idx[:, :, :64], np.array([64, 0]), 0.05, 1.0)
     np.testing.assert_array_equal(out, ref)
+    assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
+
+
+# ---------------------------------------------------------------------------------------
+# dense paged MLA
+# ---------------------------------------------------------------------------------------
+
+def _relayout(d, page_size, seed):
+    """The same logical rows of every request in a new cache with another page size and
+    the pages at other (random) pool positions; canaries elsewhere."""
+    g = torch.Generator().manual_seed(seed)
+    lens = d["lens"].tolist()
+    old = d["kv_pages"].numpy()
+    logical = []
+    for b, L in enumerate(lens):
+        pg = d["kv_indices"][int(d["kv_indptr"][b]):int(d["kv_indptr"][b + 1])].numpy()
+        logical.append(old[pg].reshape(-1, 576)[:L])
+    npg = [(L + page_size - 1) // page_size for L in lens]
+    P = sum(npg) + 3
+    perm = torch.randperm(P, generator=g).numpy()
+    cache = np.full((P, page_size, 576), synth.E4M3_NAN, np.uint8)
+    indptr = np.concatenate([[0], np.cumsum(npg)]).astype(np.int32)
+    indices = perm[:sum(npg)].astype(np.int32)
+    last = np.zeros(len(lens), np.int32)
+    for b, L in enumerate(lens):
+        for t in range(L):
+            cache[indices[indptr[b] + t // page_size], t % page_size] = logical[b][t]
+        if npg[b]:
+            last[b] = L - (npg[b] - 1) * page_size
+    return cache, indptr, indices, last
+
+
+def test_mla_paged_page_size_one_equals_sparse():
+    d = synth.mla_paged_inputs(51, batch=3, heads=8, page_size=1, len_lo=0, len_hi=0,
+                               lens=[37, 1, 90])
+    q, cache = d["query"].numpy(), d["kv_pages"].numpy()
+    ip, ix, lp = d["kv_indptr"].numpy(), d["kv_indices"].numpy(), d["kv_last_page_len"].numpy()
+    out, lse = att.mla_paged_decode(q, cache, ip, ix, lp, 1, 0.05, 1.5)
+    top = 128
+    idx = np.zeros((3, 1, top), np.int32)
+    for b in range(3):
+        n = ip[b + 1] - ip[b]
+        idx[b, 0, :n] = ix[ip[b]:ip[b + 1]]
+    ref, ref_lse = att.mla_sparse_decode(q[:, None], cache.reshape(-1, 576), idx,
+                                         d["lens"].numpy(), 0.05, 1.5)
+    np.testing.assert_array_equal(out, ref)
+    np.testing.assert_array_equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("ps_from,ps_to", [(16, 64), (64, 1), (7, 16)])
+def test_mla_paged_invariant_to_page_size_and_placement(ps_from, ps_to):
+    d = synth.mla_paged_inputs(52, batch=4, heads=8, page_size=ps_from, len_lo=0, len_hi=0,
+                               lens=[200, 64, 1, 129])
+    q = d["query"].numpy()
+    out, lse = att.mla_paged_decode(q, d["kv_pages"].numpy(), d["kv_indptr"].numpy(),
+                                    d["kv_indices"].numpy(), d["kv_last_page_len"].numpy(),
+                                    ps_from, 1 / math.sqrt(576), 1.0)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()  # no canary slot was read
+    cache, ip, ix, lp = _relayout(d, ps_to, seed=5)
+    out2, lse2 = att.mla_paged_decode(q, cache, ip, ix, lp, ps_to, 1 / math.sqrt(576), 1.0)
+    np.testing.assert_array_equal(out2, out)
+    np.testing.assert_array_equal(lse2, lse)
+
+
+def test_mla_paged_full_request_equals_dense_and_empty_request():
+    d = synth.mla_paged_inputs(53, batch=2, heads=4, page_size=16, len_lo=0, len_hi=0,
+                               lens=[40, 0])
+    q, cache = d["query"].numpy(), d["kv_pages"].numpy()
+    out, lse = att.mla_paged_decode(q, cache, d["kv_indptr"].numpy(), d["kv_indices"].numpy(),
+                                    d["kv_last_page_len"].numpy(), 16, 0.07, 1.0)
+    pages = d["kv_indices"].numpy()[:3]
+    K = nx.e4m3_decode(cache[pages].reshape(-1, 576)[:40])
+    Q = nx.e4m3_decode(q[0])
+    ref = _sdpa(Q[None], K[:, None, :], K[:, None, :512], 0.07)[0]
+    np.testing.assert_allclose(out[0], ref, rtol=1e-12, atol=1e-14)
     assert (out[1] == 0).all() and np.isneginf(lse[1]).all()

@@ -145,6 +145,20 @@ def test_mla_plan_bit_exact(lib, batch, q_len, seq):
     assert plan_ref.sections(meta)["grid"] == 2 * plan_ref.sections(meta)["workers"]
 
 
+@pytest.mark.parametrize("lens,ps", [([5, 0, 130], 16), ([2048] * 7, 64), ([1, 64, 65, 300], 1)])
+def test_mla_paged_plan_bit_exact(lib, lens, ps):
+    d = synth.mla_paged_inputs(61, batch=len(lens), heads=16, page_size=ps, len_lo=0, len_hi=0,
+                               lens=lens)
+    ip, ix, lp = d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"]
+    p = bskv.bskv_plan_mla_paged(ip, ix, lp, len(lens), d["num_pages"], ps, 128, num_sms=SMS)
+    meta = p.metadata()
+    assert meta == plan_ref.mla_paged_meta(ip.tolist(), ix.tolist(), lp.tolist(), len(lens), ps, SMS)
+    _check_linear(meta, lens, 128)
+    _, fb = p.workspace_sizes()
+    top = max(64, (max(lens) + 63) // 64 * 64)
+    assert fb >= len(lens) * top * 4
+
+
 # ---------------------------------------------------------------------------------------
 # fault injection on the host: each malformed input returns an error and plans nothing
 # ---------------------------------------------------------------------------------------
@@ -190,6 +204,21 @@ def test_mla_plan_rejects_bad_inputs(lib):
     _expect("ERR_INVALID_ARG", f, [65], 1, 1, 128, 64, num_sms=2)    # seq_len > top_k
     _expect("ERR_INVALID_ARG", f, [-1], 1, 1, 128, 64, num_sms=2)
     _expect("ERR_UNSUPPORTED", f, [64], 1, 1, 256, 64, num_sms=2)    # heads > 128
+
+
+def test_mla_paged_plan_rejects_bad_inputs(lib):
+    f = bskv.bskv_plan_mla_paged
+    ok = dict(num_pages=4, page_size=16, num_heads=128, num_sms=4)
+    f([0, 2], [0, 1], [5], 1, **ok)  # valid
+    _expect("ERR_INVALID_ARG", f, [1, 2], [0, 1], [5], 1, **ok)          # indptr[0] != 0
+    _expect("ERR_INVALID_ARG", f, [0, 2, 1], [0, 1], [5, 1], 2, **ok)    # decreasing
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 4], [5], 1, **ok)          # page id >= num_pages
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, -1], [5], 1, **ok)
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 1], [0], 1, **ok)          # last page len 0
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 1], [17], 1, **ok)         # > page_size
+    _expect("ERR_INVALID_ARG", f, [0, 2], [0, 1], [5], 1, **{**ok, "page_size": 0})
+    _expect("ERR_UNSUPPORTED", f, [0, 2], [0, 1], [5], 1, **{**ok, "num_heads": 129})
+    _expect("ERR_UNSUPPORTED", f, [0, 2], [0, 1], [5], 1, **{**ok, "num_pages": 1 << 30, "page_size": 4})
 
 
 def test_run_without_upload_is_rejected(lib):
