@@ -15,9 +15,10 @@
 // O += P V over the same 128 keys (K = 128, N = head_dim = 128).
 //   warp 0   TMA producer: Q tiles (3-D tensor map, 128B swizzle) once per unit; K and V of
 //            a block pair into one stage ([128 keys x 128 B] panels), 2 stages (3 for g = 2);
-//   warp 1   allocates 512 TMEM columns; lane 0 issues the MMAs. With two M tiles the jobs
-//            alternate tile 0 / tile 1 (ping-pong): while one warpgroup turns S into P, the
-//            tensor core runs the other tile's PV and next QK. With one M tile, S is double
+//   warp 1   allocates 512 TMEM columns and issues the MMAs (the warp stays converged, one
+//            elected lane executes them). With two M tiles the jobs alternate tile 0 /
+//            tile 1 (ping-pong): while one warpgroup turns S into P, the tensor core runs
+//            the other tile's PV and next QK. With one M tile, S is double
 //            buffered instead. P is written back into TMEM over S (16-bit, two per column)
 //            and feeds the PV MMA as its A operand; V is an MN-major shared-memory operand;
 //   warps 4-7 / 8-11  one warpgroup per M tile: thread = row = TMEM lane. It reads its

@@ -20,9 +20,10 @@
 //              128B-swizzled panels), then the leader arms kv_full for the partner's half and
 //              pushes this half to the partner with five shared-to-shared bulk copies. Row ids
 //              are fetched one tile ahead;
-//   warp 6     allocates TMEM; lane 0 issues QK (16 MMAs with A in TMEM, 2 with the tail in
-//              shared memory, N = 128) and PV (A = P in shared memory, B = the V part read
-//              MN-major, N = 256); slot releases are committed to both CTAs' barriers;
+//   warp 6     allocates TMEM; one elected lane of the converged warp issues QK (16 MMAs
+//              with A in TMEM, 2 with the tail in shared memory, N = 128) and PV (A = P in
+//              shared memory, B = the V part read MN-major, N = 256); slot releases are
+//              committed to both CTAs' barriers;
 //   warp 7     TMA-loads the query tail once per token;
 //   warps 8-15 two softmax warpgroups; thread = head = TMEM lane, each group owns 64 of a
 //              tile's columns and 128 of the 256 output values: it reads S (and releases it
