@@ -699,20 +699,23 @@ __global__ void __launch_bounds__(128)
 }
 
 // Row list of the paged decode, from the page table in the metadata (aux0 = kv_indptr,
-// aux1 = kv_indices): rows[b * stride + t] = the cache row of token t of request b while
-// t is inside the request's pages, 0 beyond them (the decode reads only t < L_b).
+// aux1 = kv_indices): rows[b * stride + t] = the cache row of token t of request b, for the
+// tokens its pages hold (the decode reads only t < L_b; entries past them stay unwritten).
+// Grid: y strides over requests, x over a request's tokens.
 __global__ void __launch_bounds__(256) mla_page_rows_kernel(const int32_t* __restrict__ meta,
                                                             int32_t batch, int32_t stride,
                                                             int32_t page_size,
                                                             int32_t* __restrict__ rows) {
   const int32_t* indptr = meta + meta[H_OFF_AUX0];
   const int32_t* pages = meta + meta[H_OFF_AUX1];
-  const int64_t total = int64_t(batch) * stride;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int32_t b = int32_t(i / stride), t = int32_t(i % stride);
-    const int32_t slot = indptr[b] + t / page_size;
-    rows[i] = slot < indptr[b + 1] ? pages[slot] * page_size + t % page_size : 0;
+  for (int32_t b = blockIdx.y; b < batch; b += gridDim.y) {
+    const int32_t p0 = indptr[b];
+    const int32_t lim = int32_t(min(int64_t(indptr[b + 1] - p0) * page_size, int64_t(stride)));
+    int32_t* out = rows + int64_t(b) * stride;
+    for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < lim; t += gridDim.x * blockDim.x) {
+      const int32_t pi = t / page_size;
+      out[t] = pages[p0 + pi] * page_size + (t - pi * page_size);
+    }
   }
 }
 
@@ -835,10 +838,10 @@ extern "C" bskv_status bskv_run_mla_paged(const bskv_plan* plan, const void* que
   if (!aligned16(float_ws)) { set_error("run_mla_paged: float workspace must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* rows = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(float_ws) + plan->mla_rows_off);
-  const int64_t total = int64_t(plan->batch) * plan->top_k;
-  const int blocks = int(std::min<int64_t>((total + 255) / 256, 1024));
-  mla_page_rows_kernel<<<blocks, 256, 0, st>>>(plan->meta_dev, plan->batch, plan->top_k,
-                                               plan->page_size, rows);
+  const dim3 grid_rows(unsigned(std::min((plan->top_k + 255) / 256, 32)),
+                       unsigned(std::min(plan->batch, 65535)));
+  mla_page_rows_kernel<<<grid_rows, 256, 0, st>>>(plan->meta_dev, plan->batch, plan->top_k,
+                                                  plan->page_size, rows);
   if (bskv_status s = cuda_check(cudaGetLastError(), "mla page rows launch")) return s;
   return run_mla(plan, query, kv_pages, int64_t(plan->num_pages) * plan->page_size, rows,
                  bmm1_scale, bmm2_scale, out, lse, float_ws, st);
