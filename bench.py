@@ -444,6 +444,24 @@ def bench_mla_paged(bskv, synth, steps, warmup, peaks):
                 launches_per_step=2 + (1 if plan.metadata()[6] > 0 else 0))
 
 
+def bench_mla_append(bskv, synth, steps, warmup, peaks):
+    """RoPE + FP8 of 128 requests x 512 new key rows appended into the page-64 latent cache
+    (an HBM stream: 1152 bytes in, 576 out and 256 of cos/sin per row)."""
+    d = synth.make("mla_append", device="cuda")
+    cache = d["kv_pages"]
+    args = [d["k_rope"], d["k_nope"], d["pos_k"].cuda(), d["cos_sin"], d["batch_indices"].cuda(),
+            d["positions"].cuda(), d["kv_indptr"].cuda(), d["kv_indices"].cuda(), cache]
+    fn = lambda: bskv.bskv_rope_quantize_fp8_append_paged(*args)  # noqa
+    ms = time_iters(fn, steps, warmup, flush=True)
+    rows = d["k_rope"].shape[0]
+    nbytes = rows * (1152 + 576 + 256)
+    gbs = nbytes / (statistics.median(ms) * 1e-3) / 1e9
+    return dict(workload="mla_append: 128 requests x 512 new rows (65536) appended to the page-64 "
+                         "latent cache (L2 flushed)",
+                **summary(ms), bytes=nbytes, gbs=gbs, frac=gbs / peaks["hbm_gbs"],
+                launches_per_step=1)
+
+
 # ---------------------------------------------------------------------------------------
 # CPU baseline: the float64 oracle on the host cores, on a bounded sample
 # ---------------------------------------------------------------------------------------
@@ -509,7 +527,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of extra rows: bsr_prefill,bsr_tiny,mla,mla_paged,split,e2e,cpu "
+                    help="comma list of extra rows: bsr_prefill,bsr_tiny,mla,mla_paged,mla_append,split,e2e,cpu "
                          "or all/none")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -521,7 +539,7 @@ def main():
     bskv.build()
     dist, rank, ws = dist_setup(args.gpus)
     peaks, peak_src = load_peaks()
-    rows = set(["bsr_prefill", "bsr_tiny", "mla", "mla_paged", "split", "e2e", "cpu"]
+    rows = set(["bsr_prefill", "bsr_tiny", "mla", "mla_paged", "mla_append", "split", "e2e", "cpu"]
                if args.rows == "all" else [] if args.rows == "none" else args.rows.split(","))
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -543,7 +561,9 @@ def main():
                  lambda: bench_bsr(bskv, synth, "bsr_tiny", K, args.warmup, peaks, True)),
                 ("mla", "mla_decode", lambda: bench_mla(bskv, synth, K, args.warmup, peaks)),
                 ("mla_paged", "mla_paged",
-                 lambda: bench_mla_paged(bskv, synth, K, args.warmup, peaks))]
+                 lambda: bench_mla_paged(bskv, synth, K, args.warmup, peaks)),
+                ("mla_append", "mla_append",
+                 lambda: bench_mla_append(bskv, synth, K, args.warmup, peaks))]
         for key, name, job in jobs:
             if key in rows:
                 try:

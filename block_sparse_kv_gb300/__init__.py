@@ -76,6 +76,10 @@ _SIGS = {
     "bskv_rope_quantize_fp8": ([_P, _I64P, _P, _I64P, _P, _I64, _I32, _P, _I64P, _P, _I64P,
                                 _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64,
                                 _I32, _P, _I32, _I64, _I32, _F, _F, _P], _I32),
+    "bskv_rope_quantize_fp8_append_paged": ([_P, _I64P, _P, _I64P, _P, _I64, _I32, _P, _I64P,
+                                             _P, _I64P, _P, _I64, _P, _I64, _P, _I64, _P, _P,
+                                             _P, _P, _I32, _I32, _I64, _P,
+                                             _I32, _P, _I32, _I64, _I32, _F, _F, _P], _I32),
     "bskv_merge_states": ([_P, _P, _I64, _I32, _I32, _I32, _P, _I32, _P, _P], _I32),
     "bskv_get_device_status": ([_I32P, _I32], _I32),
     "bskv_set_debug_force_timeout": ([_I32], _I32),
@@ -410,6 +414,44 @@ def bskv_rope_quantize_fp8(q_rope, k_rope, q_nope, k_nope, cos_sin_cache, pos_id
              float(quant_scale_kv), _stream(cos_sin_cache)]
     _check("bskv_rope_quantize_fp8", lib.bskv_rope_quantize_fp8(*args))
     return q_rope_out, k_rope_out, q_nope_out, k_nope_out
+
+
+def bskv_rope_quantize_fp8_append_paged(k_rope, k_nope, pos_k, cos_sin_cache, batch_indices,
+                                        positions, kv_indptr, kv_indices, kv_pages,
+                                        q_rope=None, q_nope=None, pos_q=None, is_neox=True,
+                                        quant_scale_q=1.0, quant_scale_kv=1.0, q_rope_out=None,
+                                        q_nope_out=None):
+    """RoPE + FP8 with the key rows written into kv_pages [num_pages, page_size, 576] (uint8)
+    through the device page table (int32 batch_indices, positions, kv_indptr, kv_indices).
+    The optional query group is handled as by bskv_rope_quantize_fp8. Returns the query
+    outputs (or None)."""
+    lib = load_library()
+    dev = k_rope.device
+    u8 = torch.uint8
+    args = []
+    if q_rope is not None:
+        nq, H, _ = q_rope.shape
+        if q_rope_out is None:
+            q_rope_out = torch.empty((nq, H, 64), dtype=u8, device=dev)
+        if q_nope_out is None:
+            q_nope_out = torch.empty((nq, H, 512), dtype=u8, device=dev)
+        args += [q_rope.data_ptr(), _strides(q_rope.stride(0), q_rope.stride(1)), q_nope.data_ptr(),
+                 _strides(q_nope.stride(0), q_nope.stride(1)), pos_q.data_ptr(), nq, H,
+                 q_rope_out.data_ptr(), _strides(q_rope_out.stride(0), q_rope_out.stride(1)),
+                 q_nope_out.data_ptr(), _strides(q_nope_out.stride(0), q_nope_out.stride(1))]
+    else:
+        args += [None, None, None, None, None, 0, 0, None, None, None, None]
+    num_pages, page_size, _ = kv_pages.shape
+    batch = kv_indptr.numel() - 1
+    args += [k_rope.data_ptr(), k_rope.stride(0), k_nope.data_ptr(), k_nope.stride(0),
+             pos_k.data_ptr(), k_rope.shape[0], batch_indices.data_ptr(), positions.data_ptr(),
+             kv_indptr.data_ptr(), kv_indices.data_ptr(), int(batch), int(page_size),
+             int(num_pages), kv_pages.data_ptr(),
+             _DT[pos_k.dtype], cos_sin_cache.data_ptr(), _DT[cos_sin_cache.dtype],
+             cos_sin_cache.shape[0], int(bool(is_neox)), float(quant_scale_q),
+             float(quant_scale_kv), _stream(cos_sin_cache)]
+    _check("bskv_rope_quantize_fp8_append_paged", lib.bskv_rope_quantize_fp8_append_paged(*args))
+    return q_rope_out, q_nope_out
 
 
 def bskv_merge_states(v, s, out_dtype=torch.float32, v_out=None, s_out=None):

@@ -49,6 +49,14 @@ struct RopeParams {
   int64_t kro_s;
   uint8_t* k_nope_out;
   int64_t kno_s;
+  // paged append (app_indptr non-NULL): key row t goes to cache row page * page_size + slot
+  // of the page table entry of (app_batch[t], app_pos[t]); k_*_out then address the cache
+  const int32_t* app_batch;
+  const int32_t* app_pos;
+  const int32_t* app_indptr;
+  const int32_t* app_indices;
+  int32_t app_requests, app_page_size;
+  int64_t app_num_pages;
   // shared
   const void* cos_sin;
   int64_t max_seq_len;
@@ -87,11 +95,24 @@ struct RowIn {
   bool valid;        // position inside [0, max_seq_len)
 };
 
+// Cache row of appended key row t, or -1 when its request, position or page is out of
+// range (three dependent loads; the row's data loads do not wait for them).
+__device__ __forceinline__ int64_t append_row(const RopeParams& p, int64_t t) {
+  const int32_t b = __ldg(p.app_batch + t), q = __ldg(p.app_pos + t);
+  if (b < 0 || b >= p.app_requests || q < 0) return -1;
+  const int64_t slot = int64_t(__ldg(p.app_indptr + b)) + q / p.app_page_size;
+  if (slot >= __ldg(p.app_indptr + b + 1)) return -1;
+  const int32_t page = __ldg(p.app_indices + slot);
+  if (page < 0 || page >= p.app_num_pages) return -1;
+  return int64_t(page) * p.app_page_size + q % p.app_page_size;
+}
+
 template <bool kNeox, typename PosT, typename CacheT>
 __device__ __forceinline__ void row_ptrs(const RopeParams& p, int64_t r, int64_t q_rows,
                                          const __nv_bfloat16*& rope, const __nv_bfloat16*& nope,
                                          uint8_t*& rope_out, uint8_t*& nope_out, int64_t& pos,
-                                         float& scale) {
+                                         float& scale, bool& dst_ok) {
+  dst_ok = true;
   if (r < q_rows) {
     const int64_t t = r / p.heads;
     const int h = int(r % p.heads);
@@ -105,11 +126,25 @@ __device__ __forceinline__ void row_ptrs(const RopeParams& p, int64_t r, int64_t
     const int64_t t = r - q_rows;
     rope = p.k_rope + t * p.kr_s;
     nope = p.k_nope + t * p.kn_s;
+    // a paged append resolves the destination later (resolve_dst), after the row's data
+    // loads are in flight
     rope_out = p.k_rope_out + t * p.kro_s;
     nope_out = p.k_nope_out + t * p.kno_s;
     pos = int64_t(__ldg(static_cast<const PosT*>(p.pos_k) + t));
     scale = p.scale_kv;
   }
+}
+
+// Destination of appended key row r (rows past the query rows only): the page table lookup.
+__device__ __forceinline__ void resolve_dst(const RopeParams& p, int64_t r, int64_t q_rows,
+                                            uint8_t*& rope_out, uint8_t*& nope_out,
+                                            bool& dst_ok) {
+  if (!p.app_indptr || r < q_rows) return;
+  int64_t d = append_row(p, r - q_rows);
+  dst_ok = d >= 0;
+  if (!dst_ok) d = 0;
+  rope_out = p.k_rope_out + d * p.kro_s;
+  nope_out = p.k_nope_out + d * p.kno_s;
 }
 
 template <bool kNeox, typename CacheT>
@@ -141,7 +176,8 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* rope, const __nv_b
 
 template <bool kNeox>
 __device__ __forceinline__ void store_row(const RowIn& in, uint8_t* rope_out, uint8_t* nope_out,
-                                          float scale, int lane, const StatusArgs& st) {
+                                          float scale, int lane, const StatusArgs& st,
+                                          bool dst_ok) {
   // The neox partner exchange is a warp shuffle, so it runs before the validity test.
   const float e0 = bf16_lo(in.rw), e1 = bf16_hi(in.rw);
   float r0, r1;
@@ -160,7 +196,7 @@ __device__ __forceinline__ void store_row(const RowIn& in, uint8_t* rope_out, ui
     r0 = __fsub_rn(__fmul_rn(e0, in.c0), __fmul_rn(e1, in.s0));
     r1 = __fadd_rn(__fmul_rn(e1, in.c0), __fmul_rn(e0, in.s0));
   }
-  if (!in.valid) {
+  if (!in.valid || !dst_ok) {
     if (lane == 0) record_error(st, BSKV_ERR_DEVICE_INDEX);
     return;
   }
@@ -193,13 +229,17 @@ __global__ void __launch_bounds__(256) rope_quant_kernel(const RopeParams p) {
     uint8_t *ro_a, *no_a, *ro_b, *no_b;
     int64_t pos_a, pos_b;
     float sc_a, sc_b;
-    row_ptrs<kNeox, PosT, CacheT>(p, ra, q_rows, rope_a, nope_a, ro_a, no_a, pos_a, sc_a);
-    row_ptrs<kNeox, PosT, CacheT>(p, has_b ? rb : ra, q_rows, rope_b, nope_b, ro_b, no_b, pos_b, sc_b);
+    bool ok_a, ok_b;
+    row_ptrs<kNeox, PosT, CacheT>(p, ra, q_rows, rope_a, nope_a, ro_a, no_a, pos_a, sc_a, ok_a);
+    row_ptrs<kNeox, PosT, CacheT>(p, has_b ? rb : ra, q_rows, rope_b, nope_b, ro_b, no_b, pos_b,
+                                  sc_b, ok_b);
     RowIn a, b;
     load_row<kNeox, CacheT>(rope_a, nope_a, pos_a, p.max_seq_len, cache, lane, a);
     load_row<kNeox, CacheT>(rope_b, nope_b, pos_b, p.max_seq_len, cache, lane, b);
-    store_row<kNeox>(a, ro_a, no_a, sc_a, lane, p.st);
-    if (has_b) store_row<kNeox>(b, ro_b, no_b, sc_b, lane, p.st);
+    resolve_dst(p, ra, q_rows, ro_a, no_a, ok_a);
+    resolve_dst(p, has_b ? rb : ra, q_rows, ro_b, no_b, ok_b);
+    store_row<kNeox>(a, ro_a, no_a, sc_a, lane, p.st, ok_a);
+    if (has_b) store_row<kNeox>(b, ro_b, no_b, sc_b, lane, p.st, ok_b);
   }
 }
 
@@ -252,7 +292,12 @@ bskv_status launch_rope(const RopeParams& p, int pos_dtype, int cache_dtype, cud
 
 using namespace bskv;
 
-extern "C" bskv_status bskv_rope_quantize_fp8(
+namespace bskv {
+namespace {
+
+// The checks and launch shared by both entry points; `app` (nullable) fills the paged
+// append fields of the parameters.
+bskv_status rope_entry(
     const void* q_rope, const int64_t* q_rope_strides, const void* q_nope,
     const int64_t* q_nope_strides, const void* pos_q, int64_t nnz_q, int32_t num_heads,
     void* q_rope_out, const int64_t* q_rope_out_strides, void* q_nope_out,
@@ -260,8 +305,15 @@ extern "C" bskv_status bskv_rope_quantize_fp8(
     const void* k_nope, int64_t k_nope_stride, const void* pos_k, int64_t nnz_k,
     void* k_rope_out, int64_t k_rope_out_stride, void* k_nope_out, int64_t k_nope_out_stride,
     int32_t pos_dtype, const void* cos_sin, int32_t cos_sin_dtype, int64_t max_seq_len,
-    int32_t is_neox, float quant_scale_q, float quant_scale_kv, void* stream) {
+    int32_t is_neox, float quant_scale_q, float quant_scale_kv, void* stream,
+    const RopeParams* app) {
   RopeParams p{};
+  if (app) {
+    p.app_batch = app->app_batch; p.app_pos = app->app_pos;
+    p.app_indptr = app->app_indptr; p.app_indices = app->app_indices;
+    p.app_requests = app->app_requests; p.app_page_size = app->app_page_size;
+    p.app_num_pages = app->app_num_pages;
+  }
   const bool has_q = q_rope || q_nope || q_rope_out || q_nope_out || pos_q;
   const bool has_k = k_rope || k_nope || k_rope_out || k_nope_out || pos_k;
   if (pos_dtype != BSKV_INT32 && pos_dtype != BSKV_INT64) { set_error("rope_quantize_fp8: pos dtype %s unsupported", dtype_name(pos_dtype)); return BSKV_ERR_UNSUPPORTED; }
@@ -314,4 +366,63 @@ extern "C" bskv_status bskv_rope_quantize_fp8(
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return is_neox ? launch_rope<true>(p, pos_dtype, cos_sin_dtype, st)
                  : launch_rope<false>(p, pos_dtype, cos_sin_dtype, st);
+}
+
+}  // namespace
+}  // namespace bskv
+
+extern "C" bskv_status bskv_rope_quantize_fp8(
+    const void* q_rope, const int64_t* q_rope_strides, const void* q_nope,
+    const int64_t* q_nope_strides, const void* pos_q, int64_t nnz_q, int32_t num_heads,
+    void* q_rope_out, const int64_t* q_rope_out_strides, void* q_nope_out,
+    const int64_t* q_nope_out_strides, const void* k_rope, int64_t k_rope_stride,
+    const void* k_nope, int64_t k_nope_stride, const void* pos_k, int64_t nnz_k,
+    void* k_rope_out, int64_t k_rope_out_stride, void* k_nope_out, int64_t k_nope_out_stride,
+    int32_t pos_dtype, const void* cos_sin, int32_t cos_sin_dtype, int64_t max_seq_len,
+    int32_t is_neox, float quant_scale_q, float quant_scale_kv, void* stream) {
+  return rope_entry(q_rope, q_rope_strides, q_nope, q_nope_strides, pos_q, nnz_q, num_heads,
+                    q_rope_out, q_rope_out_strides, q_nope_out, q_nope_out_strides, k_rope,
+                    k_rope_stride, k_nope, k_nope_stride, pos_k, nnz_k, k_rope_out,
+                    k_rope_out_stride, k_nope_out, k_nope_out_stride, pos_dtype, cos_sin,
+                    cos_sin_dtype, max_seq_len, is_neox, quant_scale_q, quant_scale_kv, stream,
+                    nullptr);
+}
+
+extern "C" bskv_status bskv_rope_quantize_fp8_append_paged(
+    const void* q_rope, const int64_t* q_rope_strides, const void* q_nope,
+    const int64_t* q_nope_strides, const void* pos_q, int64_t nnz_q, int32_t num_heads,
+    void* q_rope_out, const int64_t* q_rope_out_strides, void* q_nope_out,
+    const int64_t* q_nope_out_strides, const void* k_rope, int64_t k_rope_stride,
+    const void* k_nope, int64_t k_nope_stride, const void* pos_k, int64_t nnz_k,
+    const int32_t* batch_indices, const int32_t* positions, const int32_t* kv_indptr,
+    const int32_t* kv_indices, int32_t batch, int32_t page_size, int64_t num_pages,
+    void* kv_pages, int32_t pos_dtype, const void* cos_sin, int32_t cos_sin_dtype,
+    int64_t max_seq_len, int32_t is_neox, float quant_scale_q, float quant_scale_kv,
+    void* stream) {
+  if (!k_rope || !k_nope || !pos_k || !batch_indices || !positions || !kv_indptr ||
+      !kv_indices || !kv_pages) {
+    set_error("rope_quantize_fp8_append_paged: the key rows, their positions, batch_indices, "
+              "positions, the page table and kv_pages are all required");
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (batch < 1 || page_size < 1 || num_pages < 1 || nnz_k < 0) {
+    set_error("rope_quantize_fp8_append_paged: batch=%d page_size=%d num_pages=%lld nnz_k=%lld",
+              batch, page_size, (long long)num_pages, (long long)nnz_k);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if ((reinterpret_cast<uintptr_t>(batch_indices) | reinterpret_cast<uintptr_t>(positions) |
+       reinterpret_cast<uintptr_t>(kv_indptr) | reinterpret_cast<uintptr_t>(kv_indices)) & 3) {
+    set_error("rope_quantize_fp8_append_paged: index arrays must be 4-byte aligned");
+    return BSKV_ERR_INVALID_ARG;
+  }
+  RopeParams app{};
+  app.app_batch = batch_indices; app.app_pos = positions;
+  app.app_indptr = kv_indptr; app.app_indices = kv_indices;
+  app.app_requests = batch; app.app_page_size = page_size; app.app_num_pages = num_pages;
+  uint8_t* cache = static_cast<uint8_t*>(kv_pages);
+  return rope_entry(q_rope, q_rope_strides, q_nope, q_nope_strides, pos_q, nnz_q, num_heads,
+                    q_rope_out, q_rope_out_strides, q_nope_out, q_nope_out_strides, k_rope,
+                    k_rope_stride, k_nope, k_nope_stride, pos_k, nnz_k, cache + 512, 576, cache,
+                    576, pos_dtype, cos_sin, cos_sin_dtype, max_seq_len, is_neox, quant_scale_q,
+                    quant_scale_kv, stream, &app);
 }

@@ -329,6 +329,37 @@ bskv_status bskv_rope_quantize_fp8(
     int32_t is_neox, float quant_scale_q, float quant_scale_kv, void* stream);
 
 /*
+ * RoPE + FP8 quantisation with the key rows appended to a paged latent cache ([CHEAT]
+ * benchmark README: rope_quantize_fp8_append_paged_kv_cache, RoPE with FP8 quantization and
+ * paged KV cache append; page table as in [SKILL] KV-Cache Formats). The arithmetic is that
+ * of bskv_rope_quantize_fp8; only the destination of a key row differs.
+ *   Query group: exactly as bskv_rope_quantize_fp8 (all NULL to skip).
+ *   Key rows: k_rope [nnz_k, 64], k_nope [nnz_k, 512] bf16 with row strides; pos_k [nnz_k]
+ *     rotary positions (pos_dtype).
+ *   Destination, all int32 on the device: key row i belongs to request batch_indices[i]
+ *     (in [0, batch)) at token position positions[i] (>= 0) of that request; the request's
+ *     pages are kv_indices[kv_indptr[b] .. kv_indptr[b+1]) and the row is written to page
+ *     kv_indices[kv_indptr[b] + positions[i] / page_size], slot positions[i] % page_size of
+ *     kv_pages [num_pages, page_size, 576] E4M3 (512 NoPE then 64 rotated values), the
+ *     layout the paged MLA decode reads. A row whose position lies past the request's pages,
+ *     whose page id lies outside [0, num_pages), whose request lies outside [0, batch) or
+ *     whose rotary position lies outside [0, max_seq_len) is not written and raises
+ *     BSKV_ERR_DEVICE_INDEX in the device status word. Other cache bytes are not touched.
+ *   Rows that share a destination race (the last writer wins).
+ */
+bskv_status bskv_rope_quantize_fp8_append_paged(
+    const void* q_rope, const int64_t* q_rope_strides, const void* q_nope,
+    const int64_t* q_nope_strides, const void* pos_q, int64_t nnz_q, int32_t num_heads,
+    void* q_rope_out, const int64_t* q_rope_out_strides, void* q_nope_out,
+    const int64_t* q_nope_out_strides,
+    const void* k_rope, int64_t k_rope_stride, const void* k_nope, int64_t k_nope_stride,
+    const void* pos_k, int64_t nnz_k, const int32_t* batch_indices, const int32_t* positions,
+    const int32_t* kv_indptr, const int32_t* kv_indices, int32_t batch, int32_t page_size,
+    int64_t num_pages, void* kv_pages,
+    int32_t pos_dtype, const void* cos_sin, int32_t cos_sin_dtype, int64_t max_seq_len,
+    int32_t is_neox, float quant_scale_q, float quant_scale_kv, void* stream);
+
+/*
  * Merge attention states ([CHEAT] cascade.rst merge_states; [SKILL] Cascade Inference):
  *   v [seq_len, num_states, num_heads, head_dim] float32 (normalised partial outputs),
  *   s [seq_len, num_states, num_heads] float32 natural-log LSE, both contiguous;

@@ -16,6 +16,14 @@ Reading taken where the pages are silent: pair i (i < 32) uses cos = cache[pos, 
 and sin = cache[pos, 32 + i] in both layouts, and rotates (x, y) to
 (x*cos - y*sin, y*cos + x*sin). The arithmetic is exact float64 on the stored cache
 values; the single rounding is the E4M3 cast.
+
+The paged append (FlashInfer cheat page, benchmark README:
+rope_quantize_fp8_append_paged_kv_cache, RoPE with FP8 quantization and paged KV cache
+append; page table of the "FlashInfer" agent-skill summary, KV-Cache Formats) writes the
+same key rows into a paged latent cache. Reading: key row i belongs to request
+batch_indices[i] at token position positions[i]; it lands in page
+kv_indices[kv_indptr[b] + positions[i] // page_size], slot positions[i] % page_size, as
+512 NoPE codes followed by the 64 rotated codes.
 """
 
 import numpy as np
@@ -79,3 +87,22 @@ def mla_rope_quantize_fp8(q_rope_bits, k_rope_bits, q_nope_bits, k_nope_bits, co
         outs[1] = e4m3_encode(rk * quant_scale_kv)
         outs[3] = e4m3_encode(bf16_bits_to_f64(k_nope_bits) * quant_scale_kv)
     return tuple(outs)
+
+
+def rope_quantize_fp8_append_paged(k_rope_bits, k_nope_bits, cos_sin, pos_k, batch_indices,
+                                   positions, kv_indptr, kv_indices, kv_pages, page_size,
+                                   is_neox=True, quant_scale_kv=1.0, cache_dtype="f32"):
+    """The key rows of mla_rope_quantize_fp8, appended: returns a copy of the paged cache
+    kv_pages [num_pages, page_size, 576] (E4M3 codes) with each row written to its slot."""
+    _, kr, _, kn = mla_rope_quantize_fp8(None, k_rope_bits, None, k_nope_bits, cos_sin, None,
+                                         pos_k, is_neox, 1.0, quant_scale_kv, cache_dtype)
+    out = np.array(kv_pages, dtype=np.uint8, copy=True)
+    for i in range(len(kn)):
+        b, q = int(batch_indices[i]), int(positions[i])
+        slot = int(kv_indptr[b]) + q // page_size
+        if slot >= int(kv_indptr[b + 1]):
+            raise ValueError("position past the request's pages")
+        page = int(kv_indices[slot])
+        out[page, q % page_size, :NOPE_DIM] = kn[i]
+        out[page, q % page_size, NOPE_DIM:] = kr[i]
+    return out

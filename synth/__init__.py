@@ -13,6 +13,7 @@ from .gen import (  # noqa: F401
     paged_decode_inputs,
     mla_inputs,
     mla_paged_inputs,
+    mla_append_inputs,
     E4M3_NAN,
     rope_cos_sin_cache,
     CONFIGS,

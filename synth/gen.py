@@ -275,6 +275,40 @@ def mla_paged_inputs(seed, batch, heads, page_size, len_lo, len_hi, spare=0.1, l
                 batch=batch, heads=heads, page_size=page_size, num_pages=P, seed=seed)
 
 
+def mla_append_inputs(seed, batch, page_size, len_lo, len_hi, new_tokens, lens=None,
+                      max_seq_len=65536, theta=1e4, device="cpu"):
+    """Inputs of the RoPE + FP8 append into a paged latent cache.
+
+    Request b holds L_b ~ U[len_lo, len_hi] tokens (or ``lens``) plus ``new_tokens`` more,
+    in the pages of mla_paged_inputs (canary-filled cache, permuted pages). The appended
+    rows are the last ``new_tokens`` positions of every request: batch_indices,
+    positions (also their rotary positions pos_k), k_rope [nnz, 64] and k_nope [nnz, 512]
+    bf16 ~ N(0,1), and the cos/sin cache.
+    """
+    g = _cpu_gen(seed + 7)
+    if lens is None:
+        lens = [int(x) for x in _uniform_int(g, len_lo, len_hi, batch)]
+    total = [int(L) + new_tokens for L in lens]
+    d = mla_paged_inputs(seed, batch=batch, heads=1, page_size=page_size, len_lo=0, len_hi=0,
+                         lens=total, device=device)
+    bi, pos = [], []
+    for b, L in enumerate(lens):
+        bi += [b] * new_tokens
+        pos += list(range(int(L), int(L) + new_tokens))
+    assert max(pos, default=0) < max_seq_len
+    nnz = len(pos)
+    dg = _dev_gen(seed + 11, device)
+    k_rope = _randn((nnz, 64), torch.bfloat16, dg, device)
+    k_nope = _randn((nnz, 512), torch.bfloat16, dg, device)
+    cos_sin = rope_cos_sin_cache(max_seq_len, 64, theta, torch.float32).to(device)
+    positions = torch.tensor(pos, dtype=torch.int32)
+    return dict(kv_pages=d["kv_pages"], kv_indptr=d["kv_indptr"], kv_indices=d["kv_indices"],
+                kv_last_page_len=d["kv_last_page_len"], num_pages=d["num_pages"],
+                page_size=page_size, batch=batch, batch_indices=torch.tensor(bi, dtype=torch.int32),
+                positions=positions, pos_k=positions.clone(), k_rope=k_rope, k_nope=k_nope,
+                cos_sin=cos_sin, max_seq_len=max_seq_len, seed=seed)
+
+
 # --------------------------------------------------------------------------------------
 # The five workloads at full size (seeds 1000 + index)
 # --------------------------------------------------------------------------------------
@@ -296,6 +330,8 @@ CONFIGS = {
                          dtype=torch.bfloat16),
     "mla_paged": dict(kind="mla_paged", seed=1005, batch=128, heads=128, page_size=64,
                       len_lo=2048, len_hi=8192),
+    "mla_append": dict(kind="mla_append", seed=1006, batch=128, page_size=64, len_lo=2048,
+                       len_hi=8192, new_tokens=512),
 }
 
 
@@ -312,4 +348,6 @@ def make(name, device="cpu", **overrides):
         return mla_inputs(device=device, **cfg)
     if kind == "mla_paged":
         return mla_paged_inputs(device=device, **cfg)
+    if kind == "mla_append":
+        return mla_append_inputs(device=device, **cfg)
     raise ValueError(kind)

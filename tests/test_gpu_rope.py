@@ -92,3 +92,82 @@ def test_rope_position_out_of_range_is_reported(cuda):
     torch.cuda.synchronize()
     assert bskv.STATUS[bskv.bskv_get_device_status(reset=True)] == "ERR_DEVICE_INDEX"
     assert bskv.bskv_get_device_status() == 0
+
+
+# ---------------------------------------------------------------------------------------
+# RoPE + FP8 appended into a paged latent cache
+# ---------------------------------------------------------------------------------------
+
+def _append(cuda, d, neox=True, skv=1.0, batch_indices=None, positions=None):
+    cache = d["kv_pages"].to(cuda).clone()
+    bi = d["batch_indices"] if batch_indices is None else batch_indices
+    pos = d["positions"] if positions is None else positions
+    bskv.bskv_rope_quantize_fp8_append_paged(
+        d["k_rope"].to(cuda), d["k_nope"].to(cuda), d["pos_k"].to(cuda), d["cos_sin"].to(cuda),
+        bi.to(cuda), pos.to(cuda), d["kv_indptr"].to(cuda), d["kv_indices"].to(cuda), cache,
+        is_neox=neox, quant_scale_kv=skv)
+    torch.cuda.synchronize()
+    return u8(cache)
+
+
+def _append_ref(d, neox=True, skv=1.0):
+    return rope.rope_quantize_fp8_append_paged(
+        bits(d["k_rope"]), bits(d["k_nope"]), d["cos_sin"].cpu().numpy(), d["pos_k"].numpy(),
+        d["batch_indices"].numpy(), d["positions"].numpy(), d["kv_indptr"].numpy(),
+        d["kv_indices"].numpy(), u8(d["kv_pages"]), d["page_size"], neox, skv)
+
+
+def _check_append(got, ref, d, exact_nope):
+    """Untouched cache bytes identical; appended rows under the prologue's byte gate."""
+    ps = d["page_size"]
+    ip, ix = d["kv_indptr"].numpy(), d["kv_indices"].numpy()
+    bi, pos = d["batch_indices"].numpy(), d["positions"].numpy()
+    pages = ix[ip[bi] + pos // ps]
+    slots = pos % ps
+    touched = np.zeros(got.shape[:2], bool)
+    touched[pages, slots] = True
+    np.testing.assert_array_equal(got[~touched], ref[~touched])
+    _check_bytes(got[pages, slots, 512:], ref[pages, slots, 512:], what="k_rope")
+    _check_bytes(got[pages, slots, :512], ref[pages, slots, :512], exact=exact_nope, what="k_nope")
+
+
+@pytest.mark.parametrize("ps,neox,skv", [(16, True, 1.0), (64, False, 1.0), (7, True, 0.75)])
+def test_rope_append_paged_small(cuda, ps, neox, skv):
+    d = synth.mla_append_inputs(31, batch=4, page_size=ps, len_lo=0, len_hi=0, new_tokens=9,
+                                lens=[0, 15, 64, 200], max_seq_len=512)
+    bskv.bskv_get_device_status(reset=True)
+    got = _append(cuda, d, neox, skv)
+    assert bskv.bskv_get_device_status() == 0
+    _check_append(got, _append_ref(d, neox, skv), d, exact_nope=skv == 1.0)
+
+
+def test_rope_append_paged_full_workload(cuda):
+    """The benchmark's append: 128 requests x 512 new tokens into the page-64 cache."""
+    d = synth.make("mla_append", device="cuda")
+    bskv.bskv_get_device_status(reset=True)
+    got = _append(cuda, d)
+    assert bskv.bskv_get_device_status() == 0
+    _check_append(got, _append_ref(d), d, exact_nope=True)
+
+
+def test_rope_append_paged_bad_destination_is_reported(cuda):
+    d = synth.mla_append_inputs(32, batch=2, page_size=16, len_lo=0, len_hi=0, new_tokens=4,
+                                lens=[3, 20], max_seq_len=256)
+    pos = d["positions"].clone()
+    bi = d["batch_indices"].clone()
+    pos[1] = 10 ** 6            # past the request's pages
+    bi[5] = 7                   # no such request
+    bskv.bskv_get_device_status(reset=True)
+    got = _append(cuda, d, batch_indices=bi, positions=pos)
+    assert bskv.STATUS[bskv.bskv_get_device_status(reset=True)] == "ERR_DEVICE_INDEX"
+    ref = _append_ref(d)
+    keep = [i for i in range(len(pos)) if i not in (1, 5)]
+    ps = 16
+    ip, ix = d["kv_indptr"].numpy(), d["kv_indices"].numpy()
+    b0, p0 = d["batch_indices"].numpy(), d["positions"].numpy()
+    for i in keep:   # the valid rows were written as usual
+        pg, sl = ix[ip[b0[i]] + p0[i] // ps], p0[i] % ps
+        _check_bytes(got[pg, sl], ref[pg, sl], what="row %d" % i)
+    for i in (1, 5):  # the rejected rows' own slots keep their old bytes
+        pg, sl = ix[ip[b0[i]] + p0[i] // ps], p0[i] % ps
+        np.testing.assert_array_equal(got[pg, sl], u8(d["kv_pages"])[pg, sl])

@@ -3,7 +3,10 @@
 Pins: position 0 is the identity rotation (bytes equal the plain cast); the two layouts
 differ by a fixed permutation of the 64 tail values; each rotated pair keeps its norm;
 the rotation equals multiplication by exp(i*angle) on the complex pair (closed form
-from the cache's own angle definition); quant scales act as plain multipliers.
+from the cache's own angle definition); quant scales act as plain multipliers. The paged
+append places exactly the prologue's key rows: read back through the page table in token
+order they sit at their positions, every other cache byte is unchanged, and with
+page_size 1 and pages in order the cache is the prologue's row array.
 """
 
 import numpy as np
@@ -96,3 +99,53 @@ def test_bad_position_rejected():
     d = _inputs()
     with pytest.raises(ValueError):
         rope.cache_rows(d["cos_sin"].numpy(), np.array([64]))
+
+
+def _logical_rows(cache, indptr, indices, b, ps, n):
+    """Rows [0, n) of request b in token order, gathered through the page table."""
+    return np.stack([cache[indices[indptr[b] + t // ps], t % ps] for t in range(n)])
+
+
+@pytest.mark.parametrize("ps,neox", [(16, True), (7, False)])
+def test_paged_append_places_the_prologue_rows(ps, neox):
+    d = synth.mla_append_inputs(21, batch=3, page_size=ps, len_lo=0, len_hi=0, new_tokens=5,
+                                lens=[9, 0, 40], max_seq_len=128)
+    cache0 = d["kv_pages"].numpy()
+    ip, ix = d["kv_indptr"].numpy(), d["kv_indices"].numpy()
+    bi, pos = d["batch_indices"].numpy(), d["positions"].numpy()
+    new = rope.rope_quantize_fp8_append_paged(
+        _bits(d["k_rope"]), _bits(d["k_nope"]), d["cos_sin"].numpy(), d["pos_k"].numpy(), bi, pos,
+        ip, ix, cache0, ps, neox)
+    _, kr, _, kn = rope.mla_rope_quantize_fp8(None, _bits(d["k_rope"]), None, _bits(d["k_nope"]),
+                                              d["cos_sin"].numpy(), None, d["pos_k"].numpy(), neox)
+    touched = np.zeros(cache0.shape[:2], bool)
+    for b in range(3):
+        n = int(pos[bi == b].max()) + 1 if (bi == b).any() else 0
+        rows = _logical_rows(new, ip, ix, b, ps, n)
+        old = _logical_rows(cache0, ip, ix, b, ps, n)
+        for i in np.nonzero(bi == b)[0]:
+            np.testing.assert_array_equal(rows[pos[i], :512], kn[i])
+            np.testing.assert_array_equal(rows[pos[i], 512:], kr[i])
+            touched[ix[ip[b] + pos[i] // ps], pos[i] % ps] = True
+        keep = np.setdiff1d(np.arange(n), pos[bi == b])
+        np.testing.assert_array_equal(rows[keep], old[keep])
+    np.testing.assert_array_equal(new[~touched], cache0[~touched])
+
+
+def test_paged_append_page_size_one_in_order_is_the_row_array():
+    d = synth.mla_append_inputs(22, batch=2, page_size=1, len_lo=0, len_hi=0, new_tokens=3,
+                                lens=[2, 4], max_seq_len=64)
+    n_pages = d["num_pages"]
+    ip = d["kv_indptr"].numpy()
+    ix = np.arange(int(ip[-1]), dtype=np.int32)      # pages in order: row = indptr[b] + t
+    cache0 = d["kv_pages"].numpy()
+    bi, pos = d["batch_indices"].numpy(), d["positions"].numpy()
+    new = rope.rope_quantize_fp8_append_paged(
+        _bits(d["k_rope"]), _bits(d["k_nope"]), d["cos_sin"].numpy(), d["pos_k"].numpy(), bi, pos,
+        ip, ix, cache0, 1)
+    _, kr, _, kn = rope.mla_rope_quantize_fp8(None, _bits(d["k_rope"]), None, _bits(d["k_nope"]),
+                                              d["cos_sin"].numpy(), None, d["pos_k"].numpy(), True)
+    flat = new.reshape(n_pages, 576)
+    for i in range(len(bi)):
+        r = int(ip[bi[i]]) + int(pos[i])
+        np.testing.assert_array_equal(flat[r], np.concatenate([kn[i], kr[i]]))
