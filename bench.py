@@ -369,6 +369,37 @@ def bench_bsr(bskv, synth, name, steps, warmup, peaks, flush):
                 peak="bf16 dense burst (fp16 rate equal)")
 
 
+def bench_bsr_masked(bskv, synth, steps, warmup, peaks):
+    """The BSR prefill workload expressed as a per-block token mask (diagonal blocks carry
+    the causal pattern, the listed off-diagonal blocks are full): the same visible pairs as
+    the causal run, through the masked entry point."""
+    d = synth.make("bsr_prefill", device="cuda")
+    R, C = d["R"], d["C"]
+    ip, ix = d["indptr"].numpy(), d["indices"].numpy()
+    nnz = int(ip[-1])
+    tri = np.tril(np.ones((R, C), bool))
+    bm = np.ones((nnz, R, C), bool)
+    for a in range(len(ip) - 1):
+        for e in range(int(ip[a]), int(ip[a + 1])):
+            if int(ix[e]) == a:
+                bm[e] = tri
+    packed = torch.from_numpy(np.packbits(bm.reshape(-1), bitorder="little").copy()).cuda()
+    plan = bskv.bskv_plan_bsr_masked(d["indptr"], d["indices"], d["M"], d["N"], R, C,
+                                     d["num_qo_heads"], d["num_kv_heads"], d["head_dim"],
+                                     dtype=torch.float16)
+    plan.upload("cuda")
+    out = torch.empty_like(d["q"])
+    fn = lambda: bskv.bskv_run_bsr_masked(plan, d["q"], d["k"], d["v"], packed, out=out)  # noqa
+    ms = time_iters(fn, steps, warmup, flush=True)
+    fl = bsr_flops(d)
+    tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+    return dict(workload="bsr_prefill as a token mask (causal pattern in the diagonal blocks)",
+                flops=fl, kernel="tcgen05" if plan.metadata()[15] == 1 else "general",
+                **summary(ms), tflops=tf,
+                frac=tf / peaks["bf16_tflops"], peak="bf16 dense burst (fp16 rate equal)",
+                mask_bytes=int(packed.numel()))
+
+
 def bench_mla(bskv, synth, steps, warmup, peaks):
     m = synth.make("mla_decode", device="cuda")
     B, H, K = m["batch"], m["heads"], m["top_k"]
@@ -527,7 +558,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of extra rows: bsr_prefill,bsr_tiny,mla,mla_paged,mla_append,split,e2e,cpu "
+                    help="comma list of extra rows: bsr_prefill,bsr_tiny,bsr_masked,mla,mla_paged,mla_append,"
+                         "split,e2e,cpu "
                          "or all/none")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -539,7 +571,8 @@ def main():
     bskv.build()
     dist, rank, ws = dist_setup(args.gpus)
     peaks, peak_src = load_peaks()
-    rows = set(["bsr_prefill", "bsr_tiny", "mla", "mla_paged", "mla_append", "split", "e2e", "cpu"]
+    rows = set(["bsr_prefill", "bsr_tiny", "bsr_masked", "mla", "mla_paged", "mla_append", "split",
+                "e2e", "cpu"]
                if args.rows == "all" else [] if args.rows == "none" else args.rows.split(","))
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -563,7 +596,9 @@ def main():
                 ("mla_paged", "mla_paged",
                  lambda: bench_mla_paged(bskv, synth, K, args.warmup, peaks)),
                 ("mla_append", "mla_append",
-                 lambda: bench_mla_append(bskv, synth, K, args.warmup, peaks))]
+                 lambda: bench_mla_append(bskv, synth, K, args.warmup, peaks)),
+                ("bsr_masked", "bsr_masked",
+                 lambda: bench_bsr_masked(bskv, synth, K, args.warmup, peaks))]
         for key, name, job in jobs:
             if key in rows:
                 try:

@@ -59,6 +59,10 @@ _SIGS = {
                           _I32, ctypes.POINTER(_P)], _I32),
     "bskv_plan_bsr": ([_I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                        ctypes.POINTER(_P)], _I32),
+    "bskv_plan_bsr_masked": ([_I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                              ctypes.POINTER(_P)], _I32),
+    "bskv_run_bsr_masked": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _SZ, _P, _I64P, _P, _F,
+                             _P], _I32),
     "bskv_plan_mla_sparse": ([_I32P, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(_P)], _I32),
     "bskv_plan_mla_paged": ([_I32P, _I32P, _I32P, _I32, _I32, _I32, _I32, _I32,
                              ctypes.POINTER(_P)], _I32),
@@ -305,6 +309,43 @@ def bskv_run_bsr(plan, q, k, v, out=None, lse=None, return_lse=False, sm_scale=N
         _strides(k.stride(0), k.stride(1)), v.data_ptr(), _strides(v.stride(0), v.stride(1)),
         out.data_ptr(), _strides(out.stride(0), out.stride(1)), _ptr(lse), float(sm_scale),
         _ptr(fw), 0 if fw is None else fw.numel(), _stream(q)))
+    return (out, lse) if return_lse else out
+
+
+def bskv_plan_bsr_masked(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim,
+                         dtype=torch.float16, num_sms=None):
+    """BSR plan whose runs take a per-block token mask (packed bits, bskv_run_bsr_masked)."""
+    lib = load_library()
+    ip, ipp = _i32_array(indptr)
+    ix, ixp = _i32_array(indices)
+    h = ctypes.c_void_p()
+    ns = _num_sms() if num_sms is None else num_sms
+    _check("bskv_plan_bsr_masked", lib.bskv_plan_bsr_masked(
+        ctypes.cast(ipp, _I32P), ctypes.cast(ixp, _I32P), int(M), int(N), int(R), int(C),
+        int(num_qo_heads), int(num_kv_heads), int(head_dim), _DT[dtype], int(ns),
+        ctypes.byref(h)))
+    return Plan(h.value, "bsr_masked", M=M, N=N, R=R, C=C, num_qo_heads=num_qo_heads,
+                num_kv_heads=num_kv_heads, head_dim=head_dim, dtype=dtype)
+
+
+def bskv_run_bsr_masked(plan, q, k, v, packed_mask, out=None, lse=None, return_lse=False,
+                        sm_scale=None):
+    """packed_mask: uint8 device tensor, the (nnz, R, C) mask packed little-endian per byte."""
+    lib = load_library()
+    if plan.int_ws is None:
+        plan.upload(q.device)
+    M, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((M, Hq), dtype=torch.float32, device=q.device)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    _check("bskv_run_bsr_masked", lib.bskv_run_bsr_masked(
+        plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), k.data_ptr(),
+        _strides(k.stride(0), k.stride(1)), v.data_ptr(), _strides(v.stride(0), v.stride(1)),
+        packed_mask.data_ptr(), packed_mask.numel(), out.data_ptr(),
+        _strides(out.stride(0), out.stride(1)), _ptr(lse), float(sm_scale), _stream(q)))
     return (out, lse) if return_lse else out
 
 

@@ -35,6 +35,9 @@ struct BsrParams {
   int64_t o_s0, o_s1;
   float* lse;
   int M, N, R, C, Hq, Hkv, group, causal;
+  // per-block token mask, bits packed little-endian within bytes over (nnz, R, C); NULL =
+  // every listed block is full
+  const uint8_t* mask;
   float scale_log2;
   StatusArgs st;
 };
@@ -117,7 +120,8 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
       }
       __syncthreads();
       const int buf = n & 1;
-      const int j = indices[e0 + n / subtiles];
+      const int eb = e0 + n / subtiles;  // the block's position in indices
+      const int j = indices[eb];
       const int kt0 = j * p.C + (n % subtiles) * kKT;
       const int kend = j * p.C + p.C;  // end of this column block
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -141,7 +145,13 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
           const int kt = kt0 + nt * 8 + 2 * cq + (e & 1);
           const int qt = (e < 2) ? tok0 : tok1;
           bool vis = kt < kend;
-          if (p.causal) vis = vis && (kt <= qt + (p.N - p.M));
+          if (p.mask) {
+            // bit (eb * R + row in block) * C + column in block; rows past M are never stored
+            const int64_t bit = (int64_t(eb) * p.R + (qt - i * p.R)) * p.C + (kt - j * p.C);
+            vis = vis && qt < p.M && ((__ldg(p.mask + (bit >> 3)) >> (bit & 7)) & 1);
+          } else if (p.causal) {
+            vis = vis && (kt <= qt + (p.N - p.M));
+          }
           s[nt][e] = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
         }
         mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
@@ -221,19 +231,18 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
 bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64_t* qs,
                                const void* k, const int64_t* ks, const void* v,
                                const int64_t* vs, void* out, const int64_t* os, float* lse,
-                               float sm_scale, cudaStream_t st);
+                               float sm_scale, const uint8_t* mask, cudaStream_t st);
 
 }  // namespace bskv
 
 using namespace bskv;
 
-extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strides,
-                                    const void* k, const int64_t* k_strides, const void* v,
-                                    const int64_t* v_strides, void* out,
-                                    const int64_t* out_strides, float* lse, float sm_scale,
-                                    void* float_ws, size_t float_ws_bytes, void* stream) {
-  (void)float_ws;
-  (void)float_ws_bytes;
+namespace {
+
+bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strides,
+                    const void* k, const int64_t* k_strides, const void* v,
+                    const int64_t* v_strides, void* out, const int64_t* out_strides, float* lse,
+                    float sm_scale, const uint8_t* mask, void* stream) {
   if (!plan || plan->kind != KIND_BSR) { set_error("run_bsr: not a BSR plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_bsr: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (!q_strides || !k_strides || !v_strides || !out_strides) { set_error("run_bsr: NULL strides"); return BSKV_ERR_INVALID_ARG; }
@@ -248,7 +257,7 @@ extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (meta_word(plan, H_VARIANT) == BSR_TCGEN05)
     return launch_bsr_tcgen05(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides,
-                              lse, sm_scale, st);
+                              lse, sm_scale, mask, st);
   BsrParams p{};
   p.meta = plan->meta_dev;
   p.q = q; p.q_s0 = q_strides[0]; p.q_s1 = q_strides[1];
@@ -259,6 +268,7 @@ extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const 
   p.M = plan->M; p.N = plan->N; p.R = plan->R; p.C = plan->C;
   p.Hq = plan->num_qo_heads; p.Hkv = plan->num_kv_heads; p.group = p.Hq / p.Hkv;
   p.causal = plan->causal;
+  p.mask = mask;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   if (bskv_status s = status_args(&p.st)) return s;
   const int grid = meta_word(plan, H_GRID);
@@ -272,4 +282,39 @@ extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const 
     else bsr_generic_kernel<__half, 64><<<grid, 128, 0, st>>>(p);
   }
   return cuda_check(cudaGetLastError(), "bsr kernel launch");
+}
+
+}  // namespace
+
+extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strides,
+                                    const void* k, const int64_t* k_strides, const void* v,
+                                    const int64_t* v_strides, void* out,
+                                    const int64_t* out_strides, float* lse, float sm_scale,
+                                    void* float_ws, size_t float_ws_bytes, void* stream) {
+  (void)float_ws;
+  (void)float_ws_bytes;
+  if (plan && plan->masked) { set_error("run_bsr: the plan expects a token mask (bskv_run_bsr_masked)"); return BSKV_ERR_INVALID_ARG; }
+  return run_bsr(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides, lse, sm_scale,
+                 nullptr, stream);
+}
+
+extern "C" bskv_status bskv_run_bsr_masked(const bskv_plan* plan, const void* q,
+                                           const int64_t* q_strides, const void* k,
+                                           const int64_t* k_strides, const void* v,
+                                           const int64_t* v_strides, const void* packed_mask,
+                                           size_t packed_mask_bytes, void* out,
+                                           const int64_t* out_strides, float* lse,
+                                           float sm_scale, void* stream) {
+  if (!plan || plan->kind != KIND_BSR || !plan->masked) { set_error("run_bsr_masked: not a masked BSR plan (bskv_plan_bsr_masked)"); return BSKV_ERR_INVALID_ARG; }
+  const int32_t MB = (plan->M + plan->R - 1) / plan->R;
+  const int32_t* meta = plan->meta.data();
+  const int64_t nnz = plan->M > 0 ? meta[meta[H_OFF_AUX0] + MB] : 0;
+  const size_t need = size_t((nnz * plan->R * plan->C + 7) / 8);
+  if (need > 0 && (!packed_mask || packed_mask_bytes < need)) {
+    set_error("run_bsr_masked: packed mask of %zu bytes, %zu needed", packed_mask_bytes, need);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (reinterpret_cast<uintptr_t>(packed_mask) & 15) { set_error("run_bsr_masked: packed mask must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  return run_bsr(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides, lse, sm_scale,
+                 static_cast<const uint8_t*>(packed_mask), stream);
 }

@@ -58,6 +58,9 @@ struct TcParams {
   int64_t o_s0, o_s1;
   float* lse;
   int M, N, Hq, Hkv, group, causal;
+  // per-block token mask (bits little-endian over (nnz, 64, 64): one 64-bit word per row of
+  // a block, bit c = key c), or NULL
+  const unsigned long long* mask;
   float scale_log2;
   StatusArgs st;
 };
@@ -153,7 +156,9 @@ __device__ __forceinline__ uint32_t exp2_pack<__nv_bfloat16>(float x0, float x1,
   return pack2(__nv_bfloat16(), v0, v1);
 }
 
-template <typename T, int NM>
+// kMask: runs with a per-block token mask (a separate instantiation, so that the unmasked
+// softmax carries none of its code).
+template <typename T, int NM, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -397,6 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb = min(2, n - 2 * j);
         const int jb0 = indices[e0 + 2 * j];
         const int jb1 = nb == 2 ? indices[e0 + 2 * j + 1] : jb0;
+        // this row's token-mask words of the step's blocks, read before the wait as well
+        unsigned long long mw0 = ~0ull, mw1 = ~0ull;
+        if (kMask) {
+          mw0 = __ldg(p.mask + (int64_t(e0 + 2 * j) * kBlk + (r & (kBlk - 1))));
+          if (nb == 2) mw1 = __ldg(p.mask + (int64_t(e0 + 2 * j + 1) * kBlk + (r & (kBlk - 1))));
+        }
         if (!warp_wait(&B.s_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t scol = tmem + lane_base + 128 + 256 * z;
@@ -417,6 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int bb = 0; bb < 2; ++bb) {
           if (bb < nb) {
             const int k0 = (bb ? jb1 : jb0) * kBlk;
+            const unsigned long long mw = bb ? mw1 : mw0;
+            if (kMask && mw != ~0ull) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (!((mw >> c) & 1ull)) sr[64 * bb + c] = __float_as_uint(-INFINITY);
+            }
             if (p.causal && (k0 + kBlk - 1 > lim)) {
 #pragma unroll
               for (int c = 0; c < 64; ++c)
@@ -572,14 +589,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int NM>
+template <typename T, int NM, bool kMask>
 bskv_status launch_t(const bskv_plan* plan, const CUtensorMap& qm, const CUtensorMap& km,
                      const CUtensorMap& vm, const CUtensorMap& om, const TcParams& tp,
                      cudaStream_t st) {
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
   const size_t smem = Cfg<NM>::kBytes + 1024;
-  auto kern = bsr_tc_kernel<T, NM>;
+  auto kern = bsr_tc_kernel<T, NM, kMask>;
   if (bskv_status s = cuda_check(
           cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
           "bsr_tc: cudaFuncSetAttribute"))
@@ -593,7 +610,7 @@ bskv_status launch_t(const bskv_plan* plan, const CUtensorMap& qm, const CUtenso
 bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64_t* qs,
                                const void* k, const int64_t* ks, const void* v,
                                const int64_t* vs, void* out, const int64_t* os, float* lse,
-                               float sm_scale, cudaStream_t st) {
+                               float sm_scale, const uint8_t* mask, cudaStream_t st) {
   const int g = plan->num_qo_heads / plan->num_kv_heads;
   if (!(plan->R == kBlk && plan->C == kBlk && plan->head_dim == kD && (g == 2 || g == 4))) {
     set_error("run_bsr: tensor-core kernel needs R = C = 64, head_dim 128, group 2 or 4");
@@ -605,6 +622,7 @@ bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64
   tp.lse = lse;
   tp.M = plan->M; tp.N = plan->N; tp.Hq = plan->num_qo_heads; tp.Hkv = plan->num_kv_heads;
   tp.group = g; tp.causal = plan->causal;
+  tp.mask = reinterpret_cast<const unsigned long long*>(mask);
   tp.scale_log2 = sm_scale * 1.4426950408889634f;
   if (bskv_status s = status_args(&tp.st)) return s;
   const CUtensorMapDataType dt =
@@ -633,11 +651,18 @@ bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64
     if (bskv_status s = encode_tiled(&vm, dt, 3, v, dims, sv, box, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
   }
   const bool bf = plan->dtype == BSKV_BF16;
+  if (mask) {
+    if (g == 4)
+      return bf ? launch_t<__nv_bfloat16, 2, true>(plan, qm, km, vm, om, tp, st)
+                : launch_t<__half, 2, true>(plan, qm, km, vm, om, tp, st);
+    return bf ? launch_t<__nv_bfloat16, 1, true>(plan, qm, km, vm, om, tp, st)
+              : launch_t<__half, 1, true>(plan, qm, km, vm, om, tp, st);
+  }
   if (g == 4)
-    return bf ? launch_t<__nv_bfloat16, 2>(plan, qm, km, vm, om, tp, st)
-              : launch_t<__half, 2>(plan, qm, km, vm, om, tp, st);
-  return bf ? launch_t<__nv_bfloat16, 1>(plan, qm, km, vm, om, tp, st)
-            : launch_t<__half, 1>(plan, qm, km, vm, om, tp, st);
+    return bf ? launch_t<__nv_bfloat16, 2, false>(plan, qm, km, vm, om, tp, st)
+              : launch_t<__half, 2, false>(plan, qm, km, vm, om, tp, st);
+  return bf ? launch_t<__nv_bfloat16, 1, false>(plan, qm, km, vm, om, tp, st)
+            : launch_t<__half, 1, false>(plan, qm, km, vm, om, tp, st);
 }
 
 }  // namespace bskv

@@ -80,8 +80,8 @@ struct bskv_plan {
   int32_t batch = 0, num_pages = 0, page_size = 0;
   // shared
   int32_t num_qo_heads = 0, num_kv_heads = 0, head_dim = 0, dtype = 0;
-  // bsr
-  int32_t M = 0, N = 0, R = 0, C = 0, causal = 0;
+  // bsr (masked: runs take a per-block token mask, the general kernel serves them)
+  int32_t M = 0, N = 0, R = 0, C = 0, causal = 0, masked = 0;
   // mla (paged: batch, num_pages and page_size as for decode; top_k is the row-list
   // stride, the longest request rounded up to 64)
   int32_t q_len = 0, top_k = 0, mla_variant = 0;

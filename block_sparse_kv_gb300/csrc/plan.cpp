@@ -216,10 +216,13 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
   return BSKV_OK;
 }
 
-extern "C" bskv_status bskv_plan_bsr(const int32_t* indptr, const int32_t* indices, int32_t M,
-                                     int32_t N, int32_t R, int32_t C, int32_t num_qo_heads,
-                                     int32_t num_kv_heads, int32_t head_dim, int32_t causal,
-                                     int32_t dtype, int32_t num_sms, bskv_plan** out_plan) {
+namespace {
+
+// BSR plan; `masked`: a per-block token mask comes with every run (no causal flag then).
+bskv_status plan_bsr(const int32_t* indptr, const int32_t* indices, int32_t M, int32_t N,
+                     int32_t R, int32_t C, int32_t num_qo_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t causal, int32_t dtype, int32_t num_sms,
+                     bool masked, bskv_plan** out_plan) {
   if (!out_plan) { set_error("plan_bsr: out_plan is NULL"); return BSKV_ERR_INVALID_ARG; }
   *out_plan = nullptr;
   if (M < 0 || N < 0 || R < 1 || C < 1 || num_sms < 1) {
@@ -306,8 +309,28 @@ extern "C" bskv_status bskv_plan_bsr(const int32_t* indptr, const int32_t* indic
   assemble(p, KIND_BSR, int32_t(U), worker_ptr, chunks, 0, no_merges, rows_per_unit, indptr,
            size_t(MB) + 1, indices, size_t(nnz), G, tc ? BSR_TCGEN05 : BSR_GENERIC);
   p->float_ws_bytes = 0;
+  p->masked = masked ? 1 : 0;
   *out_plan = p;
   return BSKV_OK;
+}
+
+}  // namespace
+
+extern "C" bskv_status bskv_plan_bsr(const int32_t* indptr, const int32_t* indices, int32_t M,
+                                     int32_t N, int32_t R, int32_t C, int32_t num_qo_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t causal,
+                                     int32_t dtype, int32_t num_sms, bskv_plan** out_plan) {
+  return plan_bsr(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, causal,
+                  dtype, num_sms, false, out_plan);
+}
+
+extern "C" bskv_status bskv_plan_bsr_masked(const int32_t* indptr, const int32_t* indices,
+                                            int32_t M, int32_t N, int32_t R, int32_t C,
+                                            int32_t num_qo_heads, int32_t num_kv_heads,
+                                            int32_t head_dim, int32_t dtype, int32_t num_sms,
+                                            bskv_plan** out_plan) {
+  return plan_bsr(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, 0, dtype,
+                  num_sms, true, out_plan);
 }
 
 extern "C" bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t batch, int32_t q_len,

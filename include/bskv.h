@@ -127,6 +127,17 @@ bskv_status bskv_plan_bsr(const int32_t* indptr, const int32_t* indices, int32_t
                           bskv_plan** out_plan);
 
 /*
+ * BSR plan for runs with a per-block token mask ([SPARSE] plan(..., mask, packed_mask):
+ * a mask of shape (nnz, R, C) selects the visible (query, key) pairs inside each listed
+ * block; causal applies only when no mask is given, so this plan has no causal flag).
+ * Arguments and kernel choice as for bskv_plan_bsr.
+ */
+bskv_status bskv_plan_bsr_masked(const int32_t* indptr, const int32_t* indices, int32_t M,
+                                 int32_t N, int32_t R, int32_t C, int32_t num_qo_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                                 int32_t num_sms, bskv_plan** out_plan);
+
+/*
  * Sparse MLA FP8 decode plan ([MLA] get_batch_decode_metadata_mla(query, seq_lens,
  * sparse_mla_top_k): reusable while seq_lens, the query shape and top_k are unchanged).
  *   seq_lens[batch]: HOST int32 valid sparse lengths, 0 <= seq_lens[b] <= top_k.
@@ -264,6 +275,23 @@ bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_
                          const int64_t* v_strides, void* out, const int64_t* out_strides,
                          float* lse, float sm_scale, void* float_ws, size_t float_ws_bytes,
                          void* stream);
+
+/*
+ * BSR block-sparse attention with a per-block token mask ([SPARSE] run() of a plan made
+ * with mask / packed_mask), for a plan of bskv_plan_bsr_masked:
+ *   q, k, v, out, lse as for bskv_run_bsr.
+ *   packed_mask: device bytes holding the (nnz, R, C) boolean mask flattened in that order
+ *     (nnz in the order of indices), eight entries per byte, entry t in bit t % 8 of byte
+ *     t / 8 (numpy.packbits(..., bitorder="little")); packed_mask_bytes >= ceil(nnz*R*C/8);
+ *     16-byte aligned.
+ *   Query i sees key j iff the block (i / R, j / C) is listed and its mask entry
+ *   (i % R, j % C) is set; a row that sees nothing gets out = 0 and lse = -inf.
+ */
+bskv_status bskv_run_bsr_masked(const bskv_plan* plan, const void* q, const int64_t* q_strides,
+                                const void* k, const int64_t* k_strides, const void* v,
+                                const int64_t* v_strides, const void* packed_mask,
+                                size_t packed_mask_bytes, void* out, const int64_t* out_strides,
+                                float* lse, float sm_scale, void* stream);
 
 /*
  * Sparse MLA FP8 decode ([MLA] sparse_mla_fp8_decode; [WRAP] scale folding):

@@ -13,7 +13,10 @@ Sources:
   * BSR mask and GQA: "flashinfer.sparse - FlashInfer 0.7.4 documentation",
     BlockSparseAttentionWrapper: the mask is a SciPy bsr_matrix (indptr of length
     MB+1, MB = ceil_div(M, R); indices < NB = N // C); the 3x3 worked example checks
-    the result against dense attention with the same boolean mask; num_qo_heads must
+    the result against dense attention with the same boolean mask; plan(mask=(nnz, R, C))
+    selects the visible pairs inside each listed block and then causal does not apply
+    (packed_mask: the same entries packed as bits; reading: little-endian bit order within
+    a byte, as numpy.packbits(bitorder="little")); num_qo_heads must
     be a multiple of num_kv_heads (grouped-query attention); sm_scale defaults to
     1/sqrt(head_dim); run() returns out [M, Hq, D] and lse [M, Hq].
   * causal: plan() parameter "causal"; for M != N the mask is aligned bottom-right,
@@ -83,8 +86,12 @@ def masked_attention(q, k, v, sm_scale, mask=None):
 # BSR block-sparse mask
 # ---------------------------------------------------------------------------------------
 
-def bsr_mask(indptr, indices, M, N, R, C, causal=False, rows=None):
-    """Dense boolean mask [len(rows), N] of a BSR block mask (rows default to all M)."""
+def bsr_mask(indptr, indices, M, N, R, C, causal=False, rows=None, block_mask=None):
+    """Dense boolean mask [len(rows), N] of a BSR block mask (rows default to all M).
+
+    ``block_mask`` (nnz, R, C) optionally selects the visible pairs inside each listed block
+    (entry [e, i % R, j % C] for the block at position e of ``indices``); causal is then not
+    applied (it only acts when no mask is given)."""
     indptr = np.asarray(indptr, dtype=np.int64)
     indices = np.asarray(indices, dtype=np.int64)
     MB = (M + R - 1) // R
@@ -97,18 +104,22 @@ def bsr_mask(indptr, indices, M, N, R, C, causal=False, rows=None):
     mask = np.zeros((len(rows), N), dtype=bool)
     for r, i in enumerate(rows):
         bi = i // R
-        for j in indices[indptr[bi]:indptr[bi + 1]]:
+        for e in range(indptr[bi], indptr[bi + 1]):
+            j = indices[e]
             if not (0 <= j < NB):
                 raise ValueError("column block index out of range")
-            mask[r, j * C:(j + 1) * C] = True
-    if causal:
+            if block_mask is None:
+                mask[r, j * C:(j + 1) * C] = True
+            else:
+                mask[r, j * C:(j + 1) * C] = block_mask[e, i % R]
+    if causal and block_mask is None:
         cols = np.arange(N)
         mask &= cols[None, :] <= (rows[:, None] + (N - M))
     return mask
 
 
 def bsr_attention(q_bits, k_bits, v_bits, dtype, indptr, indices, M, N, R, C,
-                  sm_scale=None, causal=False, rows=None):
+                  sm_scale=None, causal=False, rows=None, block_mask=None):
     """BSR block-sparse attention from stored 16-bit inputs.
 
     q [M, Hq, D], k/v [N, Hkv, D] as uint16 bit patterns of ``dtype`` ('fp16'/'bf16').
@@ -119,7 +130,7 @@ def bsr_attention(q_bits, k_bits, v_bits, dtype, indptr, indices, M, N, R, C,
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
     rows_idx = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
-    mask = bsr_mask(indptr, indices, M, N, R, C, causal, rows_idx)
+    mask = bsr_mask(indptr, indices, M, N, R, C, causal, rows_idx, block_mask)
     k = bits_to_f64(k_bits, dtype)
     v = bits_to_f64(v_bits, dtype)
     return masked_attention(q[rows_idx], k, v, sm_scale, mask)

@@ -42,7 +42,8 @@ i, kv head h), rows_per_unit = R*g, at most num_sms CTAs. Otherwise the general
 variant 0: rows_per_unit = 64, row_tiles = ceil(R*g / 64) units per (i, h), at most
 4*num_sms CTAs. Unit u = (i*Hkv + h)*row_tiles + rt. With n = blocks in row i, cost_u =
 2 + 4*(n // 2) + 3*(n % 2) for a tensor-core unit with n > 0 (1 when n == 0), and 1 + n
-for a general unit.
+for a general unit. A plan for runs with a per-block token mask follows the same
+rule.
 Units sorted by cost descending (stable); each goes to the CTA of least current load
 (ties: lowest CTA index). Chunks list each CTA's units in assignment order as
 (u, i, h, rt); tile = rows_per_unit; grid = number of CTAs; aux0 = indptr,

@@ -338,3 +338,85 @@ def test_mla_paged_full_request_equals_dense_and_empty_request():
     ref = _sdpa(Q[None], K[:, None, :], K[:, None, :512], 0.07)[0]
     np.testing.assert_allclose(out[0], ref, rtol=1e-12, atol=1e-14)
     assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
+
+
+# ---------------------------------------------------------------------------------------
+# BSR with a per-block token mask
+# ---------------------------------------------------------------------------------------
+
+def _bsr_small(seed, M, N, R, C, Hq=4, Hkv=2, D=16, density=0.6):
+    d = synth.bsr_inputs(seed, M, N, R, C, Hq, Hkv, D, pattern="random", density=density)
+    return d, _bits(d["q"]), _bits(d["k"]), _bits(d["v"])
+
+
+def test_bsr_all_true_token_mask_equals_unmasked():
+    d, q, k, v = _bsr_small(61, 20, 24, 4, 8)
+    nnz = int(d["indptr"][-1])
+    full = np.ones((nnz, 4, 8), bool)
+    a = att.bsr_attention(q, k, v, "fp16", d["indptr"], d["indices"], 20, 24, 4, 8)
+    b = att.bsr_attention(q, k, v, "fp16", d["indptr"], d["indices"], 20, 24, 4, 8, block_mask=full)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_bsr_token_mask_of_the_causal_pattern_equals_causal():
+    """All blocks listed; each block's mask is the causal pattern restricted to it."""
+    M = N = 16
+    R = C = 4
+    MB = NB = 4
+    indptr = np.arange(0, MB * NB + 1, NB)
+    indices = np.tile(np.arange(NB), MB)
+    bm = np.zeros((MB * NB, R, C), bool)
+    for a in range(MB):
+        for c in range(NB):
+            for r in range(R):
+                for cc in range(C):
+                    bm[a * NB + c, r, cc] = c * C + cc <= a * R + r
+    d, q, k, v = _bsr_small(62, M, N, R, C)
+    ref = att.bsr_attention(q, k, v, "fp16", indptr, indices, M, N, R, C, causal=True)
+    got = att.bsr_attention(q, k, v, "fp16", indptr, indices, M, N, R, C, block_mask=bm,
+                            causal=True)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+
+
+def test_bsr_token_mask_brute_force_and_empty_rows():
+    """Pure-Python loops over the pairs the mask keeps; a row whose pairs are all masked
+    gives 0 and -inf."""
+    M, N, R, C = 6, 8, 3, 4
+    d, qb, kb, vb = _bsr_small(63, M, N, R, C, Hq=2, Hkv=1, D=4, density=1.0)
+    nnz = int(d["indptr"][-1])
+    bm = np.asarray(torch.rand((nnz, R, C), generator=torch.Generator().manual_seed(5)) < 0.5)
+    bm[:, 1, :] = False  # rows 1 and 4 see nothing
+    out, lse = att.bsr_attention(qb, kb, vb, "fp16", d["indptr"], d["indices"], M, N, R, C,
+                                 sm_scale=0.5, block_mask=bm)
+    q = nx.bits_to_f64(qb, "fp16"); k = nx.bits_to_f64(kb, "fp16"); v = nx.bits_to_f64(vb, "fp16")
+    ip, ix = d["indptr"], d["indices"]
+    for i in range(M):
+        for h in range(2):
+            keys = []
+            for e in range(int(ip[i // R]), int(ip[i // R + 1])):
+                for cc in range(C):
+                    if bm[e, i % R, cc]:
+                        keys.append(int(ix[e]) * C + cc)
+            if not keys:
+                assert (out[i, h] == 0).all() and math.isinf(lse[i, h]) and lse[i, h] < 0
+                continue
+            logits = [0.5 * sum(q[i, h, t] * k[j, 0, t] for t in range(4)) for j in keys]
+            mx = max(logits)
+            w = [math.exp(x - mx) for x in logits]
+            den = sum(w)
+            for t in range(4):
+                ref = sum(wi * v[j, 0, t] for wi, j in zip(w, keys)) / den
+                assert abs(out[i, h, t] - ref) <= 1e-12
+            assert abs(lse[i, h] - (mx + math.log(den))) <= 1e-12
+
+
+def test_packed_mask_bit_order_reading():
+    """The reading of packed_mask: entry t of the flattened (nnz, R, C) mask is bit t % 8 of
+    byte t // 8, which is numpy.packbits with bitorder='little'."""
+    g = np.random.default_rng(7)
+    m = g.random(77) < 0.5
+    packed = np.packbits(m, bitorder="little")
+    for t in range(77):
+        assert bool((packed[t // 8] >> (t % 8)) & 1) == m[t]

@@ -206,6 +206,17 @@ def test_mla_plan_rejects_bad_inputs(lib):
     _expect("ERR_UNSUPPORTED", f, [64], 1, 1, 256, 64, num_sms=2)    # heads > 128
 
 
+@pytest.mark.parametrize("M,N,R,C,Hq,Hkv,D", [(200, 256, 64, 64, 32, 8, 128), (64, 64, 16, 16, 4, 2, 64)])
+def test_bsr_masked_plan_bit_exact(lib, M, N, R, C, Hq, Hkv, D):
+    d = synth.bsr_inputs(95, M, N, R, C, Hq, Hkv, D, pattern="random", density=0.5,
+                         tensors=False)
+    p = bskv.bskv_plan_bsr_masked(d["indptr"], d["indices"], M, N, R, C, Hq, Hkv, D, num_sms=SMS)
+    meta = p.metadata()
+    assert meta == plan_ref.bsr_meta(d["indptr"].tolist(), d["indices"].tolist(), M, N, R, C,
+                                     Hq, Hkv, D, SMS)
+    assert plan_ref.sections(meta)["variant"] == (1 if R == 64 else 0)
+
+
 def test_mla_paged_plan_rejects_bad_inputs(lib):
     f = bskv.bskv_plan_mla_paged
     ok = dict(num_pages=4, page_size=16, num_heads=128, num_sms=4)
