@@ -400,6 +400,49 @@ def bench_bsr_masked(bskv, synth, steps, warmup, peaks):
                 mask_bytes=int(packed.numel()))
 
 
+def variable_block_flops(d):
+    """4 * head_dim * (query heads per kv head) * visible (query, key) pairs, over kv heads."""
+    bm = np.asarray(d["block_mask_map"], bool)
+    rs = np.asarray(d["block_row_sz"], np.int64)
+    cs = np.asarray(d["block_col_sz"], np.int64)
+    H, MB, NB = bm.shape
+    shift = d["kv_len"] - d["qo_len"]
+    pairs = 0
+    for h in range(H):
+        r0 = np.concatenate([[0], np.cumsum(rs[h])])
+        c0 = np.concatenate([[0], np.cumsum(cs[h])])
+        for a in range(MB):
+            rows = np.arange(r0[a], r0[a + 1])
+            for c in np.nonzero(bm[h, a])[0]:
+                if d["causal"]:
+                    pairs += int(np.clip(np.minimum(c0[c + 1], rows + shift + 1) - c0[c], 0,
+                                         c0[c + 1] - c0[c]).sum())
+                else:
+                    pairs += len(rows) * int(c0[c + 1] - c0[c])
+    g = d["num_qo_heads"] // d["num_kv_heads"]
+    return 4.0 * d["head_dim"] * g * pairs
+
+
+def bench_bsr_variable(bskv, synth, steps, warmup, peaks):
+    """Variable-block sparse attention: 16384 query and key tokens, 32/8 heads, head_dim 128,
+    fp16; every kv head cuts them into 128 x 128 blocks of its own random sizes and keeps
+    10 % of them, causal."""
+    d = synth.make("bsr_variable", device="cuda")
+    plan = bskv.bskv_plan_bsr_variable(d["block_mask_map"], d["block_row_sz"], d["block_col_sz"],
+                                       d["num_qo_heads"], d["num_kv_heads"], d["head_dim"],
+                                       causal=d["causal"], dtype=torch.float16)
+    plan.upload("cuda")
+    out = torch.empty_like(d["q"])
+    fn = lambda: bskv.bskv_run_bsr_variable(plan, d["q"], d["k"], d["v"], out=out)  # noqa
+    ms = time_iters(fn, steps, warmup, flush=True)
+    fl = variable_block_flops(d)
+    tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+    return dict(workload="bsr_variable: 16384 tokens, 32/8 heads, D 128, fp16, 128 x 128 "
+                         "blocks of random sizes per kv head, 10 % kept, causal (L2 flushed)",
+                flops=fl, kernel="general", **summary(ms), tflops=tf,
+                frac=tf / peaks["bf16_tflops"], peak="bf16 dense burst (fp16 rate equal)")
+
+
 def bench_mla(bskv, synth, steps, warmup, peaks):
     m = synth.make("mla_decode", device="cuda")
     B, H, K = m["batch"], m["heads"], m["top_k"]
@@ -558,7 +601,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of extra rows: bsr_prefill,bsr_tiny,bsr_masked,mla,mla_paged,mla_append,"
+                    help="comma list of extra rows: bsr_prefill,bsr_tiny,bsr_masked,bsr_variable,mla,mla_paged,"
+                         "mla_append,"
                          "split,e2e,cpu "
                          "or all/none")
     args = ap.parse_args()
@@ -571,8 +615,8 @@ def main():
     bskv.build()
     dist, rank, ws = dist_setup(args.gpus)
     peaks, peak_src = load_peaks()
-    rows = set(["bsr_prefill", "bsr_tiny", "bsr_masked", "mla", "mla_paged", "mla_append", "split",
-                "e2e", "cpu"]
+    rows = set(["bsr_prefill", "bsr_tiny", "bsr_masked", "bsr_variable", "mla", "mla_paged",
+                "mla_append", "split", "e2e", "cpu"]
                if args.rows == "all" else [] if args.rows == "none" else args.rows.split(","))
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -598,7 +642,9 @@ def main():
                 ("mla_append", "mla_append",
                  lambda: bench_mla_append(bskv, synth, K, args.warmup, peaks)),
                 ("bsr_masked", "bsr_masked",
-                 lambda: bench_bsr_masked(bskv, synth, K, args.warmup, peaks))]
+                 lambda: bench_bsr_masked(bskv, synth, K, args.warmup, peaks)),
+                ("bsr_variable", "bsr_variable",
+                 lambda: bench_bsr_variable(bskv, synth, K, args.warmup, peaks))]
         for key, name, job in jobs:
             if key in rows:
                 try:

@@ -59,6 +59,10 @@ _SIGS = {
                           _I32, ctypes.POINTER(_P)], _I32),
     "bskv_plan_bsr": ([_I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                        ctypes.POINTER(_P)], _I32),
+    "bskv_plan_bsr_variable": ([_P, _I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                _I32, ctypes.POINTER(_P)], _I32),
+    "bskv_run_bsr_variable": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P],
+                              _I32),
     "bskv_plan_bsr_masked": ([_I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                               ctypes.POINTER(_P)], _I32),
     "bskv_run_bsr_masked": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _SZ, _P, _I64P, _P, _F,
@@ -346,6 +350,46 @@ def bskv_run_bsr_masked(plan, q, k, v, packed_mask, out=None, lse=None, return_l
         _strides(k.stride(0), k.stride(1)), v.data_ptr(), _strides(v.stride(0), v.stride(1)),
         packed_mask.data_ptr(), packed_mask.numel(), out.data_ptr(),
         _strides(out.stride(0), out.stride(1)), _ptr(lse), float(sm_scale), _stream(q)))
+    return (out, lse) if return_lse else out
+
+
+def bskv_plan_bsr_variable(block_mask_map, block_row_sz, block_col_sz, num_qo_heads,
+                           num_kv_heads, head_dim, causal=False, dtype=torch.float16,
+                           num_sms=None):
+    """Variable-block plan: block_mask_map [Hkv, MB, NB] bool, block_row_sz [Hkv, MB],
+    block_col_sz [Hkv, NB] int (host copies are made)."""
+    lib = load_library()
+    bm = torch.as_tensor(block_mask_map).to(torch.uint8).contiguous().cpu()
+    rs, rsp = _i32_array(block_row_sz)
+    cs, csp = _i32_array(block_col_sz)
+    Hkv, MB, NB = bm.shape
+    h = ctypes.c_void_p()
+    ns = _num_sms() if num_sms is None else num_sms
+    _check("bskv_plan_bsr_variable", lib.bskv_plan_bsr_variable(
+        ctypes.c_void_p(bm.data_ptr()), ctypes.cast(rsp, _I32P), ctypes.cast(csp, _I32P), int(MB),
+        int(NB), int(num_qo_heads), int(num_kv_heads), int(head_dim), int(bool(causal)),
+        _DT[dtype], int(ns), ctypes.byref(h)))
+    return Plan(h.value, "bsr_variable", num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                head_dim=head_dim, dtype=dtype, qo_len=int(rs.view(Hkv, MB)[0].sum()))
+
+
+def bskv_run_bsr_variable(plan, q, k, v, out=None, lse=None, return_lse=False, sm_scale=None):
+    """q [Hq, qo_len, D], k/v [Hkv, kv_len, D] -> out [Hq, qo_len, D] (and lse [Hq, qo_len])."""
+    lib = load_library()
+    if plan.int_ws is None:
+        plan.upload(q.device)
+    Hq, L, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, L), dtype=torch.float32, device=q.device)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    _check("bskv_run_bsr_variable", lib.bskv_run_bsr_variable(
+        plan.handle, q.data_ptr(), _strides(q.stride(1), q.stride(0)), k.data_ptr(),
+        _strides(k.stride(1), k.stride(0)), v.data_ptr(), _strides(v.stride(1), v.stride(0)),
+        out.data_ptr(), _strides(out.stride(1), out.stride(0)), _ptr(lse), float(sm_scale),
+        _stream(q)))
     return (out, lse) if return_lse else out
 
 

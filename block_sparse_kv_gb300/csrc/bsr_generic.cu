@@ -34,6 +34,7 @@ struct BsrParams {
   void* out;
   int64_t o_s0, o_s1;
   float* lse;
+  int64_t lse_st, lse_sh;  // lse element strides of a token and of a head
   int M, N, R, C, Hq, Hkv, group, causal;
   // per-block token mask, bits packed little-endian within bytes over (nnz, R, C); NULL =
   // every listed block is full
@@ -44,7 +45,8 @@ struct BsrParams {
 
 constexpr int kKT = 16;  // key tokens per tile
 
-template <typename T, int D>
+// kVar: a variable-block plan (the unit's rows and key tiles come from the metadata lists).
+template <typename T, int D, bool kVar>
 __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
   constexpr int kRowBytes = D * 2;
   constexpr int kChunks = kRowBytes / 16;
@@ -63,13 +65,23 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
   for (int ui = wptr[blockIdx.x]; ui < wptr[blockIdx.x + 1]; ++ui) {
     const int4 un = units[ui];
     const int i = un.y, h = un.z, rt = un.w;
+    // The unit's query rows and key tiles: row block i of R rows and its listed column
+    // blocks, or (variable blocks) the lists of descriptor un.x.
+    int row0 = i * p.R, nrows = p.R, tb = 0, te = 0;
+    if constexpr (kVar) {
+      const int32_t* dsc = indptr + 4 * int64_t(un.x);
+      row0 = dsc[0];
+      nrows = dsc[1];
+      tb = dsc[2];
+      te = dsc[3];
+    }
     // This thread's two packed rows (mma rows r0 and r0 + 8 of the warp's 16).
     const int pr0 = rt * kBsrGenericRows + warp * 16 + (lane >> 2);
     const int pr1 = pr0 + 8;
-    const int tok0 = i * p.R + pr0 / g, tok1 = i * p.R + pr1 / g;
+    const int tok0 = row0 + pr0 / g, tok1 = row0 + pr1 / g;
     const int hd0 = h * g + pr0 % g, hd1 = h * g + pr1 % g;
-    const bool v0 = pr0 < p.R * g && tok0 < p.M;
-    const bool v1 = pr1 < p.R * g && tok1 < p.M;
+    const bool v0 = pr0 < nrows * g && tok0 < p.M;
+    const bool v1 = pr1 < nrows * g && tok1 < p.M;
     const T* qb = static_cast<const T*>(p.q);
     const int cq = lane & 3;
     uint32_t qa[D / 16][4];
@@ -88,12 +100,17 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    const int e0 = indptr[i], e1 = indptr[i + 1];
-    const int ntiles = (e1 - e0) * subtiles;
+    const int e0 = kVar ? 0 : indptr[i], e1 = kVar ? 0 : indptr[i + 1];
+    const int ntiles = kVar ? te - tb : (e1 - e0) * subtiles;
     // Stage tile n (block e0 + n / subtiles, sub-tile n % subtiles) into buffer `buf`.
     auto load = [&](int n, int buf) {
-      const int j = indices[e0 + n / subtiles];
-      const int kt0 = j * p.C + (n % subtiles) * kKT;
+      int kt0;
+      if constexpr (kVar) {
+        kt0 = indices[2 * (tb + n)];
+      } else {
+        const int j = indices[e0 + n / subtiles];
+        kt0 = j * p.C + (n % subtiles) * kKT;
+      }
       for (int c = threadIdx.x; c < kKT * kChunks; c += 128) {
         const int row = c / kChunks, ch = c % kChunks;
         const int tok = kt0 + row;
@@ -121,9 +138,10 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
       __syncthreads();
       const int buf = n & 1;
       const int eb = e0 + n / subtiles;  // the block's position in indices
-      const int j = indices[eb];
-      const int kt0 = j * p.C + (n % subtiles) * kKT;
-      const int kend = j * p.C + p.C;  // end of this column block
+      const int j = kVar ? 0 : indices[eb];
+      // first key of the tile and end of its column block (of its key range)
+      const int kt0 = kVar ? indices[2 * (tb + n)] : j * p.C + (n % subtiles) * kKT;
+      const int kend = kVar ? indices[2 * (tb + n) + 1] : j * p.C + p.C;
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       {
         const int mi = lane >> 3;
@@ -145,7 +163,7 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
           const int kt = kt0 + nt * 8 + 2 * cq + (e & 1);
           const int qt = (e < 2) ? tok0 : tok1;
           bool vis = kt < kend;
-          if (p.mask) {
+          if (!kVar && p.mask) {
             // bit (eb * R + row in block) * C + column in block; rows past M are never stored
             const int64_t bit = (int64_t(eb) * p.R + (qt - i * p.R)) * p.C + (kt - j * p.C);
             vis = vis && qt < p.M && ((__ldg(p.mask + (bit >> 3)) >> (bit & 7)) & 1);
@@ -220,8 +238,8 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
             Mma::pack(o[n][2] * inv1, o[n][3] * inv1);
     }
     if (p.lse && cq == 0) {
-      if (v0) p.lse[int64_t(tok0) * p.Hq + hd0] = lt0 > 0.f ? (m0 + __log2f(lt0)) * kLn2 : -INFINITY;
-      if (v1) p.lse[int64_t(tok1) * p.Hq + hd1] = lt1 > 0.f ? (m1 + __log2f(lt1)) * kLn2 : -INFINITY;
+      if (v0) p.lse[int64_t(tok0) * p.lse_st + int64_t(hd0) * p.lse_sh] = lt0 > 0.f ? (m0 + __log2f(lt0)) * kLn2 : -INFINITY;
+      if (v1) p.lse[int64_t(tok1) * p.lse_st + int64_t(hd1) * p.lse_sh] = lt1 > 0.f ? (m1 + __log2f(lt1)) * kLn2 : -INFINITY;
     }
   }
 }
@@ -243,6 +261,7 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
                     const void* k, const int64_t* k_strides, const void* v,
                     const int64_t* v_strides, void* out, const int64_t* out_strides, float* lse,
                     float sm_scale, const uint8_t* mask, void* stream) {
+  const bool var = plan && plan->kind == KIND_BSR && meta_word(plan, H_VARIANT) == BSR_VARIABLE;
   if (!plan || plan->kind != KIND_BSR) { set_error("run_bsr: not a BSR plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_bsr: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (!q_strides || !k_strides || !v_strides || !out_strides) { set_error("run_bsr: NULL strides"); return BSKV_ERR_INVALID_ARG; }
@@ -265,6 +284,9 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
   p.v = v; p.v_s0 = v_strides[0]; p.v_s1 = v_strides[1];
   p.out = out; p.o_s0 = out_strides[0]; p.o_s1 = out_strides[1];
   p.lse = lse;
+  // lse [M, Hq] for block-sparse plans, [Hq, M] (head-major) for variable-block plans
+  p.lse_st = var ? 1 : plan->num_qo_heads;
+  p.lse_sh = var ? plan->M : 1;
   p.M = plan->M; p.N = plan->N; p.R = plan->R; p.C = plan->C;
   p.Hq = plan->num_qo_heads; p.Hkv = plan->num_kv_heads; p.group = p.Hq / p.Hkv;
   p.causal = plan->causal;
@@ -274,12 +296,20 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
   const bool bf = plan->dtype == BSKV_BF16;
-  if (plan->head_dim == 128) {
-    if (bf) bsr_generic_kernel<__nv_bfloat16, 128><<<grid, 128, 0, st>>>(p);
-    else bsr_generic_kernel<__half, 128><<<grid, 128, 0, st>>>(p);
+  if (var) {
+    if (plan->head_dim == 128) {
+      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, true><<<grid, 128, 0, st>>>(p);
+      else bsr_generic_kernel<__half, 128, true><<<grid, 128, 0, st>>>(p);
+    } else {
+      if (bf) bsr_generic_kernel<__nv_bfloat16, 64, true><<<grid, 128, 0, st>>>(p);
+      else bsr_generic_kernel<__half, 64, true><<<grid, 128, 0, st>>>(p);
+    }
+  } else if (plan->head_dim == 128) {
+    if (bf) bsr_generic_kernel<__nv_bfloat16, 128, false><<<grid, 128, 0, st>>>(p);
+    else bsr_generic_kernel<__half, 128, false><<<grid, 128, 0, st>>>(p);
   } else {
-    if (bf) bsr_generic_kernel<__nv_bfloat16, 64><<<grid, 128, 0, st>>>(p);
-    else bsr_generic_kernel<__half, 64><<<grid, 128, 0, st>>>(p);
+    if (bf) bsr_generic_kernel<__nv_bfloat16, 64, false><<<grid, 128, 0, st>>>(p);
+    else bsr_generic_kernel<__half, 64, false><<<grid, 128, 0, st>>>(p);
   }
   return cuda_check(cudaGetLastError(), "bsr kernel launch");
 }
@@ -294,6 +324,7 @@ extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const 
   (void)float_ws;
   (void)float_ws_bytes;
   if (plan && plan->masked) { set_error("run_bsr: the plan expects a token mask (bskv_run_bsr_masked)"); return BSKV_ERR_INVALID_ARG; }
+  if (plan && plan->kind == KIND_BSR && meta_word(plan, H_VARIANT) == BSR_VARIABLE) { set_error("run_bsr: a variable-block plan runs through bskv_run_bsr_variable"); return BSKV_ERR_INVALID_ARG; }
   return run_bsr(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides, lse, sm_scale,
                  nullptr, stream);
 }
@@ -317,4 +348,19 @@ extern "C" bskv_status bskv_run_bsr_masked(const bskv_plan* plan, const void* q,
   if (reinterpret_cast<uintptr_t>(packed_mask) & 15) { set_error("run_bsr_masked: packed mask must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
   return run_bsr(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides, lse, sm_scale,
                  static_cast<const uint8_t*>(packed_mask), stream);
+}
+
+extern "C" bskv_status bskv_run_bsr_variable(const bskv_plan* plan, const void* q,
+                                             const int64_t* q_strides, const void* k,
+                                             const int64_t* k_strides, const void* v,
+                                             const int64_t* v_strides, void* out,
+                                             const int64_t* out_strides, float* lse,
+                                             float sm_scale, void* stream) {
+  if (!plan || plan->kind != KIND_BSR || !plan->meta.size() ||
+      plan->meta[H_VARIANT] != BSR_VARIABLE) {
+    set_error("run_bsr_variable: not a variable-block plan (bskv_plan_bsr_variable)");
+    return BSKV_ERR_INVALID_ARG;
+  }
+  return run_bsr(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides, lse, sm_scale,
+                 nullptr, stream);
 }

@@ -324,6 +324,125 @@ extern "C" bskv_status bskv_plan_bsr(const int32_t* indptr, const int32_t* indic
                   dtype, num_sms, false, out_plan);
 }
 
+extern "C" bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map,
+                                              const int32_t* block_row_sz,
+                                              const int32_t* block_col_sz, int32_t MB, int32_t NB,
+                                              int32_t num_qo_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t causal, int32_t dtype,
+                                              int32_t num_sms, bskv_plan** out_plan) {
+  if (!out_plan) { set_error("plan_bsr_variable: out_plan is NULL"); return BSKV_ERR_INVALID_ARG; }
+  *out_plan = nullptr;
+  if (MB < 1 || NB < 1 || num_sms < 1 || !block_mask_map || !block_row_sz || !block_col_sz) {
+    set_error("plan_bsr_variable: MB=%d NB=%d num_sms=%d or a NULL array", MB, NB, num_sms);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0) {
+    set_error("plan_bsr_variable: num_qo_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+              num_qo_heads, num_kv_heads);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (head_dim != 64 && head_dim != 128) { set_error("plan_bsr_variable: head_dim %d not in {64,128}", head_dim); return BSKV_ERR_UNSUPPORTED; }
+  if (dtype != BSKV_BF16 && dtype != BSKV_FP16) { set_error("plan_bsr_variable: dtype %s unsupported", dtype_name(dtype)); return BSKV_ERR_UNSUPPORTED; }
+  const int32_t H = num_kv_heads, g = num_qo_heads / num_kv_heads;
+  int64_t qo_len = -1, kv_len = -1;
+  for (int32_t h = 0; h < H; ++h) {
+    int64_t sr = 0, sc = 0;
+    for (int32_t a = 0; a < MB; ++a) {
+      const int32_t r = block_row_sz[int64_t(h) * MB + a];
+      if (r < 1) { set_error("plan_bsr_variable: block_row_sz[%d][%d] = %d must be positive", h, a, r); return BSKV_ERR_INVALID_ARG; }
+      sr += r;
+    }
+    for (int32_t c = 0; c < NB; ++c) {
+      const int32_t w = block_col_sz[int64_t(h) * NB + c];
+      if (w < 1) { set_error("plan_bsr_variable: block_col_sz[%d][%d] = %d must be positive", h, c, w); return BSKV_ERR_INVALID_ARG; }
+      sc += w;
+    }
+    if ((qo_len >= 0 && sr != qo_len) || (kv_len >= 0 && sc != kv_len)) {
+      set_error("plan_bsr_variable: kv head %d covers %lld query / %lld key tokens, head 0 %lld / %lld",
+                h, (long long)sr, (long long)sc, (long long)qo_len, (long long)kv_len);
+      return BSKV_ERR_INVALID_ARG;
+    }
+    qo_len = sr;
+    kv_len = sc;
+  }
+  if (qo_len > INT32_MAX / 2 || kv_len > INT32_MAX / 2 || qo_len * g > INT32_MAX / 2) { set_error("plan_bsr_variable: sequence too long"); return BSKV_ERR_UNSUPPORTED; }
+  // Per (kv head h, row block a): its query rows and the 16-token tiles of the key ranges it
+  // sees (adjacent selected column blocks merged into one range).
+  std::vector<int32_t> desc(size_t(H) * MB * 4), tiles;
+  std::vector<int32_t> cstart(static_cast<size_t>(NB));
+  for (int32_t h = 0; h < H; ++h) {
+    int32_t acc = 0;
+    for (int32_t c = 0; c < NB; ++c) { cstart[size_t(c)] = acc; acc += block_col_sz[int64_t(h) * NB + c]; }
+    int32_t row = 0;
+    for (int32_t a = 0; a < MB; ++a) {
+      const uint8_t* mrow = block_mask_map + (int64_t(h) * MB + a) * NB;
+      const size_t d = (size_t(h) * MB + a) * 4;
+      desc[d] = row;
+      desc[d + 1] = block_row_sz[int64_t(h) * MB + a];
+      desc[d + 2] = int32_t(tiles.size() / 2);
+      for (int32_t c = 0; c < NB;) {
+        if (!mrow[c]) { ++c; continue; }
+        const int32_t s0 = cstart[size_t(c)];
+        int32_t e = s0;
+        while (c < NB && mrow[c]) { e += block_col_sz[int64_t(h) * NB + c]; ++c; }
+        for (int32_t t = s0; t < e; t += kBsrVarTile) { tiles.push_back(t); tiles.push_back(e); }
+        if (tiles.size() > size_t(INT32_MAX) / 2) { set_error("plan_bsr_variable: too many key tiles"); return BSKV_ERR_UNSUPPORTED; }
+      }
+      desc[d + 3] = int32_t(tiles.size() / 2);
+      row += desc[d + 1];
+    }
+  }
+  // Units (h, a, row tile of 64 grouped rows), h-major; longest processing time first on at
+  // most 4 CTAs per SM, cost 1 + tiles.
+  std::vector<Chunk> units;
+  std::vector<int64_t> cost;
+  for (int32_t h = 0; h < H; ++h)
+    for (int32_t a = 0; a < MB; ++a) {
+      const size_t d = (size_t(h) * MB + a) * 4;
+      const int32_t rts = (desc[d + 1] * g + kBsrGenericRows - 1) / kBsrGenericRows;
+      for (int32_t rt = 0; rt < rts; ++rt) {
+        units.push_back(Chunk{h * MB + a, a, h, rt});
+        cost.push_back(1 + desc[d + 3] - desc[d + 2]);
+      }
+    }
+  const int64_t U = int64_t(units.size());
+  std::vector<int32_t> order(static_cast<size_t>(U));
+  for (int64_t u = 0; u < U; ++u) order[size_t(u)] = int32_t(u);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t x, int32_t y) { return cost[size_t(x)] > cost[size_t(y)]; });
+  const int32_t G = int32_t(std::min<int64_t>(int64_t(num_sms) * kBsrGenericCtasPerSm, std::max<int64_t>(U, 1)));
+  using Item = std::pair<int64_t, int32_t>;
+  std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+  for (int32_t c = 0; c < G; ++c) heap.push(Item(0, c));
+  std::vector<std::vector<int32_t>> lists(static_cast<size_t>(G));
+  for (int32_t u : order) {
+    Item it = heap.top();
+    heap.pop();
+    lists[size_t(it.second)].push_back(u);
+    it.first += cost[size_t(u)];
+    heap.push(it);
+  }
+  std::vector<int32_t> worker_ptr(size_t(G) + 1, 0);
+  std::vector<Chunk> chunks;
+  chunks.reserve(size_t(U));
+  for (int32_t c = 0; c < G; ++c) {
+    worker_ptr[size_t(c)] = int32_t(chunks.size());
+    for (int32_t u : lists[size_t(c)]) chunks.push_back(units[size_t(u)]);
+  }
+  worker_ptr[size_t(G)] = int32_t(chunks.size());
+  bskv_plan* p = new bskv_plan();
+  p->kind = KIND_BSR;
+  p->M = int32_t(qo_len); p->N = int32_t(kv_len); p->R = 0; p->C = 0; p->causal = causal ? 1 : 0;
+  p->num_qo_heads = num_qo_heads; p->num_kv_heads = num_kv_heads; p->head_dim = head_dim;
+  p->dtype = dtype;
+  std::vector<int32_t> no_merges;
+  assemble(p, KIND_BSR, int32_t(U), worker_ptr, chunks, 0, no_merges, kBsrGenericRows,
+           desc.data(), desc.size(), tiles.data(), tiles.size(), U > 0 ? G : 0, BSR_VARIABLE);
+  p->float_ws_bytes = 0;
+  *out_plan = p;
+  return BSKV_OK;
+}
+
 extern "C" bskv_status bskv_plan_bsr_masked(const int32_t* indptr, const int32_t* indices,
                                             int32_t M, int32_t N, int32_t R, int32_t C,
                                             int32_t num_qo_heads, int32_t num_kv_heads,

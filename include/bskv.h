@@ -138,6 +138,24 @@ bskv_status bskv_plan_bsr_masked(const int32_t* indptr, const int32_t* indices, 
                                  int32_t num_sms, bskv_plan** out_plan);
 
 /*
+ * Variable-block sparse attention plan ([SPARSE] VariableBlockSparseAttentionWrapper.plan:
+ * block sizes given by block_row_sz and block_col_sz, and each kv head with its own block
+ * mask; the query heads of a group share their kv head's pattern).
+ *   block_mask_map [num_kv_heads, MB, NB] (HOST bytes, nonzero = the block is visible),
+ *   block_row_sz [num_kv_heads, MB] and block_col_sz [num_kv_heads, NB] (HOST int32, all
+ *   positive): kv head h splits the qo_len query tokens into MB consecutive row blocks and the
+ *   kv_len keys into NB consecutive column blocks; every head must cover the same qo_len and
+ *   kv_len. Query token i of row block a sees key j of column block c of its kv head iff
+ *   block_mask_map[h][a][c] (and, when causal, j <= i + kv_len - qo_len).
+ *   head_dim 64 or 128; dtype BSKV_FP16 or BSKV_BF16; the general kernel serves these plans.
+ */
+bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map, const int32_t* block_row_sz,
+                                   const int32_t* block_col_sz, int32_t MB, int32_t NB,
+                                   int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t causal, int32_t dtype, int32_t num_sms,
+                                   bskv_plan** out_plan);
+
+/*
  * Sparse MLA FP8 decode plan ([MLA] get_batch_decode_metadata_mla(query, seq_lens,
  * sparse_mla_top_k): reusable while seq_lens, the query shape and top_k are unchanged).
  *   seq_lens[batch]: HOST int32 valid sparse lengths, 0 <= seq_lens[b] <= top_k.
@@ -292,6 +310,20 @@ bskv_status bskv_run_bsr_masked(const bskv_plan* plan, const void* q, const int6
                                 const int64_t* v_strides, const void* packed_mask,
                                 size_t packed_mask_bytes, void* out, const int64_t* out_strides,
                                 float* lse, float sm_scale, void* stream);
+
+/*
+ * Variable-block sparse attention ([SPARSE] VariableBlockSparseAttentionWrapper.run), for a
+ * plan of bskv_plan_bsr_variable:
+ *   q [num_qo_heads, qo_len, head_dim], k and v [num_kv_heads, kv_len, head_dim], out like
+ *   q; strides are given as {token, head} in elements (the pages' head-major tensors have
+ *   token stride head_dim and head stride len * head_dim); lse [num_qo_heads, qo_len]
+ *   float32 contiguous, or NULL. A token that sees no key gets out = 0 and lse = -inf.
+ */
+bskv_status bskv_run_bsr_variable(const bskv_plan* plan, const void* q, const int64_t* q_strides,
+                                  const void* k, const int64_t* k_strides, const void* v,
+                                  const int64_t* v_strides, void* out,
+                                  const int64_t* out_strides, float* lse, float sm_scale,
+                                  void* stream);
 
 /*
  * Sparse MLA FP8 decode ([MLA] sparse_mla_fp8_decode; [WRAP] scale folding):

@@ -22,6 +22,12 @@ Sources:
   * causal: plan() parameter "causal"; for M != N the mask is aligned bottom-right,
     key j visible to query i iff j <= i + (N - M) (FlashInfer cheat page, benchmark
     README flag --causal: multi-query decode uses bottom-right causal masking).
+  * Variable blocks: "flashinfer.sparse", VariableBlockSparseAttentionWrapper: plan(
+    block_mask_map (num_kv_heads, MB, NB), block_row_sz (num_kv_heads, MB), block_col_sz
+    (num_kv_heads, NB)); each kv head its own pattern, shared by its query heads; run(q
+    (num_qo_heads, qo_len, head_dim), k/v (num_kv_heads, kv_len, head_dim)) returns out of
+    q's shape and lse (num_qo_heads, qo_len). Reading: blocks are consecutive in the order
+    given, and causal keeps key j for query i iff j <= i + (kv_len - qo_len).
   * Paged KV: "FlashInfer" agent-skill summary, KV-Cache Formats / Paged KV-Cache:
     kv_cache (num_pages, 2, num_kv_heads, page_size, head_dim), kv_indptr (batch+1,),
     kv_indices, kv_last_page_len (batch,). Reading: request b owns pages
@@ -134,6 +140,60 @@ def bsr_attention(q_bits, k_bits, v_bits, dtype, indptr, indices, M, N, R, C,
     k = bits_to_f64(k_bits, dtype)
     v = bits_to_f64(v_bits, dtype)
     return masked_attention(q[rows_idx], k, v, sm_scale, mask)
+
+
+# ---------------------------------------------------------------------------------------
+# Variable-block sparse attention
+# ---------------------------------------------------------------------------------------
+
+def variable_block_mask(block_mask_map, block_row_sz, block_col_sz, causal=False):
+    """Dense boolean masks [Hkv, qo_len, kv_len]: kv head h cuts the query tokens into
+    consecutive row blocks of block_row_sz[h] tokens and the keys into consecutive column
+    blocks of block_col_sz[h]; block (a, c) is visible iff block_mask_map[h, a, c]."""
+    bm = np.asarray(block_mask_map, dtype=bool)
+    rs = np.asarray(block_row_sz, dtype=np.int64)
+    cs = np.asarray(block_col_sz, dtype=np.int64)
+    H, MB, NB = bm.shape
+    qo, kv = int(rs[0].sum()), int(cs[0].sum())
+    out = np.zeros((H, qo, kv), dtype=bool)
+    for h in range(H):
+        if rs[h].sum() != qo or cs[h].sum() != kv:
+            raise ValueError("every kv head must cover the same lengths")
+        r0 = np.concatenate([[0], np.cumsum(rs[h])])
+        c0 = np.concatenate([[0], np.cumsum(cs[h])])
+        for a in range(MB):
+            for c in range(NB):
+                if bm[h, a, c]:
+                    out[h, r0[a]:r0[a + 1], c0[c]:c0[c + 1]] = True
+    if causal:
+        i = np.arange(qo)[:, None]
+        j = np.arange(kv)[None, :]
+        out &= (j <= i + (kv - qo))[None]
+    return out
+
+
+def variable_block_attention(q_bits, k_bits, v_bits, dtype, block_mask_map, block_row_sz,
+                             block_col_sz, sm_scale=None, causal=False):
+    """Variable-block sparse attention from stored 16-bit inputs, head-major as on the page:
+    q [Hq, qo_len, D], k/v [Hkv, kv_len, D]. Returns out [Hq, qo_len, D] and lse [Hq, qo_len];
+    query head hq uses kv head hq // (Hq / Hkv) and that head's mask."""
+    q = bits_to_f64(q_bits, dtype)
+    k = bits_to_f64(k_bits, dtype)
+    v = bits_to_f64(v_bits, dtype)
+    Hq, L, D = q.shape
+    Hkv = k.shape[0]
+    g = Hq // Hkv
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    masks = variable_block_mask(block_mask_map, block_row_sz, block_col_sz, causal)
+    out = np.zeros((Hq, L, v.shape[-1]))
+    lse = np.zeros((Hq, L))
+    for h in range(Hkv):
+        qg = q[h * g:(h + 1) * g].transpose(1, 0, 2)           # [L, g, D]
+        o, l = masked_attention(qg, k[h][:, None, :], v[h][:, None, :], sm_scale, masks[h])
+        out[h * g:(h + 1) * g] = o.transpose(1, 0, 2)
+        lse[h * g:(h + 1) * g] = l.T
+    return out, lse
 
 
 # ---------------------------------------------------------------------------------------

@@ -32,6 +32,13 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
   * MLA: units = query tokens n = b*q_len + t, len = seq_lens[b], tile 128,
     max_workers = max(1, num_sms // 2) (a worker is a pair of CTAs, one per latent half),
     grid = 2 P, no aux, variant 0.
+  * variable-block BSR (variant 2): per kv head h and row block a, in that order, a
+    descriptor (first query token, row count, first tile, end tile); the tiles split each
+    maximal run of consecutive visible column blocks [s, e) into (t, e) for t = s, s + 16,
+    ... < e. Units (h, a, row tile of 64 grouped rows) h-major, chunk (h*MB + a, a, h, rt);
+    cost 1 + tiles, the same longest-processing-time rule on at most 4 * num_sms CTAs
+    (max(units, 1) when smaller); grid = CTAs, 0 without units; aux0 = descriptors,
+    aux1 = tiles, tile field 64.
   * paged MLA: one unit per request, len = its length from the page table (as for
     decode), tile 128, max_workers = max(1, num_sms // 2), grid = 2 P, aux0 = kv_indptr,
     aux1 = kv_indices, variant 1.
@@ -210,6 +217,62 @@ def bsr_meta(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, 
     nnz = int(indptr[MB])
     return _assemble(2, U, wp, ch, 0, [], rows, [int(x) for x in indptr[:MB + 1]],
                      [int(x) for x in indices[:nnz]], G, 1 if tc else 0)
+
+
+def bsr_variable_meta(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, num_kv_heads,
+                      num_sms):
+    H = num_kv_heads
+    g = num_qo_heads // num_kv_heads
+    MB = len(block_row_sz[0])
+    NB = len(block_col_sz[0])
+    desc, tiles = [], []
+    for h in range(H):
+        cstart, acc = [], 0
+        for c in range(NB):
+            cstart.append(acc)
+            acc += int(block_col_sz[h][c])
+        row = 0
+        for a in range(MB):
+            nrow = int(block_row_sz[h][a])
+            tb = len(tiles) // 2
+            c = 0
+            while c < NB:
+                if not block_mask_map[h][a][c]:
+                    c += 1
+                    continue
+                s0 = cstart[c]
+                e = s0
+                while c < NB and block_mask_map[h][a][c]:
+                    e += int(block_col_sz[h][c])
+                    c += 1
+                for t in range(s0, e, 16):
+                    tiles += [t, e]
+            desc += [row, nrow, tb, len(tiles) // 2]
+            row += nrow
+    units, cost = [], []
+    for h in range(H):
+        for a in range(MB):
+            d = (h * MB + a) * 4
+            for rt in range((desc[d + 1] * g + 63) // 64):
+                units.append([h * MB + a, a, h, rt])
+                cost.append(1 + desc[d + 3] - desc[d + 2])
+    U = len(units)
+    order = sorted(range(U), key=lambda u: -cost[u])
+    G = min(4 * num_sms, max(U, 1))
+    heap = [(0, c) for c in range(G)]
+    heapq.heapify(heap)
+    lists = [[] for _ in range(G)]
+    for u in order:
+        load, c = heapq.heappop(heap)
+        lists[c].append(u)
+        heapq.heappush(heap, (load + cost[u], c))
+    wp, ch = [], []
+    for c in range(G):
+        wp.append(len(ch))
+        for u in lists[c]:
+            ch.append(units[u])
+    wp.append(len(ch))
+    return _assemble(2, U, wp, ch, 0, [], 64, desc, tiles, G if U > 0 else 0, 2)
 
 
 def sections(meta):

@@ -10,6 +10,7 @@ stored values.
 
 from .gen import (  # noqa: F401
     bsr_inputs,
+    variable_block_inputs,
     paged_decode_inputs,
     mla_inputs,
     mla_paged_inputs,

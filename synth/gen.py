@@ -219,6 +219,40 @@ def mla_inputs(seed, batch, heads, top_k, pool_rows, ctx_lo, ctx_hi, q_len=1,
                 max_seq_len=max_seq_len, seed=seed)
 
 
+def variable_block_inputs(seed, num_qo_heads, num_kv_heads, head_dim, MB, NB, qo_len, kv_len,
+                          density=0.5, dtype=torch.float16, causal=False, empty_row_block=None,
+                          device="cpu"):
+    """Variable-block sparse attention inputs (head-major tensors, as on the page).
+
+    Every kv head cuts qo_len query tokens into MB and kv_len keys into NB consecutive blocks
+    of random positive sizes (a fresh cut per head) and keeps each block with probability
+    ``density`` (``empty_row_block``: that row block of every head keeps none).
+    q [Hq, qo_len, D], k/v [Hkv, kv_len, D] ~ N(0,1) cast to ``dtype``.
+    """
+    g = _cpu_gen(seed)
+    H = num_kv_heads
+
+    def parts(total, n):
+        out = []
+        for _ in range(H):
+            cuts = sorted((torch.randperm(total - 1, generator=g)[:n - 1] + 1).tolist())
+            out.append([b - a for a, b in zip([0] + cuts, cuts + [total])])
+        return torch.tensor(out, dtype=torch.int32)
+
+    row_sz = parts(qo_len, MB)
+    col_sz = parts(kv_len, NB)
+    bm = torch.rand((H, MB, NB), generator=g) < density
+    if empty_row_block is not None:
+        bm[:, empty_row_block, :] = False
+    dg = _dev_gen(seed, device)
+    q = _randn((num_qo_heads, qo_len, head_dim), dtype, dg, device)
+    k = _randn((H, kv_len, head_dim), dtype, dg, device)
+    v = _randn((H, kv_len, head_dim), dtype, dg, device)
+    return dict(q=q, k=k, v=v, block_mask_map=bm, block_row_sz=row_sz, block_col_sz=col_sz,
+                num_qo_heads=num_qo_heads, num_kv_heads=H, head_dim=head_dim, MB=MB, NB=NB,
+                qo_len=qo_len, kv_len=kv_len, causal=causal, dtype=dtype, seed=seed)
+
+
 E4M3_NAN = 0x7F  # canary code for cache slots no request may read
 
 
@@ -330,6 +364,9 @@ CONFIGS = {
                          dtype=torch.bfloat16),
     "mla_paged": dict(kind="mla_paged", seed=1005, batch=128, heads=128, page_size=64,
                       len_lo=2048, len_hi=8192),
+    "bsr_variable": dict(kind="bsr_variable", seed=1007, num_qo_heads=32, num_kv_heads=8,
+                         head_dim=128, MB=128, NB=128, qo_len=16384, kv_len=16384,
+                         density=0.1, dtype=torch.float16, causal=True),
     "mla_append": dict(kind="mla_append", seed=1006, batch=128, page_size=64, len_lo=2048,
                        len_hi=8192, new_tokens=512),
 }
@@ -348,6 +385,8 @@ def make(name, device="cpu", **overrides):
         return mla_inputs(device=device, **cfg)
     if kind == "mla_paged":
         return mla_paged_inputs(device=device, **cfg)
+    if kind == "bsr_variable":
+        return variable_block_inputs(device=device, **cfg)
     if kind == "mla_append":
         return mla_append_inputs(device=device, **cfg)
     raise ValueError(kind)

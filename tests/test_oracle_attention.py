@@ -420,3 +420,70 @@ def test_packed_mask_bit_order_reading():
     packed = np.packbits(m, bitorder="little")
     for t in range(77):
         assert bool((packed[t // 8] >> (t % 8)) & 1) == m[t]
+
+
+# ---------------------------------------------------------------------------------------
+# variable-block sparse attention
+# ---------------------------------------------------------------------------------------
+
+def test_variable_block_page_example_mask_and_result():
+    ex = json.load(open(os.path.join(HERE, "golden", "variable_block_example.json")))
+    m = att.variable_block_mask(ex["block_mask_map"], ex["block_row_sz"], ex["block_col_sz"])
+    np.testing.assert_array_equal(m[0], np.array(ex["dense_mask"], bool))
+    g = torch.Generator().manual_seed(9)
+    L, D = ex["seq_len"], 16
+    q = torch.randn((1, L, D), generator=g).to(torch.float16)
+    k = torch.randn((1, L, D), generator=g).to(torch.float16)
+    v = torch.randn((1, L, D), generator=g).to(torch.float16)
+    out, lse = att.variable_block_attention(_bits(q), _bits(k), _bits(v), "fp16",
+                                            ex["block_mask_map"], ex["block_row_sz"],
+                                            ex["block_col_sz"])
+    qd = nx.bits_to_f64(_bits(q), "fp16")[0][:, None, :]
+    kd = nx.bits_to_f64(_bits(k), "fp16")[0][:, None, :]
+    vd = nx.bits_to_f64(_bits(v), "fp16")[0][:, None, :]
+    ref = _sdpa(qd, kd, vd, 1 / math.sqrt(D), mask=np.array(ex["dense_mask"], bool))
+    np.testing.assert_allclose(out[0], ref[:, 0, :], rtol=1e-12, atol=1e-14)
+
+
+def test_variable_blocks_of_equal_size_are_bsr():
+    """Uniform sizes R x C with the same map for every kv head give BSR attention."""
+    M, N, R, C, Hq, Hkv, D = 24, 32, 4, 8, 4, 2, 16
+    d = synth.bsr_inputs(71, M, N, R, C, Hq, Hkv, D, pattern="random", density=0.5)
+    MB, NB = M // R, N // C
+    bm = np.zeros((MB, NB), bool)
+    ip, ix = d["indptr"].numpy(), d["indices"].numpy()
+    for a in range(MB):
+        bm[a, ix[ip[a]:ip[a + 1]]] = True
+    qh = d["q"].permute(1, 0, 2).contiguous()
+    kh = d["k"].permute(1, 0, 2).contiguous()
+    vh = d["v"].permute(1, 0, 2).contiguous()
+    for causal in (False, True):
+        out, lse = att.variable_block_attention(
+            _bits(qh), _bits(kh), _bits(vh), "fp16", np.stack([bm] * Hkv), [[R] * MB] * Hkv,
+            [[C] * NB] * Hkv, causal=causal)
+        ref, ref_lse = att.bsr_attention(_bits(d["q"]), _bits(d["k"]), _bits(d["v"]), "fp16", ip,
+                                         ix, M, N, R, C, causal=causal)
+        np.testing.assert_allclose(out.transpose(1, 0, 2), ref, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse.T, ref_lse, rtol=1e-12)
+
+
+def test_variable_block_heads_follow_their_kv_head():
+    """Query heads 0-1 use kv head 0's map and sizes, heads 2-3 kv head 1's: each pair equals
+    a one-kv-head computation with that head's pattern alone."""
+    g = torch.Generator().manual_seed(11)
+    L, Lk, D = 10, 12, 8
+    q = torch.randn((4, L, D), generator=g).to(torch.float16)
+    k = torch.randn((2, Lk, D), generator=g).to(torch.float16)
+    v = torch.randn((2, Lk, D), generator=g).to(torch.float16)
+    bmap = [[[1, 0, 1], [0, 1, 0]], [[0, 1, 1], [1, 1, 0]]]
+    rsz = [[4, 6], [7, 3]]
+    csz = [[5, 4, 3], [2, 2, 8]]
+    out, lse = att.variable_block_attention(_bits(q), _bits(k), _bits(v), "fp16", bmap, rsz, csz)
+    for h in range(2):
+        o1, l1 = att.variable_block_attention(_bits(q[2 * h:2 * h + 2]), _bits(k[h:h + 1]),
+                                              _bits(v[h:h + 1]), "fp16", [bmap[h]], [rsz[h]],
+                                              [csz[h]])
+        np.testing.assert_array_equal(out[2 * h:2 * h + 2], o1)
+        np.testing.assert_array_equal(lse[2 * h:2 * h + 2], l1)
+    m = att.variable_block_mask(bmap, rsz, csz)
+    assert m[1, 0, :].tolist() == [False] * 2 + [True] * 10   # row block 0 of head 1: cols 1, 2

@@ -239,3 +239,35 @@ def test_run_without_upload_is_rejected(lib):
     code = lib_.bskv_run_bsr(p.handle, 16, s, 16, s, 16, s, 16, s, None, 1.0, None, 0, None)
     assert bskv.STATUS[code] == "ERR_INVALID_ARG"
     assert "not uploaded" in bskv.bskv_last_error_message()
+
+
+@pytest.mark.parametrize("seed,H,MB,NB", [(1, 2, 3, 4), (2, 8, 16, 16), (3, 1, 1, 1)])
+def test_bsr_variable_plan_bit_exact(lib, seed, H, MB, NB):
+    g = torch.Generator().manual_seed(seed)
+    bm = (torch.rand((H, MB, NB), generator=g) < 0.5).to(torch.uint8)
+
+    def parts(total, n):  # n positive sizes summing to total, a fresh cut per kv head
+        out = []
+        for _ in range(H):
+            cuts = sorted((torch.randperm(total - 1, generator=g)[:n - 1] + 1).tolist())
+            out.append([b - a for a, b in zip([0] + cuts, cuts + [total])])
+        return torch.tensor(out, dtype=torch.int32)
+
+    rs = parts(50 * MB, MB)
+    cs = parts(40 * NB, NB)
+    p = bskv.bskv_plan_bsr_variable(bm, rs, cs, 2 * H, H, 128, num_sms=SMS)
+    meta = p.metadata()
+    assert meta == plan_ref.bsr_variable_meta(bm.tolist(), rs.tolist(), cs.tolist(), 2 * H, H, SMS)
+    s = plan_ref.sections(meta)
+    assert s["variant"] == 2
+
+
+def test_bsr_variable_plan_rejects_bad_inputs(lib):
+    f = bskv.bskv_plan_bsr_variable
+    bm = torch.ones((2, 2, 2), dtype=torch.uint8)
+    f(bm, [[1, 2], [2, 1]], [[3, 1], [2, 2]], 2, 2, 64, num_sms=2)  # valid
+    _expect("ERR_INVALID_ARG", f, bm, [[1, 2], [2, 2]], [[3, 1], [2, 2]], 2, 2, 64, num_sms=2)  # qo lengths differ
+    _expect("ERR_INVALID_ARG", f, bm, [[1, 2], [2, 1]], [[3, 1], [2, 3]], 2, 2, 64, num_sms=2)  # kv lengths differ
+    _expect("ERR_INVALID_ARG", f, bm, [[0, 3], [2, 1]], [[3, 1], [2, 2]], 2, 2, 64, num_sms=2)  # empty block
+    _expect("ERR_INVALID_ARG", f, bm, [[1, 2], [2, 1]], [[3, 1], [2, 2]], 3, 2, 64, num_sms=2)  # heads
+    _expect("ERR_UNSUPPORTED", f, bm, [[1, 2], [2, 1]], [[3, 1], [2, 2]], 2, 2, 96, num_sms=2)  # head_dim
