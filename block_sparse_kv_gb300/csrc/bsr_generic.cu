@@ -7,9 +7,10 @@
 //
 // Design: persistent CTAs of 4 warps; each unit is (row block i, kv head h, 64-row tile),
 // its 64 rows being the (token, query head) pairs of row block i that share kv head h, so
-// every K/V tile loaded serves all grouped heads. K/V tiles of 16 tokens are staged with
-// cp.async into a double-buffered, XOR-swizzled shared-memory tile and consumed by
-// mma.sync m16n8k16 (fp32 accumulate) with an online softmax, FlashAttention-2 style.
+// every K/V tile loaded serves all grouped heads. K/V tiles of 32 tokens (16 for blocks of at
+// most 16 columns) are staged with cp.async into a double-buffered, XOR-swizzled
+// shared-memory tile and consumed by mma.sync m16n8k16 (fp32 accumulate) with an online
+// softmax, FlashAttention-2 style.
 // The tensor-core (tcgen05) kernel covers the large R = C = 64 shapes; this one covers
 // everything else.
 #include <math.h>
@@ -43,11 +44,14 @@ struct BsrParams {
   StatusArgs st;
 };
 
-constexpr int kKT = 16;  // key tokens per tile
+// Key tokens per tile (KT): 32, two 16-key sub-blocks per online-softmax update, or 16 for
+// blocks of at most 16 columns (a 32-key tile would be half empty there).
+static_assert(kBsrVarTile == 32, "variable-block plans list 32-key tiles");
 
 // kVar: a variable-block plan (the unit's rows and key tiles come from the metadata lists).
-template <typename T, int D, bool kVar>
+template <typename T, int D, bool kVar, int kKT>
 __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
+  constexpr int kSub = kKT / 16;
   constexpr int kRowBytes = D * 2;
   constexpr int kChunks = kRowBytes / 16;
   constexpr int kTileBytes = kKT * kRowBytes;
@@ -142,22 +146,27 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
       // first key of the tile and end of its column block (of its key range)
       const int kt0 = kVar ? indices[2 * (tb + n)] : j * p.C + (n % subtiles) * kKT;
       const int kend = kVar ? indices[2 * (tb + n) + 1] : j * p.C + p.C;
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float s[2 * kSub][4];
+#pragma unroll
+      for (int nt = 0; nt < 2 * kSub; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
       {
         const int mi = lane >> 3;
-        const int trow = (mi >> 1) * 8 + (lane & 7);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int ch = kk * 2 + (mi & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(smem_u32(&sm[buf][0][0]) + swz(trow, ch, kRowBytes), b0, b1, b2, b3);
-          Mma::run(s[0], qa[kk], b0, b1);
-          Mma::run(s[1], qa[kk], b2, b3);
+        for (int sb = 0; sb < kSub; ++sb) {
+          const int trow = sb * 16 + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int ch = kk * 2 + (mi & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(smem_u32(&sm[buf][0][0]) + swz(trow, ch, kRowBytes), b0, b1, b2, b3);
+            Mma::run(s[2 * sb], qa[kk], b0, b1);
+            Mma::run(s[2 * sb + 1], qa[kk], b2, b3);
+          }
         }
       }
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < 2 * kSub; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int kt = kt0 + nt * 8 + 2 * cq + (e & 1);
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
       m1 = mn1;
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < 2 * kSub; ++nt) {
         s[nt][0] = fast_exp2(s[nt][0] - ref0);
         s[nt][1] = fast_exp2(s[nt][1] - ref0);
         s[nt][2] = fast_exp2(s[nt][2] - ref1);
@@ -205,11 +214,14 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
         o[nn][2] *= a1;
         o[nn][3] *= a1;
       }
-      uint32_t pa[4] = {Mma::pack(s[0][0], s[0][1]), Mma::pack(s[0][2], s[0][3]),
-                        Mma::pack(s[1][0], s[1][1]), Mma::pack(s[1][2], s[1][3])};
-      {
+#pragma unroll
+      for (int sb = 0; sb < kSub; ++sb) {
+        uint32_t pa[4] = {Mma::pack(s[2 * sb][0], s[2 * sb][1]),
+                          Mma::pack(s[2 * sb][2], s[2 * sb][3]),
+                          Mma::pack(s[2 * sb + 1][0], s[2 * sb + 1][1]),
+                          Mma::pack(s[2 * sb + 1][2], s[2 * sb + 1][3])};
         const int mi = lane >> 3;
-        const int trow = (mi & 1) * 8 + (lane & 7);
+        const int trow = sb * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
         for (int dd = 0; dd < D / 16; ++dd) {
           const int ch = dd * 2 + (mi >> 1);
@@ -296,20 +308,29 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
   const bool bf = plan->dtype == BSKV_BF16;
+  const bool narrow = !var && plan->C <= 16;  // 16-key tiles
   if (var) {
     if (plan->head_dim == 128) {
-      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, true><<<grid, 128, 0, st>>>(p);
-      else bsr_generic_kernel<__half, 128, true><<<grid, 128, 0, st>>>(p);
+      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, true, 32><<<grid, 128, 0, st>>>(p);
+      else bsr_generic_kernel<__half, 128, true, 32><<<grid, 128, 0, st>>>(p);
     } else {
-      if (bf) bsr_generic_kernel<__nv_bfloat16, 64, true><<<grid, 128, 0, st>>>(p);
-      else bsr_generic_kernel<__half, 64, true><<<grid, 128, 0, st>>>(p);
+      if (bf) bsr_generic_kernel<__nv_bfloat16, 64, true, 32><<<grid, 128, 0, st>>>(p);
+      else bsr_generic_kernel<__half, 64, true, 32><<<grid, 128, 0, st>>>(p);
     }
   } else if (plan->head_dim == 128) {
-    if (bf) bsr_generic_kernel<__nv_bfloat16, 128, false><<<grid, 128, 0, st>>>(p);
-    else bsr_generic_kernel<__half, 128, false><<<grid, 128, 0, st>>>(p);
+    if (narrow) {
+      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, false, 16><<<grid, 128, 0, st>>>(p);
+      else bsr_generic_kernel<__half, 128, false, 16><<<grid, 128, 0, st>>>(p);
+    } else {
+      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, false, 32><<<grid, 128, 0, st>>>(p);
+      else bsr_generic_kernel<__half, 128, false, 32><<<grid, 128, 0, st>>>(p);
+    }
+  } else if (narrow) {
+    if (bf) bsr_generic_kernel<__nv_bfloat16, 64, false, 16><<<grid, 128, 0, st>>>(p);
+    else bsr_generic_kernel<__half, 64, false, 16><<<grid, 128, 0, st>>>(p);
   } else {
-    if (bf) bsr_generic_kernel<__nv_bfloat16, 64, false><<<grid, 128, 0, st>>>(p);
-    else bsr_generic_kernel<__half, 64, false><<<grid, 128, 0, st>>>(p);
+    if (bf) bsr_generic_kernel<__nv_bfloat16, 64, false, 32><<<grid, 128, 0, st>>>(p);
+    else bsr_generic_kernel<__half, 64, false, 32><<<grid, 128, 0, st>>>(p);
   }
   return cuda_check(cudaGetLastError(), "bsr kernel launch");
 }

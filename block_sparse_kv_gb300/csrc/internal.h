@@ -50,10 +50,10 @@ constexpr int kDecodeGroupMaxPage = 16; // largest page_size that takes the page
 constexpr int kFusedMergeMaxPieces = 8;
 
 // BSR_VARIABLE: per-kv-head variable block sizes; the general kernel walks, per unit, the
-// query row range and the 16-token key tiles listed in the metadata (aux0: per (kv head,
+// query row range and the 32-token key tiles listed in the metadata (aux0: per (kv head,
 // row block) {row start, row count, first tile, end tile}; aux1: tiles {key start, range end}).
 enum BsrVariant : int32_t { BSR_GENERIC = 0, BSR_TCGEN05 = 1, BSR_VARIABLE = 2 };
-constexpr int kBsrVarTile = 16;  // key tokens per tile of a variable-block plan
+constexpr int kBsrVarTile = 32;  // key tokens per tile of a variable-block plan
 // MLA_SPARSE: row lists given by the caller. MLA_PAGED: row lists expanded on the device
 // from the page table in the metadata (aux0 = kv_indptr, aux1 = kv_indices).
 enum MlaVariant : int32_t { MLA_SPARSE = 0, MLA_PAGED = 1 };

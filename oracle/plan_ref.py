@@ -34,7 +34,7 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
     grid = 2 P, no aux, variant 0.
   * variable-block BSR (variant 2): per kv head h and row block a, in that order, a
     descriptor (first query token, row count, first tile, end tile); the tiles split each
-    maximal run of consecutive visible column blocks [s, e) into (t, e) for t = s, s + 16,
+    maximal run of consecutive visible column blocks [s, e) into (t, e) for t = s, s + 32,
     ... < e. Units (h, a, row tile of 64 grouped rows) h-major, chunk (h*MB + a, a, h, rt);
     cost 1 + tiles, the same longest-processing-time rule on at most 4 * num_sms CTAs
     (max(units, 1) when smaller); grid = CTAs, 0 without units; aux0 = descriptors,
@@ -245,7 +245,7 @@ def bsr_variable_meta(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, 
                 while c < NB and block_mask_map[h][a][c]:
                     e += int(block_col_sz[h][c])
                     c += 1
-                for t in range(s0, e, 16):
+                for t in range(s0, e, 32):
                     tiles += [t, e]
             desc += [row, nrow, tb, len(tiles) // 2]
             row += nrow
