@@ -443,6 +443,29 @@ def bench_bsr_variable(bskv, synth, steps, warmup, peaks):
                 frac=tf / peaks["bf16_tflops"], peak="bf16 dense burst (fp16 rate equal)")
 
 
+def bench_prefill_paged(bskv, synth, steps, warmup, peaks):
+    """Batch prefill over the paged cache: 16 requests of 2048-8192 tokens whose last 1024
+    tokens are the queries (causal, bottom-right), 32/8 heads, head_dim 128, bf16, page 16."""
+    d = synth.make("prefill_paged", device="cuda")
+    plan = bskv.bskv_plan_prefill_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                                        d["kv_last_page_len"], d["num_pages"], d["page_size"],
+                                        d["num_qo_heads"], d["num_kv_heads"], d["head_dim"],
+                                        causal=True, dtype=torch.bfloat16)
+    plan.upload("cuda")
+    out = torch.empty_like(d["q"])
+    fn = lambda: bskv.bskv_run_prefill_paged(plan, d["q"], d["kv_cache"], out=out)  # noqa
+    ms = time_iters(fn, steps, warmup, flush=True)
+    pairs = 0
+    for L, nq in zip(d["kv_lens"].tolist(), d["qo_lens"].tolist()):
+        pairs += sum(min(L, t + L - nq + 1) for t in range(nq))
+    fl = 4.0 * d["head_dim"] * d["num_qo_heads"] * pairs
+    tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+    return dict(workload="prefill_paged: 16 requests, L ~ U[2048,8192], 1024 new tokens each, "
+                         "32/8 heads, D 128, bf16, page 16, causal (L2 flushed)",
+                flops=fl, kernel="general", **summary(ms), tflops=tf,
+                frac=tf / peaks["bf16_tflops"], peak="bf16 dense burst")
+
+
 def bench_mla(bskv, synth, steps, warmup, peaks):
     m = synth.make("mla_decode", device="cuda")
     B, H, K = m["batch"], m["heads"], m["top_k"]
@@ -601,7 +624,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of extra rows: bsr_prefill,bsr_tiny,bsr_masked,bsr_variable,mla,mla_paged,"
+                    help="comma list of extra rows: bsr_prefill,bsr_tiny,bsr_masked,bsr_variable,prefill_paged,"
+                         "mla,mla_paged,"
                          "mla_append,"
                          "split,e2e,cpu "
                          "or all/none")
@@ -615,8 +639,8 @@ def main():
     bskv.build()
     dist, rank, ws = dist_setup(args.gpus)
     peaks, peak_src = load_peaks()
-    rows = set(["bsr_prefill", "bsr_tiny", "bsr_masked", "bsr_variable", "mla", "mla_paged",
-                "mla_append", "split", "e2e", "cpu"]
+    rows = set(["bsr_prefill", "bsr_tiny", "bsr_masked", "bsr_variable", "prefill_paged", "mla",
+                "mla_paged", "mla_append", "split", "e2e", "cpu"]
                if args.rows == "all" else [] if args.rows == "none" else args.rows.split(","))
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -644,7 +668,9 @@ def main():
                 ("bsr_masked", "bsr_masked",
                  lambda: bench_bsr_masked(bskv, synth, K, args.warmup, peaks)),
                 ("bsr_variable", "bsr_variable",
-                 lambda: bench_bsr_variable(bskv, synth, K, args.warmup, peaks))]
+                 lambda: bench_bsr_variable(bskv, synth, K, args.warmup, peaks)),
+                ("prefill_paged", "prefill_paged",
+                 lambda: bench_prefill_paged(bskv, synth, K, args.warmup, peaks))]
         for key, name, job in jobs:
             if key in rows:
                 try:

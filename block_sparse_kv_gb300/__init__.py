@@ -59,6 +59,9 @@ _SIGS = {
                           _I32, ctypes.POINTER(_P)], _I32),
     "bskv_plan_bsr": ([_I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                        ctypes.POINTER(_P)], _I32),
+    "bskv_plan_prefill_paged": ([_I32P, _I32P, _I32P, _I32P, _I32, _I32, _I32, _I32, _I32,
+                                 _I32, _I32, _I32, _I32, ctypes.POINTER(_P)], _I32),
+    "bskv_run_prefill_paged": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P], _I32),
     "bskv_plan_bsr_variable": ([_P, _I32P, _I32P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                 _I32, ctypes.POINTER(_P)], _I32),
     "bskv_run_bsr_variable": ([_P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _I64P, _P, _F, _P],
@@ -390,6 +393,47 @@ def bskv_run_bsr_variable(plan, q, k, v, out=None, lse=None, return_lse=False, s
         _strides(k.stride(1), k.stride(0)), v.data_ptr(), _strides(v.stride(1), v.stride(0)),
         out.data_ptr(), _strides(out.stride(1), out.stride(0)), _ptr(lse), float(sm_scale),
         _stream(q)))
+    return (out, lse) if return_lse else out
+
+
+def bskv_plan_prefill_paged(qo_indptr, kv_indptr, kv_indices, kv_last_page_len, num_pages,
+                            page_size, num_qo_heads, num_kv_heads, head_dim, causal=True,
+                            dtype=torch.bfloat16, num_sms=None):
+    """Paged prefill plan from HOST ragged query and page-table arrays."""
+    lib = load_library()
+    qi, qip = _i32_array(qo_indptr)
+    ip, ipp = _i32_array(kv_indptr)
+    ix, ixp = _i32_array(kv_indices)
+    lp, lpp = _i32_array(kv_last_page_len)
+    batch = qi.numel() - 1
+    h = ctypes.c_void_p()
+    ns = _num_sms() if num_sms is None else num_sms
+    _check("bskv_plan_prefill_paged", lib.bskv_plan_prefill_paged(
+        ctypes.cast(qip, _I32P), ctypes.cast(ipp, _I32P), ctypes.cast(ixp, _I32P),
+        ctypes.cast(lpp, _I32P), int(batch), int(num_pages), int(page_size), int(num_qo_heads),
+        int(num_kv_heads), int(head_dim), int(bool(causal)), _DT[dtype], int(ns),
+        ctypes.byref(h)))
+    return Plan(h.value, "prefill_paged", batch=batch, num_qo_heads=num_qo_heads,
+                num_kv_heads=num_kv_heads, head_dim=head_dim, dtype=dtype)
+
+
+def bskv_run_prefill_paged(plan, q, kv_cache, out=None, lse=None, return_lse=False,
+                           sm_scale=None):
+    """q [total_qo, Hq, D]; kv_cache [pages, 2, Hkv, page_size, D] (any strides)."""
+    lib = load_library()
+    if plan.int_ws is None:
+        plan.upload(q.device)
+    T, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    _check("bskv_run_prefill_paged", lib.bskv_run_prefill_paged(
+        plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), kv_cache.data_ptr(),
+        _strides(*kv_cache.stride()[:4]), out.data_ptr(), _strides(out.stride(0), out.stride(1)),
+        _ptr(lse), float(sm_scale), _stream(q)))
     return (out, lse) if return_lse else out
 
 

@@ -32,6 +32,9 @@ struct BsrParams {
   int64_t k_s0, k_s1;
   const void* v;
   int64_t v_s0, v_s1;
+  // paged KV cache (paged prefill): element (page, K/V, kv head, slot) at these strides
+  const void* kv;
+  int64_t kv_s0, kv_s1, kv_s2, kv_s3;
   void* out;
   int64_t o_s0, o_s1;
   float* lse;
@@ -48,10 +51,15 @@ struct BsrParams {
 // blocks of at most 16 columns (a 32-key tile would be half empty there).
 static_assert(kBsrVarTile == 32, "variable-block plans list 32-key tiles");
 
-// kVar: a variable-block plan (the unit's rows and key tiles come from the metadata lists).
-template <typename T, int D, bool kVar, int kKT>
+// kMode 0: block-sparse (row block, listed column blocks); 1: variable blocks and 2: paged
+// prefill, whose unit rows and key tiles come from the metadata lists (paged tiles also
+// name their page and first slot, and causal is aligned per request).
+template <typename T, int D, int kMode, int kKT>
 __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
   constexpr int kSub = kKT / 16;
+  constexpr bool kList = kMode != 0;
+  constexpr int kDesc = kMode == 2 ? 5 : 4;   // words per unit descriptor
+  constexpr int kTileW = kMode == 2 ? 4 : 2;  // words per key tile
   constexpr int kRowBytes = D * 2;
   constexpr int kChunks = kRowBytes / 16;
   constexpr int kTileBytes = kKT * kRowBytes;
@@ -71,13 +79,14 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
     const int i = un.y, h = un.z, rt = un.w;
     // The unit's query rows and key tiles: row block i of R rows and its listed column
     // blocks, or (variable blocks) the lists of descriptor un.x.
-    int row0 = i * p.R, nrows = p.R, tb = 0, te = 0;
-    if constexpr (kVar) {
-      const int32_t* dsc = indptr + 4 * int64_t(un.x);
+    int row0 = i * p.R, nrows = p.R, tb = 0, te = 0, shift = p.N - p.M;
+    if constexpr (kList) {
+      const int32_t* dsc = indptr + kDesc * int64_t(un.x);
       row0 = dsc[0];
       nrows = dsc[1];
       tb = dsc[2];
       te = dsc[3];
+      if constexpr (kMode == 2) shift = dsc[4];
     }
     // This thread's two packed rows (mma rows r0 and r0 + 8 of the warp's 16).
     const int pr0 = rt * kBsrGenericRows + warp * 16 + (lane >> 2);
@@ -104,24 +113,37 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    const int e0 = kVar ? 0 : indptr[i], e1 = kVar ? 0 : indptr[i + 1];
-    const int ntiles = kVar ? te - tb : (e1 - e0) * subtiles;
+    const int e0 = kList ? 0 : indptr[i], e1 = kList ? 0 : indptr[i + 1];
+    const int ntiles = kList ? te - tb : (e1 - e0) * subtiles;
     // Stage tile n (block e0 + n / subtiles, sub-tile n % subtiles) into buffer `buf`.
     auto load = [&](int n, int buf) {
-      int kt0;
-      if constexpr (kVar) {
-        kt0 = indices[2 * (tb + n)];
+      int kt0, lim = p.N;
+      int64_t base = 0;  // paged: element offset of the tile's first K row
+      if constexpr (kMode == 2) {
+        const int32_t* tl = indices + kTileW * int64_t(tb + n);
+        kt0 = tl[0];
+        lim = tl[1];
+        base = int64_t(tl[2]) * p.kv_s0 + int64_t(h) * p.kv_s2 + int64_t(tl[3]) * p.kv_s3;
+      } else if constexpr (kMode == 1) {
+        kt0 = indices[kTileW * (tb + n)];
       } else {
-        const int j = indices[e0 + n / subtiles];
+        const int j = indices[e0 + n / subtiles];  // block-sparse mode only: subtiles >= 1
         kt0 = j * p.C + (n % subtiles) * kKT;
       }
       for (int c = threadIdx.x; c < kKT * kChunks; c += 128) {
         const int row = c / kChunks, ch = c % kChunks;
         const int tok = kt0 + row;
         const uint32_t off = swz(row, ch, kRowBytes);
-        if (tok < p.N) {
-          const T* ks = static_cast<const T*>(p.k) + int64_t(tok) * p.k_s0 + int64_t(h) * p.k_s1;
-          const T* vs = static_cast<const T*>(p.v) + int64_t(tok) * p.v_s0 + int64_t(h) * p.v_s1;
+        if (tok < lim) {
+          const T* ks;
+          const T* vs;
+          if constexpr (kMode == 2) {
+            ks = static_cast<const T*>(p.kv) + base + int64_t(row) * p.kv_s3;
+            vs = ks + p.kv_s1;
+          } else {
+            ks = static_cast<const T*>(p.k) + int64_t(tok) * p.k_s0 + int64_t(h) * p.k_s1;
+            vs = static_cast<const T*>(p.v) + int64_t(tok) * p.v_s0 + int64_t(h) * p.v_s1;
+          }
           cp_async_16(&sm[buf][0][off], ks + ch * 8);
           cp_async_16(&sm[buf][1][off], vs + ch * 8);
         } else {
@@ -141,11 +163,11 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
       }
       __syncthreads();
       const int buf = n & 1;
-      const int eb = e0 + n / subtiles;  // the block's position in indices
-      const int j = kVar ? 0 : indices[eb];
-      // first key of the tile and end of its column block (of its key range)
-      const int kt0 = kVar ? indices[2 * (tb + n)] : j * p.C + (n % subtiles) * kKT;
-      const int kend = kVar ? indices[2 * (tb + n) + 1] : j * p.C + p.C;
+      const int eb = kList ? 0 : e0 + n / subtiles;  // the block's position in indices
+      const int j = kList ? 0 : indices[eb];
+      // first key of the tile and end of its column block (of its key range, of its tile)
+      const int kt0 = kList ? indices[kTileW * (tb + n)] : j * p.C + (n % subtiles) * kKT;
+      const int kend = kList ? indices[kTileW * (tb + n) + 1] : j * p.C + p.C;
       float s[2 * kSub][4];
 #pragma unroll
       for (int nt = 0; nt < 2 * kSub; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -172,12 +194,14 @@ __global__ void __launch_bounds__(128) bsr_generic_kernel(const BsrParams p) {
           const int kt = kt0 + nt * 8 + 2 * cq + (e & 1);
           const int qt = (e < 2) ? tok0 : tok1;
           bool vis = kt < kend;
-          if (!kVar && p.mask) {
+          if (kMode == 0 && p.mask) {
             // bit (eb * R + row in block) * C + column in block; rows past M are never stored
             const int64_t bit = (int64_t(eb) * p.R + (qt - i * p.R)) * p.C + (kt - j * p.C);
             vis = vis && qt < p.M && ((__ldg(p.mask + (bit >> 3)) >> (bit & 7)) & 1);
           } else if (p.causal) {
-            vis = vis && (kt <= qt + (p.N - p.M));
+            // bottom-right aligned: query qt - row0 of its request (or row qt of the whole
+            // sequence) sees keys up to itself plus the shift
+            vis = vis && (kt <= (kMode == 2 ? qt - row0 : qt) + shift);
           }
           s[nt][e] = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
         }
@@ -269,11 +293,27 @@ using namespace bskv;
 
 namespace {
 
+template <int kMode, int kKT>
+void launch_generic(const bskv_plan* plan, const BsrParams& p, int grid, cudaStream_t st) {
+  const bool bf = plan->dtype == BSKV_BF16;
+  if (plan->head_dim == 128) {
+    if (bf) bsr_generic_kernel<__nv_bfloat16, 128, kMode, kKT><<<grid, 128, 0, st>>>(p);
+    else bsr_generic_kernel<__half, 128, kMode, kKT><<<grid, 128, 0, st>>>(p);
+  } else {
+    if (bf) bsr_generic_kernel<__nv_bfloat16, 64, kMode, kKT><<<grid, 128, 0, st>>>(p);
+    else bsr_generic_kernel<__half, 64, kMode, kKT><<<grid, 128, 0, st>>>(p);
+  }
+}
+
 bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strides,
                     const void* k, const int64_t* k_strides, const void* v,
                     const int64_t* v_strides, void* out, const int64_t* out_strides, float* lse,
                     float sm_scale, const uint8_t* mask, void* stream) {
   const bool var = plan && plan->kind == KIND_BSR && meta_word(plan, H_VARIANT) == BSR_VARIABLE;
+  if (plan && plan->kind == KIND_BSR && meta_word(plan, H_VARIANT) == BSR_PAGED_PREFILL) {
+    set_error("run_bsr: a paged prefill plan runs through bskv_run_prefill_paged");
+    return BSKV_ERR_INVALID_ARG;
+  }
   if (!plan || plan->kind != KIND_BSR) { set_error("run_bsr: not a BSR plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_bsr: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (!q_strides || !k_strides || !v_strides || !out_strides) { set_error("run_bsr: NULL strides"); return BSKV_ERR_INVALID_ARG; }
@@ -307,31 +347,10 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
   if (bskv_status s = status_args(&p.st)) return s;
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
-  const bool bf = plan->dtype == BSKV_BF16;
   const bool narrow = !var && plan->C <= 16;  // 16-key tiles
-  if (var) {
-    if (plan->head_dim == 128) {
-      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, true, 32><<<grid, 128, 0, st>>>(p);
-      else bsr_generic_kernel<__half, 128, true, 32><<<grid, 128, 0, st>>>(p);
-    } else {
-      if (bf) bsr_generic_kernel<__nv_bfloat16, 64, true, 32><<<grid, 128, 0, st>>>(p);
-      else bsr_generic_kernel<__half, 64, true, 32><<<grid, 128, 0, st>>>(p);
-    }
-  } else if (plan->head_dim == 128) {
-    if (narrow) {
-      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, false, 16><<<grid, 128, 0, st>>>(p);
-      else bsr_generic_kernel<__half, 128, false, 16><<<grid, 128, 0, st>>>(p);
-    } else {
-      if (bf) bsr_generic_kernel<__nv_bfloat16, 128, false, 32><<<grid, 128, 0, st>>>(p);
-      else bsr_generic_kernel<__half, 128, false, 32><<<grid, 128, 0, st>>>(p);
-    }
-  } else if (narrow) {
-    if (bf) bsr_generic_kernel<__nv_bfloat16, 64, false, 16><<<grid, 128, 0, st>>>(p);
-    else bsr_generic_kernel<__half, 64, false, 16><<<grid, 128, 0, st>>>(p);
-  } else {
-    if (bf) bsr_generic_kernel<__nv_bfloat16, 64, false, 32><<<grid, 128, 0, st>>>(p);
-    else bsr_generic_kernel<__half, 64, false, 32><<<grid, 128, 0, st>>>(p);
-  }
+  if (var) launch_generic<1, 32>(plan, p, grid, st);
+  else if (narrow) launch_generic<0, 16>(plan, p, grid, st);
+  else launch_generic<0, 32>(plan, p, grid, st);
   return cuda_check(cudaGetLastError(), "bsr kernel launch");
 }
 
@@ -384,4 +403,50 @@ extern "C" bskv_status bskv_run_bsr_variable(const bskv_plan* plan, const void* 
   }
   return run_bsr(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides, lse, sm_scale,
                  nullptr, stream);
+}
+
+extern "C" bskv_status bskv_run_prefill_paged(const bskv_plan* plan, const void* q,
+                                              const int64_t* q_strides, const void* kv_cache,
+                                              const int64_t* kv_strides, void* out,
+                                              const int64_t* out_strides, float* lse,
+                                              float sm_scale, void* stream) {
+  if (!plan || plan->kind != KIND_BSR || plan->meta.empty() ||
+      plan->meta[H_VARIANT] != BSR_PAGED_PREFILL) {
+    set_error("run_prefill_paged: not a paged prefill plan (bskv_plan_prefill_paged)");
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (!plan->meta_dev) { set_error("run_prefill_paged: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
+  if (!q_strides || !kv_strides || !out_strides) { set_error("run_prefill_paged: NULL strides"); return BSKV_ERR_INVALID_ARG; }
+  if (plan->M == 0) return BSKV_OK;
+  if (!q || !kv_cache || !out) { set_error("run_prefill_paged: NULL tensor"); return BSKV_ERR_INVALID_ARG; }
+  const int64_t* qo[2] = {q_strides, out_strides};
+  for (auto st2 : qo)
+    if (st2[0] <= 0 || st2[1] <= 0 || (st2[0] * 2) % 16 || (st2[1] * 2) % 16) {
+      set_error("run_prefill_paged: q/out strides must be positive multiples of 8 elements"); return BSKV_ERR_INVALID_ARG;
+    }
+  for (int i = 0; i < 4; ++i)
+    if (kv_strides[i] < 0 || (kv_strides[i] * 2) % 16) {
+      set_error("run_prefill_paged: kv strides must be non-negative multiples of 8 elements"); return BSKV_ERR_INVALID_ARG;
+    }
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) { set_error("run_prefill_paged: tensors must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  BsrParams p{};
+  p.meta = plan->meta_dev;
+  p.q = q; p.q_s0 = q_strides[0]; p.q_s1 = q_strides[1];
+  p.kv = kv_cache;
+  p.kv_s0 = kv_strides[0]; p.kv_s1 = kv_strides[1]; p.kv_s2 = kv_strides[2]; p.kv_s3 = kv_strides[3];
+  p.out = out; p.o_s0 = out_strides[0]; p.o_s1 = out_strides[1];
+  p.lse = lse;
+  p.lse_st = plan->num_qo_heads;
+  p.lse_sh = 1;
+  p.M = plan->M; p.N = 0; p.R = 0; p.C = 0;
+  p.Hq = plan->num_qo_heads; p.Hkv = plan->num_kv_heads; p.group = p.Hq / p.Hkv;
+  p.causal = plan->causal;
+  p.mask = nullptr;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  if (bskv_status s = status_args(&p.st)) return s;
+  const int grid = meta_word(plan, H_GRID);
+  if (grid == 0) return BSKV_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  launch_generic<2, 32>(plan, p, grid, st);
+  return cuda_check(cudaGetLastError(), "prefill kernel launch");
 }

@@ -52,7 +52,11 @@ constexpr int kFusedMergeMaxPieces = 8;
 // BSR_VARIABLE: per-kv-head variable block sizes; the general kernel walks, per unit, the
 // query row range and the 32-token key tiles listed in the metadata (aux0: per (kv head,
 // row block) {row start, row count, first tile, end tile}; aux1: tiles {key start, range end}).
-enum BsrVariant : int32_t { BSR_GENERIC = 0, BSR_TCGEN05 = 1, BSR_VARIABLE = 2 };
+// BSR_PAGED_PREFILL: batch prefill over a paged KV cache on the general kernel; aux0: per
+// request {first query token, query tokens, first tile, end tile, causal shift L_b - qo_len_b};
+// aux1: tiles {first key, tile end, page, first slot}, never crossing a page.
+enum BsrVariant : int32_t { BSR_GENERIC = 0, BSR_TCGEN05 = 1, BSR_VARIABLE = 2,
+                            BSR_PAGED_PREFILL = 3 };
 constexpr int kBsrVarTile = 32;  // key tokens per tile of a variable-block plan
 // MLA_SPARSE: row lists given by the caller. MLA_PAGED: row lists expanded on the device
 // from the page table in the metadata (aux0 = kv_indptr, aux1 = kv_indices).

@@ -443,6 +443,124 @@ extern "C" bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map,
   return BSKV_OK;
 }
 
+extern "C" bskv_status bskv_plan_prefill_paged(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                               const int32_t* kv_indices,
+                                               const int32_t* kv_last_page_len, int32_t batch,
+                                               int32_t num_pages, int32_t page_size,
+                                               int32_t num_qo_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t causal, int32_t dtype,
+                                               int32_t num_sms, bskv_plan** out_plan) {
+  if (!out_plan) { set_error("plan_prefill_paged: out_plan is NULL"); return BSKV_ERR_INVALID_ARG; }
+  *out_plan = nullptr;
+  if (batch < 0 || num_pages < 1 || page_size < 1 || num_sms < 1) {
+    set_error("plan_prefill_paged: batch=%d num_pages=%d page_size=%d num_sms=%d", batch,
+              num_pages, page_size, num_sms);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0) {
+    set_error("plan_prefill_paged: num_qo_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+              num_qo_heads, num_kv_heads);
+    return BSKV_ERR_INVALID_ARG;
+  }
+  if (head_dim != 64 && head_dim != 128) { set_error("plan_prefill_paged: head_dim %d not in {64,128}", head_dim); return BSKV_ERR_UNSUPPORTED; }
+  if (dtype != BSKV_BF16 && dtype != BSKV_FP16) { set_error("plan_prefill_paged: dtype %s unsupported", dtype_name(dtype)); return BSKV_ERR_UNSUPPORTED; }
+  if (batch > 0 && (!qo_indptr || !kv_indptr || !kv_last_page_len)) { set_error("plan_prefill_paged: NULL index array"); return BSKV_ERR_INVALID_ARG; }
+  if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) { set_error("plan_prefill_paged: qo_indptr[0] and kv_indptr[0] must be 0"); return BSKV_ERR_INVALID_ARG; }
+  const int32_t g = num_qo_heads / num_kv_heads;
+  std::vector<int32_t> desc(size_t(batch) * 5), tiles;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t nq = int64_t(qo_indptr[b + 1]) - qo_indptr[b];
+    const int64_t n = int64_t(kv_indptr[b + 1]) - kv_indptr[b];
+    if (nq < 0 || n < 0) { set_error("plan_prefill_paged: qo_indptr or kv_indptr decreases at %d", b); return BSKV_ERR_INVALID_ARG; }
+    int64_t L = 0;
+    if (n > 0) {
+      const int32_t lp = kv_last_page_len[b];
+      if (lp < 1 || lp > page_size) {
+        set_error("plan_prefill_paged: kv_last_page_len[%d] = %d outside [1, %d]", b, lp, page_size);
+        return BSKV_ERR_INVALID_ARG;
+      }
+      L = (n - 1) * page_size + lp;
+    }
+    if (L > INT32_MAX / 2 || nq * g > INT32_MAX / 2) { set_error("plan_prefill_paged: request %d too long", b); return BSKV_ERR_UNSUPPORTED; }
+    for (int64_t i = kv_indptr[b]; i < kv_indptr[b + 1]; ++i) {
+      if (!kv_indices || kv_indices[i] < 0 || kv_indices[i] >= num_pages) {
+        set_error("plan_prefill_paged: kv_indices[%lld] outside [0, %d)", (long long)i, num_pages);
+        return BSKV_ERR_INVALID_ARG;
+      }
+    }
+    const size_t d = size_t(b) * 5;
+    desc[d] = qo_indptr[b];
+    desc[d + 1] = int32_t(nq);
+    desc[d + 2] = int32_t(tiles.size() / 4);
+    // tiles of up to 32 keys that never cross a page
+    for (int64_t t = 0; t < L;) {
+      const int64_t pi = t / page_size;
+      const int64_t e = std::min({t + kBsrVarTile, (pi + 1) * page_size, L});
+      tiles.push_back(int32_t(t));
+      tiles.push_back(int32_t(e));
+      tiles.push_back(kv_indices[kv_indptr[b] + pi]);
+      tiles.push_back(int32_t(t - pi * page_size));
+      t = e;
+      if (tiles.size() > size_t(INT32_MAX) / 2) { set_error("plan_prefill_paged: too many key tiles"); return BSKV_ERR_UNSUPPORTED; }
+    }
+    desc[d + 3] = int32_t(tiles.size() / 4);
+    desc[d + 4] = int32_t(L - nq);
+  }
+  const int64_t total_qo = batch > 0 ? qo_indptr[batch] : 0;
+  if (total_qo > INT32_MAX / 2) { set_error("plan_prefill_paged: too many query tokens"); return BSKV_ERR_UNSUPPORTED; }
+  // Units (request b, kv head h, row tile of 64 grouped rows), b-major; the same longest-
+  // processing-time rule as the variable-block plans, cost 1 + tiles.
+  std::vector<Chunk> units;
+  std::vector<int64_t> cost;
+  for (int32_t b = 0; b < batch; ++b) {
+    const size_t d = size_t(b) * 5;
+    const int32_t rts = (desc[d + 1] * g + kBsrGenericRows - 1) / kBsrGenericRows;
+    for (int32_t h = 0; h < num_kv_heads; ++h)
+      for (int32_t rt = 0; rt < rts; ++rt) {
+        units.push_back(Chunk{b, b, h, rt});
+        cost.push_back(1 + desc[d + 3] - desc[d + 2]);
+      }
+  }
+  const int64_t U = int64_t(units.size());
+  std::vector<int32_t> order(static_cast<size_t>(U));
+  for (int64_t u = 0; u < U; ++u) order[size_t(u)] = int32_t(u);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t x, int32_t y) { return cost[size_t(x)] > cost[size_t(y)]; });
+  const int32_t G = int32_t(std::min<int64_t>(int64_t(num_sms) * kBsrGenericCtasPerSm, std::max<int64_t>(U, 1)));
+  using Item = std::pair<int64_t, int32_t>;
+  std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+  for (int32_t c = 0; c < G; ++c) heap.push(Item(0, c));
+  std::vector<std::vector<int32_t>> lists(static_cast<size_t>(G));
+  for (int32_t u : order) {
+    Item it = heap.top();
+    heap.pop();
+    lists[size_t(it.second)].push_back(u);
+    it.first += cost[size_t(u)];
+    heap.push(it);
+  }
+  std::vector<int32_t> worker_ptr(size_t(G) + 1, 0);
+  std::vector<Chunk> chunks;
+  chunks.reserve(size_t(U));
+  for (int32_t c = 0; c < G; ++c) {
+    worker_ptr[size_t(c)] = int32_t(chunks.size());
+    for (int32_t u : lists[size_t(c)]) chunks.push_back(units[size_t(u)]);
+  }
+  worker_ptr[size_t(G)] = int32_t(chunks.size());
+  bskv_plan* p = new bskv_plan();
+  p->kind = KIND_BSR;
+  p->batch = batch; p->num_pages = num_pages; p->page_size = page_size;
+  p->M = int32_t(total_qo); p->N = 0; p->R = 0; p->C = 0; p->causal = causal ? 1 : 0;
+  p->num_qo_heads = num_qo_heads; p->num_kv_heads = num_kv_heads; p->head_dim = head_dim;
+  p->dtype = dtype;
+  std::vector<int32_t> no_merges;
+  assemble(p, KIND_BSR, int32_t(U), worker_ptr, chunks, 0, no_merges, kBsrGenericRows,
+           desc.data(), desc.size(), tiles.data(), tiles.size(), U > 0 ? G : 0,
+           BSR_PAGED_PREFILL);
+  p->float_ws_bytes = 0;
+  *out_plan = p;
+  return BSKV_OK;
+}
+
 extern "C" bskv_status bskv_plan_bsr_masked(const int32_t* indptr, const int32_t* indices,
                                             int32_t M, int32_t N, int32_t R, int32_t C,
                                             int32_t num_qo_heads, int32_t num_kv_heads,

@@ -156,6 +156,24 @@ bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map, const int32_t*
                                    bskv_plan** out_plan);
 
 /*
+ * Batch prefill over a paged KV cache ([CHEAT] benchmark README:
+ * BatchPrefillWithPagedKVCacheWrapper, prefill attention with paged KV cache; [SKILL]
+ * KV-Cache Formats and Batch prefill / Append): request b owns query tokens
+ * [qo_indptr[b], qo_indptr[b+1]) (the last qo_len_b tokens of its sequence) and the pages of
+ * its kv_indptr/kv_indices/kv_last_page_len entry (L_b tokens, as for bskv_plan_decode).
+ *   qo_indptr[batch+1], kv_indptr[batch+1], kv_indices, kv_last_page_len[batch]: HOST int32;
+ *   page ids in [0, num_pages). causal: query token t of request b (0-based within its
+ *   queries) sees key j iff j <= t + L_b - qo_len_b (bottom-right aligned).
+ *   head_dim 64 or 128; dtype BSKV_FP16 or BSKV_BF16; the general kernel serves these plans.
+ */
+bskv_status bskv_plan_prefill_paged(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                    const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                                    int32_t batch, int32_t num_pages, int32_t page_size,
+                                    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t causal, int32_t dtype, int32_t num_sms,
+                                    bskv_plan** out_plan);
+
+/*
  * Sparse MLA FP8 decode plan ([MLA] get_batch_decode_metadata_mla(query, seq_lens,
  * sparse_mla_top_k): reusable while seq_lens, the query shape and top_k are unchanged).
  *   seq_lens[batch]: HOST int32 valid sparse lengths, 0 <= seq_lens[b] <= top_k.
@@ -324,6 +342,18 @@ bskv_status bskv_run_bsr_variable(const bskv_plan* plan, const void* q, const in
                                   const int64_t* v_strides, void* out,
                                   const int64_t* out_strides, float* lse, float sm_scale,
                                   void* stream);
+
+/*
+ * Batch prefill over a paged KV cache, for a plan of bskv_plan_prefill_paged:
+ *   q [total_qo, num_qo_heads, head_dim], strides {token, head}; kv_cache and kv_strides as
+ *   for bskv_run_decode (4 strides: page, K/V, kv head, slot); out like q; lse
+ *   [total_qo, num_qo_heads] float32 contiguous, or NULL. A query that sees no key gets
+ *   out = 0 and lse = -inf.
+ */
+bskv_status bskv_run_prefill_paged(const bskv_plan* plan, const void* q, const int64_t* q_strides,
+                                   const void* kv_cache, const int64_t* kv_strides, void* out,
+                                   const int64_t* out_strides, float* lse, float sm_scale,
+                                   void* stream);
 
 /*
  * Sparse MLA FP8 decode ([MLA] sparse_mla_fp8_decode; [WRAP] scale folding):

@@ -33,6 +33,10 @@ Sources:
     kv_indices, kv_last_page_len (batch,). Reading: request b owns pages
     kv_indices[kv_indptr[b]:kv_indptr[b+1]] in order, and its length is
     (n_pages - 1) * page_size + kv_last_page_len[b].
+  * Paged prefill: FlashInfer cheat page, benchmark README (BatchPrefillWithPagedKVCacheWrapper,
+    prefill attention with paged KV cache); "FlashInfer" agent-skill summary, Batch prefill
+    and Append (causal prefill of new tokens against the cache). Reading: request b's queries
+    are the last qo_len_b tokens of its sequence, so causal is aligned bottom-right.
   * Sparse MLA: "Sparse MLA" (MATE 0.2.6), sparse_mla_fp8_decode: FP8 query
     [batch, q_len, heads, 576], FP8 cache rows of 576 values, int32 physical-token
     indices [batch, q_len, top_k] shared by all heads, seq_lens[b] valid entries,
@@ -239,6 +243,31 @@ def paged_decode(q_bits, kv_bits, dtype, kv_indptr, kv_indices, kv_last_page_len
         outs.append(o[0])
         lses.append(l[0])
     return np.stack(outs), np.stack(lses)
+
+
+def paged_prefill(q_bits, kv_bits, dtype, qo_indptr, kv_indptr, kv_indices, kv_last_page_len,
+                  page_size, sm_scale=None, causal=True, requests=None):
+    """Batch prefill over a paged KV cache: request b's query tokens
+    q[qo_indptr[b]:qo_indptr[b+1]] (the last qo_len_b tokens of its sequence) attend to the
+    L_b keys of its pages; causal keeps key j for local query t iff j <= t + L_b - qo_len_b.
+    q [total_qo, Hq, D] and the cache as 16-bit patterns. Returns the rows of the requested
+    requests (all by default) in order: out [n, Hq, D], lse [n, Hq]."""
+    D = q_bits.shape[-1]
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    reqs = range(len(qo_indptr) - 1) if requests is None else requests
+    outs, lses = [], []
+    for b in reqs:
+        q = bits_to_f64(q_bits[int(qo_indptr[b]):int(qo_indptr[b + 1])], dtype)
+        k, v = paged_kv(kv_bits, dtype, kv_indptr, kv_indices, kv_last_page_len, page_size, b)
+        nq, L = q.shape[0], k.shape[0]
+        mask = None
+        if causal:
+            mask = np.arange(L)[None, :] <= (np.arange(nq)[:, None] + (L - nq))
+        o, l = masked_attention(q, k, v, sm_scale, mask)
+        outs.append(o)
+        lses.append(l)
+    return np.concatenate(outs), np.concatenate(lses)
 
 
 # ---------------------------------------------------------------------------------------

@@ -39,6 +39,11 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
     cost 1 + tiles, the same longest-processing-time rule on at most 4 * num_sms CTAs
     (max(units, 1) when smaller); grid = CTAs, 0 without units; aux0 = descriptors,
     aux1 = tiles, tile field 64.
+  * paged prefill (variant 3): per request a descriptor (first query token, query tokens,
+    first tile, end tile, L_b - qo_len_b); the request's keys [0, L_b) split into tiles
+    (t, e, page, first slot) of at most 32 keys that never cross a page; units (b, kv head,
+    row tile of 64 grouped rows) b-major, chunk (b, b, h, rt), cost 1 + tiles, the
+    variable-block assignment rule; aux0 = descriptors, aux1 = tiles.
   * paged MLA: one unit per request, len = its length from the page table (as for
     decode), tile 128, max_workers = max(1, num_sms // 2), grid = 2 P, aux0 = kv_indptr,
     aux1 = kv_indices, variant 1.
@@ -273,6 +278,48 @@ def bsr_variable_meta(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, 
             ch.append(units[u])
     wp.append(len(ch))
     return _assemble(2, U, wp, ch, 0, [], 64, desc, tiles, G if U > 0 else 0, 2)
+
+
+def prefill_paged_meta(qo_indptr, kv_indptr, kv_indices, kv_last_page_len, page_size,
+                       num_qo_heads, num_kv_heads, num_sms):
+    batch = len(qo_indptr) - 1
+    g = num_qo_heads // num_kv_heads
+    desc, tiles = [], []
+    for b in range(batch):
+        nq = int(qo_indptr[b + 1]) - int(qo_indptr[b])
+        L = paged_request_len(kv_indptr, kv_last_page_len, page_size, b)
+        tb = len(tiles) // 4
+        t = 0
+        while t < L:
+            pi = t // page_size
+            e = min(t + 32, (pi + 1) * page_size, L)
+            tiles += [t, e, int(kv_indices[int(kv_indptr[b]) + pi]), t - pi * page_size]
+            t = e
+        desc += [int(qo_indptr[b]), nq, tb, len(tiles) // 4, L - nq]
+    units, cost = [], []
+    for b in range(batch):
+        d = b * 5
+        for h in range(num_kv_heads):
+            for rt in range((desc[d + 1] * g + 63) // 64):
+                units.append([b, b, h, rt])
+                cost.append(1 + desc[d + 3] - desc[d + 2])
+    U = len(units)
+    order = sorted(range(U), key=lambda u: -cost[u])
+    G = min(4 * num_sms, max(U, 1))
+    heap = [(0, c) for c in range(G)]
+    heapq.heapify(heap)
+    lists = [[] for _ in range(G)]
+    for u in order:
+        load, c = heapq.heappop(heap)
+        lists[c].append(u)
+        heapq.heappush(heap, (load + cost[u], c))
+    wp, ch = [], []
+    for c in range(G):
+        wp.append(len(ch))
+        for u in lists[c]:
+            ch.append(units[u])
+    wp.append(len(ch))
+    return _assemble(2, U, wp, ch, 0, [], 64, desc, tiles, G if U > 0 else 0, 3)
 
 
 def sections(meta):

@@ -12,6 +12,7 @@ from .gen import (  # noqa: F401
     bsr_inputs,
     variable_block_inputs,
     paged_decode_inputs,
+    paged_prefill_inputs,
     mla_inputs,
     mla_paged_inputs,
     mla_append_inputs,

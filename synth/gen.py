@@ -157,6 +157,27 @@ def paged_decode_inputs(seed, batch, num_qo_heads, num_kv_heads, head_dim, page_
                 seed=seed)
 
 
+def paged_prefill_inputs(seed, batch, num_qo_heads, num_kv_heads, head_dim, page_size, len_lo,
+                         len_hi, qo_lo, qo_hi, dtype=torch.bfloat16, lengths=None,
+                         qo_lens=None, device="cpu"):
+    """Batch prefill over a paged KV cache: the cache of paged_decode_inputs (lengths L_b,
+    permuted pages, NaN canaries) plus qo_len_b = min(U[qo_lo, qo_hi], L_b) query tokens per
+    request (or ``qo_lens``), ragged in q [total_qo, Hq, D] with qo_indptr."""
+    d = paged_decode_inputs(seed, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                            len_lo, len_hi, dtype=dtype, lengths=lengths, device=device)
+    g = _cpu_gen(seed + 3)
+    if qo_lens is None:
+        qo_lens = [min(int(x), int(L)) for x, L in zip(_uniform_int(g, qo_lo, qo_hi, batch),
+                                                         d["kv_lens"])]
+    qo_indptr = torch.zeros(batch + 1, dtype=torch.int32)
+    qo_indptr[1:] = torch.cumsum(torch.tensor(qo_lens, dtype=torch.int64), 0).to(torch.int32)
+    dg = _dev_gen(seed + 5, device)
+    q = _randn((int(qo_indptr[-1]), num_qo_heads, head_dim), dtype, dg, device)
+    d.update(q=q, qo_indptr=qo_indptr, qo_lens=torch.tensor(qo_lens, dtype=torch.int32),
+             dtype=dtype)
+    return d
+
+
 # --------------------------------------------------------------------------------------
 # MLA sparse FP8 decode and its RoPE + FP8 prologue
 # --------------------------------------------------------------------------------------
@@ -367,6 +388,9 @@ CONFIGS = {
     "bsr_variable": dict(kind="bsr_variable", seed=1007, num_qo_heads=32, num_kv_heads=8,
                          head_dim=128, MB=128, NB=128, qo_len=16384, kv_len=16384,
                          density=0.1, dtype=torch.float16, causal=True),
+    "prefill_paged": dict(kind="prefill_paged", seed=1008, batch=16, num_qo_heads=32,
+                          num_kv_heads=8, head_dim=128, page_size=16, len_lo=2048,
+                          len_hi=8192, qo_lo=1024, qo_hi=1024, dtype=torch.bfloat16),
     "mla_append": dict(kind="mla_append", seed=1006, batch=128, page_size=64, len_lo=2048,
                        len_hi=8192, new_tokens=512),
 }
@@ -387,6 +411,8 @@ def make(name, device="cpu", **overrides):
         return mla_paged_inputs(device=device, **cfg)
     if kind == "bsr_variable":
         return variable_block_inputs(device=device, **cfg)
+    if kind == "prefill_paged":
+        return paged_prefill_inputs(device=device, **cfg)
     if kind == "mla_append":
         return mla_append_inputs(device=device, **cfg)
     raise ValueError(kind)

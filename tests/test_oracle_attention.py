@@ -487,3 +487,60 @@ def test_variable_block_heads_follow_their_kv_head():
         np.testing.assert_array_equal(lse[2 * h:2 * h + 2], l1)
     m = att.variable_block_mask(bmap, rsz, csz)
     assert m[1, 0, :].tolist() == [False] * 2 + [True] * 10   # row block 0 of head 1: cols 1, 2
+
+
+# ---------------------------------------------------------------------------------------
+# batch prefill over a paged KV cache
+# ---------------------------------------------------------------------------------------
+
+def test_paged_prefill_one_query_is_decode():
+    """qo_len 1 with causal: the last token sees its whole request, i.e. paged decode."""
+    d = synth.paged_prefill_inputs(81, 4, 8, 2, 16, 16, 1, 90, 1, 1, lengths=[1, 17, 40, 90])
+    ip, ix, lp = d["kv_indptr"].numpy(), d["kv_indices"].numpy(), d["kv_last_page_len"].numpy()
+    out, lse = att.paged_prefill(_bits(d["q"]), _bits(d["kv_cache"]), "bf16",
+                                 d["qo_indptr"].numpy(), ip, ix, lp, 16)
+    ref, ref_lse = att.paged_decode(_bits(d["q"]), _bits(d["kv_cache"]), "bf16", ip, ix, lp, 16)
+    np.testing.assert_array_equal(out, ref)
+    np.testing.assert_array_equal(lse, ref_lse)
+
+
+def test_paged_prefill_whole_sequence_is_sdpa_causal():
+    """One request whose queries are its whole sequence: standard causal attention."""
+    d = synth.paged_prefill_inputs(82, 1, 4, 2, 16, 8, 0, 0, 0, 0, lengths=[37], qo_lens=[37])
+    k, v = att.paged_kv(_bits(d["kv_cache"]), "bf16", d["kv_indptr"].numpy(),
+                        d["kv_indices"].numpy(), d["kv_last_page_len"].numpy(), 8, 0)
+    out, _ = att.paged_prefill(_bits(d["q"]), _bits(d["kv_cache"]), "bf16",
+                               d["qo_indptr"].numpy(), d["kv_indptr"].numpy(),
+                               d["kv_indices"].numpy(), d["kv_last_page_len"].numpy(), 8)
+    q = nx.bits_to_f64(_bits(d["q"]), "bf16")
+    ref = _sdpa(q, k, v, 1 / math.sqrt(16), causal=True)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_paged_prefill_bottom_right_and_page_size_invariance():
+    """The first of qo_len queries sees L - qo_len + 1 keys; relayout with another page size
+    changes nothing."""
+    lengths, qo = [30, 64], [5, 64]
+    d = synth.paged_prefill_inputs(83, 2, 4, 4, 16, 16, 0, 0, 0, 0, lengths=lengths, qo_lens=qo)
+    args = (d["qo_indptr"].numpy(), d["kv_indptr"].numpy(), d["kv_indices"].numpy(),
+            d["kv_last_page_len"].numpy(), 16)
+    out, lse = att.paged_prefill(_bits(d["q"]), _bits(d["kv_cache"]), "bf16", *args)
+    k, v = att.paged_kv(_bits(d["kv_cache"]), "bf16", *args[1:], 0)
+    q0 = nx.bits_to_f64(_bits(d["q"][:1]), "bf16")
+    one, _ = att.masked_attention(q0, k[:26], v[:26], 1 / math.sqrt(16))
+    np.testing.assert_allclose(out[0], one[0], rtol=1e-12, atol=1e-14)
+    other = synth.paged_prefill_inputs(84, 2, 4, 4, 16, 7, 0, 0, 0, 0, lengths=lengths, qo_lens=qo)
+    cache = other["kv_cache"].clone()
+    for b in range(2):
+        kb, vb = att.paged_kv(_bits(d["kv_cache"]), "bf16", *args[1:], b)
+        pages = other["kv_indices"][other["kv_indptr"][b]:other["kv_indptr"][b + 1]]
+        for n, p in enumerate(pages.tolist()):
+            seg = slice(n * 7, min((n + 1) * 7, lengths[b]))
+            cnt = seg.stop - seg.start
+            cache[p, 0, :, :cnt] = torch.from_numpy(kb[seg]).to(torch.bfloat16).transpose(0, 1)
+            cache[p, 1, :, :cnt] = torch.from_numpy(vb[seg]).to(torch.bfloat16).transpose(0, 1)
+    out2, lse2 = att.paged_prefill(_bits(d["q"]), _bits(cache), "bf16", d["qo_indptr"].numpy(),
+                                   other["kv_indptr"].numpy(), other["kv_indices"].numpy(),
+                                   other["kv_last_page_len"].numpy(), 7)
+    np.testing.assert_array_equal(out2, out)
+    np.testing.assert_array_equal(lse2, lse)

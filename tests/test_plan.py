@@ -271,3 +271,14 @@ def test_bsr_variable_plan_rejects_bad_inputs(lib):
     _expect("ERR_INVALID_ARG", f, bm, [[0, 3], [2, 1]], [[3, 1], [2, 2]], 2, 2, 64, num_sms=2)  # empty block
     _expect("ERR_INVALID_ARG", f, bm, [[1, 2], [2, 1]], [[3, 1], [2, 2]], 3, 2, 64, num_sms=2)  # heads
     _expect("ERR_UNSUPPORTED", f, bm, [[1, 2], [2, 1]], [[3, 1], [2, 2]], 2, 2, 96, num_sms=2)  # head_dim
+
+
+@pytest.mark.parametrize("lengths,qo,ps", [([1, 17, 40, 90], [1, 17, 3, 64], 16),
+                                           ([2048, 300], [1024, 300], 64), ([5], [5], 1)])
+def test_prefill_paged_plan_bit_exact(lib, lengths, qo, ps):
+    d = synth.paged_prefill_inputs(85, len(lengths), 32, 8, 128, ps, 0, 0, 0, 0,
+                                   lengths=lengths, qo_lens=qo)
+    args = [d["qo_indptr"].tolist(), d["kv_indptr"].tolist(), d["kv_indices"].tolist(),
+            d["kv_last_page_len"].tolist()]
+    p = bskv.bskv_plan_prefill_paged(*args, d["num_pages"], ps, 32, 8, 128, num_sms=SMS)
+    assert p.metadata() == plan_ref.prefill_paged_meta(*args, ps, 32, 8, SMS)
