@@ -263,16 +263,8 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int32_t c0,
-                                                 int32_t c1, int32_t c2, uint64_t* bar,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-// tma_load_3d_hint executed by the lane of a converged warp whose `leader` is nonzero.
+// 3-D tiled TMA load with an L2 cache policy, executed by the lane of a converged warp whose
+// `leader` is nonzero.
 __device__ __forceinline__ void tma_load_3d_hint_w(uint32_t leader, void* dst,
                                                    const CUtensorMap* map, int32_t c0,
                                                    int32_t c1, int32_t c2, uint64_t* bar,
@@ -470,44 +462,6 @@ __host__ __device__ constexpr uint32_t umma_idesc(uint32_t M, uint32_t N, uint32
          ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// A operand read from TMEM (rows = lanes; 16-bit elements packed two per 32-bit column,
-// the even element in the low half; 8-bit elements four per column, element k in byte
-// k mod 4); a k-step of 16 (f16) or 32 (f8) elements spans 8 columns.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // ---- MMA issue from a converged warp ---------------------------------------------------
 // The whole issuer warp runs the issue loop and the lane whose `leader` is nonzero executes
 // every tcgen05.mma / tcgen05.commit (commits track the MMAs of the thread that executes
@@ -529,6 +483,9 @@ __device__ __forceinline__ void umma_f16_w(uint32_t leader, uint32_t d_tmem, uin
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
+// The TS forms read the A operand from TMEM (rows = lanes; 16-bit elements packed two per
+// 32-bit column, the even element in the low half; 8-bit elements four per column, element k
+// in byte k mod 4); a k-step of 16 (f16) or 32 (f8) elements spans 8 columns.
 __device__ __forceinline__ void umma_f16_ts_w(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
                                               uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -567,24 +524,6 @@ __device__ __forceinline__ void umma_commit_w(uint32_t leader, uint64_t* bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar)),
       "r"(leader)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
-// Commit the issuing thread's MMAs to the mbarrier at the same offset in every CTA of
-// `cta_mask` (one arrival each).
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-          "r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
       : "memory");
 }
 
