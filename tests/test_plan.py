@@ -7,6 +7,7 @@ import torch
 
 import block_sparse_kv_gb300 as bskv
 import synth
+from oracle import attention as att
 from oracle import plan_ref
 
 SMS = 152
@@ -282,3 +283,62 @@ def test_prefill_paged_plan_bit_exact(lib, lengths, qo, ps):
             d["kv_last_page_len"].tolist()]
     p = bskv.bskv_plan_prefill_paged(*args, d["num_pages"], ps, 32, 8, 128, num_sms=SMS)
     assert p.metadata() == plan_ref.prefill_paged_meta(*args, ps, 32, 8, SMS)
+
+
+# ---------------------------------------------------------------------------------------
+# invariants of the list-driven plans, checked against the oracle's definitions (not
+# against the restated rule)
+# ---------------------------------------------------------------------------------------
+
+def _aux(meta):
+    return meta[meta[11]:meta[12]], meta[meta[12]:meta[14]]
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_variable_plan_tiles_cover_exactly_the_visible_keys(lib, seed):
+    d = synth.variable_block_inputs(seed, 8, 4, 64, 7, 9, 500, 700, density=0.45)
+    bm, rs, cs = d["block_mask_map"], d["block_row_sz"], d["block_col_sz"]
+    p = bskv.bskv_plan_bsr_variable(bm, rs, cs, 8, 4, 64, num_sms=SMS)
+    meta = p.metadata()
+    desc, tiles = _aux(meta)
+    mask = att.variable_block_mask(bm.numpy(), rs.numpy(), cs.numpy())   # [H, qo, kv]
+    H, MB = 4, 7
+    g = 2
+    seen_rows = np.zeros((H, 500 * g), int)
+    for c in plan_ref.sections(meta)["chunks"]:
+        x, a, h, rt = c
+        r0, nr, tb, te = desc[4 * x:4 * x + 4]
+        assert x == h * MB + a
+        keys = np.zeros(700, bool)
+        for t in range(tb, te):
+            k0, ke = tiles[2 * t], tiles[2 * t + 1]
+            assert 0 <= k0 < ke <= 700
+            keys[k0:min(ke, k0 + 32)] = True
+        for row in range(r0, r0 + nr):
+            np.testing.assert_array_equal(keys, mask[h, row])
+        lo, hi = rt * 64, min((rt + 1) * 64, nr * g)
+        seen_rows[h, r0 * g + lo:r0 * g + hi] += 1
+    assert (seen_rows == 1).all()  # every (token, query head) row in exactly one unit
+
+
+def test_prefill_plan_tiles_address_every_key_once(lib):
+    lengths, qo, ps = [1, 17, 40, 90, 0], [1, 17, 3, 64, 0], 16
+    d = synth.paged_prefill_inputs(86, 5, 8, 2, 64, ps, 0, 0, 0, 0, lengths=lengths,
+                                   qo_lens=qo, device="cpu")
+    p = bskv.bskv_plan_prefill_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                                     d["kv_last_page_len"], d["num_pages"], ps, 8, 2, 64,
+                                     num_sms=SMS)
+    meta = p.metadata()
+    desc, tiles = _aux(meta)
+    ip, ix = d["kv_indptr"].numpy(), d["kv_indices"].numpy()
+    for b in range(5):
+        r0, nq, tb, te, shift = desc[5 * b:5 * b + 5]
+        assert r0 == int(d["qo_indptr"][b]) and nq == qo[b] and shift == lengths[b] - qo[b]
+        covered = []
+        for t in range(tb, te):
+            k0, ke, page, slot = tiles[4 * t:4 * t + 4]
+            assert ke - k0 <= 32 and slot + (ke - k0) <= ps      # never crosses its page
+            for k in range(k0, ke):
+                assert page == ix[ip[b] + k // ps] and slot + (k - k0) == k % ps
+                covered.append(k)
+        assert covered == list(range(lengths[b]))
