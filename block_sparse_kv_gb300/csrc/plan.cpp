@@ -130,6 +130,42 @@ void linear_partition(const std::vector<int64_t>& unit_len, int64_t tile, int64_
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Longest-processing-time assignment of units with costs `cost` to G workers: units taken by
+// cost, largest first (stable), each given to the worker of least load so far (ties: the
+// lowest worker index). Returns every worker's units in assignment order.
+std::vector<std::vector<int32_t>> lpt_assign(const std::vector<int64_t>& cost, int32_t G) {
+  std::vector<int32_t> order(cost.size());
+  for (size_t u = 0; u < cost.size(); ++u) order[u] = int32_t(u);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t a, int32_t b) { return cost[size_t(a)] > cost[size_t(b)]; });
+  using Item = std::pair<int64_t, int32_t>;  // (load, worker), smallest first
+  std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+  for (int32_t c = 0; c < G; ++c) heap.push(Item(0, c));
+  std::vector<std::vector<int32_t>> lists(static_cast<size_t>(G));
+  for (int32_t u : order) {
+    Item it = heap.top();
+    heap.pop();
+    lists[size_t(it.second)].push_back(u);
+    it.first += cost[size_t(u)];
+    heap.push(it);
+  }
+  return lists;
+}
+
+// Worker pointers and chunks of an assignment whose unit u is chunk units[u].
+void lists_to_chunks(const std::vector<std::vector<int32_t>>& lists,
+                     const std::vector<Chunk>& units, std::vector<int32_t>& worker_ptr,
+                     std::vector<Chunk>& chunks) {
+  worker_ptr.assign(lists.size() + 1, 0);
+  chunks.clear();
+  chunks.reserve(units.size());
+  for (size_t c = 0; c < lists.size(); ++c) {
+    worker_ptr[c] = int32_t(chunks.size());
+    for (int32_t u : lists[c]) chunks.push_back(units[size_t(u)]);
+  }
+  worker_ptr[lists.size()] = int32_t(chunks.size());
+}
+
 }  // namespace
 
 }  // namespace bskv
@@ -264,42 +300,20 @@ bskv_status plan_bsr(const int32_t* indptr, const int32_t* indices, int32_t M, i
   // quarters of a step of its kernel: 4 per pair of blocks, 3 for a last single block (its
   // QK takes as long as a pair's), 2 for the unit's start and epilogue (1 with no blocks);
   // of a general unit: 1 + n.
-  std::vector<int32_t> order(static_cast<size_t>(U));
   std::vector<int64_t> cost(static_cast<size_t>(U));
+  std::vector<Chunk> units(static_cast<size_t>(U));
   for (int64_t u = 0; u < U; ++u) {
     const int32_t i = int32_t(u / (int64_t(num_kv_heads) * row_tiles));
     const int64_t n = indptr[i + 1] - indptr[i];
     cost[size_t(u)] = tc ? (n > 0 ? 2 + 4 * (n / 2) + 3 * (n % 2) : 1) : 1 + n;
-    order[size_t(u)] = int32_t(u);
+    units[size_t(u)] = Chunk{int32_t(u), i, int32_t((u / row_tiles) % num_kv_heads),
+                             int32_t(u % row_tiles)};
   }
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t a, int32_t b) { return cost[size_t(a)] > cost[size_t(b)]; });
   const int64_t cap = tc ? num_sms : int64_t(num_sms) * kBsrGenericCtasPerSm;
   const int32_t G = int32_t(std::min<int64_t>(cap, U));
-  using Item = std::pair<int64_t, int32_t>;  // (load, cta), smallest first
-  std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
-  for (int32_t c = 0; c < G; ++c) heap.push(Item(0, c));
-  std::vector<std::vector<int32_t>> lists(static_cast<size_t>(G));
-  for (int32_t u : order) {
-    Item it = heap.top();
-    heap.pop();
-    lists[size_t(it.second)].push_back(u);
-    it.first += cost[size_t(u)];
-    heap.push(it);
-  }
-  std::vector<int32_t> worker_ptr(size_t(G) + 1, 0);
+  std::vector<int32_t> worker_ptr;
   std::vector<Chunk> chunks;
-  chunks.reserve(size_t(U));
-  for (int32_t c = 0; c < G; ++c) {
-    worker_ptr[size_t(c)] = int32_t(chunks.size());
-    for (int32_t u : lists[size_t(c)]) {
-      const int32_t rt = u % row_tiles;
-      const int32_t h = (u / row_tiles) % num_kv_heads;
-      const int32_t i = u / (row_tiles * num_kv_heads);
-      chunks.push_back(Chunk{u, i, h, rt});
-    }
-  }
-  worker_ptr[size_t(G)] = int32_t(chunks.size());
+  lists_to_chunks(lpt_assign(cost, G), units, worker_ptr, chunks);
   bskv_plan* p = new bskv_plan();
   p->kind = KIND_BSR;
   p->M = M; p->N = N; p->R = R; p->C = C; p->causal = causal ? 1 : 0;
@@ -406,30 +420,10 @@ extern "C" bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map,
       }
     }
   const int64_t U = int64_t(units.size());
-  std::vector<int32_t> order(static_cast<size_t>(U));
-  for (int64_t u = 0; u < U; ++u) order[size_t(u)] = int32_t(u);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t x, int32_t y) { return cost[size_t(x)] > cost[size_t(y)]; });
   const int32_t G = int32_t(std::min<int64_t>(int64_t(num_sms) * kBsrGenericCtasPerSm, std::max<int64_t>(U, 1)));
-  using Item = std::pair<int64_t, int32_t>;
-  std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
-  for (int32_t c = 0; c < G; ++c) heap.push(Item(0, c));
-  std::vector<std::vector<int32_t>> lists(static_cast<size_t>(G));
-  for (int32_t u : order) {
-    Item it = heap.top();
-    heap.pop();
-    lists[size_t(it.second)].push_back(u);
-    it.first += cost[size_t(u)];
-    heap.push(it);
-  }
-  std::vector<int32_t> worker_ptr(size_t(G) + 1, 0);
+  std::vector<int32_t> worker_ptr;
   std::vector<Chunk> chunks;
-  chunks.reserve(size_t(U));
-  for (int32_t c = 0; c < G; ++c) {
-    worker_ptr[size_t(c)] = int32_t(chunks.size());
-    for (int32_t u : lists[size_t(c)]) chunks.push_back(units[size_t(u)]);
-  }
-  worker_ptr[size_t(G)] = int32_t(chunks.size());
+  lists_to_chunks(lpt_assign(cost, G), units, worker_ptr, chunks);
   bskv_plan* p = new bskv_plan();
   p->kind = KIND_BSR;
   p->M = int32_t(qo_len); p->N = int32_t(kv_len); p->R = 0; p->C = 0; p->causal = causal ? 1 : 0;
@@ -522,30 +516,10 @@ extern "C" bskv_status bskv_plan_prefill_paged(const int32_t* qo_indptr, const i
       }
   }
   const int64_t U = int64_t(units.size());
-  std::vector<int32_t> order(static_cast<size_t>(U));
-  for (int64_t u = 0; u < U; ++u) order[size_t(u)] = int32_t(u);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t x, int32_t y) { return cost[size_t(x)] > cost[size_t(y)]; });
   const int32_t G = int32_t(std::min<int64_t>(int64_t(num_sms) * kBsrGenericCtasPerSm, std::max<int64_t>(U, 1)));
-  using Item = std::pair<int64_t, int32_t>;
-  std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
-  for (int32_t c = 0; c < G; ++c) heap.push(Item(0, c));
-  std::vector<std::vector<int32_t>> lists(static_cast<size_t>(G));
-  for (int32_t u : order) {
-    Item it = heap.top();
-    heap.pop();
-    lists[size_t(it.second)].push_back(u);
-    it.first += cost[size_t(u)];
-    heap.push(it);
-  }
-  std::vector<int32_t> worker_ptr(size_t(G) + 1, 0);
+  std::vector<int32_t> worker_ptr;
   std::vector<Chunk> chunks;
-  chunks.reserve(size_t(U));
-  for (int32_t c = 0; c < G; ++c) {
-    worker_ptr[size_t(c)] = int32_t(chunks.size());
-    for (int32_t u : lists[size_t(c)]) chunks.push_back(units[size_t(u)]);
-  }
-  worker_ptr[size_t(G)] = int32_t(chunks.size());
+  lists_to_chunks(lpt_assign(cost, G), units, worker_ptr, chunks);
   bskv_plan* p = new bskv_plan();
   p->kind = KIND_BSR;
   p->batch = batch; p->num_pages = num_pages; p->page_size = page_size;
