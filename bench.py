@@ -40,6 +40,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention KV GB/s (decode) and TFLOPS (BSR/MLA) as % of 1×GB300 roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+HEADLINE_WORKLOAD = ("paged_decode: batch 64, 32/8 heads, head_dim 128, bf16, page_size 16, "
+                     "kv len U[512,4096], pages permuted in a shared pool")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -216,9 +218,78 @@ def profile_traffic(summary_name, kernel_sources):
     return float(t.group(1))
 
 
+def measure_tensor_peaks(n=8192, iters=10):
+    """Dense tensor-core peaks of this GPU, measured in this run with library GEMMs
+    (n x n x n, 2 n^3 flops, best of `iters` CUDA-event timings after warm-up): bf16 and fp16
+    through torch.matmul, E4M3 x E4M3 -> bf16 through torch._scaled_mm (per-tensor scales).
+    These are the denominators of the fp16 (BSR) and FP8 (MLA) fractions; the bf16 figure is
+    reported beside MEASURED_PEAKS.json's."""
+    res = {"how": "2 n^3 / best of %d CUDA-event times, n = %d, after 3 warm-up calls" % (iters, n)}
+    g = torch.Generator(device="cuda").manual_seed(5)
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(iters):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return 2.0 * n ** 3 / (min(ts) * 1e-3) / 1e12
+
+    for name, dt in (("bf16", torch.bfloat16), ("fp16", torch.float16)):
+        try:
+            x = torch.randn((n, n), device="cuda", generator=g).to(dt)
+            y = torch.randn((n, n), device="cuda", generator=g).to(dt)
+            res[name + "_tflops"] = best(lambda: torch.matmul(x, y))
+            del x, y
+        except Exception as e:  # noqa: BLE001
+            res[name + "_tflops"] = None
+            res[name + "_error"] = str(e)[:200]
+    try:
+        x = torch.randn((n, n), device="cuda", generator=g).to(torch.float8_e4m3fn)
+        yt = torch.randn((n, n), device="cuda", generator=g).to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device="cuda")
+        res["fp8_e4m3_tflops"] = best(
+            lambda: torch._scaled_mm(x, yt.t(), scale_a=one, scale_b=one,
+                                     out_dtype=torch.bfloat16))
+        del x, yt
+    except Exception as e:  # noqa: BLE001
+        res["fp8_e4m3_tflops"] = None
+        res["fp8_e4m3_error"] = str(e)[:200]
+    torch.cuda.empty_cache()
+    return res
+
+
+def tensor_peak(peaks, tp, kind):
+    """(denominator, source) of a tensor-core fraction: fp16 and fp8 from this run's
+    measurement, bf16 from MEASURED_PEAKS.json (burst)."""
+    if kind == "bf16":
+        return peaks["bf16_tflops"], "bf16 dense burst (MEASURED_PEAKS.json)"
+    key = {"fp16": "fp16_tflops", "fp8": "fp8_e4m3_tflops"}[kind]
+    if tp and tp.get(key):
+        return tp[key], "%s dense, measured in this run (%s)" % (kind, tp["how"])
+    ratio = 2.0 if kind == "fp8" else 1.0
+    return ratio * peaks["bf16_tflops"], "%s = %g x bf16 burst (measurement failed: nominal ratio)" % (kind, ratio)
+
+
 # ---------------------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------------------
+
+TP = None  # tensor peaks measured in this run (rank 0), set by main()
+
+
+def variant_name(plan):
+    """Kernel that serves a BSR-family plan (metadata header word 15)."""
+    return {0: "general (mma.sync)", 1: "tcgen05", 2: "general (mma.sync)",
+            3: "general (mma.sync)", 4: "tcgen05", 5: "tcgen05"}.get(plan.metadata()[15], "?")
+
 
 def decode_kv_bytes(d):
     return int(d["kv_lens"].to(torch.int64).sum()) * d["num_kv_heads"] * d["head_dim"] * 2 * 2
@@ -364,9 +435,10 @@ def bench_bsr(bskv, synth, name, steps, warmup, peaks, flush):
     med = statistics.median(ms)
     tf = fl / (med * 1e-3) / 1e12
     variant = plan.metadata()[15]
+    pk, src = tensor_peak(peaks, TP, "fp16")
     return dict(workload=name, flops=fl, kernel="tcgen05" if variant == 1 else "general",
-                **summary(ms), tflops=tf, frac=tf / peaks["bf16_tflops"],
-                peak="bf16 dense burst (fp16 rate equal)")
+                **summary(ms), tflops=tf, frac=tf / pk, peak=src, peak_tflops=pk,
+                frac_of_bf16_burst=tf / peaks["bf16_tflops"])
 
 
 def bench_bsr_masked(bskv, synth, steps, warmup, peaks):
@@ -393,10 +465,10 @@ def bench_bsr_masked(bskv, synth, steps, warmup, peaks):
     ms = time_iters(fn, steps, warmup, flush=True)
     fl = bsr_flops(d)
     tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+    pk, src = tensor_peak(peaks, TP, "fp16")
     return dict(workload="bsr_prefill as a token mask (causal pattern in the diagonal blocks)",
                 flops=fl, kernel="tcgen05" if plan.metadata()[15] == 1 else "general",
-                **summary(ms), tflops=tf,
-                frac=tf / peaks["bf16_tflops"], peak="bf16 dense burst (fp16 rate equal)",
+                **summary(ms), tflops=tf, frac=tf / pk, peak=src, peak_tflops=pk,
                 mask_bytes=int(packed.numel()))
 
 
@@ -437,10 +509,11 @@ def bench_bsr_variable(bskv, synth, steps, warmup, peaks):
     ms = time_iters(fn, steps, warmup, flush=True)
     fl = variable_block_flops(d)
     tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+    pk, src = tensor_peak(peaks, TP, "fp16")
     return dict(workload="bsr_variable: 16384 tokens, 32/8 heads, D 128, fp16, 128 x 128 "
                          "blocks of random sizes per kv head, 10 % kept, causal (L2 flushed)",
-                flops=fl, kernel="general", **summary(ms), tflops=tf,
-                frac=tf / peaks["bf16_tflops"], peak="bf16 dense burst (fp16 rate equal)")
+                flops=fl, kernel=variant_name(plan), **summary(ms), tflops=tf,
+                frac=tf / pk, peak=src, peak_tflops=pk)
 
 
 def bench_prefill_paged(bskv, synth, steps, warmup, peaks):
@@ -460,10 +533,11 @@ def bench_prefill_paged(bskv, synth, steps, warmup, peaks):
         pairs += sum(min(L, t + L - nq + 1) for t in range(nq))
     fl = 4.0 * d["head_dim"] * d["num_qo_heads"] * pairs
     tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+    pk, src = tensor_peak(peaks, TP, "bf16")
     return dict(workload="prefill_paged: 16 requests, L ~ U[2048,8192], 1024 new tokens each, "
                          "32/8 heads, D 128, bf16, page 16, causal (L2 flushed)",
-                flops=fl, kernel="general", **summary(ms), tflops=tf,
-                frac=tf / peaks["bf16_tflops"], peak="bf16 dense burst")
+                flops=fl, kernel=variant_name(plan), **summary(ms), tflops=tf,
+                frac=tf / pk, peak=src, peak_tflops=pk)
 
 
 def bench_mla(bskv, synth, steps, warmup, peaks):
@@ -505,10 +579,10 @@ def bench_mla(bskv, synth, steps, warmup, peaks):
             ms = time_iters(fn, steps, warmup, flush=flush)
             fl = 2.0 * H * int(m["seq_lens"].sum()) * (576 + 512)
             tf = fl / (statistics.median(ms) * 1e-3) / 1e12
-            fp8_peak = 2.0 * peaks["bf16_tflops"]
+            fp8_peak, src = tensor_peak(peaks, TP, "fp8")
             res["decode_l2_flushed" if flush else "decode_l2_warm"] = dict(
-                **summary(ms), flops=fl, tflops=tf, frac=tf / fp8_peak,
-                peak="fp8 = 2 x measured bf16 dense burst (nominal ratio)")
+                **summary(ms), flops=fl, tflops=tf, frac=tf / fp8_peak, peak=src,
+                peak_tflops=fp8_peak)
     except bskv.BskvError as e:
         res["decode"] = "not available: %s" % e.status
     return res
@@ -533,10 +607,11 @@ def bench_mla_paged(bskv, synth, steps, warmup, peaks):
     med = statistics.median(ms) * 1e-3
     tf = fl / med / 1e12
     gbs = nbytes / med / 1e9
+    fp8_peak, src = tensor_peak(peaks, TP, "fp8")
     return dict(workload="mla_paged: batch 128, 128 heads, E4M3 rows of 576, page_size 64, "
                          "kv len U[2048,8192], pages permuted in a pool (L2 flushed)",
-                **summary(ms), flops=fl, tflops=tf, frac=tf / (2.0 * peaks["bf16_tflops"]),
-                peak="fp8 = 2 x measured bf16 dense burst (nominal ratio)",
+                **summary(ms), flops=fl, tflops=tf, frac=tf / fp8_peak, peak=src,
+                peak_tflops=fp8_peak,
                 bytes=nbytes, gbs=gbs, hbm_frac=gbs / peaks["hbm_gbs"],
                 launches_per_step=2 + (1 if plan.metadata()[6] > 0 else 0))
 
@@ -609,8 +684,7 @@ def run_reference(args):
             "ms_per_step": 1e3 * statistics.mean(x["seconds"] for x in vals),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": "paged_decode: batch 64, 32/8 heads, head_dim 128, bf16 "
-                                   "storage, page_size 16, kv len U[512,4096]",
+            "config": {"workload": HEADLINE_WORKLOAD,
                        "parallelism": "replicas" if args.gpus > 1 else "single"},
             "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -653,6 +727,10 @@ def main():
     status = bskv.bskv_get_device_status()
 
     extra = {}
+    global TP
+    if rank == 0 and rows & {"bsr_prefill", "bsr_tiny", "bsr_masked", "bsr_variable",
+                             "prefill_paged", "mla", "mla_paged"}:
+        TP = measure_tensor_peaks()
     if rank == 0:
         K = max(5, min(args.steps, 50))  # timed iterations per row (median and std reported)
         jobs = [("split", "split_decode", lambda: bench_split(bskv, synth, K, args.warmup, peaks)),
@@ -695,8 +773,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, random page permutation, NaN canary pages)",
-        "config": {"workload": "paged_decode: batch 64, 32/8 heads, head_dim 128, bf16, "
-                               "page_size 16, kv len U[512,4096], pages permuted in a shared pool",
+        "config": {"workload": HEADLINE_WORKLOAD,
                    "global_batch": 64 * args.gpus, "kv_bytes_per_step": head["kv_bytes"],
                    "l2": "inputs larger than L2 (0.6 GB KV per step)",
                    "parallelism": "replicas x%d" % args.gpus if args.gpus > 1 else "single"},
@@ -713,6 +790,7 @@ def main():
         "device_status": bskv.STATUS.get(status, status),
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "tensor_peaks": TP,
         "rows": extra,
     }
     print(json.dumps(line))

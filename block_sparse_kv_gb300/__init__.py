@@ -9,7 +9,6 @@ library's CUDA kernels; there is no CPU fallback. Importing works without a GPU
 """
 
 import ctypes
-import math
 import os
 
 import torch
@@ -241,7 +240,7 @@ def bskv_run_decode(plan, q, kv_cache, out=None, lse=None, return_lse=False, sm_
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     if sm_scale is None:
-        sm_scale = 1.0 / math.sqrt(D)
+        sm_scale = 0.0  # the library applies 1/sqrt(head_dim)
     fw = plan.float_ws
     ks = kv_cache.stride()
     _check(_entry, getattr(lib, _entry)(
@@ -274,8 +273,21 @@ def bskv_run_decode_noalloc(plan, q, kv_cache, out, lse=None, sm_scale=None):
     that cannot allocate (see bskv.h). The caller passes the output (and optional lse);
     the plan is not uploaded, its metadata goes into a library-owned static array."""
     lib = load_library()
+    B, Hq, D = q.shape
+    if plan.kind != "decode" or (B, Hq, D) != (plan.info["batch"], plan.info["num_qo_heads"],
+                                                plan.info["head_dim"]):
+        raise ValueError("q %s does not match the decode plan" % (tuple(q.shape),))
+    if tuple(out.shape) != (B, Hq, D) or out.dtype != plan.info["dtype"] or out.device != q.device:
+        raise ValueError("out must be a %s tensor of shape %s on %s"
+                         % (plan.info["dtype"], (B, Hq, D), q.device))
+    if lse is not None and (tuple(lse.shape) != (B, Hq) or lse.dtype != torch.float32
+                            or lse.device != q.device or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 tensor of shape %s on %s"
+                         % ((B, Hq), q.device))
+    if kv_cache.device != q.device:
+        raise ValueError("kv_cache must be on %s" % q.device)
     if sm_scale is None:
-        sm_scale = 1.0 / math.sqrt(q.shape[-1])
+        sm_scale = 0.0  # the library applies 1/sqrt(head_dim)
     ks = kv_cache.stride()
     _check("bskv_run_decode_noalloc", lib.bskv_run_decode_noalloc(
         plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), kv_cache.data_ptr(),
@@ -309,7 +321,7 @@ def bskv_run_bsr(plan, q, k, v, out=None, lse=None, return_lse=False, sm_scale=N
     if lse is None and return_lse:
         lse = torch.empty((M, Hq), dtype=torch.float32, device=q.device)
     if sm_scale is None:
-        sm_scale = 1.0 / math.sqrt(D)
+        sm_scale = 0.0  # the library applies 1/sqrt(head_dim)
     fw = plan.float_ws
     _check("bskv_run_bsr", lib.bskv_run_bsr(
         plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), k.data_ptr(),
@@ -347,7 +359,7 @@ def bskv_run_bsr_masked(plan, q, k, v, packed_mask, out=None, lse=None, return_l
     if lse is None and return_lse:
         lse = torch.empty((M, Hq), dtype=torch.float32, device=q.device)
     if sm_scale is None:
-        sm_scale = 1.0 / math.sqrt(D)
+        sm_scale = 0.0  # the library applies 1/sqrt(head_dim)
     _check("bskv_run_bsr_masked", lib.bskv_run_bsr_masked(
         plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), k.data_ptr(),
         _strides(k.stride(0), k.stride(1)), v.data_ptr(), _strides(v.stride(0), v.stride(1)),
@@ -387,7 +399,7 @@ def bskv_run_bsr_variable(plan, q, k, v, out=None, lse=None, return_lse=False, s
     if lse is None and return_lse:
         lse = torch.empty((Hq, L), dtype=torch.float32, device=q.device)
     if sm_scale is None:
-        sm_scale = 1.0 / math.sqrt(D)
+        sm_scale = 0.0  # the library applies 1/sqrt(head_dim)
     _check("bskv_run_bsr_variable", lib.bskv_run_bsr_variable(
         plan.handle, q.data_ptr(), _strides(q.stride(1), q.stride(0)), k.data_ptr(),
         _strides(k.stride(1), k.stride(0)), v.data_ptr(), _strides(v.stride(1), v.stride(0)),
@@ -429,7 +441,7 @@ def bskv_run_prefill_paged(plan, q, kv_cache, out=None, lse=None, return_lse=Fal
     if lse is None and return_lse:
         lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
     if sm_scale is None:
-        sm_scale = 1.0 / math.sqrt(D)
+        sm_scale = 0.0  # the library applies 1/sqrt(head_dim)
     _check("bskv_run_prefill_paged", lib.bskv_run_prefill_paged(
         plan.handle, q.data_ptr(), _strides(q.stride(0), q.stride(1)), kv_cache.data_ptr(),
         _strides(*kv_cache.stride()[:4]), out.data_ptr(), _strides(out.stride(0), out.stride(1)),

@@ -343,7 +343,7 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
   p.Hq = plan->num_qo_heads; p.Hkv = plan->num_kv_heads; p.group = p.Hq / p.Hkv;
   p.causal = plan->causal;
   p.mask = mask;
-  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
   if (bskv_status s = status_args(&p.st)) return s;
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
@@ -361,6 +361,7 @@ extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const 
                                     const int64_t* v_strides, void* out,
                                     const int64_t* out_strides, float* lse, float sm_scale,
                                     void* float_ws, size_t float_ws_bytes, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_bsr");
   (void)float_ws;
   (void)float_ws_bytes;
   if (plan && plan->masked) { set_error("run_bsr: the plan expects a token mask (bskv_run_bsr_masked)"); return BSKV_ERR_INVALID_ARG; }
@@ -376,6 +377,7 @@ extern "C" bskv_status bskv_run_bsr_masked(const bskv_plan* plan, const void* q,
                                            size_t packed_mask_bytes, void* out,
                                            const int64_t* out_strides, float* lse,
                                            float sm_scale, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_bsr_masked");
   if (!plan || plan->kind != KIND_BSR || !plan->masked) { set_error("run_bsr_masked: not a masked BSR plan (bskv_plan_bsr_masked)"); return BSKV_ERR_INVALID_ARG; }
   const int32_t MB = (plan->M + plan->R - 1) / plan->R;
   const int32_t* meta = plan->meta.data();
@@ -396,6 +398,7 @@ extern "C" bskv_status bskv_run_bsr_variable(const bskv_plan* plan, const void* 
                                              const int64_t* v_strides, void* out,
                                              const int64_t* out_strides, float* lse,
                                              float sm_scale, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_bsr_variable");
   if (!plan || plan->kind != KIND_BSR || !plan->meta.size() ||
       plan->meta[H_VARIANT] != BSR_VARIABLE) {
     set_error("run_bsr_variable: not a variable-block plan (bskv_plan_bsr_variable)");
@@ -410,6 +413,7 @@ extern "C" bskv_status bskv_run_prefill_paged(const bskv_plan* plan, const void*
                                               const int64_t* kv_strides, void* out,
                                               const int64_t* out_strides, float* lse,
                                               float sm_scale, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_prefill_paged");
   if (!plan || plan->kind != KIND_BSR || plan->meta.empty() ||
       plan->meta[H_VARIANT] != BSR_PAGED_PREFILL) {
     set_error("run_prefill_paged: not a paged prefill plan (bskv_plan_prefill_paged)");
@@ -442,7 +446,7 @@ extern "C" bskv_status bskv_run_prefill_paged(const bskv_plan* plan, const void*
   p.Hq = plan->num_qo_heads; p.Hkv = plan->num_kv_heads; p.group = p.Hq / p.Hkv;
   p.causal = plan->causal;
   p.mask = nullptr;
-  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
   if (bskv_status s = status_args(&p.st)) return s;
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;

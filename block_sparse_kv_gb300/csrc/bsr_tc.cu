@@ -623,7 +623,7 @@ bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64
   tp.M = plan->M; tp.N = plan->N; tp.Hq = plan->num_qo_heads; tp.Hkv = plan->num_kv_heads;
   tp.group = g; tp.causal = plan->causal;
   tp.mask = reinterpret_cast<const unsigned long long*>(mask);
-  tp.scale_log2 = sm_scale * 1.4426950408889634f;
+  tp.scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
   if (bskv_status s = status_args(&tp.st)) return s;
   const CUtensorMapDataType dt =
       plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;

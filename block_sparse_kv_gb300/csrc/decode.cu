@@ -929,7 +929,7 @@ bskv_status prepare_decode(const char* who, const bskv_plan* plan, const int32_t
   dp->num_kv_heads = Hkv; dp->group = plan->num_qo_heads / Hkv; dp->page_size = ps;
   dp->num_qo_heads = plan->num_qo_heads;
   dp->heads_per_unit = sh.heads_per_unit;
-  dp->scale_log2 = sm_scale * 1.4426950408889634f;
+  dp->scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
   if (bskv_status s = status_args(&dp->st)) return s;
   const uint64_t dims[5] = {uint64_t(D), uint64_t(ps), uint64_t(Hkv), 2, uint64_t(plan->num_pages)};
   const uint64_t strides[4] = {uint64_t(kv_strides[3]) * esz, uint64_t(kv_strides[2]) * esz,
@@ -963,6 +963,7 @@ extern "C" bskv_status bskv_run_decode_partial(const bskv_plan* plan, const void
                                        const int64_t* kv_strides, void* out,
                                        const int64_t* out_strides, float* lse, float sm_scale,
                                        void* float_ws, size_t float_ws_bytes, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_decode_partial");
   if (!plan || plan->kind != KIND_DECODE) { set_error("run_decode: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_decode: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (bskv_status s = check_decode_ws(plan, float_ws, float_ws_bytes)) return s;
@@ -978,6 +979,7 @@ extern "C" bskv_status bskv_run_decode_partial(const bskv_plan* plan, const void
 extern "C" bskv_status bskv_decode_merge(const bskv_plan* plan, void* out,
                                          const int64_t* out_strides, float* lse,
                                          void* float_ws, size_t float_ws_bytes, void* stream) {
+  BSKV_NVTX_RANGE("bskv_decode_merge");
   if (!plan || plan->kind != KIND_DECODE) { set_error("decode_merge: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("decode_merge: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (!out_strides) { set_error("decode_merge: NULL strides"); return BSKV_ERR_INVALID_ARG; }
@@ -998,6 +1000,7 @@ extern "C" bskv_status bskv_run_decode(const bskv_plan* plan, const void* q,
                                        const int64_t* kv_strides, void* out,
                                        const int64_t* out_strides, float* lse, float sm_scale,
                                        void* float_ws, size_t float_ws_bytes, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_decode");
   if (!plan || plan->kind != KIND_DECODE) { set_error("run_decode: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_decode: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (bskv_status s = check_decode_ws(plan, float_ws, float_ws_bytes)) return s;
@@ -1027,6 +1030,7 @@ extern "C" bskv_status bskv_merge_states(const float* v, const float* s, int64_t
                                          int32_t num_states, int32_t num_heads,
                                          int32_t head_dim, void* v_out, int32_t out_dtype,
                                          float* s_out, void* stream) {
+  BSKV_NVTX_RANGE("bskv_merge_states");
   if (seq_len < 0 || num_states < 1 || num_heads < 1 || head_dim < 4 || head_dim % 4) {
     set_error("merge_states: seq_len=%lld num_states=%d num_heads=%d head_dim=%d", (long long)seq_len, num_states, num_heads, head_dim);
     return BSKV_ERR_INVALID_ARG;
@@ -1116,6 +1120,7 @@ extern "C" bskv_status bskv_run_decode_noalloc(const bskv_plan* plan, const void
                                                const int64_t* kv_strides, void* out,
                                                const int64_t* out_strides, float* lse,
                                                float sm_scale, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_decode_noalloc");
   if (!plan || plan->kind != KIND_DECODE) { set_error("run_decode_noalloc: not a decode plan"); return BSKV_ERR_INVALID_ARG; }
   const size_t meta_words = plan->meta.size();
   if (meta_words > kNoAllocMetaWords || plan->float_ws_bytes > kNoAllocScratchBytes) {

@@ -1,10 +1,13 @@
 // Internal declarations shared by the host core and the kernel launchers of libbskv.
 #pragma once
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 #include <string>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/bskv.h"
 
@@ -75,6 +78,27 @@ inline int32_t decode_group_heads(int32_t num_kv_heads, int32_t page_size) {
 
 // Byte offset in the int workspace of the merge counters (after the metadata).
 inline size_t merge_counter_offset(size_t meta_words) { return ((meta_words * 4 + 255) / 256) * 256; }
+
+// Softmax scale of a run: the caller's value, or for 0 the pages' default 1/sqrt(head_dim)
+// ("flashinfer.sparse", BlockSparseAttentionWrapper.plan: sm_scale defaults to
+// 1/sqrt(head_dim)), as log2(e) * scale for the kernels' exp2 arithmetic.
+inline float sm_scale_log2(float sm_scale, int32_t head_dim) {
+  const float s = sm_scale == 0.f ? float(1.0 / std::sqrt(double(head_dim))) : sm_scale;
+  return s * 1.4426950408889634f;
+}
+
+// NVTX range around one public call (its launches show up under the call's name in a
+// profiler timeline; without a profiler attached the push and pop return at once).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define BSKV_NVTX_RANGE(name) ::bskv::NvtxRange bskv_nvtx_range_(name)
+
+// BSKV_LOGLEVEL from the environment (0 when unset): 1 = one line per plan, 2 = more.
+int log_level();
 
 void set_error(const char* fmt, ...);
 const char* dtype_name(int32_t dt);

@@ -801,6 +801,7 @@ extern "C" bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* qu
                                            const int32_t* indices, float bmm1_scale,
                                            float bmm2_scale, void* out, float* lse,
                                            void* float_ws, size_t float_ws_bytes, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_mla_sparse");
   if (!plan || plan->kind != KIND_MLA || plan->mla_variant != MLA_SPARSE) { set_error("run_mla_sparse: not a sparse MLA plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_mla_sparse: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (plan->batch == 0) return BSKV_OK;
@@ -823,6 +824,7 @@ extern "C" bskv_status bskv_run_mla_paged(const bskv_plan* plan, const void* que
                                           const void* kv_pages, float bmm1_scale,
                                           float bmm2_scale, void* out, float* lse,
                                           void* float_ws, size_t float_ws_bytes, void* stream) {
+  BSKV_NVTX_RANGE("bskv_run_mla_paged");
   if (!plan || plan->kind != KIND_MLA || plan->mla_variant != MLA_PAGED) { set_error("run_mla_paged: not a paged MLA plan"); return BSKV_ERR_INVALID_ARG; }
   if (!plan->meta_dev) { set_error("run_mla_paged: plan not uploaded (bskv_plan_upload)"); return BSKV_ERR_INVALID_ARG; }
   if (plan->batch == 0) return BSKV_OK;

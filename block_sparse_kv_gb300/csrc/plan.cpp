@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <queue>
 #include <utility>
@@ -166,7 +167,55 @@ void lists_to_chunks(const std::vector<std::vector<int32_t>>& lists,
   worker_ptr[lists.size()] = int32_t(chunks.size());
 }
 
+// One line per plan on stderr when BSKV_LOGLEVEL >= 1 (plus the spread of work items over
+// the workers at level 2), taken from the metadata the kernels will read.
+void log_plan(const char* name, const bskv_plan* p) {
+  const int lvl = log_level();
+  if (lvl < 1) return;
+  const std::vector<int32_t>& m = p->meta;
+  const char* kernel = "?";
+  switch (m[H_KIND]) {
+    case KIND_DECODE:
+      kernel = m[H_VARIANT] == DECODE_GROUP ? "decode_group_kernel (page-major CTAs)"
+                                            : "decode_kernel (one worker per warp)";
+      break;
+    case KIND_BSR:
+      kernel = m[H_VARIANT] == BSR_TCGEN05 ? "bsr_tc_kernel (tcgen05)"
+               : m[H_VARIANT] == BSR_VARIABLE ? "bsr_generic_kernel (variable blocks)"
+               : m[H_VARIANT] == BSR_PAGED_PREFILL ? "bsr_generic_kernel (paged prefill)"
+                                                   : "bsr_generic_kernel";
+      break;
+    case KIND_MLA:
+      kernel = p->mla_variant == MLA_PAGED ? "mla_page_rows_kernel + mla_kernel (paged rows)"
+                                           : "mla_kernel (sparse rows)";
+      break;
+    default:
+      break;
+  }
+  const size_t int_ws = merge_counter_offset(m.size()) + p->counter_words * 4;
+  std::fprintf(stderr,
+               "[bskv] %s: kernel %s; units %d, workers %d, work items %d, split pieces %d, "
+               "merged units %d, grid %d CTAs; int workspace %zu B, float workspace %zu B\n",
+               name, kernel, m[H_UNITS], m[H_WORKERS], m[H_CHUNKS], m[H_SLOTS], m[H_MERGES],
+               m[H_GRID], int_ws, p->float_ws_bytes);
+  if (lvl >= 2 && m[H_WORKERS] > 0) {
+    const int32_t* wp = m.data() + m[H_OFF_WORKERS];
+    int32_t lo = wp[1] - wp[0], hi = lo;
+    for (int32_t w = 1; w < m[H_WORKERS]; ++w) {
+      lo = std::min(lo, wp[w + 1] - wp[w]);
+      hi = std::max(hi, wp[w + 1] - wp[w]);
+    }
+    std::fprintf(stderr, "[bskv] %s: work items per worker min %d, mean %.2f, max %d\n", name, lo,
+                 double(m[H_CHUNKS]) / m[H_WORKERS], hi);
+  }
+}
+
 }  // namespace
+
+int log_level() {
+  const char* e = std::getenv("BSKV_LOGLEVEL");
+  return e ? std::atoi(e) : 0;
+}
 
 }  // namespace bskv
 
@@ -249,6 +298,7 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
   p->counter_words = merges.size() / 3 * size_t(num_kv_heads / upb);
   for (size_t i = 2; i < merges.size(); i += 3) p->max_merge_count = std::max(p->max_merge_count, merges[i]);
   *out_plan = p;
+  log_plan("bskv_plan_decode", p);
   return BSKV_OK;
 }
 
@@ -325,6 +375,7 @@ bskv_status plan_bsr(const int32_t* indptr, const int32_t* indices, int32_t M, i
   p->float_ws_bytes = 0;
   p->masked = masked ? 1 : 0;
   *out_plan = p;
+  log_plan(masked ? "bskv_plan_bsr_masked" : "bskv_plan_bsr", p);
   return BSKV_OK;
 }
 
@@ -434,6 +485,7 @@ extern "C" bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map,
            desc.data(), desc.size(), tiles.data(), tiles.size(), U > 0 ? G : 0, BSR_VARIABLE);
   p->float_ws_bytes = 0;
   *out_plan = p;
+  log_plan("bskv_plan_bsr_variable", p);
   return BSKV_OK;
 }
 
@@ -532,6 +584,7 @@ extern "C" bskv_status bskv_plan_prefill_paged(const int32_t* qo_indptr, const i
            BSR_PAGED_PREFILL);
   p->float_ws_bytes = 0;
   *out_plan = p;
+  log_plan("bskv_plan_prefill_paged", p);
   return BSKV_OK;
 }
 
@@ -582,6 +635,7 @@ extern "C" bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t bat
       : align256(size_t(slots) * kMlaVSplit * 128 * kMlaVDim * 4) +
             align256(size_t(slots) * kMlaVSplit * 128 * 4);
   *out_plan = p;
+  log_plan("bskv_plan_mla_sparse", p);
   return BSKV_OK;
 }
 
@@ -648,6 +702,7 @@ extern "C" bskv_status bskv_plan_mla_paged(const int32_t* kv_indptr, const int32
   p->mla_rows_off = partials;
   p->float_ws_bytes = partials + align256(size_t(batch) * size_t(stride) * 4);
   *out_plan = p;
+  log_plan("bskv_plan_mla_paged", p);
   return BSKV_OK;
 }
 

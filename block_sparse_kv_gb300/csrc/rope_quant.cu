@@ -380,6 +380,7 @@ extern "C" bskv_status bskv_rope_quantize_fp8(
     void* k_rope_out, int64_t k_rope_out_stride, void* k_nope_out, int64_t k_nope_out_stride,
     int32_t pos_dtype, const void* cos_sin, int32_t cos_sin_dtype, int64_t max_seq_len,
     int32_t is_neox, float quant_scale_q, float quant_scale_kv, void* stream) {
+  BSKV_NVTX_RANGE("bskv_rope_quantize_fp8");
   return rope_entry(q_rope, q_rope_strides, q_nope, q_nope_strides, pos_q, nnz_q, num_heads,
                     q_rope_out, q_rope_out_strides, q_nope_out, q_nope_out_strides, k_rope,
                     k_rope_stride, k_nope, k_nope_stride, pos_k, nnz_k, k_rope_out,
@@ -399,6 +400,7 @@ extern "C" bskv_status bskv_rope_quantize_fp8_append_paged(
     void* kv_pages, int32_t pos_dtype, const void* cos_sin, int32_t cos_sin_dtype,
     int64_t max_seq_len, int32_t is_neox, float quant_scale_q, float quant_scale_kv,
     void* stream) {
+  BSKV_NVTX_RANGE("bskv_rope_quantize_fp8_append_paged");
   if (!k_rope || !k_nope || !pos_k || !batch_indices || !positions || !kv_indptr ||
       !kv_indices || !kv_pages) {
     set_error("rope_quantize_fp8_append_paged: the key rows, their positions, batch_indices, "

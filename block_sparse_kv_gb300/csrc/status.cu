@@ -95,6 +95,7 @@ extern "C" bskv_status bskv_set_debug_force_timeout(int32_t on) {
 
 extern "C" bskv_status bskv_plan_upload(bskv_plan* plan, void* int_ws, size_t int_ws_bytes,
                                         void* stream) {
+  BSKV_NVTX_RANGE("bskv_plan_upload");
   if (!plan) { set_error("plan_upload: NULL plan"); return BSKV_ERR_INVALID_ARG; }
   const size_t meta_bytes = plan->meta.size() * sizeof(int32_t);
   const size_t cnt_off = merge_counter_offset(plan->meta.size());

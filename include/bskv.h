@@ -43,6 +43,14 @@
  *   - LSE is the natural-log log-sum-exp of the scaled logits ([SPARSE] run(): "the
  *     log-sum-exp of attention logits"); a row that sees no key gets out = 0 and
  *     lse = -inf.
+ *   - sm_scale (decode, prefill and BSR runs) multiplies q.k before the softmax; the value
+ *     0 selects the pages' default 1/sqrt(head_dim) ([SPARSE] plan(): sm_scale defaults to
+ *     1/sqrt(head_dim)). The MLA runs take their scales explicitly (bmm1/bmm2).
+ *   - Setting the environment variable BSKV_LOGLEVEL to 1 makes every bskv_plan_* call print
+ *     one line about its decisions (units, workers, split pieces, kernel, workspace bytes) to
+ *     stderr; 2 adds the per-worker load spread. Every bskv_run_* / bskv_rope_* /
+ *     bskv_merge_states call opens an NVTX range of its own name around its launches (a
+ *     no-op unless a profiler is attached).
  */
 #ifndef BSKV_H_
 #define BSKV_H_
@@ -294,6 +302,8 @@ bskv_status bskv_decode_merge(const bskv_plan* plan, void* out, const int64_t* o
  * make that first call before any stream capture. All calls share the two arrays, and
  * each call overwrites what the previous one left there, so calls that overlap on the GPU
  * (e.g. on two streams) race: serialise them. No call allocates or frees device memory.
+ * The metadata copy reads the plan's own host memory, which is pageable: the call can wait
+ * while the driver stages those bytes, and the plan is no longer read once the call returns.
  */
 bskv_status bskv_run_decode_noalloc(const bskv_plan* plan, const void* q,
                                     const int64_t* q_strides, const void* kv_cache,

@@ -1,5 +1,9 @@
 """GPU parity of merge_states and of the general BSR kernel against the oracle."""
 
+import json
+import math
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -44,6 +48,33 @@ def _bsr_case(cuda, d, dtype):
     st = assert_close(to64(out), ref, TOL, TOL, "out")
     assert_close(lse.cpu().numpy(), ref_lse, TOL, TOL, "lse")
     return st, p
+
+
+def test_bsr_worked_example(cuda):
+    """The page's own example: M = N = 3, R = C = 1, 32 query / 8 kv heads, head_dim 128,
+    fp16, the 3 x 3 block mask from tests/golden (its dense mask as printed). The GPU result
+    equals the oracle's dense attention under that mask, and the default scale (0 = the
+    library's 1/sqrt(head_dim)) gives the same bits as passing 1/sqrt(128)."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    ex = json.load(open(os.path.join(here, "golden", "bsr_worked_example.json")))
+    M, N, R, C = ex["M"], ex["N"], ex["R"], ex["C"]
+    Hq, Hkv, D = ex["num_qo_heads"], ex["num_kv_heads"], ex["head_dim"]
+    d = synth.bsr_inputs(7, M, N, R, C, Hq, Hkv, D, pattern="full")
+    indptr = torch.tensor(ex["indptr"], dtype=torch.int32)
+    indices = torch.tensor(ex["indices"], dtype=torch.int32)
+    p = bskv.bskv_plan_bsr(indptr, indices, M, N, R, C, Hq, Hkv, D, dtype=torch.float16)
+    q, k, v = d["q"].to(cuda), d["k"].to(cuda), d["v"].to(cuda)
+    out, lse = bskv.bskv_run_bsr(p, q, k, v, return_lse=True)
+    out2 = bskv.bskv_run_bsr(p, q, k, v, sm_scale=1.0 / math.sqrt(D))
+    torch.cuda.synchronize()
+    assert bskv.bskv_get_device_status() == 0
+    assert torch.equal(out, out2)
+    mask = att.bsr_mask(ex["indptr"], ex["indices"], M, N, R, C)
+    np.testing.assert_array_equal(mask, np.array(ex["mask"], dtype=bool))
+    ref, ref_lse = att.bsr_attention(bits(d["q"]), bits(d["k"]), bits(d["v"]), "fp16",
+                                     ex["indptr"], ex["indices"], M, N, R, C)
+    assert_close(to64(out), ref, TOL, TOL, "out")
+    assert_close(lse.cpu().numpy(), ref_lse, TOL, TOL, "lse")
 
 
 def test_bsr_tiny_workload(cuda):

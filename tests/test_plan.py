@@ -1,6 +1,10 @@
 """Plans: bit-exact metadata against the oracle's restatement, invariants, and host-side
 fault injection (every malformed input is rejected before anything is launched)."""
 
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -342,3 +346,28 @@ def test_prefill_plan_tiles_address_every_key_once(lib):
                 assert page == ix[ip[b] + k // ps] and slot + (k - k0) == k % ps
                 covered.append(k)
         assert covered == list(range(lengths[b]))
+
+
+def test_plan_log_lines():
+    """BSKV_LOGLEVEL=2 makes a plan print its decisions (kernel, units, workers, workspace
+    bytes) and the per-worker spread to stderr; unset, a plan prints nothing."""
+    code = ("import torch, block_sparse_kv_gb300 as b, synth\n"
+            "d = synth.make('paged_decode')\n"
+            "b.bskv_plan_decode(d['kv_indptr'], d['kv_indices'], d['kv_last_page_len'],"
+            " d['num_pages'], 16, 32, 8, 128, torch.bfloat16, num_sms=152)\n"
+            "t = synth.make('bsr_tiny')\n"
+            "b.bskv_plan_bsr(t['indptr'], t['indices'], 64, 64, 16, 16, 4, 2, 64, num_sms=152)\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, BSKV_LOGLEVEL="2", PYTHONPATH=root)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       cwd=root, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[bskv]")]
+    assert any("bskv_plan_decode: kernel decode_group_kernel" in ln and "workers 152" in ln
+               for ln in lines), lines
+    assert any("bskv_plan_bsr: kernel bsr_generic_kernel" in ln for ln in lines), lines
+    assert any("work items per worker" in ln for ln in lines), lines
+    env["BSKV_LOGLEVEL"] = "0"
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       cwd=root, timeout=300)
+    assert r.returncode == 0 and "[bskv]" not in r.stderr
