@@ -13,7 +13,7 @@
 // each CTA gathers half of a tile's rows and pushes them into its partner's shared memory.
 // TMEM (512 columns): O (256), the query's 512 latent bytes as the E4M3 A operand of QK
 // (128, four values per column), S (128). Shared memory: the query's 64-byte rotated tail,
-// P (E4M3, two buffers), and the gathered tiles split by lifetime: a K part (the other
+// P (the hi and lo E4M3 terms of one tile), and the gathered tiles split by lifetime: a K part (the other
 // latent half and the tail, freed once QK has read it; two slots) and a V part (the unit's
 // latent half, freed after PV; three slots).
 //   warps 0-5  gather: 192 threads copy this CTA's 64 rows of a tile (16-byte cp.async into
@@ -22,14 +22,16 @@
 //              are fetched one tile ahead;
 //   warp 6     allocates TMEM; one elected lane of the converged warp issues QK (16 MMAs
 //              with A in TMEM, 2 with the tail in shared memory, N = 128) and PV (A = P in
-//              shared memory, B = the V part read MN-major, N = 256); slot releases are
+//              shared memory, B = the V part read MN-major, N = 256; once for the hi and once
+//              for the lo terms of P, into the same accumulator); slot releases are
 //              committed to both CTAs' barriers;
 //   warp 7     TMA-loads the query tail once per token;
 //   warps 8-15 two softmax warpgroups; thread = head = TMEM lane, each group owns 64 of a
 //              tile's columns and 128 of the 256 output values: it reads S (and releases it
 //              for the next QK at once), combines the row max with the other group, applies
-//              lazy rescaling (threshold 2^8), forms P with packed f16x2 exponentials converted
-//              to E4M3, and writes O (bf16) or the split-KV partial state in the epilogue
+//              lazy rescaling (threshold 2^4), forms 16 P with packed f16x2 exponentials and
+//              splits it into two E4M3 terms (hi = e4m3(16 P), lo = e4m3(16 P - hi)), and writes
+//              O (bf16) or the split-KV partial state in the epilogue
 //              (per warp, 128B-swizzled boxes in the idle P buffers and tensor stores); at a
 //              token's last tile it also writes the next token's query into TMEM.
 #include <cuda_fp8.h>
@@ -91,7 +93,7 @@ struct MlaParams {
 struct Bars {
   uint64_t q_full, qr_full, q_empty, drain;
   uint64_t kv_full[kVSlots], v_empty[kVSlots], k_empty[kKSlots];
-  uint64_t s_full, s_empty, p_full[2], o_done[2];
+  uint64_t s_full, s_empty, p_full, o_done;
   uint64_t o_free;
   uint32_t tmem_base;
   int abort;
@@ -113,9 +115,23 @@ __device__ __forceinline__ uint32_t half2_to_e4m3x2(__half2 x) {
   return out;
 }
 
+// Two E4M3 values (low byte, high byte) to f16 (low, high); exact.
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t x) {
+  const uint16_t in = uint16_t(x);
+  uint32_t out;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(in));
+  return *reinterpret_cast<__half2*>(&out);
+}
+
 // Query token of a chunk (a unit is one query token; the CTA pair splits its latent halves).
 __device__ __forceinline__ int chunk_token(const int4& ch) { return ch.x; }
 
+// The softmax weights enter PV as two E4M3 terms: 16 p ~ hi + lo with hi = e4m3(16 p) and
+// lo = e4m3(16 p - hi), both multiplied with the same V into the same accumulator, so a weight
+// carries about 2^-8 relative rounding instead of the 2^-4 of a single E4M3 code (which, with
+// the weights split between two groups of rows of different values, can move an output by
+// twice the FP8 tolerance at any list length). The two P buffers hold hi and lo of one tile,
+// a tile's PV is 8 MMAs, and the lazy-rescale threshold is 2^4 so that 16 p stays below 448.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap qmap_rope, const __grid_constant__ CUtensorMap omap,
                const __grid_constant__ CUtensorMap wmap, const MlaParams p) {
@@ -147,10 +163,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kKSlots; ++s) mbar_init(&B.k_empty[s], 2);
     mbar_init(&B.s_full, 1);
     mbar_init(&B.s_empty, 256);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&B.p_full[b], 256);
-      mbar_init(&B.o_done[b], 1);
-    }
+    mbar_init(&B.p_full, 256);
+    mbar_init(&B.o_done, 1);
     mbar_init(&B.o_free, 256);
     B.abort = 0;
     fence_mbar_init();
@@ -324,17 +338,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t dkn = umma_desc(sbase + kSmemK, 16, 1024, kSwz128);
       const uint64_t dvn = umma_desc(sbase + kSmemV, 16, 1024, kSwz128);
       const uint64_t dkr = umma_desc(sbase + kSmemK + 2 * kPanel, 16, 512, kSwz64);
+      // PV of tile g: P buffer 0 holds the hi terms, buffer 1 the lo terms (one p_full and
+      // one o_done phase per tile)
       auto pv = [&](uint32_t g, bool first) -> bool {
-        const uint32_t b = g & 1u, v = g % kVSlots;
-        if (!issuer_wait(&B.p_full[b], (g >> 1) & 1u, p.st, forced, abort_flag)) return false;
+        const uint32_t v = g % kVSlots;
+        if (!issuer_wait(&B.p_full, g & 1u, p.st, forced, abort_flag)) return false;
         if (first && !issuer_wait(&B.o_free, (cc & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
         tc_fence_after();
-        const uint64_t a0 = dp + ((b * kPBytes) >> 4);
         const uint64_t b0 = dv + ((v * kVPart) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kRows / 32; ++kk)
-          umma_f8_w(leader, tmem, a0 + kk * 2, b0 + kk * 256, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        umma_commit_w(leader, &B.o_done[b]);
+          umma_f8_w(leader, tmem, dp + kk * 2, b0 + kk * 256, idesc_pv, (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+        for (int kk = 0; kk < kRows / 32; ++kk)
+          umma_f8_w(leader, tmem, dp + (kPBytes >> 4) + kk * 2, b0 + kk * 256, idesc_pv, 1u);
+        umma_commit_w(leader, &B.o_done);
         umma_commit_mc_w(leader, &B.v_empty[v], 0x3);  // both CTAs' V part free
         return true;
       };
@@ -391,17 +409,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(q4 * 32) << 16;
     float* red = reinterpret_cast<float*>(sm + kSmemRed);  // [slot][group][row]
     uint32_t G = 0, qc = 0;
-    uint32_t od_next[2] = {0u, 1u};  // next tile of each parity whose PV is not yet waited for
+    uint32_t od_next = 0;  // next tile whose PV is not yet waited for
     bool ok = true;
-    // Wait for the PVs of all tiles up to `upto` (the two o_done barriers take alternate
-    // tiles, so neither falls two phases behind).
+    // Wait for the PVs of all tiles up to `upto` (o_done completes one phase per tile).
     auto consume = [&](int64_t upto) -> bool {
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        while (int64_t(od_next[b]) <= upto) {
-          if (!warp_wait(&B.o_done[b], (od_next[b] >> 1) & 1u, p.st, forced, abort_flag)) return false;
-          od_next[b] += 2;
-        }
+      while (int64_t(od_next) <= upto) {
+        if (!warp_wait(&B.o_done, od_next & 1u, p.st, forced, abort_flag)) return false;
+        ++od_next;
       }
       return true;
     };
@@ -448,7 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int n_next = ci + 1 < c1 && chunk_token(chunks[ci + 1]) != n ? chunk_token(chunks[ci + 1]) : -1;
       float m_run = -INFINITY, l_run = 0.f;
       for (int t = 0; t < nt; ++t, ++G) {
-        const uint32_t b = G & 1u;
+        const uint32_t b = G & 1u;  // tile parity: slot of the row-max exchange
         bool good = warp_wait(&B.s_full, G & 1u, p.st, forced, abort_flag);
         uint32_t sr[64];
         if (good) {
@@ -495,23 +509,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool rescale = false;
         if (m_run == -INFINITY) {
           m_use = mx;
-        } else if (mx > m_run + 8.f) {
+        } else if (mx > m_run + 4.f) {
           m_use = mx;
           alpha = fast_exp2(m_run - mx);
           rescale = true;
         }
         const float ref = m_use == -INFINITY ? 0.f : m_use;
         rescale = __any_sync(0xffffffffu, rescale);
-        // P buffer b was last read by the PV of tile G - 2.
-        if (!consume(int64_t(G) - 2)) { ok = false; break; }
-        // p = 2^(x - ref) in f16x2 pairs, straight to E4M3 pairs, 16 keys (one 16-byte chunk
-        // of the 128B-swizzled P row) at a time; row sum in f16x2.
-        uint8_t* prow = sm + kSmemP + b * kPBytes + r * 128;
-        const float2 one2 = make_float2(1.f, 1.f), nr2 = make_float2(-ref, -ref);
+        // The P buffers were last read by the PV of tile G - 1.
+        if (!consume(int64_t(G) - 1)) { ok = false; break; }
+        // 16 p = 2^(x - ref + 4) in f16x2 pairs, straight to E4M3 pairs (hi and lo terms),
+        // 16 keys (one 16-byte chunk of the 128B-swizzled P row) at a time; row sum of 16 p in
+        // f16x2 (the LSE takes the 2^4 out again).
+        uint8_t* prow = sm + kSmemP + r * 128;
+        const float2 one2 = make_float2(1.f, 1.f), nr2 = make_float2(4.f - ref, 4.f - ref);
         __half2 hs[4];
 #pragma unroll
         for (int c16 = 0; c16 < 4; ++c16) {
-          uint32_t pk[4];
+          uint32_t pk[4], lk[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int c = c16 * 16 + j * 4;
@@ -521,10 +536,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const __half2 e1 = h2exp2_approx(__floats2half2_rn(d1.x, d1.y));
             const __half2 s2 = __hadd2(e0, e1);
             hs[j] = c16 == 0 ? s2 : __hadd2(hs[j], s2);
-            pk[j] = half2_to_e4m3x2(e0) | (half2_to_e4m3x2(e1) << 16);
+            const uint32_t h0 = half2_to_e4m3x2(e0), h1 = half2_to_e4m3x2(e1);
+            pk[j] = h0 | (h1 << 16);
+            // the remainder after the first code is exact in f16; its own code is the lo term
+            const __half2 r0 = __hsub2(e0, e4m3x2_to_half2(h0));
+            const __half2 r1 = __hsub2(e1, e4m3x2_to_half2(h1));
+            lk[j] = half2_to_e4m3x2(r0) | (half2_to_e4m3x2(r1) << 16);
           }
           const int cc = 4 * wg + c16;
           *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(prow + kPBytes + ((cc ^ (r & 7)) << 4)) =
+              make_uint4(lk[0], lk[1], lk[2], lk[3]);
         }
         const float2 fs = __half22float2(__hadd2(__hadd2(hs[0], hs[1]), __hadd2(hs[2], hs[3])));
         l_run = l_run * alpha + (fs.x + fs.y);
@@ -546,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&B.p_full[b]);
+        mbar_arrive(&B.p_full);
       }
       if (!ok) break;
       // Epilogue: combine the two partial row sums, then each group stores its 128 values.
@@ -557,7 +579,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!consume(int64_t(G) - 1)) { ok = false; break; }
       tc_fence_after();
       const float scale = l_tot > 0.f ? p.bmm2 / l_tot : 0.f;
-      const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
+      // (l_tot sums 16 p: the LSE takes the 2^4 out)
+      const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot) - 4.f) * kLn2 : -INFINITY;
       const bool row_ok = r < p.heads;
       const int slot = ch.w;
       // Each warp stages its 32 heads x 128 bytes of a box (128B-swizzled) in its own 4 KB of
