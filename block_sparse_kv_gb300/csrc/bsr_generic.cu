@@ -286,6 +286,10 @@ bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64
                                const void* k, const int64_t* ks, const void* v,
                                const int64_t* vs, void* out, const int64_t* os, float* lse,
                                float sm_scale, const uint8_t* mask, cudaStream_t st);
+bskv_status launch_prefill_tcgen05(const bskv_plan* plan, const void* q, const int64_t* qs,
+                                   const void* kv, const int64_t* kvs, void* out,
+                                   const int64_t* os, float* lse, float sm_scale,
+                                   cudaStream_t st);
 
 }  // namespace bskv
 
@@ -309,8 +313,9 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
                     const void* k, const int64_t* k_strides, const void* v,
                     const int64_t* v_strides, void* out, const int64_t* out_strides, float* lse,
                     float sm_scale, const uint8_t* mask, void* stream) {
-  const bool var = plan && plan->kind == KIND_BSR && meta_word(plan, H_VARIANT) == BSR_VARIABLE;
-  if (plan && plan->kind == KIND_BSR && meta_word(plan, H_VARIANT) == BSR_PAGED_PREFILL) {
+  const int variant = plan && plan->kind == KIND_BSR ? meta_word(plan, H_VARIANT) : -1;
+  const bool var = variant == BSR_VARIABLE;
+  if (variant == BSR_PAGED_PREFILL || variant == BSR_PAGED_PREFILL_TC) {
     set_error("run_bsr: a paged prefill plan runs through bskv_run_prefill_paged");
     return BSKV_ERR_INVALID_ARG;
   }
@@ -326,7 +331,7 @@ bskv_status run_bsr(const bskv_plan* plan, const void* q, const int64_t* q_strid
     }
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) { set_error("run_bsr: tensors must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (meta_word(plan, H_VARIANT) == BSR_TCGEN05)
+  if (variant == BSR_TCGEN05 || variant == BSR_VARIABLE_TC)
     return launch_bsr_tcgen05(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides,
                               lse, sm_scale, mask, st);
   BsrParams p{};
@@ -365,7 +370,11 @@ extern "C" bskv_status bskv_run_bsr(const bskv_plan* plan, const void* q, const 
   (void)float_ws;
   (void)float_ws_bytes;
   if (plan && plan->masked) { set_error("run_bsr: the plan expects a token mask (bskv_run_bsr_masked)"); return BSKV_ERR_INVALID_ARG; }
-  if (plan && plan->kind == KIND_BSR && meta_word(plan, H_VARIANT) == BSR_VARIABLE) { set_error("run_bsr: a variable-block plan runs through bskv_run_bsr_variable"); return BSKV_ERR_INVALID_ARG; }
+  if (plan && plan->kind == KIND_BSR &&
+      (meta_word(plan, H_VARIANT) == BSR_VARIABLE || meta_word(plan, H_VARIANT) == BSR_VARIABLE_TC)) {
+    set_error("run_bsr: a variable-block plan runs through bskv_run_bsr_variable");
+    return BSKV_ERR_INVALID_ARG;
+  }
   return run_bsr(plan, q, q_strides, k, k_strides, v, v_strides, out, out_strides, lse, sm_scale,
                  nullptr, stream);
 }
@@ -400,7 +409,7 @@ extern "C" bskv_status bskv_run_bsr_variable(const bskv_plan* plan, const void* 
                                              float sm_scale, void* stream) {
   BSKV_NVTX_RANGE("bskv_run_bsr_variable");
   if (!plan || plan->kind != KIND_BSR || !plan->meta.size() ||
-      plan->meta[H_VARIANT] != BSR_VARIABLE) {
+      (plan->meta[H_VARIANT] != BSR_VARIABLE && plan->meta[H_VARIANT] != BSR_VARIABLE_TC)) {
     set_error("run_bsr_variable: not a variable-block plan (bskv_plan_bsr_variable)");
     return BSKV_ERR_INVALID_ARG;
   }
@@ -415,7 +424,7 @@ extern "C" bskv_status bskv_run_prefill_paged(const bskv_plan* plan, const void*
                                               float sm_scale, void* stream) {
   BSKV_NVTX_RANGE("bskv_run_prefill_paged");
   if (!plan || plan->kind != KIND_BSR || plan->meta.empty() ||
-      plan->meta[H_VARIANT] != BSR_PAGED_PREFILL) {
+      (plan->meta[H_VARIANT] != BSR_PAGED_PREFILL && plan->meta[H_VARIANT] != BSR_PAGED_PREFILL_TC)) {
     set_error("run_prefill_paged: not a paged prefill plan (bskv_plan_prefill_paged)");
     return BSKV_ERR_INVALID_ARG;
   }
@@ -433,6 +442,9 @@ extern "C" bskv_status bskv_run_prefill_paged(const bskv_plan* plan, const void*
       set_error("run_prefill_paged: kv strides must be non-negative multiples of 8 elements"); return BSKV_ERR_INVALID_ARG;
     }
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) { set_error("run_prefill_paged: tensors must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  if (plan->meta[H_VARIANT] == BSR_PAGED_PREFILL_TC)
+    return launch_prefill_tcgen05(plan, q, q_strides, kv_cache, kv_strides, out, out_strides, lse,
+                                  sm_scale, static_cast<cudaStream_t>(stream));
   BsrParams p{};
   p.meta = plan->meta_dev;
   p.q = q; p.q_s0 = q_strides[0]; p.q_s1 = q_strides[1];

@@ -29,6 +29,14 @@
 //            stores out and lse. With two M tiles each warp stages its 32 rows of a 64-value
 //            panel (128B-swizzled, 4 KB) in shared memory and writes them with one tensor
 //            store, so the output leaves in whole lines instead of one row per thread.
+// The same engine serves the list-driven rows ("flashinfer.sparse",
+// VariableBlockSparseAttentionWrapper; batch prefill over a paged KV cache): a unit is then a
+// 64-token tile of a variable row block or of a request's queries, its keys a list of steps
+// of up to 128 contiguous keys (paged: whole pages, one TMA box per page through a 5-D map of
+// the cache). Columns past a step's last key, or past the causal limit of a row, are masked;
+// V rows past the last key of a partial step (garbage slots of a page, rows the step did not
+// load) are zeroed before PV so that 0 * NaN cannot reach O; rows past the tile's last token
+// are computed but not stored.
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs, frees TMEM and
 // returns after recording BSKV_ERR_TIMEOUT.
 #include <math.h>
@@ -57,7 +65,9 @@ struct TcParams {
   void* out;
   int64_t o_s0, o_s1;
   float* lse;
+  int64_t lse_st, lse_sh;  // lse element strides of a token and of a head
   int M, N, Hq, Hkv, group, causal;
+  int step_words, page_size;  // list plans: words per key step; paged: tokens per page
   // per-block token mask (bits little-endian over (nnz, 64, 64): one 64-bit word per row of
   // a block, bit c = key c), or NULL
   const unsigned long long* mask;
@@ -156,15 +166,25 @@ __device__ __forceinline__ uint32_t exp2_pack<__nv_bfloat16>(float x0, float x1,
   return pack2(__nv_bfloat16(), v0, v1);
 }
 
-// kMask: runs with a per-block token mask (a separate instantiation, so that the unmasked
-// softmax carries none of its code).
-template <typename T, int NM, bool kMask>
+// A unit as every role sees it: tokens [tok0, tok0 + ntok) of the tile (ntok <= 64), kv
+// head h, its blocks (BSR: indices[e0, e0 + n)) or its key steps (lists: steps e0 .. e0 +
+// n - 1), and the causal key limit of its first token (row t sees keys <= lim + t).
+struct Unit {
+  int tok0, ntok, h, e0, n, lim;
+};
+
+// kMode 0: block-sparse; 1: block-sparse with a per-block token mask (a separate
+// instantiation, so that the unmasked softmax carries none of its code); 2: variable
+// blocks; 3: paged prefill (2 and 3 read their units and key steps from the plan's lists).
+template <typename T, int NM, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
                   const TcParams p) {
   using L = Cfg<NM>;
   constexpr int S = L::kStages;
+  constexpr bool kMask = kMode == 1;
+  constexpr bool kList = kMode >= 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -173,10 +193,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* hdr = p.meta;
   const int32_t* wptr = hdr + hdr[H_OFF_WORKERS];
   const int4* units = reinterpret_cast<const int4*>(hdr + hdr[H_OFF_CHUNKS]);
-  const int32_t* indptr = hdr + hdr[H_OFF_AUX0];
-  const int32_t* indices = hdr + hdr[H_OFF_AUX1];
+  const int32_t* indptr = hdr + hdr[H_OFF_AUX0];   // lists: unit descriptors
+  const int32_t* indices = hdr + hdr[H_OFF_AUX1];  // lists: key steps
   const int u0 = wptr[blockIdx.x], u1 = wptr[blockIdx.x + 1];
   const bool forced = forced_timeout(p.st);
+  auto unit_of = [&](int ui) -> Unit {
+    const int4 un = units[ui];
+    Unit u;
+    u.h = un.z;
+    if constexpr (kList) {
+      const int32_t* d = indptr + kBsrTcUnitWords * int64_t(un.x);
+      u.tok0 = d[0];
+      u.ntok = d[1];
+      u.e0 = d[2];
+      u.n = d[3] - d[2];
+      u.lim = d[4];
+    } else {
+      const int i = un.y;
+      u.tok0 = i * kBlk;
+      u.ntok = min(kBlk, p.M - u.tok0);
+      u.e0 = indptr[i];
+      u.n = indptr[i + 1] - u.e0;
+      u.lim = u.tok0 + (p.N - p.M);
+    }
+    return u;
+  };
+  // steps of a unit (a BSR step is a pair of blocks) and 64-key halves of step j
+  auto nsteps = [&](const Unit& u) -> int { return kList ? u.n : (u.n + 1) >> 1; };
+  auto step_halves = [&](const Unit& u, int j) -> int {
+    if constexpr (kList) {
+      const int32_t* st = indices + int64_t(p.step_words) * (u.e0 + j);
+      return st[1] - st[0] > kBlk ? 2 : 1;
+    } else {
+      return min(2, u.n - 2 * j);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int m = 0; m < 2; ++m) {
@@ -224,46 +275,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (evict last), so it stays in L2 while the Q and output streams pass through.
       const uint64_t pol_q = l2_evict_first_policy(), pol_kv = l2_evict_last_policy();
       bool ok = true;
-      // Q of M tile m for the unit (row block i, kv head h), once the previous unit's last QK
-      // on that tile has completed.
-      auto load_q = [&](int m, int i, int h) -> bool {
+      // Q of M tile m for the unit (64 tokens from tok0, kv head h), once the previous unit's
+      // last QK on that tile has completed.
+      auto load_q = [&](int m, const Unit& u) -> bool {
         if (!issuer_wait(&B.q_empty[m], (qc & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
         mbar_arrive_expect_tx_w(leader, &B.q_full[m], kQTile);
         for (int hl = 0; hl < 2; ++hl)
           for (int pn = 0; pn < 2; ++pn)
             tma_load_3d_hint_w(leader, sm + L::kQ + m * kQTile + pn * (kQTile / 2) + hl * kKPanel, &qmap,
-                             pn * 64, h * p.group + m * 2 + hl, i * kBlk, &B.q_full[m], pol_q);
+                             pn * 64, u.h * p.group + m * 2 + hl, u.tok0, &B.q_full[m], pol_q);
         ++qi[m];
         return true;
       };
-      // K and V of column blocks e, e+1 (< e1) of kv head h into the next stage.
-      auto load_kv = [&](int e, int e1, int h) -> bool {
+      // K and V of step j of the unit into the next stage: BSR, column blocks e0 + 2j and
+      // e0 + 2j + 1; variable blocks, the keys from the step's start in 64-key boxes; paged
+      // prefill, the step's pages, one box of page_size slots each.
+      auto load_kv = [&](const Unit& u, int j) -> bool {
         const int s = kvc % S;
         if (!issuer_wait(&B.kv_empty[s], ((kvc / S) & 1u) ^ 1u, p.st, forced, abort_flag)) return false;
-        const int nb = min(2, e1 - e);
         uint8_t* dst = sm + L::kKV + s * kStageBytes;
-        mbar_arrive_expect_tx_w(leader, &B.kv_full[s], nb * 4 * kKPanel);
-        for (int b = 0; b < nb; ++b) {
-          const int j = indices[e + b];
-          for (int pn = 0; pn < 2; ++pn) {
-            tma_load_3d_hint_w(leader, dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, h, j * kBlk,
-                             &B.kv_full[s], pol_kv);
-            tma_load_3d_hint_w(leader, dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap, pn * 64,
-                             h, j * kBlk, &B.kv_full[s], pol_kv);
+        if constexpr (kMode == 3) {
+          const int32_t* st = indices + int64_t(p.step_words) * (u.e0 + j);
+          const int ps = p.page_size;
+          const int npg = (st[1] - st[0] + ps - 1) / ps;
+          mbar_arrive_expect_tx_w(leader, &B.kv_full[s], uint32_t(npg * ps * 128 * 4));
+          for (int k = 0; k < npg; ++k) {
+            const int page = st[2 + k];
+            for (int pn = 0; pn < 2; ++pn) {
+              tma_load_5d_hint_w(leader, dst + pn * kPairPanel + k * ps * 128, &kmap, pn * 64, 0, u.h, 0,
+                                 page, &B.kv_full[s], pol_kv);
+              tma_load_5d_hint_w(leader, dst + 2 * kPairPanel + pn * kPairPanel + k * ps * 128, &kmap,
+                                 pn * 64, 0, u.h, 1, page, &B.kv_full[s], pol_kv);
+            }
+          }
+        } else {
+          const int nb = step_halves(u, j);
+          mbar_arrive_expect_tx_w(leader, &B.kv_full[s], nb * 4 * kKPanel);
+          const int k0 = kList ? indices[int64_t(p.step_words) * (u.e0 + j)] : 0;
+          for (int b = 0; b < nb; ++b) {
+            const int key = kList ? k0 + b * kBlk : indices[u.e0 + 2 * j + b] * kBlk;
+            for (int pn = 0; pn < 2; ++pn) {
+              tma_load_3d_hint_w(leader, dst + pn * kPairPanel + b * kKPanel, &kmap, pn * 64, u.h, key,
+                               &B.kv_full[s], pol_kv);
+              tma_load_3d_hint_w(leader, dst + 2 * kPairPanel + pn * kPairPanel + b * kKPanel, &vmap,
+                               pn * 64, u.h, key, &B.kv_full[s], pol_kv);
+            }
           }
         }
         ++kvc;
         return true;
       };
       for (int ui = u0; ui < u1 && ok; ++ui) {
-        const int4 un = units[ui];
-        const int i = un.y, h = un.z;
-        const int e0 = indptr[i], e1 = indptr[i + 1];
-        if (e1 == e0) continue;
+        const Unit u = unit_of(ui);
+        const int ns = nsteps(u);
+        if (ns == 0) continue;
         // Order: Q of tile 0 (free one job before tile 1's), the first K/V step (its stage
         // is freed before tile 1's last QK completes), then Q of tile 1 and the other steps.
-        ok = load_q(0, i, h) && load_kv(e0, e1, h) && (NM == 1 || load_q(1, i, h));
-        for (int e = e0 + 2; e < e1 && ok; e += 2) ok = load_kv(e, e1, h);
+        ok = load_q(0, u) && load_kv(u, 0) && (NM == 1 || load_q(1, u));
+        for (int j = 1; j < ns && ok; ++j) ok = load_kv(u, j);
         ++qc;
       }
       if (!ok) {
@@ -297,12 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t qc = 0, kvc = 0, J = 0, uc = 0;
       bool ok = true;
       for (int ui = u0; ui < u1 && ok; ++ui) {
-        const int4 un = units[ui];
-        const int i = un.y;
-        const int e0 = indptr[i], e1 = indptr[i + 1];
-        const int n = e1 - e0;
-        if (n == 0) continue;
-        const int steps = (n + 1) >> 1;
+        const Unit u = unit_of(ui);
+        const int steps = nsteps(u);
+        if (steps == 0) continue;
         const int NJ = steps * NM;
         const uint32_t kv_first = kvc;
         // QK of local job jl into S slot (J + jl) & 1.
@@ -314,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (m == 0 && !issuer_wait(&B.kv_full[s], (step / S) & 1u, p.st, forced, abort_flag)) return false;
           if (jl < NM && !issuer_wait(&B.q_full[m], qc & 1u, p.st, forced, abort_flag)) return false;
           tc_fence_after();
-          const int nb = min(2, n - 2 * j);
+          const int nb = step_halves(u, j);
           const uint32_t z = (J + jl) & 1u;
           const uint32_t sd = tmem + 128 + 256 * z;
           const uint32_t qo = (m * kQTile) >> 4, ko = (s * kStageBytes) >> 4;
@@ -339,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!issuer_wait(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
           if (j == 0 && !issuer_wait(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const int nb = min(2, n - 2 * j);
+          const int nb = step_halves(u, j);
           const int s = (kv_first + j) % S;
           const uint32_t vo = (s * kStageBytes) >> 4;
           const uint32_t pa = tmem + 128 + 256 * z;
@@ -377,36 +443,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(q4 * 32) << 16;
     const int hl = m * 2 + r / kBlk;                 // head within the group
     uint32_t J = 0, cnt = 0, od = 0;
+    uint32_t kvs = 0;  // K/V steps of the previous units (the stage of step j is (kvs + j) % S)
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui) {
-      const int4 un = units[ui];
-      const int i = un.y, h = un.z;
-      const int e0 = indptr[i], e1 = indptr[i + 1];
-      const int n = e1 - e0;
-      const int tok = i * kBlk + (r % kBlk);
-      const int head = h * p.group + hl;
-      T* orow = static_cast<T*>(p.out) + int64_t(tok) * p.o_s0 + int64_t(head) * p.o_s1;
-      if (n == 0) {
-        if (tok < p.M) {
+      const Unit u = unit_of(ui);
+      const int t64 = r % kBlk;  // token of this row within the unit's 64
+      const bool row_ok = t64 < u.ntok;
+      const int tok = u.tok0 + t64;
+      const int head = u.h * p.group + hl;
+      // this row's output and lse (formed where they are written, not held across the steps)
+      auto out_row = [&]() {
+        return static_cast<T*>(p.out) + int64_t(tok) * p.o_s0 + int64_t(head) * p.o_s1;
+      };
+      auto lse_at = [&]() -> float& { return p.lse[int64_t(tok) * p.lse_st + int64_t(head) * p.lse_sh]; };
+      const int steps = nsteps(u);
+      if (steps == 0) {
+        if (row_ok) {
+          T* orow = out_row();
           for (int c = 0; c < kD; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-          if (p.lse) p.lse[int64_t(tok) * p.Hq + head] = -INFINITY;
+          if (p.lse) lse_at() = -INFINITY;
         }
         continue;
       }
-      const int steps = (n + 1) >> 1;
-      const int lim = tok + (p.N - p.M);
+      const int lim = u.lim + t64;  // causal: the last key this row sees
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < steps; ++j) {
         const uint32_t Jg = J + (NM == 2 ? 2 * j + m : j), z = Jg & 1u;
-        // the step's column blocks are read before waiting for S (off the critical path)
-        const int nb = min(2, n - 2 * j);
-        const int jb0 = indices[e0 + 2 * j];
-        const int jb1 = nb == 2 ? indices[e0 + 2 * j + 1] : jb0;
+        // the step's column blocks (lists: key range) are read before waiting for S (off the
+        // critical path)
+        const int nb = step_halves(u, j);
+        int jb0 = 0, jb1 = 0, kvalid = 2 * kBlk, cmax = 2 * kBlk;
+        if constexpr (kList) {
+          const int32_t* st = indices + int64_t(p.step_words) * (u.e0 + j);
+          kvalid = st[1] - st[0];
+          // columns at or past cmax are masked: past the step's keys, or past the causal limit
+          cmax = p.causal ? min(kvalid, lim - st[0] + 1) : kvalid;
+        } else {
+          jb0 = indices[u.e0 + 2 * j];
+          jb1 = nb == 2 ? indices[u.e0 + 2 * j + 1] : jb0;
+        }
         // this row's token-mask words of the step's blocks, read before the wait as well
         unsigned long long mw0 = ~0ull, mw1 = ~0ull;
         if (kMask) {
-          mw0 = __ldg(p.mask + (int64_t(e0 + 2 * j) * kBlk + (r & (kBlk - 1))));
-          if (nb == 2) mw1 = __ldg(p.mask + (int64_t(e0 + 2 * j + 1) * kBlk + (r & (kBlk - 1))));
+          mw0 = __ldg(p.mask + (int64_t(u.e0 + 2 * j) * kBlk + (r & (kBlk - 1))));
+          if (nb == 2) mw1 = __ldg(p.mask + (int64_t(u.e0 + 2 * j + 1) * kBlk + (r & (kBlk - 1))));
         }
         if (!warp_wait(&B.s_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -427,17 +507,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           if (bb < nb) {
-            const int k0 = (bb ? jb1 : jb0) * kBlk;
-            const unsigned long long mw = bb ? mw1 : mw0;
-            if (kMask && mw != ~0ull) {
+            if constexpr (kList) {
+              if (cmax < 64 * (bb + 1)) {
 #pragma unroll
-              for (int c = 0; c < 64; ++c)
-                if (!((mw >> c) & 1ull)) sr[64 * bb + c] = __float_as_uint(-INFINITY);
-            }
-            if (p.causal && (k0 + kBlk - 1 > lim)) {
+                for (int c = 0; c < 64; ++c)
+                  if (64 * bb + c >= cmax) sr[64 * bb + c] = __float_as_uint(-INFINITY);
+              }
+            } else {
+              const int k0 = (bb ? jb1 : jb0) * kBlk;
+              const unsigned long long mw = bb ? mw1 : mw0;
+              if (kMask && mw != ~0ull) {
 #pragma unroll
-              for (int c = 0; c < 64; ++c)
-                if (k0 + c > lim) sr[64 * bb + c] = __float_as_uint(-INFINITY);
+                for (int c = 0; c < 64; ++c)
+                  if (!((mw >> c) & 1ull)) sr[64 * bb + c] = __float_as_uint(-INFINITY);
+              }
+              if (p.causal && (k0 + kBlk - 1 > lim)) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                  if (k0 + c > lim) sr[64 * bb + c] = __float_as_uint(-INFINITY);
+              }
             }
 #pragma unroll
             for (int c = 0; c < 64; c += 2)
@@ -504,6 +592,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tmem + lane_base + 256 * m + cc, ov);
           }
         }
+        if constexpr (kList) {
+          // V rows of a partial step past its last key (a page's unused slots, rows no box of
+          // this step wrote) are zeroed before PV reads them: their P is 0, but 0 * NaN is not.
+          // The first M tile's PV is issued before the second's, so its warpgroup does it.
+          if (m == 0 && kvalid < 64 * nb && r >= kvalid && r < 64 * nb) {
+            uint8_t* vrow = sm + L::kKV + ((kvs + j) % S) * kStageBytes + 2 * kPairPanel + r * 128;
+#pragma unroll
+            for (int pn = 0; pn < 2; ++pn)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(vrow + pn * kPairPanel + c * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&B.p_full[z]);
@@ -511,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       J += steps * NM;
+      kvs += steps;
       // Epilogue: wait for the unit's last PV into this tile, normalise and store.
       while (od < cnt) {
         if (!warp_wait(&B.o_done[m], od & 1u, p.st, forced, abort_flag)) { ok = false; break; }
@@ -526,8 +629,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* stg = sm + L::kOut + (m * 4 + q4) * 4096;
         const uint64_t pol_out = l2_evict_first_policy();  // written once
         const uint32_t row_addr = smem_u32(stg) + lane * 128;
+        // a warp whose 32 tokens are not all in the unit (the last tile of a row range) stores
+        // its valid rows one by one instead: a box would reach into the next unit's rows
+        const bool full_box = (q4 & 1) * 32 + 32 <= u.ntok;
+        T* orow = out_row();
 #pragma unroll 1
-        for (int pn = 0; pn < 2; ++pn) {
+        for (int pn = 0; pn < 2 && !full_box; ++pn) {
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + lane_base + 256 * m + pn * 64 + hf * 32, ov);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 w;
+                w.x = pack2(T(), __uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+                w.y = pack2(T(), __uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+                w.z = pack2(T(), __uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+                w.w = pack2(T(), __uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+                *reinterpret_cast<uint4*>(orow + pn * 64 + hf * 32 + c) = w;
+              }
+            }
+          }
+        }
+#pragma unroll 1
+        for (int pn = 0; pn < 2 && full_box; ++pn) {
           // the box's previous store has finished reading it
           if (lane == 0) bulk_wait_read0();
           __syncwarp();
@@ -550,17 +677,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d_hint(&omap, stg, pn * 64, head, i * kBlk + (q4 & 1) * 32, pol_out);
+            tma_store_3d_hint(&omap, stg, pn * 64, head, u.tok0 + (q4 & 1) * 32, pol_out);
             bulk_commit();
           }
         }
       } else {
+        T* orow = out_row();
 #pragma unroll
         for (int cc = 0; cc < kD; cc += 32) {
           uint32_t ov[32];
           tmem_ld32(tmem + lane_base + 256 * m + cc, ov);
           tmem_ld_wait();
-          if (tok < p.M) {
+          if (row_ok) {
 #pragma unroll
             for (int c = 0; c < 32; c += 8) {
               uint4 w;
@@ -573,9 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (tok < p.M && p.lse)
-        p.lse[int64_t(tok) * p.Hq + head] =
-            l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      if (row_ok && p.lse) lse_at() = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&B.o_free[m]);
     }
@@ -589,14 +715,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int NM, bool kMask>
+template <typename T, int NM, int kMode>
 bskv_status launch_t(const bskv_plan* plan, const CUtensorMap& qm, const CUtensorMap& km,
                      const CUtensorMap& vm, const CUtensorMap& om, const TcParams& tp,
                      cudaStream_t st) {
   const int grid = meta_word(plan, H_GRID);
   if (grid == 0) return BSKV_OK;
   const size_t smem = Cfg<NM>::kBytes + 1024;
-  auto kern = bsr_tc_kernel<T, NM, kMask>;
+  auto kern = bsr_tc_kernel<T, NM, kMode>;
   if (bskv_status s = cuda_check(
           cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
           "bsr_tc: cudaFuncSetAttribute"))
@@ -605,64 +731,124 @@ bskv_status launch_t(const bskv_plan* plan, const CUtensorMap& qm, const CUtenso
   return cuda_check(cudaGetLastError(), "bsr_tc launch");
 }
 
+template <int kMode>
+bskv_status launch_mode(const bskv_plan* plan, const CUtensorMap& qm, const CUtensorMap& km,
+                        const CUtensorMap& vm, const CUtensorMap& om, const TcParams& tp,
+                        cudaStream_t st) {
+  const bool bf = plan->dtype == BSKV_BF16;
+  if (tp.group == 4)
+    return bf ? launch_t<__nv_bfloat16, 2, kMode>(plan, qm, km, vm, om, tp, st)
+              : launch_t<__half, 2, kMode>(plan, qm, km, vm, om, tp, st);
+  return bf ? launch_t<__nv_bfloat16, 1, kMode>(plan, qm, km, vm, om, tp, st)
+            : launch_t<__half, 1, kMode>(plan, qm, km, vm, om, tp, st);
+}
+
+// Parameters and the Q / output tensor maps shared by every mode: q and out as (head_dim,
+// head, token) with the caller's strides, boxes of 64 values x 1 head x 64 (Q) or 32 (out)
+// tokens.
+bskv_status tc_common(const bskv_plan* plan, const void* q, const int64_t* qs, void* out,
+                      const int64_t* os, float* lse, float sm_scale, TcParams* tp,
+                      CUtensorMap* qm, CUtensorMap* om) {
+  const int g = plan->num_qo_heads / plan->num_kv_heads;
+  if (!(plan->head_dim == kD && (g == 2 || g == 4))) {
+    set_error("bsr_tc: the tensor-core kernel needs head_dim 128 and group 2 or 4");
+    return BSKV_ERR_UNSUPPORTED;
+  }
+  *tp = TcParams{};
+  tp->meta = plan->meta_dev;
+  tp->out = out; tp->o_s0 = os[0]; tp->o_s1 = os[1];
+  tp->lse = lse;
+  tp->lse_st = plan->num_qo_heads;
+  tp->lse_sh = 1;
+  tp->M = plan->M; tp->N = plan->N; tp->Hq = plan->num_qo_heads; tp->Hkv = plan->num_kv_heads;
+  tp->group = g; tp->causal = plan->causal;
+  tp->scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
+  if (bskv_status s = status_args(&tp->st)) return s;
+  const CUtensorMapDataType dt =
+      plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint32_t box[3] = {64, 1, 64};
+  const uint64_t dims[3] = {uint64_t(kD), uint64_t(plan->num_qo_heads), uint64_t(plan->M)};
+  {
+    const uint64_t str[2] = {uint64_t(qs[1]) * 2, uint64_t(qs[0]) * 2};
+    if (bskv_status s = encode_tiled(qm, dt, 3, q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  }
+  if (g == 4) {
+    // output boxes of 32 tokens x 1 head x 64 values (the epilogue's per-warp stores)
+    const uint32_t obox[3] = {64, 1, 32};
+    const uint64_t str[2] = {uint64_t(os[1]) * 2, uint64_t(os[0]) * 2};
+    if (bskv_status s = encode_tiled(om, dt, 3, out, dims, str, obox, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  } else {
+    *om = *qm;  // unused with one M tile
+  }
+  return BSKV_OK;
+}
+
 }  // namespace
 
 bskv_status launch_bsr_tcgen05(const bskv_plan* plan, const void* q, const int64_t* qs,
                                const void* k, const int64_t* ks, const void* v,
                                const int64_t* vs, void* out, const int64_t* os, float* lse,
                                float sm_scale, const uint8_t* mask, cudaStream_t st) {
-  const int g = plan->num_qo_heads / plan->num_kv_heads;
-  if (!(plan->R == kBlk && plan->C == kBlk && plan->head_dim == kD && (g == 2 || g == 4))) {
-    set_error("run_bsr: tensor-core kernel needs R = C = 64, head_dim 128, group 2 or 4");
-    return BSKV_ERR_UNSUPPORTED;
+  const int variant = meta_word(plan, H_VARIANT);
+  if (!(variant == BSR_TCGEN05 || variant == BSR_VARIABLE_TC) ||
+      (variant == BSR_TCGEN05 && !(plan->R == kBlk && plan->C == kBlk))) {
+    set_error("run_bsr: not a tensor-core block-sparse plan");
+    return BSKV_ERR_INVALID_ARG;
   }
-  TcParams tp{};
-  tp.meta = plan->meta_dev;
-  tp.out = out; tp.o_s0 = os[0]; tp.o_s1 = os[1];
-  tp.lse = lse;
-  tp.M = plan->M; tp.N = plan->N; tp.Hq = plan->num_qo_heads; tp.Hkv = plan->num_kv_heads;
-  tp.group = g; tp.causal = plan->causal;
+  TcParams tp;
+  CUtensorMap qm, km, vm, om;
+  if (bskv_status s = tc_common(plan, q, qs, out, os, lse, sm_scale, &tp, &qm, &om)) return s;
   tp.mask = reinterpret_cast<const unsigned long long*>(mask);
-  tp.scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
-  if (bskv_status s = status_args(&tp.st)) return s;
+  if (variant == BSR_VARIABLE_TC) {
+    // head-major lse [num_qo_heads, qo_len]
+    tp.lse_st = 1;
+    tp.lse_sh = plan->M;
+    tp.step_words = 2;
+  }
   const CUtensorMapDataType dt =
       plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap qm, km, vm, om;
-  const uint32_t box[3] = {64, 1, 64};
   {
-    const uint64_t dims[3] = {uint64_t(kD), uint64_t(plan->num_qo_heads), uint64_t(plan->M)};
-    const uint64_t str[2] = {uint64_t(qs[1]) * 2, uint64_t(qs[0]) * 2};
-    if (bskv_status s = encode_tiled(&qm, dt, 3, q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
-  }
-  if (g == 4) {
-    // output boxes of 32 tokens x 1 head x 64 values (the epilogue's per-warp stores)
-    const uint32_t obox[3] = {64, 1, 32};
-    const uint64_t dims[3] = {uint64_t(kD), uint64_t(plan->num_qo_heads), uint64_t(plan->M)};
-    const uint64_t str[2] = {uint64_t(os[1]) * 2, uint64_t(os[0]) * 2};
-    if (bskv_status s = encode_tiled(&om, dt, 3, out, dims, str, obox, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
-  } else {
-    om = qm;  // unused with one M tile
-  }
-  {
+    const uint32_t box[3] = {64, 1, 64};
     const uint64_t dims[3] = {uint64_t(kD), uint64_t(plan->num_kv_heads), uint64_t(plan->N)};
     const uint64_t sk[2] = {uint64_t(ks[1]) * 2, uint64_t(ks[0]) * 2};
     const uint64_t sv[2] = {uint64_t(vs[1]) * 2, uint64_t(vs[0]) * 2};
     if (bskv_status s = encode_tiled(&km, dt, 3, k, dims, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
     if (bskv_status s = encode_tiled(&vm, dt, 3, v, dims, sv, box, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
   }
-  const bool bf = plan->dtype == BSKV_BF16;
-  if (mask) {
-    if (g == 4)
-      return bf ? launch_t<__nv_bfloat16, 2, true>(plan, qm, km, vm, om, tp, st)
-                : launch_t<__half, 2, true>(plan, qm, km, vm, om, tp, st);
-    return bf ? launch_t<__nv_bfloat16, 1, true>(plan, qm, km, vm, om, tp, st)
-              : launch_t<__half, 1, true>(plan, qm, km, vm, om, tp, st);
+  if (variant == BSR_VARIABLE_TC) return launch_mode<2>(plan, qm, km, vm, om, tp, st);
+  if (mask) return launch_mode<1>(plan, qm, km, vm, om, tp, st);
+  return launch_mode<0>(plan, qm, km, vm, om, tp, st);
+}
+
+bskv_status launch_prefill_tcgen05(const bskv_plan* plan, const void* q, const int64_t* qs,
+                                   const void* kv, const int64_t* kvs, void* out,
+                                   const int64_t* os, float* lse, float sm_scale,
+                                   cudaStream_t st) {
+  if (meta_word(plan, H_VARIANT) != BSR_PAGED_PREFILL_TC || !bsr_tc_page_size(plan->page_size)) {
+    set_error("run_prefill_paged: not a tensor-core paged prefill plan");
+    return BSKV_ERR_INVALID_ARG;
   }
-  if (g == 4)
-    return bf ? launch_t<__nv_bfloat16, 2, false>(plan, qm, km, vm, om, tp, st)
-              : launch_t<__half, 2, false>(plan, qm, km, vm, om, tp, st);
-  return bf ? launch_t<__nv_bfloat16, 1, false>(plan, qm, km, vm, om, tp, st)
-            : launch_t<__half, 1, false>(plan, qm, km, vm, om, tp, st);
+  for (int i = 0; i < 4; ++i)
+    if (kvs[i] <= 0) {
+      set_error("run_prefill_paged: kv strides must be positive for the tensor-core kernel");
+      return BSKV_ERR_INVALID_ARG;
+    }
+  TcParams tp;
+  CUtensorMap qm, km, om;
+  if (bskv_status s = tc_common(plan, q, qs, out, os, lse, sm_scale, &tp, &qm, &om)) return s;
+  tp.page_size = plan->page_size;
+  tp.step_words = 2 + kBsrTcStep / plan->page_size;
+  // the cache as (head_dim, slot, kv head, K/V, page), one page of one head per box
+  const CUtensorMapDataType dt =
+      plan->dtype == BSKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t dims[5] = {uint64_t(kD), uint64_t(plan->page_size), uint64_t(plan->num_kv_heads), 2,
+                            uint64_t(plan->num_pages)};
+  const uint64_t strides[4] = {uint64_t(kvs[3]) * 2, uint64_t(kvs[2]) * 2, uint64_t(kvs[1]) * 2,
+                               uint64_t(kvs[0]) * 2};
+  const uint32_t box[5] = {64, uint32_t(plan->page_size), 1, 1, 1};
+  if (bskv_status s = encode_tiled(&km, dt, 5, kv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return s;
+  return launch_mode<3>(plan, qm, km, km, om, tp, st);
 }
 
 }  // namespace bskv

@@ -293,6 +293,18 @@ __device__ __forceinline__ void tma_load_5d_hint(void* dst, const CUtensorMap* m
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_5d_hint_w(uint32_t leader, void* dst,
+                                                   const CUtensorMap* map, int32_t c0,
+                                                   int32_t c1, int32_t c2, int32_t c3,
+                                                   int32_t c4, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %9, 0;\n\t"
+      "@e cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)), "l"(policy),
+      "r"(leader)
+      : "memory");
+}
 
 // Device-scope atomic add with acquire-release semantics (returns the old value): the
 // writes this thread made or observed before it (a __syncwarp orders the warp's lanes'

@@ -58,9 +58,28 @@ constexpr int kFusedMergeMaxPieces = 8;
 // BSR_PAGED_PREFILL: batch prefill over a paged KV cache on the general kernel; aux0: per
 // request {first query token, query tokens, first tile, end tile, causal shift L_b - qo_len_b};
 // aux1: tiles {first key, tile end, page, first slot}, never crossing a page.
+// BSR_VARIABLE_TC / BSR_PAGED_PREFILL_TC: the same two rows on the tensor-core kernel (head_dim
+// 128, 2 or 4 query heads per kv head; paged: page_size 8, 16, 32, 64 or 128). aux0: per unit
+// (64-token row tile) {first query token, valid tokens (<= 64), first step, end step, key
+// limit of the tile's first token (causal: key j visible to tile row t iff j <= limit + t)};
+// aux1: steps of up to 128 keys {key start, key end} (variable blocks: within one run of
+// visible column blocks; paged: within one request, from a multiple of 128, followed by the
+// 128 / page_size page ids the step covers, -1 past the request's last page).
 enum BsrVariant : int32_t { BSR_GENERIC = 0, BSR_TCGEN05 = 1, BSR_VARIABLE = 2,
-                            BSR_PAGED_PREFILL = 3 };
+                            BSR_PAGED_PREFILL = 3, BSR_VARIABLE_TC = 4, BSR_PAGED_PREFILL_TC = 5 };
 constexpr int kBsrVarTile = 32;  // key tokens per tile of a variable-block plan
+constexpr int kBsrTcStep = 128;  // key tokens per step of the tensor-core list plans
+constexpr int kBsrTcUnitWords = 5;
+
+// The tensor-core kernel serves a list plan of this shape.
+inline bool bsr_tc_list_shape(int32_t head_dim, int32_t num_qo_heads, int32_t num_kv_heads) {
+  const int32_t g = num_kv_heads > 0 ? num_qo_heads / num_kv_heads : 0;
+  return head_dim == 128 && (g == 2 || g == 4);
+}
+inline bool bsr_tc_page_size(int32_t page_size) {
+  return page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 ||
+         page_size == 128;
+}
 // MLA_SPARSE: row lists given by the caller. MLA_PAGED: row lists expanded on the device
 // from the page table in the metadata (aux0 = kv_indptr, aux1 = kv_indices).
 enum MlaVariant : int32_t { MLA_SPARSE = 0, MLA_PAGED = 1 };

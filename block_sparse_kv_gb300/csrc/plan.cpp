@@ -167,6 +167,63 @@ void lists_to_chunks(const std::vector<std::vector<int32_t>>& lists,
   worker_ptr[lists.size()] = int32_t(chunks.size());
 }
 
+// Tensor-core list plans: unit descriptors and chunks from per-unit step ranges. A unit is a
+// 64-token row tile {first token, valid tokens, first step, end step, key limit}, served for
+// one kv head; cost in quarter steps of the tensor-core kernel: 2 for its start and
+// epilogue, 4 per step of more than 64 keys, 3 per step of at most 64 (1 without steps).
+// Units are placed by the longest-processing-time rule on at most num_sms CTAs.
+struct TcListPlan {
+  std::vector<int32_t> desc;   // kBsrTcUnitWords per descriptor
+  std::vector<Chunk> units;    // (descriptor, 0, kv head, 0)
+  std::vector<int64_t> cost;
+};
+
+int64_t tc_unit_cost(const std::vector<int32_t>& steps, int32_t words, int32_t tb, int32_t te) {
+  if (te == tb) return 1;
+  int64_t c = 2;
+  for (int32_t t = tb; t < te; ++t) {
+    const int32_t n = steps[size_t(t) * words + 1] - steps[size_t(t) * words];
+    c += n > 64 ? 4 : 3;
+  }
+  return c;
+}
+
+// Unit descriptors of the 64-token row tiles of [tok0, tok0 + ntok), whose keys are the steps
+// [tb, te) (in key order); with causal, a tile keeps the steps that start at or before the
+// last key its last token sees (limit0 + valid - 1). One unit per tile and kv head.
+void tc_list_units(TcListPlan& pl, const std::vector<int32_t>& steps, int32_t words,
+                   int32_t tok0, int32_t ntok, int32_t tb, int32_t te, int32_t limit_first,
+                   bool causal, const std::vector<int32_t>& heads) {
+  for (int32_t r0 = 0; r0 < ntok; r0 += 64) {
+    const int32_t valid = std::min(64, ntok - r0);
+    const int32_t lim = limit_first + r0;
+    int32_t end = te;
+    if (causal) {
+      end = tb;
+      while (end < te && int64_t(steps[size_t(end) * words]) <= int64_t(lim) + valid - 1) ++end;
+    }
+    const int32_t d = int32_t(pl.desc.size() / kBsrTcUnitWords);
+    pl.desc.insert(pl.desc.end(), {tok0 + r0, valid, tb, end, lim});
+    const int64_t c = tc_unit_cost(steps, words, tb, end);
+    for (int32_t h : heads) {
+      pl.units.push_back(Chunk{d, 0, h, 0});
+      pl.cost.push_back(c);
+    }
+  }
+}
+
+// Assemble a tensor-core list plan (variant BSR_VARIABLE_TC or BSR_PAGED_PREFILL_TC).
+void tc_list_assemble(bskv_plan* p, const TcListPlan& pl, const std::vector<int32_t>& steps,
+                      int32_t num_sms, int32_t variant) {
+  const int64_t U = int64_t(pl.units.size());
+  const int32_t G = int32_t(std::min<int64_t>(num_sms, std::max<int64_t>(U, 1)));
+  std::vector<int32_t> worker_ptr, no_merges;
+  std::vector<Chunk> chunks;
+  lists_to_chunks(lpt_assign(pl.cost, G), pl.units, worker_ptr, chunks);
+  assemble(p, KIND_BSR, int32_t(U), worker_ptr, chunks, 0, no_merges, 64, pl.desc.data(),
+           pl.desc.size(), steps.data(), steps.size(), U > 0 ? G : 0, variant);
+}
+
 // One line per plan on stderr when BSKV_LOGLEVEL >= 1 (plus the spread of work items over
 // the workers at level 2), taken from the metadata the kernels will read.
 void log_plan(const char* name, const bskv_plan* p) {
@@ -181,6 +238,8 @@ void log_plan(const char* name, const bskv_plan* p) {
       break;
     case KIND_BSR:
       kernel = m[H_VARIANT] == BSR_TCGEN05 ? "bsr_tc_kernel (tcgen05)"
+               : m[H_VARIANT] == BSR_VARIABLE_TC ? "bsr_tc_kernel (tcgen05, variable blocks)"
+               : m[H_VARIANT] == BSR_PAGED_PREFILL_TC ? "bsr_tc_kernel (tcgen05, paged prefill)"
                : m[H_VARIANT] == BSR_VARIABLE ? "bsr_generic_kernel (variable blocks)"
                : m[H_VARIANT] == BSR_PAGED_PREFILL ? "bsr_generic_kernel (paged prefill)"
                                                    : "bsr_generic_kernel";
@@ -431,6 +490,48 @@ extern "C" bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map,
     kv_len = sc;
   }
   if (qo_len > INT32_MAX / 2 || kv_len > INT32_MAX / 2 || qo_len * g > INT32_MAX / 2) { set_error("plan_bsr_variable: sequence too long"); return BSKV_ERR_UNSUPPORTED; }
+  if (bsr_tc_list_shape(head_dim, num_qo_heads, num_kv_heads)) {
+    // Tensor-core kernel: per (kv head h, row block a) the runs of visible column blocks cut
+    // into steps of at most 128 keys; units are the row block's 64-token tiles.
+    std::vector<int32_t> steps;
+    TcListPlan pl;
+    const int32_t shift = int32_t(kv_len - qo_len);
+    for (int32_t h = 0; h < H; ++h) {
+      std::vector<int32_t> cs(static_cast<size_t>(NB));
+      int32_t acc = 0;
+      for (int32_t c = 0; c < NB; ++c) { cs[size_t(c)] = acc; acc += block_col_sz[int64_t(h) * NB + c]; }
+      int32_t row = 0;
+      for (int32_t a = 0; a < MB; ++a) {
+        const uint8_t* mrow = block_mask_map + (int64_t(h) * MB + a) * NB;
+        const int32_t tb = int32_t(steps.size() / 2);
+        for (int32_t c = 0; c < NB;) {
+          if (!mrow[c]) { ++c; continue; }
+          const int32_t s0 = cs[size_t(c)];
+          int32_t e = s0;
+          while (c < NB && mrow[c]) { e += block_col_sz[int64_t(h) * NB + c]; ++c; }
+          for (int32_t t = s0; t < e; t += kBsrTcStep) {
+            steps.push_back(t);
+            steps.push_back(std::min(t + kBsrTcStep, e));
+          }
+          if (steps.size() > size_t(INT32_MAX) / 2) { set_error("plan_bsr_variable: too many key steps"); return BSKV_ERR_UNSUPPORTED; }
+        }
+        const int32_t nrow = block_row_sz[int64_t(h) * MB + a];
+        tc_list_units(pl, steps, 2, row, nrow, tb, int32_t(steps.size() / 2), row + shift,
+                      causal != 0, {h});
+        row += nrow;
+      }
+    }
+    bskv_plan* p = new bskv_plan();
+    p->kind = KIND_BSR;
+    p->M = int32_t(qo_len); p->N = int32_t(kv_len); p->R = 0; p->C = 0; p->causal = causal ? 1 : 0;
+    p->num_qo_heads = num_qo_heads; p->num_kv_heads = num_kv_heads; p->head_dim = head_dim;
+    p->dtype = dtype;
+    tc_list_assemble(p, pl, steps, num_sms, BSR_VARIABLE_TC);
+    p->float_ws_bytes = 0;
+    *out_plan = p;
+    log_plan("bskv_plan_bsr_variable", p);
+    return BSKV_OK;
+  }
   // Per (kv head h, row block a): its query rows and the 16-token tiles of the key ranges it
   // sees (adjacent selected column blocks merged into one range).
   std::vector<int32_t> desc(size_t(H) * MB * 4), tiles;
@@ -513,6 +614,62 @@ extern "C" bskv_status bskv_plan_prefill_paged(const int32_t* qo_indptr, const i
   if (batch > 0 && (!qo_indptr || !kv_indptr || !kv_last_page_len)) { set_error("plan_prefill_paged: NULL index array"); return BSKV_ERR_INVALID_ARG; }
   if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) { set_error("plan_prefill_paged: qo_indptr[0] and kv_indptr[0] must be 0"); return BSKV_ERR_INVALID_ARG; }
   const int32_t g = num_qo_heads / num_kv_heads;
+  if (bsr_tc_list_shape(head_dim, num_qo_heads, num_kv_heads) && bsr_tc_page_size(page_size)) {
+    // Tensor-core kernel: per request its keys in steps of 128 (whole pages, the step's page
+    // ids listed after its key range); units are 64-token tiles of its queries, for every
+    // kv head.
+    const int32_t ppk = kBsrTcStep / page_size, words = 2 + ppk;
+    std::vector<int32_t> steps, heads(static_cast<size_t>(num_kv_heads));
+    for (int32_t h = 0; h < num_kv_heads; ++h) heads[size_t(h)] = h;
+    TcListPlan pl;
+    for (int32_t b = 0; b < batch; ++b) {
+      const int64_t nq = int64_t(qo_indptr[b + 1]) - qo_indptr[b];
+      const int64_t n = int64_t(kv_indptr[b + 1]) - kv_indptr[b];
+      if (nq < 0 || n < 0) { set_error("plan_prefill_paged: qo_indptr or kv_indptr decreases at %d", b); return BSKV_ERR_INVALID_ARG; }
+      int64_t L = 0;
+      if (n > 0) {
+        const int32_t lp = kv_last_page_len[b];
+        if (lp < 1 || lp > page_size) {
+          set_error("plan_prefill_paged: kv_last_page_len[%d] = %d outside [1, %d]", b, lp, page_size);
+          return BSKV_ERR_INVALID_ARG;
+        }
+        L = (n - 1) * page_size + lp;
+      }
+      if (L > INT32_MAX / 2 || nq * g > INT32_MAX / 2) { set_error("plan_prefill_paged: request %d too long", b); return BSKV_ERR_UNSUPPORTED; }
+      for (int64_t i = kv_indptr[b]; i < kv_indptr[b + 1]; ++i) {
+        if (!kv_indices || kv_indices[i] < 0 || kv_indices[i] >= num_pages) {
+          set_error("plan_prefill_paged: kv_indices[%lld] outside [0, %d)", (long long)i, num_pages);
+          return BSKV_ERR_INVALID_ARG;
+        }
+      }
+      const int32_t tb = int32_t(steps.size() / size_t(words));
+      for (int64_t t = 0; t < L; t += kBsrTcStep) {
+        const int64_t e = std::min<int64_t>(t + kBsrTcStep, L);
+        steps.push_back(int32_t(t));
+        steps.push_back(int32_t(e));
+        for (int32_t k = 0; k < ppk; ++k) {
+          const int64_t k0 = t + int64_t(k) * page_size;
+          steps.push_back(k0 < e ? kv_indices[kv_indptr[b] + k0 / page_size] : -1);
+        }
+        if (steps.size() > size_t(INT32_MAX) / 2) { set_error("plan_prefill_paged: too many key steps"); return BSKV_ERR_UNSUPPORTED; }
+      }
+      tc_list_units(pl, steps, words, qo_indptr[b], int32_t(nq), tb,
+                    int32_t(steps.size() / size_t(words)), int32_t(L - nq), causal != 0, heads);
+    }
+    const int64_t total_qo = batch > 0 ? qo_indptr[batch] : 0;
+    if (total_qo > INT32_MAX / 2) { set_error("plan_prefill_paged: too many query tokens"); return BSKV_ERR_UNSUPPORTED; }
+    bskv_plan* p = new bskv_plan();
+    p->kind = KIND_BSR;
+    p->batch = batch; p->num_pages = num_pages; p->page_size = page_size;
+    p->M = int32_t(total_qo); p->N = 0; p->R = 0; p->C = 0; p->causal = causal ? 1 : 0;
+    p->num_qo_heads = num_qo_heads; p->num_kv_heads = num_kv_heads; p->head_dim = head_dim;
+    p->dtype = dtype;
+    tc_list_assemble(p, pl, steps, num_sms, BSR_PAGED_PREFILL_TC);
+    p->float_ws_bytes = 0;
+    *out_plan = p;
+    log_plan("bskv_plan_prefill_paged", p);
+    return BSKV_OK;
+  }
   std::vector<int32_t> desc(size_t(batch) * 5), tiles;
   for (int32_t b = 0; b < batch; ++b) {
     const int64_t nq = int64_t(qo_indptr[b + 1]) - qo_indptr[b];

@@ -150,37 +150,43 @@ def bsr_attention(q_bits, k_bits, v_bits, dtype, indptr, indices, M, N, R, C,
 # Variable-block sparse attention
 # ---------------------------------------------------------------------------------------
 
-def variable_block_mask(block_mask_map, block_row_sz, block_col_sz, causal=False):
+def variable_block_mask(block_mask_map, block_row_sz, block_col_sz, causal=False, rows=None):
     """Dense boolean masks [Hkv, qo_len, kv_len]: kv head h cuts the query tokens into
     consecutive row blocks of block_row_sz[h] tokens and the keys into consecutive column
-    blocks of block_col_sz[h]; block (a, c) is visible iff block_mask_map[h, a, c]."""
+    blocks of block_col_sz[h]; block (a, c) is visible iff block_mask_map[h, a, c].
+    ``rows`` optionally lists the query tokens to build (then [Hkv, len(rows), kv_len])."""
     bm = np.asarray(block_mask_map, dtype=bool)
     rs = np.asarray(block_row_sz, dtype=np.int64)
     cs = np.asarray(block_col_sz, dtype=np.int64)
     H, MB, NB = bm.shape
     qo, kv = int(rs[0].sum()), int(cs[0].sum())
-    out = np.zeros((H, qo, kv), dtype=bool)
+    sel = np.arange(qo) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((H, len(sel), kv), dtype=bool)
     for h in range(H):
         if rs[h].sum() != qo or cs[h].sum() != kv:
             raise ValueError("every kv head must cover the same lengths")
         r0 = np.concatenate([[0], np.cumsum(rs[h])])
         c0 = np.concatenate([[0], np.cumsum(cs[h])])
         for a in range(MB):
+            inside = (sel >= r0[a]) & (sel < r0[a + 1])   # the selected tokens of row block a
             for c in range(NB):
                 if bm[h, a, c]:
-                    out[h, r0[a]:r0[a + 1], c0[c]:c0[c + 1]] = True
+                    out[h, inside, c0[c]:c0[c + 1]] = True
     if causal:
-        i = np.arange(qo)[:, None]
+        i = sel[:, None]
         j = np.arange(kv)[None, :]
         out &= (j <= i + (kv - qo))[None]
     return out
 
 
 def variable_block_attention(q_bits, k_bits, v_bits, dtype, block_mask_map, block_row_sz,
-                             block_col_sz, sm_scale=None, causal=False):
+                             block_col_sz, sm_scale=None, causal=False, rows=None):
     """Variable-block sparse attention from stored 16-bit inputs, head-major as on the page:
     q [Hq, qo_len, D], k/v [Hkv, kv_len, D]. Returns out [Hq, qo_len, D] and lse [Hq, qo_len];
-    query head hq uses kv head hq // (Hq / Hkv) and that head's mask."""
+    query head hq uses kv head hq // (Hq / Hkv) and that head's mask. ``rows`` optionally lists
+    the query tokens to compute (then out [Hq, len(rows), D], lse [Hq, len(rows)])."""
+    if rows is not None:
+        q_bits = np.asarray(q_bits)[:, np.asarray(rows, dtype=np.int64)]
     q = bits_to_f64(q_bits, dtype)
     k = bits_to_f64(k_bits, dtype)
     v = bits_to_f64(v_bits, dtype)
@@ -189,7 +195,7 @@ def variable_block_attention(q_bits, k_bits, v_bits, dtype, block_mask_map, bloc
     g = Hq // Hkv
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
-    masks = variable_block_mask(block_mask_map, block_row_sz, block_col_sz, causal)
+    masks = variable_block_mask(block_mask_map, block_row_sz, block_col_sz, causal, rows)
     out = np.zeros((Hq, L, v.shape[-1]))
     lse = np.zeros((Hq, L))
     for h in range(Hkv):

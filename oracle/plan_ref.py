@@ -44,6 +44,21 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
     (t, e, page, first slot) of at most 32 keys that never cross a page; units (b, kv head,
     row tile of 64 grouped rows) b-major, chunk (b, b, h, rt), cost 1 + tiles, the
     variable-block assignment rule; aux0 = descriptors, aux1 = tiles.
+  * tensor-core list plans (variable blocks: variant 4 when head_dim == 128 and g in {2, 4};
+    paged prefill: variant 5 when also page_size in {8, 16, 32, 64, 128}): keys in steps of
+    at most 128 (variable blocks: each maximal run [s, e) of visible column blocks of (h, a)
+    cut into (t, min(t + 128, e)), 2 words; paged prefill: request b's keys [0, L_b) cut into
+    (t, min(t + 128, L_b)) followed by the 128 / page_size page ids kv_indices[kv_indptr[b] +
+    (t + k page_size) / page_size] for t + k page_size < the step's end, else -1). Units are
+    64-token row tiles: descriptor (first query token, valid tokens <= 64, first step, end
+    step, key limit), with key limit = (first token + L - qo_len) for variable blocks (first
+    token global) and (64 rt + L_b - qo_len_b) for paged prefill; with causal the end step is
+    the first step of the row range's list whose start exceeds key limit + valid - 1 (all
+    steps without causal). Variable blocks: descriptors per (h, a, rt) in that order, one
+    unit (desc, 0, h, 0) each; paged prefill: descriptors per (b, rt), units (desc, 0, h, 0)
+    for h = 0 .. Hkv - 1. Cost: 1 without steps, else 2 + sum over steps of 4 (more than 64
+    keys) or 3; longest processing time first on at most num_sms CTAs; tile field 64;
+    aux0 = descriptors, aux1 = steps.
   * paged MLA: one unit per request, len = its length from the page table (as for
     decode), tile 128, max_workers = max(1, num_sms // 2), grid = 2 P, aux0 = kv_indptr,
     aux1 = kv_indices, variant 1.
@@ -224,9 +239,87 @@ def bsr_meta(indptr, indices, M, N, R, C, num_qo_heads, num_kv_heads, head_dim, 
                      [int(x) for x in indices[:nnz]], G, 1 if tc else 0)
 
 
+def _tc_list_shape(head_dim, num_qo_heads, num_kv_heads):
+    g = num_qo_heads // num_kv_heads
+    return head_dim == 128 and g in (2, 4)
+
+
+def _tc_units(desc, units, cost, steps, words, tok0, ntok, tb, te, limit_first, causal, heads):
+    for r0 in range(0, ntok, 64):
+        valid = min(64, ntok - r0)
+        lim = limit_first + r0
+        end = te
+        if causal:
+            end = tb
+            while end < te and steps[end * words] <= lim + valid - 1:
+                end += 1
+        d = len(desc) // 5
+        desc += [tok0 + r0, valid, tb, end, lim]
+        c = 1 if end == tb else 2 + sum(
+            4 if steps[t * words + 1] - steps[t * words] > 64 else 3 for t in range(tb, end))
+        for h in heads:
+            units.append([d, 0, h, 0])
+            cost.append(c)
+
+
+def _lpt_chunks(units, cost, G):
+    order = sorted(range(len(units)), key=lambda u: -cost[u])
+    heap = [(0, c) for c in range(G)]
+    heapq.heapify(heap)
+    lists = [[] for _ in range(G)]
+    for u in order:
+        load, c = heapq.heappop(heap)
+        lists[c].append(u)
+        heapq.heappush(heap, (load + cost[u], c))
+    wp, ch = [], []
+    for c in range(G):
+        wp.append(len(ch))
+        for u in lists[c]:
+            ch.append(units[u])
+    wp.append(len(ch))
+    return wp, ch
+
+
+def _tc_list_meta(desc, units, cost, steps, num_sms, variant):
+    U = len(units)
+    G = min(num_sms, max(U, 1))
+    wp, ch = _lpt_chunks(units, cost, G)
+    return _assemble(2, U, wp, ch, 0, [], 64, desc, steps, G if U > 0 else 0, variant)
+
+
 def bsr_variable_meta(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, num_kv_heads,
-                      num_sms):
+                      num_sms, head_dim=64, causal=False):
     H = num_kv_heads
+    if _tc_list_shape(head_dim, num_qo_heads, num_kv_heads):
+        MB, NB = len(block_row_sz[0]), len(block_col_sz[0])
+        qo_len = sum(int(x) for x in block_row_sz[0])
+        kv_len = sum(int(x) for x in block_col_sz[0])
+        steps, desc, units, cost = [], [], [], []
+        for h in range(H):
+            cstart, acc = [], 0
+            for c in range(NB):
+                cstart.append(acc)
+                acc += int(block_col_sz[h][c])
+            row = 0
+            for a in range(MB):
+                tb = len(steps) // 2
+                c = 0
+                while c < NB:
+                    if not block_mask_map[h][a][c]:
+                        c += 1
+                        continue
+                    s0 = cstart[c]
+                    e = s0
+                    while c < NB and block_mask_map[h][a][c]:
+                        e += int(block_col_sz[h][c])
+                        c += 1
+                    for t in range(s0, e, 128):
+                        steps += [t, min(t + 128, e)]
+                nrow = int(block_row_sz[h][a])
+                _tc_units(desc, units, cost, steps, 2, row, nrow, tb, len(steps) // 2,
+                          row + kv_len - qo_len, causal, [h])
+                row += nrow
+        return _tc_list_meta(desc, units, cost, steps, num_sms, 4)
     g = num_qo_heads // num_kv_heads
     MB = len(block_row_sz[0])
     NB = len(block_col_sz[0])
@@ -281,9 +374,26 @@ def bsr_variable_meta(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, 
 
 
 def prefill_paged_meta(qo_indptr, kv_indptr, kv_indices, kv_last_page_len, page_size,
-                       num_qo_heads, num_kv_heads, num_sms):
+                       num_qo_heads, num_kv_heads, num_sms, head_dim=64, causal=True):
     batch = len(qo_indptr) - 1
     g = num_qo_heads // num_kv_heads
+    if _tc_list_shape(head_dim, num_qo_heads, num_kv_heads) and page_size in (8, 16, 32, 64, 128):
+        ppk = 128 // page_size
+        words = 2 + ppk
+        steps, desc, units, cost = [], [], [], []
+        for b in range(batch):
+            nq = int(qo_indptr[b + 1]) - int(qo_indptr[b])
+            L = paged_request_len(kv_indptr, kv_last_page_len, page_size, b)
+            tb = len(steps) // words
+            for t in range(0, L, 128):
+                e = min(t + 128, L)
+                steps += [t, e]
+                for k in range(ppk):
+                    k0 = t + k * page_size
+                    steps.append(int(kv_indices[int(kv_indptr[b]) + k0 // page_size]) if k0 < e else -1)
+            _tc_units(desc, units, cost, steps, words, int(qo_indptr[b]), nq, tb,
+                      len(steps) // words, L - nq, causal, list(range(num_kv_heads)))
+        return _tc_list_meta(desc, units, cost, steps, num_sms, 5)
     desc, tiles = [], []
     for b in range(batch):
         nq = int(qo_indptr[b + 1]) - int(qo_indptr[b])

@@ -1,8 +1,11 @@
-"""GPU parity of batch prefill over a paged KV cache (general kernel, paged tiles).
+"""GPU parity of batch prefill over a paged KV cache.
 
 Gate: |gpu - oracle| <= 1e-2 + 1e-2 |oracle| on out and lse (bf16/fp16 inputs, fp32
-accumulation). The cache holds NaN in every slot no request owns, so a read outside the
-page table poisons the output.
+accumulation). The cache holds NaN in every slot no request owns (past each request's last
+token and in spare pages), so a read outside the page table, or a garbage slot reaching the
+PV product, poisons the output. head_dim 128 with 2 or 4 query heads per kv head and
+page_size 8 .. 128 runs the tensor-core kernel (plan variant 5), other shapes the general
+kernel (variant 3); each case asserts which one it exercised.
 """
 
 import numpy as np
@@ -24,6 +27,9 @@ def _run(cuda, d, causal=True, requests=None):
                                      d["kv_last_page_len"], d["num_pages"], d["page_size"],
                                      d["num_qo_heads"], d["num_kv_heads"], d["head_dim"],
                                      causal=causal, dtype=dtype)
+    g = d["num_qo_heads"] // d["num_kv_heads"]
+    tc = d["head_dim"] == 128 and g in (2, 4) and d["page_size"] in (8, 16, 32, 64, 128)
+    assert p.metadata()[15] == (5 if tc else 3)
     bskv.bskv_get_device_status(reset=True)
     out, lse = bskv.bskv_run_prefill_paged(p, d["q"].to(cuda), d["kv_cache"].to(cuda),
                                            return_lse=True)
@@ -40,10 +46,11 @@ def _run(cuda, d, causal=True, requests=None):
     if requests is not None:
         rows = np.concatenate([np.arange(qi[b], qi[b + 1]) for b in requests])
         o, l = o[rows], l[rows]
-    assert_close(o, ref, TOL, TOL, "out")
+    st = assert_close(o, ref, TOL, TOL, "out")
     fin = np.isfinite(ref_lse)
     assert (np.isneginf(l) == ~fin).all()
     assert_close(l[fin], ref_lse[fin], TOL, TOL, "lse")
+    return st
 
 
 @pytest.mark.parametrize("lengths,qo,ps,Hq,Hkv,D,dtype,causal", [
@@ -51,6 +58,10 @@ def _run(cuda, d, causal=True, requests=None):
     ([300, 129, 64], [300, 100, 1], 64, 32, 8, 128, torch.bfloat16, True),
     ([77, 200], [20, 200], 7, 4, 4, 64, torch.float16, True),
     ([150, 33], [40, 33], 16, 8, 1, 128, torch.float16, False),
+    ([1000, 77, 0, 129], [257, 77, 0, 1], 8, 8, 4, 128, torch.float16, True),
+    ([700, 300], [700, 100], 128, 16, 4, 128, torch.bfloat16, False),
+    ([513, 64, 1], [200, 64, 1], 32, 8, 2, 128, torch.bfloat16, True),
+    ([130, 2000], [130, 65], 64, 8, 4, 128, torch.float16, True),
 ])
 def test_prefill_paged_small(cuda, lengths, qo, ps, Hq, Hkv, D, dtype, causal):
     d = synth.paged_prefill_inputs(90 + ps, len(lengths), Hq, Hkv, D, ps, 0, 0, 0, 0,
@@ -58,10 +69,12 @@ def test_prefill_paged_small(cuda, lengths, qo, ps, Hq, Hkv, D, dtype, causal):
     _run(cuda, d, causal)
 
 
-def test_prefill_paged_full_workload_sampled(cuda):
-    """The benchmark's workload (16 requests of 2048-8192 tokens, 1024 new, page 16)."""
+def test_prefill_paged_full_workload(cuda):
+    """The benchmark's workload (16 requests of 2048-8192 tokens, 1024 new, page 16), in the
+    launch configuration the benchmark times; every request checked."""
     d = synth.make("prefill_paged", device="cuda")
-    _run(cuda, d, True, requests=[0, 7, 15])
+    st = _run(cuda, d, True)
+    print("prefill paged full workload:", st)
 
 
 def test_prefill_paged_rejects_other_entry_points(cuda):

@@ -489,6 +489,23 @@ def test_variable_block_heads_follow_their_kv_head():
     assert m[1, 0, :].tolist() == [False] * 2 + [True] * 10   # row block 0 of head 1: cols 1, 2
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_variable_block_selected_rows_are_the_full_rows(causal):
+    """The rows= selection computes exactly the selected rows of the full result (mask and
+    attention), bit for bit, in the order given."""
+    d = synth.variable_block_inputs(30, 4, 2, 16, 3, 4, 40, 50, density=0.6, causal=causal)
+    args = (_bits(d["q"]), _bits(d["k"]), _bits(d["v"]), "fp16", d["block_mask_map"].numpy(),
+            d["block_row_sz"].numpy(), d["block_col_sz"].numpy())
+    out, lse = att.variable_block_attention(*args, causal=causal)
+    rows = [39, 0, 17, 18, 5]
+    o2, l2 = att.variable_block_attention(*args, causal=causal, rows=rows)
+    np.testing.assert_array_equal(o2, out[:, rows])
+    np.testing.assert_array_equal(l2, lse[:, rows])
+    m = att.variable_block_mask(*args[4:], causal=causal)
+    np.testing.assert_array_equal(att.variable_block_mask(*args[4:], causal=causal, rows=rows),
+                                  m[:, rows])
+
+
 # ---------------------------------------------------------------------------------------
 # batch prefill over a paged KV cache
 # ---------------------------------------------------------------------------------------

@@ -246,8 +246,11 @@ def test_run_without_upload_is_rejected(lib):
     assert "not uploaded" in bskv.bskv_last_error_message()
 
 
+@pytest.mark.parametrize("D,causal", [(64, False), (128, False), (128, True)])
 @pytest.mark.parametrize("seed,H,MB,NB", [(1, 2, 3, 4), (2, 8, 16, 16), (3, 1, 1, 1)])
-def test_bsr_variable_plan_bit_exact(lib, seed, H, MB, NB):
+def test_bsr_variable_plan_bit_exact(lib, seed, H, MB, NB, D, causal):
+    """head_dim 64: the general kernel's plan (variant 2); 128 with 2 query heads per kv head:
+    the tensor-core plan (variant 4), with and without causal trimming of the steps."""
     g = torch.Generator().manual_seed(seed)
     bm = (torch.rand((H, MB, NB), generator=g) < 0.5).to(torch.uint8)
 
@@ -260,11 +263,12 @@ def test_bsr_variable_plan_bit_exact(lib, seed, H, MB, NB):
 
     rs = parts(50 * MB, MB)
     cs = parts(40 * NB, NB)
-    p = bskv.bskv_plan_bsr_variable(bm, rs, cs, 2 * H, H, 128, num_sms=SMS)
+    p = bskv.bskv_plan_bsr_variable(bm, rs, cs, 2 * H, H, D, causal=causal, num_sms=SMS)
     meta = p.metadata()
-    assert meta == plan_ref.bsr_variable_meta(bm.tolist(), rs.tolist(), cs.tolist(), 2 * H, H, SMS)
+    assert meta == plan_ref.bsr_variable_meta(bm.tolist(), rs.tolist(), cs.tolist(), 2 * H, H, SMS,
+                                              head_dim=D, causal=causal)
     s = plan_ref.sections(meta)
-    assert s["variant"] == 2
+    assert s["variant"] == (4 if D == 128 else 2)
 
 
 def test_bsr_variable_plan_rejects_bad_inputs(lib):
@@ -278,15 +282,23 @@ def test_bsr_variable_plan_rejects_bad_inputs(lib):
     _expect("ERR_UNSUPPORTED", f, bm, [[1, 2], [2, 1]], [[3, 1], [2, 2]], 2, 2, 96, num_sms=2)  # head_dim
 
 
+@pytest.mark.parametrize("D,causal", [(64, True), (128, True), (128, False)])
 @pytest.mark.parametrize("lengths,qo,ps", [([1, 17, 40, 90], [1, 17, 3, 64], 16),
-                                           ([2048, 300], [1024, 300], 64), ([5], [5], 1)])
-def test_prefill_paged_plan_bit_exact(lib, lengths, qo, ps):
+                                           ([2048, 300], [1024, 300], 64), ([5], [5], 1),
+                                           ([700, 0, 129], [300, 0, 129], 8),
+                                           ([1000, 77], [1, 77], 128)])
+def test_prefill_paged_plan_bit_exact(lib, lengths, qo, ps, D, causal):
+    """head_dim 64 (or page_size 1): the general kernel's plan (variant 3); head_dim 128 with
+    page_size 8 .. 128: the tensor-core plan (variant 5)."""
     d = synth.paged_prefill_inputs(85, len(lengths), 32, 8, 128, ps, 0, 0, 0, 0,
                                    lengths=lengths, qo_lens=qo)
     args = [d["qo_indptr"].tolist(), d["kv_indptr"].tolist(), d["kv_indices"].tolist(),
             d["kv_last_page_len"].tolist()]
-    p = bskv.bskv_plan_prefill_paged(*args, d["num_pages"], ps, 32, 8, 128, num_sms=SMS)
-    assert p.metadata() == plan_ref.prefill_paged_meta(*args, ps, 32, 8, SMS)
+    p = bskv.bskv_plan_prefill_paged(*args, d["num_pages"], ps, 32, 8, D, causal=causal,
+                                     num_sms=SMS)
+    meta = p.metadata()
+    assert meta == plan_ref.prefill_paged_meta(*args, ps, 32, 8, SMS, head_dim=D, causal=causal)
+    assert plan_ref.sections(meta)["variant"] == (5 if D == 128 and ps != 1 else 3)
 
 
 # ---------------------------------------------------------------------------------------
@@ -371,3 +383,79 @@ def test_plan_log_lines():
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        cwd=root, timeout=300)
     assert r.returncode == 0 and "[bskv]" not in r.stderr
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_variable_tc_plan_steps_cover_exactly_the_visible_keys(lib, causal):
+    """Tensor-core variable-block plan: for every row of every unit, the keys of its steps
+    (cut at the row's causal limit) are exactly the row of the oracle's dense mask, steps
+    hold at most 128 keys, and every (token, kv head) sits in exactly one unit."""
+    H, MB, NB, L, Lk = 4, 7, 9, 500, 700
+    d = synth.variable_block_inputs(21, 8, H, 128, MB, NB, L, Lk, density=0.45, causal=causal)
+    bm, rs, cs = d["block_mask_map"], d["block_row_sz"], d["block_col_sz"]
+    p = bskv.bskv_plan_bsr_variable(bm, rs, cs, 8, H, 128, causal=causal, num_sms=SMS)
+    meta = p.metadata()
+    assert plan_ref.sections(meta)["variant"] == 4
+    desc, steps = _aux(meta)
+    mask = att.variable_block_mask(bm.numpy(), rs.numpy(), cs.numpy(), causal=causal)
+    seen = np.zeros((H, L), int)
+    for c in plan_ref.sections(meta)["chunks"]:
+        x, _, h, _ = c
+        tok0, valid, tb, te, lim = desc[5 * x:5 * x + 5]
+        assert 1 <= valid <= 64
+        keys = np.zeros(Lk, bool)
+        for t in range(tb, te):
+            k0, ke = steps[2 * t], steps[2 * t + 1]
+            assert 0 <= k0 < ke <= Lk and ke - k0 <= 128
+            keys[k0:ke] = True
+        for r in range(valid):
+            row = keys.copy()
+            if causal:
+                row[lim + r + 1:] = False
+            np.testing.assert_array_equal(row, mask[h, tok0 + r])
+        seen[h, tok0:tok0 + valid] += 1
+    assert (seen == 1).all()
+
+
+@pytest.mark.parametrize("ps,causal", [(16, True), (8, True), (128, False), (64, True)])
+def test_prefill_tc_plan_steps_address_every_visible_key_once(lib, ps, causal):
+    """Tensor-core paged-prefill plan: per row, the keys of the unit's steps (cut at the
+    row's causal limit) are exactly the keys the row sees; a step's listed pages are the
+    request's pages for its keys (-1 past them); every (query token, kv head) is in one unit."""
+    lengths, qo = [1, 17, 300, 90, 0, 257], [1, 17, 130, 64, 0, 200]
+    Hkv = 2
+    d = synth.paged_prefill_inputs(87, len(lengths), 8, Hkv, 128, ps, 0, 0, 0, 0,
+                                   lengths=lengths, qo_lens=qo, device="cpu")
+    p = bskv.bskv_plan_prefill_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                                     d["kv_last_page_len"], d["num_pages"], ps, 8, Hkv, 128,
+                                     causal=causal, num_sms=SMS)
+    meta = p.metadata()
+    assert plan_ref.sections(meta)["variant"] == 5
+    desc, steps = _aux(meta)
+    words = 2 + 128 // ps
+    qi, ip, ix = d["qo_indptr"].numpy(), d["kv_indptr"].numpy(), d["kv_indices"].numpy()
+    seen = np.zeros((int(qi[-1]), Hkv), int)
+    for c in plan_ref.sections(meta)["chunks"]:
+        x, _, h, _ = c
+        tok0, valid, tb, te, lim = desc[5 * x:5 * x + 5]
+        b = int(np.searchsorted(qi, tok0, side="right") - 1)
+        L, nq = lengths[b], qo[b]
+        keys = np.zeros(L, bool)
+        for t in range(tb, te):
+            st = steps[words * t:words * (t + 1)]
+            k0, ke = st[0], st[1]
+            assert k0 % 128 == 0 and 0 <= k0 < ke <= L and ke - k0 <= 128
+            keys[k0:ke] = True
+            for k in range(128 // ps):
+                kk = k0 + k * ps
+                want = int(ix[ip[b] + kk // ps]) if kk < ke else -1
+                assert st[2 + k] == want
+        for r in range(valid):
+            t_local = tok0 - int(qi[b]) + r
+            want = np.arange(L) <= t_local + L - nq if causal else np.ones(L, bool)
+            row = keys.copy()
+            if causal:
+                row[lim + r + 1:] = False
+            np.testing.assert_array_equal(row, want)
+        seen[tok0:tok0 + valid, h] += 1
+    assert (seen == 1).all()
