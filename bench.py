@@ -575,16 +575,27 @@ def bench_mla(bskv, synth, steps, warmup, peaks):
                                     pos_q, True, q_rope_out=query[:, 0, :, 512:],
                                     q_nope_out=query[:, 0, :, :512])
 
+    def prologue_qk():
+        # both groups in one call (one launch over the query and key rows)
+        bskv.bskv_rope_quantize_fp8(m["q_rope"], m["k_rope"], m["q_nope"], m["k_nope"],
+                                    m["cos_sin"], pos_q, True, q_rope_out=query[:, 0, :, 512:],
+                                    q_nope_out=query[:, 0, :, :512], k_rope_out=pool[:, 512:],
+                                    k_nope_out=pool[:, :512], pos_ids_k=pos_k)
+
     pk = time_iters(prologue_k, steps, warmup, flush=True)
     pq = time_iters(prologue_q, steps, warmup, flush=True)
+    pqk = time_iters(prologue_qk, steps, warmup, flush=True)
     kbytes = m["pool_rows"] * (1152 + 576 + 256)
     qbytes = B * H * (1152 + 576) + B * 256
     res = dict(workload="mla_decode",
                prologue_k=dict(**summary(pk), bytes=kbytes,
                                gbs=kbytes / (statistics.median(pk) * 1e-3) / 1e9),
                prologue_q=dict(**summary(pq), bytes=qbytes,
-                               gbs=qbytes / (statistics.median(pq) * 1e-3) / 1e9))
-    res["prologue_k"]["frac"] = res["prologue_k"]["gbs"] / peaks["hbm_gbs"]
+                               gbs=qbytes / (statistics.median(pq) * 1e-3) / 1e9),
+               prologue_qk=dict(**summary(pqk), bytes=kbytes + qbytes, launches=1,
+                                gbs=(kbytes + qbytes) / (statistics.median(pqk) * 1e-3) / 1e9))
+    for k in ("prologue_k", "prologue_q", "prologue_qk"):
+        res[k]["frac"] = res[k]["gbs"] / peaks["hbm_gbs"]
     try:
         plan = bskv.bskv_plan_mla_sparse(m["seq_lens"], B, 1, H, K)
         plan.upload("cuda")

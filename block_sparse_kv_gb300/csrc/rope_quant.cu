@@ -6,9 +6,12 @@
 // K_fp8 = cast(K * quant_scale_kv); outputs may be strided slices of 576-byte rows).
 //
 // GB300 design: a pure HBM stream (2.0 bytes in per byte out, plus the cache row). A warp
-// handles two rows per iteration and issues every load of both (row data, positions, then
-// the cos/sin values the positions select) before it converts anything, so the position ->
-// cache dependency costs one latency per two rows. Each lane loads 32 bytes of NoPE (two
+// takes its rows 32 at a time: each lane first resolves one row's index chain (its rotary
+// position; for a paged append also its request, position and page, three dependent loads),
+// so the chain costs one latency per 32 rows; then the warp handles two rows per iteration,
+// taking their positions and destinations from the owning lanes by shuffle, and issues every
+// load of both rows (row data, then the cos/sin values the positions select) before it
+// converts anything. Each lane loads 32 bytes of NoPE (two
 // 16-byte loads) and writes 16 bytes of E4M3, and 4 bytes of the RoPE tail, exchanging
 // rotation partners with one shuffle (neox) or none (even/odd).
 // cvt.rn.satfinite.e4m3x2.f32 does the cast (RNE, saturating to +-448).
@@ -95,10 +98,10 @@ struct RowIn {
   bool valid;        // position inside [0, max_seq_len)
 };
 
-// Cache row of appended key row t, or -1 when its request, position or page is out of
-// range (three dependent loads; the row's data loads do not wait for them).
-__device__ __forceinline__ int64_t append_row(const RopeParams& p, int64_t t) {
-  const int32_t b = __ldg(p.app_batch + t), q = __ldg(p.app_pos + t);
+// Cache row of an appended key row of request b at position q, or -1 when its request,
+// position or page is out of range (two dependent loads; the row's data loads do not wait
+// for them).
+__device__ __forceinline__ int64_t append_row(const RopeParams& p, int32_t b, int32_t q) {
   if (b < 0 || b >= p.app_requests || q < 0) return -1;
   const int64_t slot = int64_t(__ldg(p.app_indptr + b)) + q / p.app_page_size;
   if (slot >= __ldg(p.app_indptr + b + 1)) return -1;
@@ -107,11 +110,10 @@ __device__ __forceinline__ int64_t append_row(const RopeParams& p, int64_t t) {
   return int64_t(page) * p.app_page_size + q % p.app_page_size;
 }
 
-template <bool kNeox, typename PosT, typename CacheT>
 __device__ __forceinline__ void row_ptrs(const RopeParams& p, int64_t r, int64_t q_rows,
                                          const __nv_bfloat16*& rope, const __nv_bfloat16*& nope,
-                                         uint8_t*& rope_out, uint8_t*& nope_out, int64_t& pos,
-                                         float& scale, bool& dst_ok) {
+                                         uint8_t*& rope_out, uint8_t*& nope_out, float& scale,
+                                         bool& dst_ok) {
   dst_ok = true;
   if (r < q_rows) {
     const int64_t t = r / p.heads;
@@ -120,7 +122,6 @@ __device__ __forceinline__ void row_ptrs(const RopeParams& p, int64_t r, int64_t
     nope = p.q_nope + t * p.qn_s0 + h * p.qn_s1;
     rope_out = p.q_rope_out + t * p.qro_s0 + h * p.qro_s1;
     nope_out = p.q_nope_out + t * p.qno_s0 + h * p.qno_s1;
-    pos = int64_t(__ldg(static_cast<const PosT*>(p.pos_q) + t));
     scale = p.scale_q;
   } else {
     const int64_t t = r - q_rows;
@@ -130,17 +131,30 @@ __device__ __forceinline__ void row_ptrs(const RopeParams& p, int64_t r, int64_t
     // loads are in flight
     rope_out = p.k_rope_out + t * p.kro_s;
     nope_out = p.k_nope_out + t * p.kno_s;
-    pos = int64_t(__ldg(static_cast<const PosT*>(p.pos_k) + t));
     scale = p.scale_kv;
   }
 }
 
-// Destination of appended key row r (rows past the query rows only): the page table lookup.
+// Index chain of row r, resolved by one lane for the warp: its rotary position and, for an
+// appended key row, its cache row (-1 when the destination is out of range).
+template <typename PosT, bool kAppend>
+__device__ __forceinline__ void row_chain(const RopeParams& p, int64_t r, int64_t q_rows,
+                                          int64_t& pos, int64_t& dst) {
+  dst = 0;
+  if (r < q_rows) {
+    pos = int64_t(__ldg(static_cast<const PosT*>(p.pos_q) + r / p.heads));
+  } else {
+    const int64_t t = r - q_rows;
+    pos = int64_t(__ldg(static_cast<const PosT*>(p.pos_k) + t));
+    if (kAppend) dst = append_row(p, __ldg(p.app_batch + t), __ldg(p.app_pos + t));
+  }
+}
+
+// Destination of an appended key row r (rows past the query rows only) from its cache row.
 __device__ __forceinline__ void resolve_dst(const RopeParams& p, int64_t r, int64_t q_rows,
-                                            uint8_t*& rope_out, uint8_t*& nope_out,
+                                            int64_t d, uint8_t*& rope_out, uint8_t*& nope_out,
                                             bool& dst_ok) {
-  if (!p.app_indptr || r < q_rows) return;
-  int64_t d = append_row(p, r - q_rows);
+  if (r < q_rows) return;
   dst_ok = d >= 0;
   if (!dst_ok) d = 0;
   rope_out = p.k_rope_out + d * p.kro_s;
@@ -214,32 +228,48 @@ __device__ __forceinline__ void store_row(const RowIn& in, uint8_t* rope_out, ui
       cvt_e4m3x2(__fmul_rn(r0, scale), __fmul_rn(r1, scale));
 }
 
-template <bool kNeox, typename PosT, typename CacheT>
+// kAppend: key rows go to the paged cache through the page table.
+template <bool kNeox, typename PosT, typename CacheT, bool kAppend>
 __global__ void __launch_bounds__(256) rope_quant_kernel(const RopeParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t W = (int64_t(gridDim.x) * blockDim.x) >> 5;
   const int64_t q_rows = p.q_rope ? p.nnz_q * p.heads : 0;
   const int64_t total = q_rows + (p.k_rope ? p.nnz_k : 0);
   const CacheT* cache = static_cast<const CacheT*>(p.cos_sin);
-  // Two rows per warp per iteration (rows ra and ra + W), all loads issued before use.
-  for (int64_t ra = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; ra < total; ra += 2 * W) {
-    const int64_t rb = ra + W;
-    const bool has_b = rb < total;
-    const __nv_bfloat16 *rope_a, *nope_a, *rope_b, *nope_b;
-    uint8_t *ro_a, *no_a, *ro_b, *no_b;
-    int64_t pos_a, pos_b;
-    float sc_a, sc_b;
-    bool ok_a, ok_b;
-    row_ptrs<kNeox, PosT, CacheT>(p, ra, q_rows, rope_a, nope_a, ro_a, no_a, pos_a, sc_a, ok_a);
-    row_ptrs<kNeox, PosT, CacheT>(p, has_b ? rb : ra, q_rows, rope_b, nope_b, ro_b, no_b, pos_b,
-                                  sc_b, ok_b);
-    RowIn a, b;
-    load_row<kNeox, CacheT>(rope_a, nope_a, pos_a, p.max_seq_len, cache, lane, a);
-    load_row<kNeox, CacheT>(rope_b, nope_b, pos_b, p.max_seq_len, cache, lane, b);
-    resolve_dst(p, ra, q_rows, ro_a, no_a, ok_a);
-    resolve_dst(p, has_b ? rb : ra, q_rows, ro_b, no_b, ok_b);
-    store_row<kNeox>(a, ro_a, no_a, sc_a, lane, p.st, ok_a);
-    if (has_b) store_row<kNeox>(b, ro_b, no_b, sc_b, lane, p.st, ok_b);
+  // Rows base + i W (i < 32) of this warp: lane i resolves row i's chain, then the warp takes
+  // the rows two at a time (rows 2k and 2k + 1 of the 32), every load of both issued before
+  // use.
+  for (int64_t base = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; base < total;
+       base += 32 * W) {
+    const int64_t my_r = base + int64_t(lane) * W;
+    int64_t my_pos = 0, my_dst = 0;
+    if (my_r < total) row_chain<PosT, kAppend>(p, my_r, q_rows, my_pos, my_dst);
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k) {
+      const int64_t ra = base + int64_t(2 * k) * W;
+      if (ra >= total) break;  // warp-uniform
+      const int64_t rb = ra + W;
+      const bool has_b = rb < total;
+      const int64_t pos_a = __shfl_sync(0xffffffffu, my_pos, 2 * k);
+      const int64_t pos_b = __shfl_sync(0xffffffffu, my_pos, 2 * k + 1);
+      const __nv_bfloat16 *rope_a, *nope_a, *rope_b, *nope_b;
+      uint8_t *ro_a, *no_a, *ro_b, *no_b;
+      float sc_a, sc_b;
+      bool ok_a, ok_b;
+      row_ptrs(p, ra, q_rows, rope_a, nope_a, ro_a, no_a, sc_a, ok_a);
+      row_ptrs(p, has_b ? rb : ra, q_rows, rope_b, nope_b, ro_b, no_b, sc_b, ok_b);
+      RowIn a, b;
+      load_row<kNeox, CacheT>(rope_a, nope_a, pos_a, p.max_seq_len, cache, lane, a);
+      load_row<kNeox, CacheT>(rope_b, nope_b, has_b ? pos_b : pos_a, p.max_seq_len, cache, lane, b);
+      if (kAppend) {
+        const int64_t dst_a = __shfl_sync(0xffffffffu, my_dst, 2 * k);
+        const int64_t dst_b = __shfl_sync(0xffffffffu, my_dst, 2 * k + 1);
+        resolve_dst(p, ra, q_rows, dst_a, ro_a, no_a, ok_a);
+        if (has_b) resolve_dst(p, rb, q_rows, dst_b, ro_b, no_b, ok_b);
+      }
+      store_row<kNeox>(a, ro_a, no_a, sc_a, lane, p.st, ok_a);
+      if (has_b) store_row<kNeox>(b, ro_b, no_b, sc_b, lane, p.st, ok_b);
+    }
   }
 }
 
@@ -266,7 +296,8 @@ bskv_status resident_grid(Kernel kernel, int threads, int* out) {
 
 template <bool kNeox, typename PosT, typename CacheT>
 bskv_status launch_rope_t(const RopeParams& p, int64_t rows, cudaStream_t st) {
-  auto kernel = rope_quant_kernel<kNeox, PosT, CacheT>;
+  auto kernel = p.app_indptr ? rope_quant_kernel<kNeox, PosT, CacheT, true>
+                             : rope_quant_kernel<kNeox, PosT, CacheT, false>;
   int resident = 0;
   if (bskv_status s = resident_grid(kernel, 256, &resident)) return s;
   // One wave of resident blocks; fewer when there are fewer than one row per warp.
