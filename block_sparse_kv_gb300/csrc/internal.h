@@ -42,6 +42,12 @@ constexpr int kDecodeWarps = 8;        // decode workers (warps) per CTA, one CT
 constexpr int kBsrGenericRows = 64;    // packed (token, head) rows per general-BSR unit
 constexpr int kBsrGenericCtasPerSm = 4;
 constexpr int kMlaTile = 128;          // sparse rows per MLA tile
+// An MLA plan assigns whole query tokens (no split-KV pieces, no merge kernel) when the
+// busiest worker then has at most this many tiles more than under the balanced split
+// partition: splitting costs about that much (each piece writes fp32 partial states of both
+// latent halves and loads its query again, and the merge is a second launch; measured on the
+// 128-query sparse decode as 98.9 us split on 76 workers against 92.2 us whole on 64).
+constexpr int kMlaSplitPenaltyTiles = 7;
 constexpr int kMlaVSplit = 2;          // the 512 latent output values split in halves
 constexpr int kMlaVDim = 512 / kMlaVSplit;
 

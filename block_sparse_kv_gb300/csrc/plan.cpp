@@ -131,6 +131,55 @@ void linear_partition(const std::vector<int64_t>& unit_len, int64_t tile, int64_
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
+std::vector<std::vector<int32_t>> lpt_assign(const std::vector<int64_t>& cost, int32_t G);
+
+// MLA partition: units (query tokens or requests) of unit_len rows in tiles of `tile`, on at
+// most max_workers cluster workers. Whole units by longest processing time (units of more
+// tiles first; no slots; units without rows become zero-fill merge items) when the busiest
+// worker's tiles stay within kMlaSplitPenaltyTiles of the linear split partition's; else the
+// linear split partition.
+void mla_partition(const std::vector<int64_t>& unit_len, int64_t tile, int64_t max_workers,
+                   std::vector<int32_t>& worker_ptr, std::vector<Chunk>& chunks,
+                   int32_t& slots, std::vector<int32_t>& merges) {
+  std::vector<int64_t> tiles(unit_len.size());
+  std::vector<int32_t> live;
+  int64_t NT = 0;
+  for (size_t u = 0; u < unit_len.size(); ++u) {
+    tiles[u] = (unit_len[u] + tile - 1) / tile;
+    NT += tiles[u];
+    if (tiles[u] > 0) live.push_back(int32_t(u));
+  }
+  linear_partition(unit_len, tile, max_workers, worker_ptr, chunks, slots, merges);
+  if (NT == 0) return;
+  const int64_t P = std::min<int64_t>(max_workers, NT);
+  const int64_t split_max = (NT + P - 1) / P;
+  const int32_t G = int32_t(std::min<int64_t>(max_workers, int64_t(live.size())));
+  std::vector<int64_t> cost(live.size());
+  for (size_t i = 0; i < live.size(); ++i) cost[i] = tiles[size_t(live[i])];
+  const std::vector<std::vector<int32_t>> lists = lpt_assign(cost, G);
+  int64_t whole_max = 0;
+  for (const auto& l : lists) {
+    int64_t load = 0;
+    for (int32_t i : l) load += cost[size_t(i)];
+    whole_max = std::max(whole_max, load);
+  }
+  if (whole_max > split_max + kMlaSplitPenaltyTiles) return;
+  worker_ptr.assign(size_t(G) + 1, 0);
+  chunks.clear();
+  for (int32_t w = 0; w < G; ++w) {
+    worker_ptr[size_t(w)] = int32_t(chunks.size());
+    for (int32_t i : lists[size_t(w)]) {
+      const int32_t u = live[size_t(i)];
+      chunks.push_back(Chunk{u, 0, int32_t(unit_len[size_t(u)]), -1});
+    }
+  }
+  worker_ptr[size_t(G)] = int32_t(chunks.size());
+  slots = 0;
+  merges.clear();
+  for (size_t u = 0; u < unit_len.size(); ++u)
+    if (tiles[u] == 0) merges.insert(merges.end(), {int32_t(u), -1, 0});
+}
+
 // Longest-processing-time assignment of units with costs `cost` to G workers: units taken by
 // cost, largest first (stable), each given to the worker of least load so far (ties: the
 // lowest worker index). Returns every worker's units in assignment order.
@@ -778,8 +827,8 @@ extern "C" bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t bat
   std::vector<int32_t> worker_ptr, merges;
   std::vector<Chunk> chunks;
   int32_t slots = 0;
-  linear_partition(len, kMlaTile, std::max(1, num_sms / kMlaVSplit), worker_ptr, chunks, slots,
-                   merges);
+  mla_partition(len, kMlaTile, std::max(1, num_sms / kMlaVSplit), worker_ptr, chunks, slots,
+                merges);
   const int32_t P = int32_t(worker_ptr.size() - 1);
   bskv_plan* p = new bskv_plan();
   p->kind = KIND_MLA;
@@ -841,8 +890,8 @@ extern "C" bskv_status bskv_plan_mla_paged(const int32_t* kv_indptr, const int32
   std::vector<int32_t> worker_ptr, merges;
   std::vector<Chunk> chunks;
   int32_t slots = 0;
-  linear_partition(len, kMlaTile, std::max(1, num_sms / kMlaVSplit), worker_ptr, chunks, slots,
-                   merges);
+  mla_partition(len, kMlaTile, std::max(1, num_sms / kMlaVSplit), worker_ptr, chunks, slots,
+                merges);
   const int32_t P = int32_t(worker_ptr.size() - 1);
   bskv_plan* p = new bskv_plan();
   p->kind = KIND_MLA;

@@ -31,7 +31,12 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
     aux1 = kv_indices.
   * MLA: units = query tokens n = b*q_len + t, len = seq_lens[b], tile 128,
     max_workers = max(1, num_sms // 2) (a worker is a pair of CTAs, one per latent half),
-    grid = 2 P, no aux, variant 0.
+    grid = 2 P, no aux, variant 0. Whole units instead of the linear partition when, with
+    the units of at least one tile placed by longest processing time (tiles descending,
+    stable; least-loaded worker, lowest index on ties) on G = min(max_workers, such units)
+    workers, the busiest worker holds at most 7 tiles more than ceil(NT / P): chunks (u, 0,
+    len_u, -1) per worker in assignment order, no slots, merge items (u, -1, 0) for the units
+    without rows; P = G then.
   * variable-block BSR (variant 2): per kv head h and row block a, in that order, a
     descriptor (first query token, row count, first tile, end tile); the tiles split each
     maximal run of consecutive visible column blocks [s, e) into (t, e) for t = s, s + 32,
@@ -181,17 +186,54 @@ def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_q
     return _assemble(1, len(lens), wp, ch, slots, merges, 16, aux0, aux1, grid, 1 if G else 0)
 
 
+MLA_SPLIT_PENALTY_TILES = 7
+
+
+def mla_partition(unit_len, tile, max_workers):
+    """Whole units by longest processing time when the busiest worker's tiles stay within
+    MLA_SPLIT_PENALTY_TILES of the linear split partition's, else the linear partition."""
+    tiles = [(L + tile - 1) // tile for L in unit_len]
+    NT = sum(tiles)
+    lin = linear_partition(unit_len, tile, max_workers)
+    if NT == 0:
+        return lin
+    P = min(max_workers, NT)
+    split_max = -(-NT // P)
+    live = [u for u in range(len(unit_len)) if tiles[u] > 0]
+    G = min(max_workers, len(live))
+    order = sorted(range(len(live)), key=lambda i: -tiles[live[i]])   # stable
+    heap = [(0, w) for w in range(G)]
+    heapq.heapify(heap)
+    lists = [[] for _ in range(G)]
+    for i in order:
+        load, w = heapq.heappop(heap)
+        lists[w].append(i)
+        heapq.heappush(heap, (load + tiles[live[i]], w))
+    whole_max = max(sum(tiles[live[i]] for i in l) for l in lists)
+    if whole_max > split_max + MLA_SPLIT_PENALTY_TILES:
+        return lin
+    wp, ch = [], []
+    for w in range(G):
+        wp.append(len(ch))
+        for i in lists[w]:
+            u = live[i]
+            ch.append([u, 0, int(unit_len[u]), -1])
+    wp.append(len(ch))
+    merges = [[u, -1, 0] for u in range(len(unit_len)) if tiles[u] == 0]
+    return wp, ch, 0, merges
+
+
 def mla_meta(seq_lens, batch, q_len, num_sms):
     lens = []
     for b in range(batch):
         lens += [int(seq_lens[b])] * q_len
-    wp, ch, slots, merges = linear_partition(lens, 128, max(1, num_sms // 2))
+    wp, ch, slots, merges = mla_partition(lens, 128, max(1, num_sms // 2))
     return _assemble(3, len(lens), wp, ch, slots, merges, 128, [], [], 2 * (len(wp) - 1), 0)
 
 
 def mla_paged_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_sms):
     lens = [paged_request_len(kv_indptr, kv_last_page_len, page_size, b) for b in range(batch)]
-    wp, ch, slots, merges = linear_partition(lens, 128, max(1, num_sms // 2))
+    wp, ch, slots, merges = mla_partition(lens, 128, max(1, num_sms // 2))
     nnz = int(kv_indptr[batch]) if batch > 0 else 0
     aux0 = [int(x) for x in kv_indptr[:batch + 1]] if batch > 0 else []
     aux1 = [int(x) for x in kv_indices[:nnz]]

@@ -91,9 +91,9 @@ def test_variable_block_rows_that_see_nothing(cuda, D):
 def test_variable_block_full_workload_sampled(cuda):
     """The benchmark's workload (16384 tokens, 32/8 heads, D 128, fp16, 128 x 128 random-size
     blocks per kv head, 10 % kept, causal) in the launch configuration it times, checked on
-    256 sampled query tokens of every head (the oracle computes only those rows)."""
+    1024 sampled query tokens of every head (the oracle computes only those rows)."""
     d = synth.make("bsr_variable")
-    rows = sorted(torch.randperm(d["qo_len"], generator=torch.Generator().manual_seed(5))[:256].tolist())
+    rows = sorted(torch.randperm(d["qo_len"], generator=torch.Generator().manual_seed(5))[:1024].tolist())
     st = _run(cuda, d, rows=rows)
     print("variable blocks full workload sampled:", st)
 

@@ -150,6 +150,20 @@ def test_mla_plan_bit_exact(lib, batch, q_len, seq):
     assert plan_ref.sections(meta)["grid"] == 2 * plan_ref.sections(meta)["workers"]
 
 
+def test_mla_plan_splits_only_when_it_pays(lib):
+    """128 queries of 16 tiles on 76 cluster workers: whole queries (busiest worker 32 tiles,
+    split partition 27: within the 7-tile penalty), so no partial states and no merge; three
+    queries of 16 tiles: the split partition (1 tile per worker against 16 whole)."""
+    p = bskv.bskv_plan_mla_sparse([2048] * 128, 128, 1, 128, 2048, num_sms=SMS)
+    s = plan_ref.sections(p.metadata())
+    assert s["slots"] == 0 and s["merges_n"] == 0 and s["workers"] == 76
+    assert all(c[1] == 0 and c[2] == 2048 and c[3] == -1 for c in s["chunks"])
+    assert p.workspace_sizes()[1] == 0
+    p = bskv.bskv_plan_mla_sparse([2048] * 3, 3, 1, 128, 2048, num_sms=SMS)
+    s = plan_ref.sections(p.metadata())
+    assert s["slots"] > 0 and s["merges_n"] == 3
+
+
 @pytest.mark.parametrize("lens,ps", [([5, 0, 130], 16), ([2048] * 7, 64), ([1, 64, 65, 300], 1)])
 def test_mla_paged_plan_bit_exact(lib, lens, ps):
     d = synth.mla_paged_inputs(61, batch=len(lens), heads=16, page_size=ps, len_lo=0, len_hi=0,
