@@ -361,11 +361,36 @@ def bench_decode(bskv, synth, name, steps, warmup, dist, sampler=None, headline=
     total_ms = evs[0][0].elapsed_time(evs[-1][1])
     kern_ms = [e[0].elapsed_time(e[1]) for e in evs]
     nbytes = decode_kv_bytes(d)
+    # the same step captured once in a CUDA graph and replayed back to back (how a serving
+    # loop issues it); reported beside the eager numbers
+    graph_ms = None
+    if headline:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        graph_ms = a.elapsed_time(b) / steps
+        del g
     res = dict(workload=name, kv_bytes=nbytes, plan_us=plan_us, total_ms=total_ms,
                ms_per_step=total_ms / steps, decode_kernel=summary(kern_ms),
                variant="page-major (all kv heads of a page per CTA)" if meta[15] == 1
                else "per kv head (one worker per warp)",
-               split_units=meta[6], launches_per_step=decode_launches(meta), clocks=clocks)
+               split_units=meta[6], launches_per_step=decode_launches(meta), clocks=clocks,
+               graph_ms_per_step=graph_ms)
     res["gbs_step"] = nbytes / (res["ms_per_step"] * 1e-3) / 1e9
     res["gbs_kernel"] = nbytes / (statistics.mean(kern_ms) * 1e-3) / 1e9
     del d, kv, q
@@ -748,7 +773,8 @@ def main():
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
-    head, _ = bench_decode(bskv, synth, "paged_decode", args.steps, args.warmup, dist)
+    head, _ = bench_decode(bskv, synth, "paged_decode", args.steps, args.warmup, dist,
+                           headline=True)
     t_max = max_over_ranks(dist, head["total_ms"])
     total_bytes = sum_over_ranks(dist, head["kv_bytes"] * args.steps)
     value = total_bytes / (t_max * 1e-3) / 1e9
@@ -813,7 +839,9 @@ def main():
         "clocks": clocks,
         "gpu_launches": head["launches_per_step"] * args.steps,
         "plan_us": head["plan_us"],
-        "step_breakdown_us": {"decode_kernel_with_fused_merge": head["decode_kernel"]["mean_us"]},
+        "step_breakdown_us": {"decode_kernel_with_fused_merge": head["decode_kernel"]["mean_us"],
+                              "graph_replay_per_step": (1e3 * head["graph_ms_per_step"]
+                                                        if head["graph_ms_per_step"] else None)},
         "decode_variant": head["variant"],
         "device_status": bskv.STATUS.get(status, status),
         "e2e": e2e,
