@@ -409,8 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = (kv_first + j) % S;
           const uint32_t vo = (s * kStageBytes) >> 4;
           const uint32_t pa = tmem + 128 + 256 * z;
-          // a block pair is 8 MMAs (K = 16 keys each), a lone last block 4
-          if (nb == 2) {
+          // a block pair is 8 MMAs (K = 16 keys each), a lone last block 4; a list step only
+          // the 16-key slices that hold its keys (the V rows past them are zero, see softmax)
+          if constexpr (kList) {
+            const int32_t* st = indices + int64_t(p.step_words) * (u.e0 + j);
+            const int nk = (st[1] - st[0] + 15) >> 4;
+#pragma unroll 1
+            for (int kk = 0; kk < nk; ++kk)
+              umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
+                            (j == 0 && kk == 0) ? 0u : 1u);
+          } else if (nb == 2) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
@@ -593,10 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if constexpr (kList) {
-          // V rows of a partial step past its last key (a page's unused slots, rows no box of
-          // this step wrote) are zeroed before PV reads them: their P is 0, but 0 * NaN is not.
-          // The first M tile's PV is issued before the second's, so its warpgroup does it.
-          if (m == 0 && kvalid < 64 * nb && r >= kvalid && r < 64 * nb) {
+          // V rows of a partial step past its last key up to the next multiple of 16 (a page's
+          // unused slots, rows no box of this step wrote), which the step's last PV slice
+          // reads, are zeroed before PV: their P is 0, but 0 * NaN is not. The first M tile's
+          // PV is issued before the second's, so its warpgroup does it.
+          if (m == 0 && r >= kvalid && r < ((kvalid + 15) & ~15)) {
             uint8_t* vrow = sm + L::kKV + ((kvs + j) % S) * kStageBytes + 2 * kPairPanel + r * 128;
 #pragma unroll
             for (int pn = 0; pn < 2; ++pn)
