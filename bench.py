@@ -666,7 +666,7 @@ def bench_mla_paged(bskv, synth, steps, warmup, peaks):
                 **summary(ms), flops=fl, tflops=tf, frac=tf / fp8_peak, peak=src,
                 peak_tflops=fp8_peak,
                 bytes=nbytes, gbs=gbs, hbm_frac=gbs / peaks["hbm_gbs"],
-                launches_per_step=2 + (1 if plan.metadata()[6] > 0 else 0))
+                launches_per_step=1 + (1 if plan.metadata()[6] > 0 else 0))
 
 
 def bench_mla_append(bskv, synth, steps, warmup, peaks):

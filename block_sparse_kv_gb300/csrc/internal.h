@@ -86,8 +86,8 @@ inline bool bsr_tc_page_size(int32_t page_size) {
   return page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 ||
          page_size == 128;
 }
-// MLA_SPARSE: row lists given by the caller. MLA_PAGED: row lists expanded on the device
-// from the page table in the metadata (aux0 = kv_indptr, aux1 = kv_indices).
+// MLA_SPARSE: row lists given by the caller. MLA_PAGED: rows read from the page table in
+// the metadata (aux0 = kv_indptr, aux1 = kv_indices) by the gather itself.
 enum MlaVariant : int32_t { MLA_SPARSE = 0, MLA_PAGED = 1 };
 // DECODE_WARP: one worker per warp, units (request, kv head).
 // DECODE_GROUP: one worker per CTA, units (request, group of G kv heads), G = Hkv when
@@ -139,10 +139,9 @@ struct bskv_plan {
   int32_t num_qo_heads = 0, num_kv_heads = 0, head_dim = 0, dtype = 0;
   // bsr (masked: runs take a per-block token mask, the general kernel serves them)
   int32_t M = 0, N = 0, R = 0, C = 0, causal = 0, masked = 0;
-  // mla (paged: batch, num_pages and page_size as for decode; top_k is the row-list
-  // stride, the longest request rounded up to 64)
+  // mla (paged: batch, num_pages and page_size as for decode; top_k is the longest request
+  // rounded up to 64)
   int32_t q_len = 0, top_k = 0, mla_variant = 0;
-  size_t mla_rows_off = 0;  // paged: byte offset of the row list in the float workspace
   size_t float_ws_bytes = 0;
   // int32 merge counters after the metadata in the int workspace (decode: one per merge
   // item and kv head of the unit)

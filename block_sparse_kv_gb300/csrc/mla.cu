@@ -80,6 +80,11 @@ struct MlaParams {
   const uint8_t* kv;
   int64_t num_rows;
   const int32_t* indices;
+  // paged decode (indices NULL): request n's token t is cache row
+  // pg_indices[pg_indptr[n] + t / page_size] * page_size + t % page_size
+  const int32_t* pg_indptr;
+  const int32_t* pg_indices;
+  int page_size;
   int top_k, heads;
   float scale_log2;  // bmm1_scale * log2(e)
   float bmm2;
@@ -225,18 +230,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // a chunk), so the id is one independent load that nothing waits for until the next
     // tile: a load chained behind the descriptor's would stall the id threads, and with
     // them the whole gather group, for two L2 round trips per tile.
-    auto load_id = [&](const int4& cn, int u0) -> int32_t {
-      if (pt >= kHalfRows) return 0;
-      return u0 + tr < cn.z ? __ldg(p.indices + int64_t(cn.x) * p.top_k + u0 + tr) : 0;
+    // Paged decode: the row of token t of the chunk's request comes from the page table,
+    // page_ptr = kv_indptr of the request (read once per chunk, when its first row ids are).
+    auto load_id = [&](const int4& cn, int page_ptr, int u0) -> int32_t {
+      if (pt >= kHalfRows || u0 + tr >= cn.z) return 0;
+      const int t = u0 + tr;
+      if (p.pg_indices) {
+        const int pg = __ldg(p.pg_indices + page_ptr + t / p.page_size);
+        return pg * p.page_size + t % p.page_size;
+      }
+      return __ldg(p.indices + int64_t(cn.x) * p.top_k + t);
+    };
+    auto page_ptr_of = [&](const int4& cn) -> int {
+      return p.pg_indices && pt < kHalfRows ? __ldg(p.pg_indptr + cn.x) : 0;
     };
     int4 ch = c0 < c1 ? chunks[c0] : make_int4(0, 0, 0, 0);
-    int32_t next_id = c0 < c1 ? load_id(ch, ch.y) : 0;
+    int cptr = c0 < c1 ? page_ptr_of(ch) : 0;
+    int32_t next_id = c0 < c1 ? load_id(ch, cptr, ch.y) : 0;
     for (int ci = c0; ci < c1 && ok; ++ci) {
       const int4 nch = ci + 1 < c1 ? chunks[ci + 1] : make_int4(0, 0, 0, 0);
+      int nptr = 0;
       for (int t0 = ch.y; t0 < ch.z; t0 += kRows, ++kvc) {
         const int v = kvc % kVSlots, k = kvc % kKSlots;
         int32_t my_id = next_id;
-        next_id = t0 + kRows < ch.z ? load_id(ch, t0 + kRows) : (ci + 1 < c1 ? load_id(nch, nch.y) : 0);
+        if (t0 + kRows < ch.z) {
+          next_id = load_id(ch, cptr, t0 + kRows);
+        } else if (ci + 1 < c1) {
+          nptr = page_ptr_of(nch);
+          next_id = load_id(nch, nptr, nch.y);
+        } else {
+          next_id = 0;
+        }
         if (my_id < 0 || my_id >= p.num_rows) {
           record_error(p.st, BSKV_ERR_DEVICE_INDEX);
           my_id = 0;
@@ -287,6 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       ch = nch;
+      cptr = nptr;
     }
     if (pt == 0) bulk_wait_read0();
     if (!ok) raise_abort();
@@ -721,38 +746,24 @@ __global__ void __launch_bounds__(128)
   if (lse && vh == 0 && lane == 0) lse[int64_t(n) * heads + h] = count > 0 ? m + logf(l) : -INFINITY;
 }
 
-// Row list of the paged decode, from the page table in the metadata (aux0 = kv_indptr,
-// aux1 = kv_indices): rows[b * stride + t] = the cache row of token t of request b, for the
-// tokens its pages hold (the decode reads only t < L_b; entries past them stay unwritten).
-// Grid: y strides over requests, x over a request's tokens.
-__global__ void __launch_bounds__(256) mla_page_rows_kernel(const int32_t* __restrict__ meta,
-                                                            int32_t batch, int32_t stride,
-                                                            int32_t page_size,
-                                                            int32_t* __restrict__ rows) {
-  const int32_t* indptr = meta + meta[H_OFF_AUX0];
-  const int32_t* pages = meta + meta[H_OFF_AUX1];
-  for (int32_t b = blockIdx.y; b < batch; b += gridDim.y) {
-    const int32_t p0 = indptr[b];
-    const int32_t lim = int32_t(min(int64_t(indptr[b + 1] - p0) * page_size, int64_t(stride)));
-    int32_t* out = rows + int64_t(b) * stride;
-    for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < lim; t += gridDim.x * blockDim.x) {
-      const int32_t pi = t / page_size;
-      out[t] = pages[p0 + pi] * page_size + (t - pi * page_size);
-    }
-  }
-}
-
-// The decode over validated arguments: `indices` holds plan->top_k row ids per query token,
-// the float workspace starts with the split-KV partials.
+// The decode over validated arguments: `indices` holds plan->top_k row ids per query token
+// (NULL for a paged plan, whose rows come from its page table); the float workspace holds
+// the split-KV partials.
 bskv_status run_mla(const bskv_plan* plan, const void* query, const void* kv_rows,
                     int64_t num_rows, const int32_t* indices, float bmm1_scale, float bmm2_scale,
                     void* out, float* lse, void* float_ws, cudaStream_t st) {
+  const bool paged = plan->mla_variant == MLA_PAGED;
   const int64_t nq = int64_t(plan->batch) * plan->q_len;
   MlaParams mp{};
   mp.meta = plan->meta_dev;
   mp.kv = static_cast<const uint8_t*>(kv_rows);
   mp.num_rows = num_rows;
   mp.indices = indices;
+  if (paged) {  // the page table rides in the uploaded metadata (aux0 = kv_indptr, aux1 = kv_indices)
+    mp.pg_indptr = plan->meta_dev + meta_word(plan, H_OFF_AUX0);
+    mp.pg_indices = plan->meta_dev + meta_word(plan, H_OFF_AUX1);
+    mp.page_size = plan->page_size;
+  }
   mp.top_k = plan->top_k;
   mp.heads = plan->num_qo_heads;
   mp.scale_log2 = bmm1_scale * 1.4426950408889634f;
@@ -856,18 +867,12 @@ extern "C" bskv_status bskv_run_mla_paged(const bskv_plan* plan, const void* que
     set_error("run_mla_paged: tensors must be 16-byte aligned");
     return BSKV_ERR_INVALID_ARG;
   }
-  if (float_ws_bytes < plan->float_ws_bytes || !float_ws) {
+  if (float_ws_bytes < plan->float_ws_bytes || (plan->float_ws_bytes && !float_ws)) {
     set_error("run_mla_paged: float workspace of %zu bytes, %zu needed", float_ws_bytes, plan->float_ws_bytes);
     return BSKV_ERR_WORKSPACE_TOO_SMALL;
   }
-  if (!aligned16(float_ws)) { set_error("run_mla_paged: float workspace must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
+  if (float_ws && !aligned16(float_ws)) { set_error("run_mla_paged: float workspace must be 16-byte aligned"); return BSKV_ERR_INVALID_ARG; }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int32_t* rows = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(float_ws) + plan->mla_rows_off);
-  const dim3 grid_rows(unsigned(std::min((plan->top_k + 255) / 256, 32)),
-                       unsigned(std::min(plan->batch, 65535)));
-  mla_page_rows_kernel<<<grid_rows, 256, 0, st>>>(plan->meta_dev, plan->batch, plan->top_k,
-                                                  plan->page_size, rows);
-  if (bskv_status s = cuda_check(cudaGetLastError(), "mla page rows launch")) return s;
-  return run_mla(plan, query, kv_pages, int64_t(plan->num_pages) * plan->page_size, rows,
+  return run_mla(plan, query, kv_pages, int64_t(plan->num_pages) * plan->page_size, nullptr,
                  bmm1_scale, bmm2_scale, out, lse, float_ws, st);
 }

@@ -294,7 +294,7 @@ void log_plan(const char* name, const bskv_plan* p) {
                                                    : "bsr_generic_kernel";
       break;
     case KIND_MLA:
-      kernel = p->mla_variant == MLA_PAGED ? "mla_page_rows_kernel + mla_kernel (paged rows)"
+      kernel = p->mla_variant == MLA_PAGED ? "mla_kernel (rows from the page table)"
                                            : "mla_kernel (sparse rows)";
       break;
     default:
@@ -902,11 +902,9 @@ extern "C" bskv_status bskv_plan_mla_paged(const int32_t* kv_indptr, const int32
   assemble(p, KIND_MLA, int32_t(len.size()), worker_ptr, chunks, slots, merges, kMlaTile,
            kv_indptr, batch > 0 ? size_t(batch) + 1 : 0, kv_indices, size_t(nnz), P * kMlaVSplit,
            MLA_PAGED);
-  const size_t partials = slots == 0 ? 0
+  p->float_ws_bytes = slots == 0 ? 0
       : align256(size_t(slots) * kMlaVSplit * 128 * kMlaVDim * 4) +
             align256(size_t(slots) * kMlaVSplit * 128 * 4);
-  p->mla_rows_off = partials;
-  p->float_ws_bytes = partials + align256(size_t(batch) * size_t(stride) * 4);
   *out_plan = p;
   log_plan("bskv_plan_mla_paged", p);
   return BSKV_OK;

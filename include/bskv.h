@@ -206,8 +206,8 @@ bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t batch, int32_t
  *   Token t of request b is cache row kv_indices[kv_indptr[b] + t / page_size] *
  *   page_size + t % page_size; num_pages * page_size must stay below 2^31.
  *   num_heads in [1, 128]; num_sms: SM count of the target GPU.
- * The plan copies the page table into its metadata; runs expand it into the row list of
- * the sparse MLA kernel (in the float workspace) and run that kernel over it.
+ * The plan copies the page table into its metadata; runs read each token's cache row from
+ * it while they gather the rows (no separate row list).
  */
 bskv_status bskv_plan_mla_paged(const int32_t* kv_indptr, const int32_t* kv_indices,
                                 const int32_t* kv_last_page_len, int32_t batch,
@@ -393,8 +393,8 @@ bskv_status bskv_run_mla_sparse(const bskv_plan* plan, const void* query, const 
  *   s_j, out and lse as for bskv_run_mla_sparse over the L_b tokens of request b:
  *   out bf16 [batch, num_heads, 512]; lse float32 [batch, num_heads] or NULL. A request
  *   with no token gets out = 0 and lse = -inf.
- *   float_ws: at least bskv_plan_workspace_sizes' float bytes (split-KV partials and the
- *   expanded row list), 16-byte aligned.
+ *   float_ws: at least bskv_plan_workspace_sizes' float bytes (split-KV partials; 0 bytes,
+ *   and NULL allowed, when the plan assigns whole requests), 16-byte aligned.
  */
 bskv_status bskv_run_mla_paged(const bskv_plan* plan, const void* query, const void* kv_pages,
                                float bmm1_scale, float bmm2_scale, void* out, float* lse,

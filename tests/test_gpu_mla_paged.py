@@ -100,9 +100,13 @@ def test_mla_paged_rejects_a_sparse_plan_and_small_workspace(cuda):
     with pytest.raises(bskv.BskvError) as e:
         bskv.bskv_run_mla_paged(sp, q, kv, SCALE)
     assert e.value.status == "ERR_INVALID_ARG"
-    p = bskv.bskv_plan_mla_paged(d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"], 2,
-                                 d["num_pages"], 16, 128)
+    # one long request: split across workers, so its partial states need float workspace
+    e2 = synth.mla_paged_inputs(74, batch=1, heads=128, page_size=16, len_lo=0, len_hi=0,
+                                lens=[2048])
+    p = bskv.bskv_plan_mla_paged(e2["kv_indptr"], e2["kv_indices"], e2["kv_last_page_len"], 1,
+                                 e2["num_pages"], 16, 128)
+    assert p.workspace_sizes()[1] > 16
     p.upload(cuda, float_ws=torch.empty(16, dtype=torch.uint8, device=cuda))
     with pytest.raises(bskv.BskvError) as e:
-        bskv.bskv_run_mla_paged(p, q, kv, SCALE)
+        bskv.bskv_run_mla_paged(p, e2["query"].to(cuda), e2["kv_pages"].to(cuda), SCALE)
     assert e.value.status == "ERR_WORKSPACE_TOO_SMALL"

@@ -173,9 +173,10 @@ def test_mla_paged_plan_bit_exact(lib, lens, ps):
     meta = p.metadata()
     assert meta == plan_ref.mla_paged_meta(ip.tolist(), ix.tolist(), lp.tolist(), len(lens), ps, SMS)
     _check_linear(meta, lens, 128)
+    # the float workspace holds only split-KV partial states (both latent halves)
     _, fb = p.workspace_sizes()
-    top = max(64, (max(lens) + 63) // 64 * 64)
-    assert fb >= len(lens) * top * 4
+    slots = plan_ref.sections(meta)["slots"]
+    assert (fb == 0) == (slots == 0) and fb >= slots * 2 * 128 * 257 * 4
 
 
 # ---------------------------------------------------------------------------------------
