@@ -40,9 +40,13 @@ constexpr int kTile = kDecodeTile;  // 16 tokens per stage
 constexpr int kStages = 3;
 constexpr int kWarps = kDecodeWarps;
 constexpr int kPanelBytes = kTile * 128;  // 16 rows x 64 elements of 16 bits
-constexpr int kGroupThreads = (kDecodeGroupMax + 1) * 32;  // 8 consumer warps + 1 producer
+// Group kernel warps: 8 consumers (one per kv head of the unit), then the producer, then the
+// lookup warp.
+constexpr int kGroupProducerWarp = kDecodeGroupMax;
+constexpr int kGroupLookupWarp = kDecodeGroupMax + 1;
+constexpr int kGroupThreads = (kDecodeGroupMax + 2) * 32;
 constexpr uint32_t kGroupRingBytes = 196608;                // ring budget of the group kernel
-// The group kernel's 9 warps put 3 on one SM sub-partition, which caps a thread at 168
+// The group kernel's 10 warps put 3 on one SM sub-partition, which caps a thread at 168
 // registers; its merges keep fewer loads in flight than the 8-warp kernels' (4 x 4).
 constexpr int kGroupMergeSlots = 2, kGroupMergeRows = 2;
 
@@ -548,6 +552,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Merge of one kv head's g query rows of a split unit (pieces first..first+cnt-1) into the
+// output, for the group kernel. Not inlined: the consumers' main loop then keeps its
+// registers (inlined after the loop, the kernel spills at its 168-register cap).
+template <typename T, int D>
+__device__ __noinline__ void group_merge_head(const DecodeParams& p, int lane, int first, int cnt,
+                                              int slot_rows, int h, int b, int head) {
+  merge_rows<T, D, kGroupMergeSlots, kGroupMergeRows>(lane, p.ws_o, p.ws_lse, first, cnt,
+                                                      slot_rows, h * p.group, p.group,
+                                                      out_row<T>(p, b, head), p.o_s1,
+                                                      lse_row(p, b, head));
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kGroupThreads, 1)
     decode_group_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
@@ -565,7 +581,9 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
   const uint32_t stage_bytes = 2u * kv_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ns * stage_bytes);
   uint64_t* empty = full + ns;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + ns);
+  uint64_t* final_item_ready = empty + ns;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(final_item_ready + 1);
+  int* final_item = reinterpret_cast<int*>(final_item_ready + 1) + 1;
 
   const int32_t* hdr = p.meta;
   const int w = blockIdx.x;
@@ -583,6 +601,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], uint32_t(G));
     }
+    mbar_init(final_item_ready, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&kv_map);
@@ -591,61 +610,85 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
   const bool forced = forced_timeout(p.st);
   auto ntiles = [&](const int4& ch) { return (ch.z - ch.y + kTile - 1) / kTile; };
 
-  if (warp == kDecodeGroupMax) {
-    // Producer: one thread issues every copy, then waits for its own copies to land.
-    if (lane != 0) return;
+  if (warp == kGroupProducerWarp) {
+    // Producer: lane 0 issues every copy, then waits for its own copies to land. The warp's
+    // lanes read the ids of 32 consecutive pages of the request at once and lane 0 takes them
+    // by shuffle, so a copy never waits on a page-table read.
     const uint64_t stream_policy = l2_evict_first_policy();  // KV is read once
     uint32_t it = 0;
     bool ok = true;
     for (int k = 0; k < c1 - c0 && ok; ++k) {
       const int4 ch = chunks[chunk_at(c0, c1, k)];
       const int b = ch.x / HG, hg = ch.x % HG;
-      const int pbase = kv_indptr[b];
+      const int pbase = kv_indptr[b], npages = kv_indptr[b + 1] - pbase;
       const int nt = ntiles(ch);
+      int win = -(1 << 30), pid = 0;  // lane j holds the id of page win + j of the request
       for (int t = 0; t < nt; ++t, ++it) {
         const int stage = int(it % uint32_t(ns));
-        if (it >= uint32_t(ns) &&
-            !wait_or_abort(&empty[stage], ((it / ns) & 1u) ^ 1u, p.st, forced, abort_flag)) {
-          *abort_flag = 1;
-          ok = false;
-          break;
+        const int tok = ch.y + t * kTile;
+        const int first = tok / ps;
+        const int pieces = ps >= kTile ? 1 : min(kTile / ps, npages - first);
+        if (first + pieces > win + 32) {
+          win = first;
+          pid = win + lane < npages ? kv_indices[pbase + win + lane] : 0;
+        }
+        if (it >= uint32_t(ns)) {
+          int good = 1;
+          if (lane == 0)
+            good = wait_or_abort(&empty[stage], ((it / ns) & 1u) ^ 1u, p.st, forced, abort_flag);
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            if (lane == 0) *abort_flag = 1;
+            ok = false;
+            break;
+          }
         }
         uint8_t* kdst = smem + stage * stage_bytes;
         uint8_t* vdst = kdst + kv_bytes;
-        const int tok = ch.y + t * kTile;
         if (ps >= kTile) {
-          const int page = kv_indices[pbase + tok / ps];
+          const int page = __shfl_sync(0xffffffffu, pid, first - win);
           const int s = tok % ps;
-          mbar_arrive_expect_tx(&full[stage], 2u * (D / 64) * piece_bytes);
-#pragma unroll
-          for (int hf = 0; hf < D / 64; ++hf) {
-            tma_load_5d_hint(kdst + hf * half_bytes, &kv_map, hf * 64, s, hg * G, 0, page,
-                             &full[stage], stream_policy);
-            tma_load_5d_hint(vdst + hf * half_bytes, &kv_map, hf * 64, s, hg * G, 1, page,
-                             &full[stage], stream_policy);
-          }
-        } else {
-          const int npages = kv_indptr[b + 1] - pbase;
-          const int first = tok / ps;
-          int pieces = kTile / ps;
-          if (first + pieces > npages) pieces = npages - first;
-          mbar_arrive_expect_tx(&full[stage], 2u * (D / 64) * piece_bytes * uint32_t(pieces));
-          for (int k = 0; k < pieces; ++k) {
-            const int page = kv_indices[pbase + first + k];
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[stage], 2u * (D / 64) * piece_bytes);
 #pragma unroll
             for (int hf = 0; hf < D / 64; ++hf) {
-              tma_load_5d_hint(kdst + hf * half_bytes + k * piece_bytes, &kv_map, hf * 64, 0,
-                               hg * G, 0, page, &full[stage], stream_policy);
-              tma_load_5d_hint(vdst + hf * half_bytes + k * piece_bytes, &kv_map, hf * 64, 0,
-                               hg * G, 1, page, &full[stage], stream_policy);
+              tma_load_5d_hint(kdst + hf * half_bytes, &kv_map, hf * 64, s, hg * G, 0, page,
+                               &full[stage], stream_policy);
+              tma_load_5d_hint(vdst + hf * half_bytes, &kv_map, hf * 64, s, hg * G, 1, page,
+                               &full[stage], stream_policy);
+            }
+          }
+        } else {
+          if (lane == 0)
+            mbar_arrive_expect_tx(&full[stage], 2u * (D / 64) * piece_bytes * uint32_t(pieces));
+          for (int q = 0; q < pieces; ++q) {
+            const int page = __shfl_sync(0xffffffffu, pid, first + q - win);
+            if (lane == 0) {
+#pragma unroll
+              for (int hf = 0; hf < D / 64; ++hf) {
+                tma_load_5d_hint(kdst + hf * half_bytes + q * piece_bytes, &kv_map, hf * 64, 0,
+                                 hg * G, 0, page, &full[stage], stream_policy);
+                tma_load_5d_hint(vdst + hf * half_bytes + q * piece_bytes, &kv_map, hf * 64, 0,
+                                 hg * G, 1, page, &full[stage], stream_policy);
+              }
             }
           }
         }
       }
     }
     // Every copy issued must land before the CTA may exit (bounded, not forcible).
-    for (uint32_t k = it > uint32_t(ns) ? it - ns : 0; k < it; ++k)
-      mbar_wait(&full[k % ns], (k / ns) & 1u, p.st, false);
+    if (lane == 0)
+      for (uint32_t k = it > uint32_t(ns) ? it - ns : 0; k < it; ++k)
+        mbar_wait(&full[k % ns], (k / ns) & 1u, p.st, false);
+    return;
+  }
+  if (warp == kGroupLookupWarp) {
+    // Lookup warp: finds the merge item of the worker's last chunk while the KV streams, so
+    // that the consumers publish that piece without searching the merge list at the tail.
+    if (lane == 0 && p.counters && c1 > c0) {
+      const int4 ch = chunks[chunk_at(c0, c1, c1 - c0 - 1)];
+      *final_item = ch.w >= 0 ? find_merge_item(merges, NM, ch.x) : -1;
+      mbar_arrive(final_item_ready);
+    }
     return;
   }
   if (warp >= G) return;
@@ -701,15 +744,20 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
       __syncwarp();
       int last = 0;
       if (lane == 0) {
-        const int item = find_merge_item(merges, NM, ch.x);
+        int item;
+        if (k + 1 == c1 - c0 && mbar_wait(final_item_ready, 0, p.st, false))
+          item = *final_item;
+        else
+          item = find_merge_item(merges, NM, ch.x);
         const int old = atomic_add_acq_rel(p.counters + item * G + h, 1);
         last = old == merges[3 * item + 2] - 1 ? item + 1 : 0;
       }
       last = __shfl_sync(0xffffffffu, last, 0);
+      __syncwarp();
       if (last) {
         const int item = last - 1;
-        merge_rows<T, D, kGroupMergeSlots, kGroupMergeRows>(lane, p.ws_o, p.ws_lse, merges[3 * item + 1], merges[3 * item + 2], SR,
-                         h * g, g, out_row<T>(p, b, kvh * g), p.o_s1, lse_row(p, b, kvh * g));
+        group_merge_head<T, D>(p, lane, merges[3 * item + 1], merges[3 * item + 2], SR, h, b,
+                               kvh * g);
         if (lane == 0) p.counters[item * G + h] = 0;  // ready for the next run
       }
     }
@@ -807,7 +855,8 @@ bskv_status launch_decode_t(const bskv_plan* plan, const CUtensorMap& map, Decod
   if (meta_word(plan, H_VARIANT) == DECODE_GROUP) {
     const uint32_t sb = group_stage_bytes<D>(dp.heads_per_unit);
     dp.stages = int(kGroupRingBytes / sb) < 8 ? int(kGroupRingBytes / sb) : 8;
-    const size_t smem = size_t(dp.stages) * sb + 1024 + size_t(2 * dp.stages) * 8 + 16;
+    const size_t smem = size_t(dp.stages) * sb + 1024 +
+                        size_t(2 * dp.stages + 1) * 8 + 16;
     auto kern = decode_group_kernel<T, D>;
     if (bskv_status s = cuda_check(
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
