@@ -222,6 +222,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0,
+                                            int32_t c1, int32_t c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Tensor stores (TMA) of a shared-memory box, tracked by this thread's bulk async-groups
 // (bulk_commit; bulk_wait_read0 before the box is overwritten, bulk_wait_all0 before exit).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0,

@@ -19,7 +19,9 @@
 //   warps 0-5  gather: 192 threads copy this CTA's 64 rows of a tile (16-byte cp.async into
 //              128B-swizzled panels), then the leader arms kv_full for the partner's half and
 //              pushes this half to the partner with five shared-to-shared bulk copies. Row ids
-//              are fetched one tile ahead;
+//              are fetched one tile ahead. On a paged cache (the kPaged instantiation) a whole
+//              tile is instead loaded by each CTA with TMA boxes of page slots, issued by one
+//              thread: no cp.async and no push;
 //   warp 6     allocates TMEM; one elected lane of the converged warp issues QK (16 MMAs
 //              with A in TMEM, 2 with the tail in shared memory, N = 128) and PV (A = P in
 //              shared memory, B = the V part read MN-major, N = 256; once for the hi and once
@@ -85,6 +87,9 @@ struct MlaParams {
   const int32_t* pg_indptr;
   const int32_t* pg_indices;
   int page_size;
+  // paged decode: rows per TMA box of the cache maps (whole tiles are then loaded by TMA,
+  // page by page, into both CTAs), or 0 (every tile gathered row by row)
+  int tma_box;
   int top_k, heads;
   float scale_log2;  // bmm1_scale * log2(e)
   float bmm2;
@@ -137,9 +142,11 @@ __device__ __forceinline__ int chunk_token(const int4& ch) { return ch.x; }
 // the weights split between two groups of rows of different values, can move an output by
 // twice the FP8 tolerance at any list length). The two P buffers hold hi and lo of one tile,
 // a tile's PV is 8 MMAs, and the lazy-rescale threshold is 2^4 so that 16 p stays below 448.
+template <bool kPaged>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap qmap_rope, const __grid_constant__ CUtensorMap omap,
-               const __grid_constant__ CUtensorMap wmap, const MlaParams p) {
+               const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap kvmap,
+               const __grid_constant__ CUtensorMap kvmap_tail, const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -198,6 +205,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // uses the 64-byte pattern. The unit's latent half goes to a V part, the other half and
     // the tail to a K part; the peer, computing the other half, files the same panels the
     // other way round. Decisions go through bar_and on named barrier 1 (192 threads).
+    // A whole tile of the paged cache (its 128 tokens in whole boxes of page slots) is
+    // instead loaded by each CTA itself with TMA: five boxes per box of rows (four 128-byte
+    // latent panels, 128B-swizzled, and the tail, 64B-swizzled, the same layouts), issued by
+    // one thread, with no cp.async and no push; the partial last tile of a request is
+    // gathered as above, which zero-fills the rows past its last token.
     const int pt = threadIdx.x;
     int32_t* idx_smem = reinterpret_cast<int32_t*>(sm + kSmemIdx);
     constexpr int kPer = (kHalfRows * 36) / kGatherThreads;  // 12 chunks per thread
@@ -224,7 +236,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t peer_base = mapa_shared(sbase, peer);
     uint32_t kvc = 0, armed = 0;
     bool ok = true;
-    const int tr = int(rank) * kHalfRows + pt;  // tile row whose id this thread loads
+    // tile row whose id this thread loads: a paged cache needs every row's (the whole tile
+    // may be loaded by TMA), a sparse list only this CTA's half
+    constexpr bool all_ids = kPaged;
+    const int tr = all_ids ? pt : int(rank) * kHalfRows + pt;
+    const int nids = all_ids ? kRows : kHalfRows;
     // Row id of tile row tr of the tile of chunk cn that starts at row u0, loaded one tile
     // ahead. The chunk descriptors are held in registers (the next one read at the start of
     // a chunk), so the id is one independent load that nothing waits for until the next
@@ -233,16 +249,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Paged decode: the row of token t of the chunk's request comes from the page table,
     // page_ptr = kv_indptr of the request (read once per chunk, when its first row ids are).
     auto load_id = [&](const int4& cn, int page_ptr, int u0) -> int32_t {
-      if (pt >= kHalfRows || u0 + tr >= cn.z) return 0;
+      if (pt >= nids || u0 + tr >= cn.z) return 0;
       const int t = u0 + tr;
-      if (p.pg_indices) {
+      if constexpr (kPaged) {
         const int pg = __ldg(p.pg_indices + page_ptr + t / p.page_size);
         return pg * p.page_size + t % p.page_size;
       }
       return __ldg(p.indices + int64_t(cn.x) * p.top_k + t);
     };
     auto page_ptr_of = [&](const int4& cn) -> int {
-      return p.pg_indices && pt < kHalfRows ? __ldg(p.pg_indptr + cn.x) : 0;
+      return kPaged && pt < nids ? __ldg(p.pg_indptr + cn.x) : 0;
     };
     int4 ch = c0 < c1 ? chunks[c0] : make_int4(0, 0, 0, 0);
     int cptr = c0 < c1 ? page_ptr_of(ch) : 0;
@@ -272,12 +288,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // overwritten; the push of kvc - 1 may still be running
         if (pt == 0) bulk_wait_read1();
         int32_t* ib = idx_smem + v * kRows;
-        if (pt < kHalfRows) ib[tr] = my_id;
+        if (pt < nids) ib[tr] = my_id;
         ok = bar_and(1, kGatherThreads, good);
         if (!ok) break;
         uint8_t* vbase = sm + kSmemV + v * kVPart;
         uint8_t* kbase = sm + kSmemK + k * kKPart;
         const int valid = ch.z - t0;
+        if (kPaged && p.tma_box > 0 && valid >= kRows) {
+          if (pt == 0) {
+            mbar_arrive_expect_tx(&B.kv_full[v], kRows * 576);
+            ++armed;
+            for (int r0 = 0; r0 < kRows; r0 += p.tma_box) {
+              const int id = ib[r0];  // row id of the box's first token: page * page_size + slot
+              const int page = id / p.page_size, slot = id % p.page_size;
+#pragma unroll
+              for (int pn = 0; pn < 4; ++pn)
+                tma_load_3d(((pn >> 1) == vh ? vbase : kbase) + (pn & 1) * kPanel + r0 * 128,
+                            &kvmap, pn * 128, slot, page, &B.kv_full[v]);
+              tma_load_3d(kbase + 2 * kPanel + r0 * 64, &kvmap_tail, 512, slot, page,
+                          &B.kv_full[v]);
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
           uint8_t* dst = ((off[j] >> 31) ? vbase : kbase) + (off[j] & 0x7fffffffu);
@@ -806,13 +839,32 @@ bskv_status run_mla(const bskv_plan* plan, const void* query, const void* kv_row
   } else {
     wm = om;  // no split partials
   }
+  // paged cache as [page][slot][576] bytes: whole tiles load by boxes of min(page_size, 128)
+  // slots (a page size that is a multiple of 8 and divides 128 or is a multiple of it, so
+  // that every box lands on a swizzle-atom boundary of the panels)
+  CUtensorMap kvm = qr, kvt = qr;
+  const int ps = plan->page_size;
+  if (paged && ps >= 8 && ps % 8 == 0 && (kRows % ps == 0 || ps % kRows == 0)) {
+    const int box = std::min(ps, kRows);
+    const uint64_t kd[3] = {576, uint64_t(ps), uint64_t(plan->num_pages)};
+    const uint64_t ks[2] = {576, uint64_t(576) * uint64_t(ps)};
+    const uint32_t kb[3] = {128, uint32_t(box), 1}, kbt[3] = {64, uint32_t(box), 1};
+    if (bskv_status s = encode_tiled(&kvm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv_rows, kd, ks, kb,
+                                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return s;
+    if (bskv_status s = encode_tiled(&kvt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv_rows, kd, ks, kbt,
+                                     CU_TENSOR_MAP_SWIZZLE_64B))
+      return s;
+    mp.tma_box = box;
+  }
   const int grid = meta_word(plan, H_GRID);
   if (grid > 0) {
     const size_t smem = kSmemBytes + 1024;
-    if (bskv_status s = cuda_check(cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+    auto kern = paged ? mla_kernel<true> : mla_kernel<false>;
+    if (bskv_status s = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
                                    "mla: cudaFuncSetAttribute"))
       return s;
-    mla_kernel<<<grid, kThreads, smem, st>>>(qr, om, wm, mp);
+    kern<<<grid, kThreads, smem, st>>>(qr, om, wm, kvm, kvt, mp);
     if (bskv_status s = cuda_check(cudaGetLastError(), "mla kernel launch")) return s;
   }
   const int nm = meta_word(plan, H_MERGES);

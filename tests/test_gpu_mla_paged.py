@@ -59,6 +59,11 @@ def _check(out, lse, ref, ref_lse, reqs=None):
     ([300, 2048, 17], 64, 128),        # a long request split across workers (merge path)
     ([1, 2, 129, 1000], 1, 16),        # page_size 1, fewer heads
     ([257, 256, 255, 3], 7, 64),       # a page size that is not a power of two
+    # whole tiles by TMA boxes of page slots: 16 boxes of 8, one box of 128, boxes of 128
+    # at slot 0 and 128 of a 256-slot page; the partial last tiles gathered row by row
+    ([777, 40, 128], 8, 128),
+    ([300, 128, 513], 128, 64),
+    ([1000, 256, 129], 256, 128),
 ])
 def test_mla_paged_small(cuda, lens, ps, heads):
     d = synth.mla_paged_inputs(71, batch=len(lens), heads=heads, page_size=ps, len_lo=0,
