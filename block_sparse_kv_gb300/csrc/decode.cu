@@ -63,6 +63,9 @@ struct DecodeParams {
   int num_kv_heads, group, page_size, num_qo_heads;
   int heads_per_unit;  // kv heads of one unit: 1 (warp variant) or G (group variant)
   int stages;          // ring depth of the group variant
+  // word offsets of the metadata's sections and the merge count (the header's values,
+  // passed by value so that a worker's first loads do not wait on the header)
+  int off_workers, off_chunks, off_merges, off_aux0, off_aux1, num_merges;
   float scale_log2;
   StatusArgs st;
 };
@@ -581,18 +584,18 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
   const uint32_t stage_bytes = 2u * kv_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ns * stage_bytes);
   uint64_t* empty = full + ns;
-  uint64_t* final_item_ready = empty + ns;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(final_item_ready + 1);
-  int* final_item = reinterpret_cast<int*>(final_item_ready + 1) + 1;
+  uint64_t* items_ready = empty + ns;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(items_ready + 1);
+  int* items = reinterpret_cast<int*>(items_ready + 1) + 1;  // [0]: first chunk, [1]: last
 
   const int32_t* hdr = p.meta;
   const int w = blockIdx.x;
-  const int32_t* wptr = hdr + hdr[H_OFF_WORKERS];
-  const int4* chunks = reinterpret_cast<const int4*>(hdr + hdr[H_OFF_CHUNKS]);
-  const int32_t* merges = hdr + hdr[H_OFF_MERGES];
-  const int NM = hdr[H_MERGES];
-  const int32_t* kv_indptr = hdr + hdr[H_OFF_AUX0];
-  const int32_t* kv_indices = hdr + hdr[H_OFF_AUX1];
+  const int32_t* wptr = hdr + p.off_workers;
+  const int4* chunks = reinterpret_cast<const int4*>(hdr + p.off_chunks);
+  const int32_t* merges = hdr + p.off_merges;
+  const int NM = p.num_merges;
+  const int32_t* kv_indptr = hdr + p.off_aux0;
+  const int32_t* kv_indices = hdr + p.off_aux1;
   const int c0 = wptr[w], c1 = wptr[w + 1];
   const int HG = p.num_kv_heads / G, g = p.group, SR = G * g;
 
@@ -601,7 +604,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], uint32_t(G));
     }
-    mbar_init(final_item_ready, 1);
+    mbar_init(items_ready, 2);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&kv_map);
@@ -682,12 +685,14 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     return;
   }
   if (warp == kGroupLookupWarp) {
-    // Lookup warp: finds the merge item of the worker's last chunk while the KV streams, so
-    // that the consumers publish that piece without searching the merge list at the tail.
-    if (lane == 0 && p.counters && c1 > c0) {
-      const int4 ch = chunks[chunk_at(c0, c1, c1 - c0 - 1)];
-      *final_item = ch.w >= 0 ? find_merge_item(merges, NM, ch.x) : -1;
-      mbar_arrive(final_item_ready);
+    // Lookup warp: finds the merge items of the first and the last chunk of the worker's walk
+    // (lanes 0 and 1, in parallel) while the KV streams, so that the consumers publish those
+    // pieces without searching the merge list (a linear partition puts a worker's pieces
+    // only there; a search costs several dependent round trips while HBM is saturated).
+    if (lane < 2 && p.counters && c1 > c0) {
+      const int4 ch = chunks[chunk_at(c0, c1, lane == 0 ? 0 : c1 - c0 - 1)];
+      items[lane] = ch.w >= 0 ? find_merge_item(merges, NM, ch.x) : -1;
+      mbar_arrive(items_ready);
     }
     return;
   }
@@ -745,8 +750,8 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
       int last = 0;
       if (lane == 0) {
         int item;
-        if (k + 1 == c1 - c0 && mbar_wait(final_item_ready, 0, p.st, false))
-          item = *final_item;
+        if ((k == 0 || k + 1 == c1 - c0) && mbar_wait(items_ready, 0, p.st, false))
+          item = items[k == 0 ? 0 : 1];
         else
           item = find_merge_item(merges, NM, ch.x);
         const int old = atomic_add_acq_rel(p.counters + item * G + h, 1);
@@ -978,6 +983,12 @@ bskv_status prepare_decode(const char* who, const bskv_plan* plan, const int32_t
   dp->num_kv_heads = Hkv; dp->group = plan->num_qo_heads / Hkv; dp->page_size = ps;
   dp->num_qo_heads = plan->num_qo_heads;
   dp->heads_per_unit = sh.heads_per_unit;
+  dp->off_workers = meta_word(plan, H_OFF_WORKERS);
+  dp->off_chunks = meta_word(plan, H_OFF_CHUNKS);
+  dp->off_merges = meta_word(plan, H_OFF_MERGES);
+  dp->off_aux0 = meta_word(plan, H_OFF_AUX0);
+  dp->off_aux1 = meta_word(plan, H_OFF_AUX1);
+  dp->num_merges = meta_word(plan, H_MERGES);
   dp->scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
   if (bskv_status s = status_args(&dp->st)) return s;
   const uint64_t dims[5] = {uint64_t(D), uint64_t(ps), uint64_t(Hkv), 2, uint64_t(plan->num_pages)};
