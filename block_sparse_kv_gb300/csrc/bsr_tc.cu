@@ -90,7 +90,7 @@ struct Cfg {
 struct Bars {
   uint64_t q_full[2], q_empty[2], drain;  // Q per M tile
   uint64_t kv_full[3], kv_empty[3];
-  uint64_t s_full[2], p_full[2];  // per S slot
+  uint64_t s_full[2], p_half[2], p_full[2];  // per S slot: P of the first 64 keys / of all
   uint64_t o_done[2], o_free[2];  // per M tile
   uint32_t tmem_base;
   int abort;
@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int z = 0; z < 2; ++z) {
       mbar_init(&B.s_full[z], 1);
+      mbar_init(&B.p_half[z], 128);
       mbar_init(&B.p_full[z], 128);
       mbar_init(&B.o_done[z], 1);
       mbar_init(&B.o_free[z], 128);
@@ -402,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t Jg = J + jl, z = Jg & 1u;
           const int j = NM == 2 ? (jl >> 1) : jl;
           const int m = NM == 2 ? (jl & 1) : 0;
-          if (!issuer_wait(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+          if (!issuer_wait(kList ? &B.p_full[z] : &B.p_half[z], (Jg >> 1) & 1u, p.st, forced,
+                           abort_flag)) { ok = false; break; }
           if (j == 0 && !issuer_wait(&B.o_free[m], (uc & 1u) ^ 1u, p.st, forced, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nb = step_halves(u, j);
@@ -419,10 +421,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
                             (j == 0 && kk == 0) ? 0u : 1u);
           } else if (nb == 2) {
+            // a block pair: the first block's slices once its P is in TMEM, then the second's
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < 4; ++kk)
               umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv,
                             (j == 0 && kk == 0) ? 0u : 1u);
+            if (!issuer_wait(&B.p_full[z], (Jg >> 1) & 1u, p.st, forced, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 4; kk < 8; ++kk)
+              umma_f16_ts_w(leader, tmem + 256 * m, pa + kk * 8, dv + vo + kk * (2048 >> 4), idesc_pv, 1u);
           } else {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -555,27 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float ref = m_use == -INFINITY ? 0.f : m_use;
         rescale = __any_sync(0xffffffffu, rescale);
-        // P = 2^(s * scale - ref), 32 keys at a time into packed columns [16 ck, 16 ck + 16)
-        PSum<T> sp;
-        sp.zero();
-        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nr2 = make_float2(-ref, -ref);
-#pragma unroll
-        for (int ck = 0; ck < 4; ++ck) {
-          if (ck < 2 * nb) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float2 x = ffma2(make_float2(__uint_as_float(sr[32 * ck + c]),
-                                                 __uint_as_float(sr[32 * ck + c + 1])),
-                                     sc2, nr2);
-              pk[c / 2] = exp2_pack<T>(x.x, x.y, sp, (c >> 1) & 7);
-            }
-            tmem_st16(scol + 16 * ck, pk);
-          }
-        }
-        const float sum = sp.total();
-        l_run = l_run * alpha + sum;
-        m_run = m_use;
         // All earlier PVs into this tile's O must be complete before a rescale. With two M
         // tiles that is already implied: this tile's previous PV was issued before the QK
         // whose completion produced S, so exactly cnt PVs have completed (od = cnt keeps the
@@ -588,6 +575,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++od;
           }
           if (!ok) break;
+        }
+        // P = 2^(s * scale - ref), 32 keys at a time into packed columns [16 ck, 16 ck + 16).
+        // Block-sparse steps hand the first block's P to the issuer before forming the
+        // second's (its PV slices start meanwhile); O is rescaled in between, when the S row's
+        // first half no longer holds registers.
+        PSum<T> sp;
+        sp.zero();
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nr2 = make_float2(-ref, -ref);
+#pragma unroll
+        for (int ck = 0; ck < 2; ++ck) {
+          {  // keys 32 ck .. 32 ck + 31 of the first block
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float2 x = ffma2(make_float2(__uint_as_float(sr[32 * ck + c]),
+                                                 __uint_as_float(sr[32 * ck + c + 1])),
+                                     sc2, nr2);
+              pk[c / 2] = exp2_pack<T>(x.x, x.y, sp, (c >> 1) & 7);
+            }
+            tmem_st16(scol + 16 * ck, pk);
+          }
         }
         if (rescale && j > 0) {
 #pragma unroll 1
@@ -615,6 +623,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
           }
         }
+        if constexpr (!kList) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&B.p_half[z]);
+        }
+#pragma unroll
+        for (int ck = 2; ck < 4; ++ck) {
+          if (ck < 2 * nb) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float2 x = ffma2(make_float2(__uint_as_float(sr[32 * ck + c]),
+                                                 __uint_as_float(sr[32 * ck + c + 1])),
+                                     sc2, nr2);
+              pk[c / 2] = exp2_pack<T>(x.x, x.y, sp, (c >> 1) & 7);
+            }
+            tmem_st16(scol + 16 * ck, pk);
+          }
+        }
+        const float sum = sp.total();
+        l_run = l_run * alpha + sum;
+        m_run = m_use;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&B.p_full[z]);
