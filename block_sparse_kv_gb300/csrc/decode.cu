@@ -9,11 +9,13 @@
 // GB300 design. Decode reads every K/V byte once (O(1) flop per byte), so the kernel is an
 // HBM stream, and its efficiency follows from how large the contiguous pieces it asks
 // HBM for are. Two variants, chosen by the plan:
-//   * group (pages of 8 or 16 tokens): one CTA per SM, a producer warp and one consumer
-//     warp per kv head of a group of up to 8. Each 16-token tile is copied by TMA for all
-//     heads of the group at once, so with the contiguous layout a page's K (and V) for 8
-//     heads is one 32 KB piece instead of eight 4 KB ones. A 3-stage ring (64 KB stages
-//     for 8 heads of 128 dims) holds about 128 KB in flight per SM.
+//   * group (pages of 8 or 16 tokens): one CTA per SM, a producer warp, one consumer warp
+//     per kv head of a group of up to 8, and a lookup warp. Each 16-token tile is copied by
+//     TMA for all heads of the group at once, so with the contiguous layout a page's K (and
+//     V) for 8 heads is one 32 KB piece instead of eight 4 KB ones. A 3-stage ring (64 KB
+//     stages for 8 heads of 128 dims) holds up to 192 KB in flight per SM; the producer's
+//     lanes read the page ids of 32 pages at a time, and the lookup warp finds the merge
+//     items of the worker's first and last chunks while the KV streams.
 //   * warp (larger pages, or head counts that do not group): 8 independent worker warps
 //     per CTA, each with a private 3-stage ring over its own (request, kv head) range;
 //     a page of 64 tokens is already a 16 KB piece per head.
