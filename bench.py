@@ -327,11 +327,15 @@ def bench_decode(bskv, synth, name, steps, warmup, dist, sampler=None, headline=
                  **over):
     """Paged decode (+ merge) on one of the decode workloads."""
     d = synth.make(name, device="cuda", **over)
-    t0 = time.perf_counter()
-    plan = bskv.bskv_plan_decode(d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"],
-                                 d["num_pages"], d["page_size"], d["num_qo_heads"],
-                                 d["num_kv_heads"], d["head_dim"], torch.bfloat16)
-    plan_us = 1e6 * (time.perf_counter() - t0)
+    # host planning time: the median of 5 calls after a first one (which pays one-time costs)
+    plan_times = []
+    for _ in range(6):
+        t0 = time.perf_counter()
+        plan = bskv.bskv_plan_decode(d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"],
+                                     d["num_pages"], d["page_size"], d["num_qo_heads"],
+                                     d["num_kv_heads"], d["head_dim"], torch.bfloat16)
+        plan_times.append(1e6 * (time.perf_counter() - t0))
+    plan_us = statistics.median(plan_times[1:])
     plan.upload("cuda")
     q, kv = d["q"], d["kv_cache"]
     out = torch.empty_like(q)
