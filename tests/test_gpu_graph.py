@@ -94,3 +94,19 @@ def test_graph_mla_sparse(cuda):
     idx = g["indices"]
     _graph_equal(lambda: bskv.bskv_run_mla_sparse(p, query, pool, idx, 1 / math.sqrt(576), 1.0,
                                                   out=out, lse=lse), [out, lse])
+
+
+def test_graph_mla_paged(cuda):
+    """Dense paged MLA in a graph: whole tiles by TMA boxes of page slots, partial tiles
+    gathered by rows, and (one long request) split pieces merged by the merge kernel."""
+    d = synth.mla_paged_inputs(934, batch=3, heads=128, page_size=64, len_lo=0, len_hi=0,
+                               lens=[2048, 300, 129])
+    p = bskv.bskv_plan_mla_paged(d["kv_indptr"], d["kv_indices"], d["kv_last_page_len"], 3,
+                                 d["num_pages"], 64, 128)
+    p.upload(cuda)
+    assert p.metadata()[6] > 0  # split pieces: the merge kernel is in the graph too
+    q, kv = d["query"].to(cuda), d["kv_pages"].to(cuda)
+    out = torch.empty((3, 128, 512), dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty((3, 128), dtype=torch.float32, device=cuda)
+    _graph_equal(lambda: bskv.bskv_run_mla_paged(p, q, kv, 1 / math.sqrt(576), 1.0, out=out,
+                                                 lse=lse), [out, lse])
