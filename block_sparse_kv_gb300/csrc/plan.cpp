@@ -4,8 +4,10 @@
 // int32 metadata that the kernels read from the caller's int workspace:
 //   * decode and MLA: a linear split-KV partition. The units (one per request and kv
 //     head, or per query token and latent half) are cut into tiles; the tile sequence
-//     of all units is divided into equal contiguous ranges, one per worker; a unit that
-//     falls into several ranges is computed in pieces whose partial states are merged.
+//     of all units is divided into contiguous ranges, one per worker (equal ranges, or for
+//     the page-major decode ranges of equal cost, a chunk after a worker's first costing
+//     kDecodeBoundaryTiles tiles); a unit that falls into several ranges is computed in
+//     pieces whose partial states are merged.
 //   * BSR: longest-processing-time assignment of (row block, kv head) units to
 //     persistent CTAs, heaviest unit first.
 // The rules are deterministic given num_sms, so the metadata is reproducible bit for bit.
@@ -127,6 +129,98 @@ void linear_partition(const std::vector<int64_t>& unit_len, int64_t tile, int64_
     merges.push_back(first_slot[v]);
     merges.push_back(nchunks[v]);
   }
+}
+
+// Slots (one per piece of a unit cut into several, in chunk order) and merge items
+// (unit, first slot, pieces) of units with other than one piece.
+void assign_slots(size_t U, std::vector<Chunk>& chunks, int32_t& slots,
+                  std::vector<int32_t>& merges) {
+  std::vector<int32_t> nchunks(U, 0), first_slot(U, -1);
+  for (const Chunk& c : chunks) nchunks[size_t(c.unit)] += 1;
+  slots = 0;
+  for (Chunk& c : chunks) {
+    if (nchunks[size_t(c.unit)] >= 2) {
+      if (first_slot[size_t(c.unit)] < 0) first_slot[size_t(c.unit)] = slots;
+      c.c = slots++;
+    }
+  }
+  merges.clear();
+  for (size_t v = 0; v < U; ++v) {
+    if (nchunks[v] == 1) continue;
+    merges.push_back(int32_t(v));
+    merges.push_back(first_slot[v]);
+    merges.push_back(nchunks[v]);
+  }
+}
+
+// Greedy left-to-right fill of the unit tile sequence: each worker takes tiles while its cost
+// (its tiles, plus bc for every chunk after its first) stays within T. Returns the number of
+// workers; with `out`, appends their chunks (unit, first tile, end tile) and worker starts.
+int64_t fill_workers(const std::vector<int64_t>& tiles, int64_t T, int64_t bc,
+                     std::vector<int32_t>* worker_ptr, std::vector<Chunk>* out) {
+  const size_t U = tiles.size();
+  size_t u = 0;
+  int64_t off = 0, workers = 0;
+  while (u < U && tiles[u] == 0) ++u;
+  while (u < U) {
+    ++workers;
+    if (worker_ptr) worker_ptr->push_back(int32_t(out->size()));
+    int64_t cost = 0, n = 0;
+    while (u < U) {
+      if (tiles[u] == 0) { ++u; continue; }
+      const int64_t add = n > 0 ? bc : 0;
+      if (cost + add >= T) break;
+      const int64_t take = std::min(tiles[u] - off, T - cost - add);
+      if (out) out->push_back(Chunk{int32_t(u), int32_t(off), int32_t(off + take), -1});
+      cost += add + take;
+      ++n;
+      off += take;
+      if (off == tiles[u]) {
+        ++u;
+        off = 0;
+      } else {
+        break;
+      }
+    }
+  }
+  return workers;
+}
+
+// Contiguous partition in which a worker's cost is its tiles plus bc per chunk after its
+// first (a piece published mid-stream and a merge at the end cost a worker about that much):
+// the smallest bound T whose greedy fill needs at most max_workers workers, each filled up
+// to T. Chunks are in tokens like linear_partition's.
+void linear_partition_cost(const std::vector<int64_t>& unit_len, int64_t tile,
+                           int64_t max_workers, int64_t bc, std::vector<int32_t>& worker_ptr,
+                           std::vector<Chunk>& chunks, int32_t& slots,
+                           std::vector<int32_t>& merges) {
+  std::vector<int64_t> tiles(unit_len.size());
+  int64_t NT = 0;
+  for (size_t u = 0; u < unit_len.size(); ++u) {
+    tiles[u] = (unit_len[u] + tile - 1) / tile;
+    NT += tiles[u];
+  }
+  if (NT == 0) {
+    linear_partition(unit_len, tile, max_workers, worker_ptr, chunks, slots, merges);
+    return;
+  }
+  int64_t lo = std::max<int64_t>(1, (NT + max_workers - 1) / max_workers);
+  int64_t hi = NT + bc * int64_t(tiles.size());
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) / 2;
+    if (fill_workers(tiles, mid, bc, nullptr, nullptr) <= max_workers) hi = mid;
+    else lo = mid + 1;
+  }
+  worker_ptr.clear();
+  chunks.clear();
+  fill_workers(tiles, lo, bc, &worker_ptr, &chunks);
+  worker_ptr.push_back(int32_t(chunks.size()));
+  for (Chunk& c : chunks) {
+    const int64_t L = unit_len[size_t(c.unit)];
+    c.a = int32_t(int64_t(c.a) * tile);
+    c.b = int32_t(std::min(int64_t(c.b) * tile, L));
+  }
+  assign_slots(unit_len.size(), chunks, slots, merges);
 }
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -390,7 +484,11 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
   std::vector<int32_t> worker_ptr, merges;
   std::vector<Chunk> chunks;
   int32_t slots = 0;
-  linear_partition(len, kDecodeTile, workers_cap, worker_ptr, chunks, slots, merges);
+  if (variant == DECODE_GROUP)
+    linear_partition_cost(len, kDecodeTile, workers_cap, kDecodeBoundaryTiles, worker_ptr, chunks,
+                          slots, merges);
+  else
+    linear_partition(len, kDecodeTile, workers_cap, worker_ptr, chunks, slots, merges);
   const int32_t P = int32_t(worker_ptr.size() - 1);
   const int32_t grid = variant == DECODE_GROUP ? P : (P + kDecodeWarps - 1) / kDecodeWarps;
   const int32_t slot_rows = num_qo_heads / upb;  // query heads of one unit

@@ -25,7 +25,10 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
 0 chunks (first_slot = -1) or >= 2 chunks.
   * decode: G = decode_group_heads(num_kv_heads, page_size). G > 0 (page_size <= 16
     and num_kv_heads <= 8 or a multiple of 8): variant 1, units (b, group of G kv
-    heads) b-major, max_workers = num_sms unless given, grid = P. Otherwise variant 0,
+    heads) b-major, max_workers = num_sms unless given, grid = P, and instead of equal
+    ranges the cost partition (linear_partition_cost, 4 tiles per chunk after a worker's
+    first: the smallest bound T whose greedy left-to-right fill needs at most max_workers
+    workers; P = the workers that fill uses). Otherwise variant 0,
     units (b, kv head) b-major, max_workers = 8 * num_sms unless given,
     grid = ceil(P / 8). Both: len = request length, tile 16, aux0 = kv_indptr,
     aux1 = kv_indices.
@@ -151,6 +154,83 @@ def linear_partition(unit_len, tile, max_workers):
     return worker_ptr, chunks, slots, merges
 
 
+def _slots_and_merges(unit_len, chunks):
+    count = [0] * len(unit_len)
+    for c in chunks:
+        count[c[0]] += 1
+    first = [-1] * len(unit_len)
+    slots = 0
+    for c in chunks:
+        if count[c[0]] >= 2:
+            if first[c[0]] < 0:
+                first[c[0]] = slots
+            c[3] = slots
+            slots += 1
+    merges = [(u, first[u], count[u]) for u in range(len(unit_len)) if count[u] != 1]
+    return slots, merges
+
+
+def _fill(tiles, T, bc, record=None):
+    """Greedy left-to-right fill: each worker takes tiles while its cost (tiles, plus bc for
+    every chunk after its first) stays within T. Returns the number of workers; with
+    `record`, appends each worker's chunks as (unit, first tile, end tile) lists."""
+    U = len(tiles)
+    u, off, workers = 0, 0, 0
+    while u < U and tiles[u] == 0:
+        u += 1
+    while u < U:
+        workers += 1
+        cost, n = 0, 0
+        mine = []
+        while u < U:
+            if tiles[u] == 0:
+                u += 1
+                continue
+            add = bc if n > 0 else 0
+            if cost + add >= T:
+                break
+            take = min(tiles[u] - off, T - cost - add)
+            mine.append((u, off, off + take))
+            cost += add + take
+            n += 1
+            off += take
+            if off == tiles[u]:
+                u, off = u + 1, 0
+            else:
+                break
+        if record is not None:
+            record.append(mine)
+    return workers
+
+
+def linear_partition_cost(unit_len, tile, max_workers, bc):
+    """Contiguous partition of the unit tile sequence in which a worker's cost is its tiles
+    plus bc per chunk after its first: the smallest cost bound T whose greedy fill needs at
+    most max_workers workers, each worker filled up to T."""
+    tiles = [(L + tile - 1) // tile for L in unit_len]
+    NT = sum(tiles)
+    if NT == 0:
+        return linear_partition(unit_len, tile, max_workers)
+    lo = max(1, -(-NT // max_workers))
+    hi = NT + bc * len(tiles)
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if _fill(tiles, mid, bc) <= max_workers:
+            hi = mid
+        else:
+            lo = mid + 1
+    rec = []
+    _fill(tiles, lo, bc, rec)
+    worker_ptr, chunks = [], []
+    for mine in rec:
+        worker_ptr.append(len(chunks))
+        for u, a, b in mine:
+            chunks.append([u, a * tile, min(b * tile, int(unit_len[u])), -1])
+    worker_ptr.append(len(chunks))
+    slots, merges = _slots_and_merges(unit_len, chunks)
+    return worker_ptr, chunks, slots, merges
+
+
 def decode_group_heads(num_kv_heads, page_size):
     """kv heads per unit of the page-major decode variant (0: the variant does not apply)."""
     if page_size > 16:
@@ -172,12 +252,20 @@ def decode_units(kv_indptr, kv_last_page_len, batch, page_size, num_kv_heads):
     return lens
 
 
+# page-major decode: a worker's cost of each chunk after its first, in 16-token tiles (a
+# piece published mid-stream and a merge at the end cost a worker about this much)
+DECODE_BOUNDARY_TILES = 4
+
+
 def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_qo_heads,
                 num_kv_heads, num_sms, max_workers=0):
     G = decode_group_heads(num_kv_heads, page_size)
     lens = decode_units(kv_indptr, kv_last_page_len, batch, page_size, num_kv_heads)
     cap = max_workers if max_workers > 0 else (num_sms if G else 8 * num_sms)
-    wp, ch, slots, merges = linear_partition(lens, 16, cap)
+    if G:
+        wp, ch, slots, merges = linear_partition_cost(lens, 16, cap, DECODE_BOUNDARY_TILES)
+    else:
+        wp, ch, slots, merges = linear_partition(lens, 16, cap)
     P = len(wp) - 1
     nnz = int(kv_indptr[batch]) if batch > 0 else 0
     aux0 = [int(x) for x in kv_indptr[:batch + 1]] if batch > 0 else []

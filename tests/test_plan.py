@@ -2,6 +2,7 @@
 fault injection (every malformed input is rejected before anything is launched)."""
 
 import os
+import re
 import subprocess
 import sys
 
@@ -390,8 +391,8 @@ def test_plan_log_lines():
                        cwd=root, timeout=300)
     assert r.returncode == 0, r.stderr
     lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[bskv]")]
-    assert any("bskv_plan_decode: kernel decode_group_kernel" in ln and "workers 152" in ln
-               for ln in lines), lines
+    assert any(re.search(r"bskv_plan_decode: kernel decode_group_kernel.*workers (\d+)", ln)
+               and int(re.search(r"workers (\d+)", ln).group(1)) <= 152 for ln in lines), lines
     assert any("bskv_plan_bsr: kernel bsr_generic_kernel" in ln for ln in lines), lines
     assert any("work items per worker" in ln for ln in lines), lines
     env["BSKV_LOGLEVEL"] = "0"
