@@ -53,10 +53,13 @@ constexpr int kMlaVDim = 512 / kMlaVSplit;
 
 constexpr int kDecodeGroupMax = 8;     // kv heads per CTA in the page-major decode variant
 constexpr int kDecodeGroupMaxPage = 16; // largest page_size that takes the page-major variant
-// Page-major decode plans charge a worker this many 16-token tiles for each chunk after its
-// first: the piece it publishes mid-stream and the merge it does at the end cost about that
-// much (measured: workers holding two chunks finished ~6 us later than those holding one).
-constexpr int kDecodeBoundaryTiles = 4;
+// Page-major decode plans charge a worker, in 16-token tiles: a piece it publishes mid-stream
+// (kDecodePublishTiles), a merge at its end (kDecodeMergeTiles), each whole-unit boundary
+// (kDecodeBoundaryTiles). Measured per CTA: workers holding two split pieces finished ~6 us
+// after those holding one (~3.7 us publishing mid-stream, ~2.4 us more merging at the end).
+constexpr int kDecodePublishTiles = 3;
+constexpr int kDecodeMergeTiles = 2;
+constexpr int kDecodeBoundaryTiles = 0;
 // bskv_run_decode merges inside the attention kernel when no unit is cut into more pieces
 // than this; beyond it one warp would merge many pieces serially at the kernel's tail, and
 // the separate merge kernel (more warps per unit) is faster.

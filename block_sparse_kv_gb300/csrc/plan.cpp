@@ -5,9 +5,9 @@
 //   * decode and MLA: a linear split-KV partition. The units (one per request and kv
 //     head, or per query token and latent half) are cut into tiles; the tile sequence
 //     of all units is divided into contiguous ranges, one per worker (equal ranges, or for
-//     the page-major decode ranges of equal cost, a chunk after a worker's first costing
-//     kDecodeBoundaryTiles tiles); a unit that falls into several ranges is computed in
-//     pieces whose partial states are merged.
+//     the page-major decode ranges of equal cost, a piece published mid-stream or a merge at
+//     a worker's end costing a few tiles); a unit that falls into several ranges is computed
+//     in pieces whose partial states are merged.
 //   * BSR: longest-processing-time assignment of (row block, kv head) units to
 //     persistent CTAs, heaviest unit first.
 // The rules are deterministic given num_sms, so the metadata is reproducible bit for bit.
@@ -153,10 +153,17 @@ void assign_slots(size_t U, std::vector<Chunk>& chunks, int32_t& slots,
   }
 }
 
-// Greedy left-to-right fill of the unit tile sequence: each worker takes tiles while its cost
-// (its tiles, plus bc for every chunk after its first) stays within T. Returns the number of
-// workers; with `out`, appends their chunks (unit, first tile, end tile) and worker starts.
-int64_t fill_workers(const std::vector<int64_t>& tiles, int64_t T, int64_t bc,
+// Greedy left-to-right fill of the unit tile sequence: a worker takes tiles while its cost
+// stays within T. Its cost is its tiles plus: `whole` for every chunk after its first;
+// `merge` once it holds two chunks and its first is the tail piece of a unit begun by an
+// earlier worker (walked last: its merge lands at the worker's end); `pub` for a last chunk
+// that is the head piece of a unit continued by a later worker (walked first and published
+// mid-stream). Returns the number of workers; with `out`, appends their chunks (unit, first
+// tile, end tile) and worker starts.
+struct FillCosts {
+  int64_t pub, merge, whole;
+};
+int64_t fill_workers(const std::vector<int64_t>& tiles, int64_t T, const FillCosts& bc,
                      std::vector<int32_t>* worker_ptr, std::vector<Chunk>* out) {
   const size_t U = tiles.size();
   size_t u = 0;
@@ -166,32 +173,36 @@ int64_t fill_workers(const std::vector<int64_t>& tiles, int64_t T, int64_t bc,
     ++workers;
     if (worker_ptr) worker_ptr->push_back(int32_t(out->size()));
     int64_t cost = 0, n = 0;
+    const bool first_tail = off > 0;
     while (u < U) {
       if (tiles[u] == 0) { ++u; continue; }
-      const int64_t add = n > 0 ? bc : 0;
-      if (cost + add >= T) break;
-      const int64_t take = std::min(tiles[u] - off, T - cost - add);
-      if (out) out->push_back(Chunk{int32_t(u), int32_t(off), int32_t(off + take), -1});
-      cost += add + take;
-      ++n;
-      off += take;
-      if (off == tiles[u]) {
+      const int64_t add = n == 0 ? 0 : bc.whole + (n == 1 && first_tail ? bc.merge : 0);
+      const int64_t rem = tiles[u] - off;
+      if (cost + add + rem <= T) {
+        if (out) out->push_back(Chunk{int32_t(u), int32_t(off), int32_t(tiles[u]), -1});
+        cost += add + rem;
+        ++n;
         ++u;
         off = 0;
-      } else {
-        break;
+        continue;
       }
+      const int64_t take = T - cost - add - (n > 0 ? bc.pub : 0);
+      if (take > 0) {
+        if (out) out->push_back(Chunk{int32_t(u), int32_t(off), int32_t(off + take), -1});
+        off += take;
+        ++n;
+      }
+      break;
     }
   }
   return workers;
 }
 
-// Contiguous partition in which a worker's cost is its tiles plus bc per chunk after its
-// first (a piece published mid-stream and a merge at the end cost a worker about that much):
-// the smallest bound T whose greedy fill needs at most max_workers workers, each filled up
-// to T. Chunks are in tokens like linear_partition's.
+// Contiguous partition with the worker costs of fill_workers: the smallest bound T whose
+// greedy fill needs at most max_workers workers, each filled up to T. Chunks are in tokens
+// like linear_partition's.
 void linear_partition_cost(const std::vector<int64_t>& unit_len, int64_t tile,
-                           int64_t max_workers, int64_t bc, std::vector<int32_t>& worker_ptr,
+                           int64_t max_workers, const FillCosts& bc, std::vector<int32_t>& worker_ptr,
                            std::vector<Chunk>& chunks, int32_t& slots,
                            std::vector<int32_t>& merges) {
   std::vector<int64_t> tiles(unit_len.size());
@@ -205,7 +216,7 @@ void linear_partition_cost(const std::vector<int64_t>& unit_len, int64_t tile,
     return;
   }
   int64_t lo = std::max<int64_t>(1, (NT + max_workers - 1) / max_workers);
-  int64_t hi = NT + bc * int64_t(tiles.size());
+  int64_t hi = NT + (bc.pub + bc.merge + bc.whole) * (int64_t(tiles.size()) + 1);
   while (lo < hi) {
     const int64_t mid = (lo + hi) / 2;
     if (fill_workers(tiles, mid, bc, nullptr, nullptr) <= max_workers) hi = mid;
@@ -485,8 +496,9 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
   std::vector<Chunk> chunks;
   int32_t slots = 0;
   if (variant == DECODE_GROUP)
-    linear_partition_cost(len, kDecodeTile, workers_cap, kDecodeBoundaryTiles, worker_ptr, chunks,
-                          slots, merges);
+    linear_partition_cost(len, kDecodeTile, workers_cap,
+                          FillCosts{kDecodePublishTiles, kDecodeMergeTiles, kDecodeBoundaryTiles},
+                          worker_ptr, chunks, slots, merges);
   else
     linear_partition(len, kDecodeTile, workers_cap, worker_ptr, chunks, slots, merges);
   const int32_t P = int32_t(worker_ptr.size() - 1);

@@ -26,9 +26,10 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
   * decode: G = decode_group_heads(num_kv_heads, page_size). G > 0 (page_size <= 16
     and num_kv_heads <= 8 or a multiple of 8): variant 1, units (b, group of G kv
     heads) b-major, max_workers = num_sms unless given, grid = P, and instead of equal
-    ranges the cost partition (linear_partition_cost, 4 tiles per chunk after a worker's
-    first: the smallest bound T whose greedy left-to-right fill needs at most max_workers
-    workers; P = the workers that fill uses). Otherwise variant 0,
+    ranges the cost partition (linear_partition_cost with the costs of _fill, 3 tiles for a
+    piece published mid-stream and 2 for a merge at the worker's end: the smallest bound T
+    whose greedy left-to-right fill needs at most max_workers workers; P = the workers that
+    fill uses). Otherwise variant 0,
     units (b, kv head) b-major, max_workers = 8 * num_sms unless given,
     grid = ceil(P / 8). Both: len = request length, tile 16, aux0 = kv_indptr,
     aux1 = kv_indices.
@@ -171,9 +172,14 @@ def _slots_and_merges(unit_len, chunks):
 
 
 def _fill(tiles, T, bc, record=None):
-    """Greedy left-to-right fill: each worker takes tiles while its cost (tiles, plus bc for
-    every chunk after its first) stays within T. Returns the number of workers; with
-    `record`, appends each worker's chunks as (unit, first tile, end tile) lists."""
+    """Greedy left-to-right fill: a worker takes tiles while its cost stays within T. Its
+    cost is its tiles plus, with bc = (pub, merge, whole): `whole` for every chunk after its
+    first; `merge` once it holds two chunks and its first is the tail piece of a unit begun
+    by an earlier worker (that piece is walked last, and its merge lands at the worker's
+    end); `pub` for a last chunk that is the head piece of a unit continued by a later worker
+    (walked first and published mid-stream). Returns the number of workers; with `record`,
+    appends each worker's chunks as (unit, first tile, end tile) tuples."""
+    pub, merge, whole = bc
     U = len(tiles)
     u, off, workers = 0, 0, 0
     while u < U and tiles[u] == 0:
@@ -181,38 +187,41 @@ def _fill(tiles, T, bc, record=None):
     while u < U:
         workers += 1
         cost, n = 0, 0
+        first_tail = off > 0
         mine = []
         while u < U:
             if tiles[u] == 0:
                 u += 1
                 continue
-            add = bc if n > 0 else 0
-            if cost + add >= T:
-                break
-            take = min(tiles[u] - off, T - cost - add)
-            mine.append((u, off, off + take))
-            cost += add + take
-            n += 1
-            off += take
-            if off == tiles[u]:
+            add = 0 if n == 0 else whole + (merge if n == 1 and first_tail else 0)
+            rem = tiles[u] - off
+            if cost + add + rem <= T:
+                mine.append((u, off, tiles[u]))
+                cost += add + rem
+                n += 1
                 u, off = u + 1, 0
-            else:
-                break
+                continue
+            take = T - cost - add - (pub if n > 0 else 0)
+            if take > 0:
+                mine.append((u, off, off + take))
+                off += take
+                n += 1
+            break
         if record is not None:
             record.append(mine)
     return workers
 
 
 def linear_partition_cost(unit_len, tile, max_workers, bc):
-    """Contiguous partition of the unit tile sequence in which a worker's cost is its tiles
-    plus bc per chunk after its first: the smallest cost bound T whose greedy fill needs at
-    most max_workers workers, each worker filled up to T."""
+    """Contiguous partition of the unit tile sequence with the worker cost of _fill: the
+    smallest cost bound T whose greedy fill needs at most max_workers workers, each worker
+    filled up to T."""
     tiles = [(L + tile - 1) // tile for L in unit_len]
     NT = sum(tiles)
     if NT == 0:
         return linear_partition(unit_len, tile, max_workers)
     lo = max(1, -(-NT // max_workers))
-    hi = NT + bc * len(tiles)
+    hi = NT + sum(bc) * (len(tiles) + 1)
     while lo < hi:
         mid = (lo + hi) // 2
         if _fill(tiles, mid, bc) <= max_workers:
@@ -252,9 +261,9 @@ def decode_units(kv_indptr, kv_last_page_len, batch, page_size, num_kv_heads):
     return lens
 
 
-# page-major decode: a worker's cost of each chunk after its first, in 16-token tiles (a
-# piece published mid-stream and a merge at the end cost a worker about this much)
-DECODE_BOUNDARY_TILES = 4
+# page-major decode: a worker's extra costs in 16-token tiles (pub, merge, whole): a piece
+# published mid-stream, a merge at the worker's end, a whole-unit boundary
+DECODE_BOUNDARY_TILES = (3, 2, 0)
 
 
 def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_qo_heads,
