@@ -56,8 +56,9 @@ constexpr int kDecodeGroupMaxPage = 16; // largest page_size that takes the page
 // Page-major decode plans charge a worker, in 16-token tiles: a piece it publishes mid-stream
 // (kDecodePublishTiles), a merge at its end (kDecodeMergeTiles), each whole-unit boundary
 // (kDecodeBoundaryTiles). Measured per CTA: workers holding two split pieces finished ~6 us
-// after those holding one (~3.7 us publishing mid-stream, ~2.4 us more merging at the end).
-constexpr int kDecodePublishTiles = 3;
+// after those holding one (~3.7 us publishing mid-stream, ~2.4 us more merging at the end);
+// the charges were then chosen by timing the headline decode (2 and 2 ran best).
+constexpr int kDecodePublishTiles = 2;
 constexpr int kDecodeMergeTiles = 2;
 constexpr int kDecodeBoundaryTiles = 0;
 // bskv_run_decode merges inside the attention kernel when no unit is cut into more pieces

@@ -26,7 +26,7 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
   * decode: G = decode_group_heads(num_kv_heads, page_size). G > 0 (page_size <= 16
     and num_kv_heads <= 8 or a multiple of 8): variant 1, units (b, group of G kv
     heads) b-major, max_workers = num_sms unless given, grid = P, and instead of equal
-    ranges the cost partition (linear_partition_cost with the costs of _fill, 3 tiles for a
+    ranges the cost partition (linear_partition_cost with the costs of _fill, 2 tiles for a
     piece published mid-stream and 2 for a merge at the worker's end: the smallest bound T
     whose greedy left-to-right fill needs at most max_workers workers; P = the workers that
     fill uses). Otherwise variant 0,
@@ -263,7 +263,7 @@ def decode_units(kv_indptr, kv_last_page_len, batch, page_size, num_kv_heads):
 
 # page-major decode: a worker's extra costs in 16-token tiles (pub, merge, whole): a piece
 # published mid-stream, a merge at the worker's end, a whole-unit boundary
-DECODE_BOUNDARY_TILES = (3, 2, 0)
+DECODE_BOUNDARY_TILES = (2, 2, 0)
 
 
 def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_qo_heads,
