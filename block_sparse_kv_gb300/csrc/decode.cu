@@ -13,9 +13,10 @@
 //     per kv head of a group of up to 8, and a lookup warp. Each 16-token tile is copied by
 //     TMA for all heads of the group at once, so with the contiguous layout a page's K (and
 //     V) for 8 heads is one 32 KB piece instead of eight 4 KB ones. A 3-stage ring (64 KB
-//     stages for 8 heads of 128 dims) holds up to 192 KB in flight per SM; the producer's
-//     lanes read the page ids of 32 pages at a time, and the lookup warp finds the merge
-//     items of the worker's first and last chunks while the KV streams.
+//     stages for 8 heads of 128 dims) holds up to 192 KB in flight per SM; the producer
+//     starts from the plan's start record of its worker (first chunk, page range, first
+//     page ids) and then reads the page ids of 32 pages at a time, and the lookup warp finds
+//     the merge items of the worker's first and last chunks while the KV streams.
 //   * warp (larger pages, or head counts that do not group): 8 independent worker warps
 //     per CTA, each with a private 3-stage ring over its own (request, kv head) range;
 //     a page of 64 tokens is already a 16 KB piece per head.
@@ -68,6 +69,7 @@ struct DecodeParams {
   // word offsets of the metadata's sections and the merge count (the header's values,
   // passed by value so that a worker's first loads do not wait on the header)
   int off_workers, off_chunks, off_merges, off_aux0, off_aux1, num_merges;
+  int off_starts;  // page-major plans: the per-worker start records, else -1
   float scale_log2;
   StatusArgs st;
 };
@@ -623,18 +625,37 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int k = 0; k < c1 - c0 && ok; ++k) {
-      const int4 ch = chunks[chunk_at(c0, c1, k)];
-      const int b = ch.x / HG, hg = ch.x % HG;
-      const int pbase = kv_indptr[b], npages = kv_indptr[b + 1] - pbase;
+      int4 ch;
+      int pbase, npages;
+      // lane j holds the id of page win + j of the request, for j < wsize
+      int win = -(1 << 30), wsize = 32, pid = 0;
+      if (k == 0 && p.off_starts >= 0) {
+        // the walk's first chunk, its request's pages and their first ids from the worker's
+        // start record: words that do not depend on one another, one round trip
+        const int v = lane < kDecodeStartWords ? hdr[p.off_starts + kDecodeStartWords * w + lane] : 0;
+        ch = make_int4(__shfl_sync(0xffffffffu, v, 0), __shfl_sync(0xffffffffu, v, 1),
+                       __shfl_sync(0xffffffffu, v, 2), __shfl_sync(0xffffffffu, v, 3));
+        pbase = __shfl_sync(0xffffffffu, v, 4);
+        npages = __shfl_sync(0xffffffffu, v, 5);
+        wsize = __shfl_sync(0xffffffffu, v, 6);
+        pid = __shfl_sync(0xffffffffu, v, 8 + (lane & (kDecodeStartPages - 1)));
+        win = ch.y / ps;
+      } else {
+        ch = chunks[chunk_at(c0, c1, k)];
+        const int b = ch.x / HG;
+        pbase = kv_indptr[b];
+        npages = kv_indptr[b + 1] - pbase;
+      }
+      const int hg = ch.x % HG;
       const int nt = ntiles(ch);
-      int win = -(1 << 30), pid = 0;  // lane j holds the id of page win + j of the request
       for (int t = 0; t < nt; ++t, ++it) {
         const int stage = int(it % uint32_t(ns));
         const int tok = ch.y + t * kTile;
         const int first = tok / ps;
         const int pieces = ps >= kTile ? 1 : min(kTile / ps, npages - first);
-        if (first + pieces > win + 32) {
+        if (first + pieces > win + wsize) {
           win = first;
+          wsize = 32;
           pid = win + lane < npages ? kv_indices[pbase + win + lane] : 0;
         }
         if (it >= uint32_t(ns)) {
@@ -991,6 +1012,7 @@ bskv_status prepare_decode(const char* who, const bskv_plan* plan, const int32_t
   dp->off_aux0 = meta_word(plan, H_OFF_AUX0);
   dp->off_aux1 = meta_word(plan, H_OFF_AUX1);
   dp->num_merges = meta_word(plan, H_MERGES);
+  dp->off_starts = plan->decode_starts;
   dp->scale_log2 = sm_scale_log2(sm_scale, plan->head_dim);
   if (bskv_status s = status_args(&dp->st)) return s;
   const uint64_t dims[5] = {uint64_t(D), uint64_t(ps), uint64_t(Hkv), 2, uint64_t(plan->num_pages)};

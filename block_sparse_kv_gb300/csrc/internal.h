@@ -61,6 +61,11 @@ constexpr int kDecodeGroupMaxPage = 16; // largest page_size that takes the page
 constexpr int kDecodePublishTiles = 2;
 constexpr int kDecodeMergeTiles = 2;
 constexpr int kDecodeBoundaryTiles = 0;
+// A page-major decode plan ends with one record per worker describing the first chunk of its
+// walk: {unit, first token, end token, slot, kv_indptr[b], pages of b, n, 0, the ids of the
+// chunk's first n <= 8 pages}, so that a worker's first copies wait on one round trip.
+constexpr int kDecodeStartWords = 16;
+constexpr int kDecodeStartPages = 8;
 // bskv_run_decode merges inside the attention kernel when no unit is cut into more pieces
 // than this; beyond it one warp would merge many pieces serially at the kernel's tail, and
 // the separate merge kernel (more warps per unit) is faster.
@@ -155,6 +160,9 @@ struct bskv_plan {
   // item and kv head of the unit)
   size_t counter_words = 0;
   int32_t max_merge_count = 0;  // most pieces of one split unit
+  // page-major decode: word offset in the metadata of the per-worker start records
+  // (kDecodeStartWords each), or -1
+  int32_t decode_starts = -1;
   // set by bskv_plan_upload
   const int32_t* meta_dev = nullptr;
   int32_t* counters_dev = nullptr;  // one merge counter per merge item, zero between runs

@@ -511,6 +511,28 @@ extern "C" bskv_status bskv_plan_decode(const int32_t* kv_indptr, const int32_t*
   p->dtype = dtype;
   assemble(p, KIND_DECODE, int32_t(len.size()), worker_ptr, chunks, slots, merges, kDecodeTile,
            kv_indptr, batch > 0 ? size_t(batch) + 1 : 0, kv_indices, size_t(nnz), grid, variant);
+  if (variant == DECODE_GROUP) {
+    // start records: the first chunk of each worker's walk (its last chunk when it has
+    // several, the order in which the kernel walks them) and the first page ids it reads
+    std::vector<int32_t>& m = p->meta;
+    p->decode_starts = int32_t(m.size());
+    for (int32_t w = 0; w < P; ++w) {
+      int32_t rec[kDecodeStartWords] = {};
+      const int32_t w0 = worker_ptr[size_t(w)], w1 = worker_ptr[size_t(w) + 1];
+      if (w1 > w0) {
+        const Chunk& c = chunks[size_t(w1 - w0 >= 2 ? w1 - 1 : w0)];
+        const int32_t b = c.unit / upb;
+        const int32_t pbase = kv_indptr[b], npages = kv_indptr[b + 1] - pbase;
+        const int32_t first = c.a / page_size;
+        const int32_t n = std::min(kDecodeStartPages, npages - first);
+        rec[0] = c.unit; rec[1] = c.a; rec[2] = c.b; rec[3] = c.c;
+        rec[4] = pbase; rec[5] = npages; rec[6] = n;
+        for (int32_t i = 0; i < n; ++i) rec[8 + i] = kv_indices[pbase + first + i];
+      }
+      m.insert(m.end(), rec, rec + kDecodeStartWords);
+    }
+    m[H_TOTAL] = int32_t(m.size());
+  }
   p->float_ws_bytes = slots == 0 ? 0
       : align256(size_t(slots) * slot_rows * head_dim * 4) + align256(size_t(slots) * slot_rows * 4);
   p->counter_words = merges.size() / 3 * size_t(num_kv_heads / upb);

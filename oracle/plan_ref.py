@@ -32,7 +32,11 @@ slot = -1. Merge items (unit, first_slot, count) list, in unit order, the units 
     fill uses). Otherwise variant 0,
     units (b, kv head) b-major, max_workers = 8 * num_sms unless given,
     grid = ceil(P / 8). Both: len = request length, tile 16, aux0 = kv_indptr,
-    aux1 = kv_indices.
+    aux1 = kv_indices. Variant 1 appends, after the sections (total_words updated), one
+    16-word start record per worker for the first chunk of its walk (its last chunk when it
+    has several, else its only one): unit, first token, end token, slot, kv_indptr[b],
+    pages of b, n = min(8, pages of b - first token // page_size), 0, and the first n page
+    ids of that chunk (zeros after).
   * MLA: units = query tokens n = b*q_len + t, len = seq_lens[b], tile 128,
     max_workers = max(1, num_sms // 2) (a worker is a pair of CTAs, one per latent half),
     grid = 2 P, no aux, variant 0. Whole units instead of the linear partition when, with
@@ -280,7 +284,22 @@ def decode_meta(kv_indptr, kv_indices, kv_last_page_len, batch, page_size, num_q
     aux0 = [int(x) for x in kv_indptr[:batch + 1]] if batch > 0 else []
     aux1 = [int(x) for x in kv_indices[:nnz]]
     grid = P if G else (P + 7) // 8
-    return _assemble(1, len(lens), wp, ch, slots, merges, 16, aux0, aux1, grid, 1 if G else 0)
+    m = _assemble(1, len(lens), wp, ch, slots, merges, 16, aux0, aux1, grid, 1 if G else 0)
+    if G:
+        upb = num_kv_heads // G
+        for w in range(P):
+            rec = [0] * 16
+            if wp[w + 1] > wp[w]:
+                c = ch[wp[w + 1] - 1 if wp[w + 1] - wp[w] >= 2 else wp[w]]
+                b = c[0] // upb
+                pbase, npages = aux0[b], aux0[b + 1] - aux0[b]
+                first = c[1] // page_size
+                n = min(8, npages - first)
+                rec[:7] = [c[0], c[1], c[2], c[3], pbase, npages, n]
+                rec[8:8 + n] = aux1[pbase + first:pbase + first + n]
+            m += rec
+        m[14] = len(m)
+    return m
 
 
 MLA_SPLIT_PENALTY_TILES = 7
