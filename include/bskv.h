@@ -298,10 +298,9 @@ bskv_status bskv_decode_merge(const bskv_plan* plan, void* out, const int64_t* o
  * library-owned static device array, and the split-KV partial states (at most 8 MiB) live
  * in a second one. Every GPU that loads the library holds these 9 MiB until the process
  * exits. A plan that needs more returns BSKV_ERR_UNSUPPORTED and launches nothing.
- * The first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress);
- * make that first call before any stream capture. All calls share the two arrays, and
- * each call overwrites what the previous one left there, so calls that overlap on the GPU
- * (e.g. on two streams) race: serialise them. No call allocates or frees device memory.
+ * The first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress).
+ * All calls share the two arrays, and each call overwrites what the previous one left
+ * there, so calls that overlap on the GPU (e.g. on two streams) race: serialise them. No call allocates or frees device memory.
  * The metadata copy reads the plan's own host memory, which is pageable: the call can wait
  * while the driver stages those bytes, and the plan is no longer read once the call returns.
  */
