@@ -944,7 +944,7 @@ extern "C" bskv_status bskv_plan_mla_sparse(const int32_t* seq_lens, int32_t bat
     set_error("plan_mla_sparse: batch=%d q_len=%d num_sms=%d", batch, q_len, num_sms);
     return BSKV_ERR_INVALID_ARG;
   }
-  if (top_k < 64 || top_k % 64 != 0) { set_error("plan_mla_sparse: top_k (%d) must be a positive multiple of 64", top_k); return BSKV_ERR_INVALID_ARG; }
+  if (top_k < 64 || top_k % 64 != 0) { set_error("plan_mla_sparse: top_k (%d) must be divisible by 64 and at least 64", top_k); return BSKV_ERR_INVALID_ARG; }
   if (num_heads < 1 || num_heads > 128) { set_error("plan_mla_sparse: num_heads %d outside [1,128]", num_heads); return BSKV_ERR_UNSUPPORTED; }
   // One unit per query token; a worker is a pair of CTAs (a cluster), one per latent half.
   std::vector<int64_t> len;

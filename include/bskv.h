@@ -19,7 +19,7 @@
  *   [SKILL]   "FlashInfer" agent-skill summary: KV-Cache Formats (paged KV-cache),
  *             Cascade Inference, Roofline Analysis.
  *   [CHEAT]   FlashInfer cheat page: docs/api/cascade.rst (merge_state(s)); README
- *             ("CUDAGraph and torch.compile compatible").
+ *             (its production notes: the library is meant to run under CUDA graphs).
  *
  * Conventions (all entry points):
  *   - Every function returns a bskv_status. Unsupported shapes, dtypes, layouts and
@@ -35,13 +35,13 @@
  *     last dim must be contiguous. Device pointers must be 16-byte aligned, and every
  *     stride times the element size must be a multiple of 16 bytes.
  *   - A plan (bskv_plan*) is an opaque host object made by bskv_plan_* from host copies
- *     of the index arrays ([SPARSE] plan(): "auxiliary data structures will be created
- *     during this call and cached for multiple kernel runs"). It is re-made whenever
+ *     of the index arrays ([SPARSE] plan(): the plan step builds its helper structures
+ *     once and later runs reuse them). It is re-made whenever
  *     the index arrays, lengths or shapes change, and must not be shared between
  *     overlapping runs ([WRAP] Metadata reuse). bskv_plan_upload copies its metadata
  *     into the caller's int workspace on a stream; runs read it from there.
- *   - LSE is the natural-log log-sum-exp of the scaled logits ([SPARSE] run(): "the
- *     log-sum-exp of attention logits"); a row that sees no key gets out = 0 and
+ *   - LSE is the natural-log log-sum-exp of the scaled logits ([SPARSE] run(), its
+ *     optional second output); a row that sees no key gets out = 0 and
  *     lse = -inf.
  *   - sm_scale (decode, prefill and BSR runs) multiplies q.k before the softmax; the value
  *     0 selects the pages' default 1/sqrt(head_dim) ([SPARSE] plan(): sm_scale defaults to
@@ -165,7 +165,7 @@ bskv_status bskv_plan_bsr_variable(const uint8_t* block_mask_map, const int32_t*
 
 /*
  * Batch prefill over a paged KV cache ([CHEAT] benchmark README:
- * BatchPrefillWithPagedKVCacheWrapper, prefill attention with paged KV cache; [SKILL]
+ * BatchPrefillWithPagedKVCacheWrapper, the paged-cache prefill wrapper; [SKILL]
  * KV-Cache Formats and Batch prefill / Append): request b owns query tokens
  * [qo_indptr[b], qo_indptr[b+1]) (the last qo_len_b tokens of its sequence) and the pages of
  * its kv_indptr/kv_indices/kv_last_page_len entry (L_b tokens, as for bskv_plan_decode).
@@ -402,8 +402,8 @@ bskv_status bskv_run_mla_paged(const bskv_plan* plan, const void* query, const v
 /*
  * RoPE + FP8 E4M3 quantisation of MLA query/key rows ([MLA] mla_rope_quantize_fp8;
  * [WRAP] RoPE and FP8 quantization). Rotary arithmetic in float32 on the 64-value
- * tail; is_neox != 0 rotates the two contiguous 32-value halves, 0 rotates adjacent
- * even/odd pairs; pair i uses cos = cos_sin[pos, i], sin = cos_sin[pos, 32 + i].
+ * tail; is_neox != 0 pairs tail value i with value i + 32 (NeoX layout), 0 pairs values
+ * 2i and 2i + 1 (interleaved layout); pair i uses cos = cos_sin[pos, i], sin = cos_sin[pos, 32 + i].
  * Outputs: Q_fp8 = cast(Q * quant_scale_q), K_fp8 = cast(K * quant_scale_kv), round to
  * nearest even, saturating to +-448.
  *   Query group (all NULL to skip): q_rope [nnz_q, num_heads, 64], q_nope [nnz_q,
@@ -429,8 +429,9 @@ bskv_status bskv_rope_quantize_fp8(
 
 /*
  * RoPE + FP8 quantisation with the key rows appended to a paged latent cache ([CHEAT]
- * benchmark README: rope_quantize_fp8_append_paged_kv_cache, RoPE with FP8 quantization and
- * paged KV cache append; page table as in [SKILL] KV-Cache Formats). The arithmetic is that
+ * benchmark README: rope_quantize_fp8_append_paged_kv_cache, which rotates, quantises and
+ * writes the key rows into a paged cache in one call; page table as in [SKILL] KV-Cache
+ * Formats). The arithmetic is that
  * of bskv_rope_quantize_fp8; only the destination of a key row differs.
  *   Query group: exactly as bskv_rope_quantize_fp8 (all NULL to skip).
  *   Key rows: k_rope [nnz_k, 64], k_nope [nnz_k, 512] bf16 with row strides; pos_k [nnz_k]

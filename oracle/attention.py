@@ -34,7 +34,7 @@ Sources:
     kv_indices[kv_indptr[b]:kv_indptr[b+1]] in order, and its length is
     (n_pages - 1) * page_size + kv_last_page_len[b].
   * Paged prefill: FlashInfer cheat page, benchmark README (BatchPrefillWithPagedKVCacheWrapper,
-    prefill attention with paged KV cache); "FlashInfer" agent-skill summary, Batch prefill
+    the paged-cache prefill wrapper); "FlashInfer" agent-skill summary, Batch prefill
     and Append (causal prefill of new tokens against the cache). Reading: request b's queries
     are the last qo_len_b tokens of its sequence, so causal is aligned bottom-right.
   * Sparse MLA: "Sparse MLA" (MATE 0.2.6), sparse_mla_fp8_decode: FP8 query

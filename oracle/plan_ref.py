@@ -2,9 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
-The pages fix what plan() is for, not how it partitions work: "[plan] create
-auxiliary data structures ... cached for multiple kernel runs" ("flashinfer.sparse",
-BlockSparseAttentionWrapper.plan notes) and the MLA scheduler metadata is reusable
+The pages fix what plan() is for, not how it partitions work: it builds helper
+structures once for many later runs ("flashinfer.sparse", BlockSparseAttentionWrapper.plan
+notes) and the MLA scheduler metadata is reusable
 while seq_lens, the query shape and top-k stay unchanged ("Sparse MLA",
 get_batch_decode_metadata_mla). The partition rule below is the library's own design,
 stated here from its specification so that the C++ plan can be compared word for word:

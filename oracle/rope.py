@@ -5,10 +5,10 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 Follows "Sparse MLA" (MATE 0.2.6 API docs), section "RoPE and FP8 quantization"
 (mla_rope_quantize_fp8 parameters), and "FlashInfer Compatibility Wrapper", section
 "RoPE and FP8 quantization":
-  * the cos/sin cache has shape [max_seq_len, 64]; columns [:32] are cosines and
-    columns [32:] sines; every position must lie in [0, max_seq_len);
-  * is_neox=True rotates the two contiguous 32-value halves, is_neox=False rotates
-    adjacent even/odd pairs;
+  * the rotary cache is [max_seq_len, 64], the cosines in its first 32 columns and the
+    sines in the last 32; every position must lie in [0, max_seq_len);
+  * is_neox=True pairs tail value i with value i + 32 (the first half against the
+    second), is_neox=False pairs values 2i and 2i + 1;
   * the quant scales multiply the values before the FP8 cast:
     Q_fp8 = cast(Q * quant_scale_q), KV_fp8 = cast(KV * quant_scale_kv),
     for both the 512-value NoPE part and the rotated 64-value tail.
@@ -18,8 +18,8 @@ and sin = cache[pos, 32 + i] in both layouts, and rotates (x, y) to
 values; the single rounding is the E4M3 cast.
 
 The paged append (FlashInfer cheat page, benchmark README:
-rope_quantize_fp8_append_paged_kv_cache, RoPE with FP8 quantization and paged KV cache
-append; page table of the "FlashInfer" agent-skill summary, KV-Cache Formats) writes the
+rope_quantize_fp8_append_paged_kv_cache, which rotates, quantises and writes the key rows
+into a paged cache in one call; page table of the "FlashInfer" agent-skill summary, KV-Cache Formats) writes the
 same key rows into a paged latent cache. Reading: key row i belongs to request
 batch_indices[i] at token position positions[i]; it lands in page
 kv_indices[kv_indptr[b] + positions[i] // page_size], slot positions[i] % page_size, as

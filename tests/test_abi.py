@@ -34,7 +34,7 @@ def test_version_and_error_text(lib):
         bskv.bskv_plan_mla_sparse([8], 1, 1, 4, 100, num_sms=4)
     except bskv.BskvError as e:
         assert e.status == "ERR_INVALID_ARG"
-        assert "multiple of 64" in str(e)
+        assert "divisible by 64" in str(e)
     else:
         raise AssertionError("top_k % 64 != 0 accepted")
 
