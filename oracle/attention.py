@@ -69,7 +69,7 @@ def masked_attention(q, k, v, sm_scale, mask=None):
     Mq, Hq, _ = q.shape
     Nk, Hkv, Dv = v.shape
     if Hq % Hkv != 0:
-        raise ValueError("num_qo_heads must be a multiple of num_kv_heads")
+        raise ValueError("num_kv_heads must divide num_qo_heads")
     g = Hq // Hkv
     out = np.zeros((Mq, Hq, Dv))
     lse = np.full((Mq, Hq), -np.inf)
